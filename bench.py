@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse offloaded-KV decode step on one GB300 (or N replicas).
+
+A step is one whole decode step of the Llama-3-8B-shaped workload: 32 layers,
+each running landmark top-k selection, the predicted-vs-needed diff, the
+coalesced host->HBM gather into the two-layer ping-pong buffer (prefetch two
+layers ahead, urgent misses) and GQA attention with the log-sum-exp window
+merge, all inside libkvo's CUDA kernels.  Inputs are seeded synthetic data of
+the workload's shapes; the KV cache lives in pinned host memory.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead (the reference arm: no GPU code on that path).
+"""
+from __future__ import annotations
+
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sparse_kv_cache_landmark_gb300 import synth  # noqa: E402
+from sparse_kv_cache_landmark_gb300.workloads import WORKLOADS  # noqa: E402
+
+METRIC = "sparse decode steps/s and effective KV GB/s (1 GB300) as % of HBM/PCIe roofline"
+UNIT = "steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_decode")
+    ap.add_argument("--seed", type=int, default=1235)
+    ap.add_argument("--host-layers", type=int, default=0, help="distinct host layers (0: all that fit)")
+    ap.add_argument("--cpu-sample-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def workload_bytes(w, lens):
+    """Algorithmic bytes of one step (all layers): HBM and host link."""
+    G, d, k, B, W, L = w.batch * w.n_kv_heads, w.head_dim, w.top_k, w.block_size, w.window, w.n_layers
+    tok = 4 * d                                             # K+V bf16 bytes per token per KV head
+    C = [(n - W) // B for n in lens]
+    lm_bytes = sum(C) * w.n_kv_heads * d * (4 if B > 1 else 2)
+    gathered = G * k * B * tok                              # written to the ping-pong half
+    attended = G * (k * B + W) * tok                        # read by attention
+    q_bytes = w.batch * w.n_q_heads * d * 2 * 3             # select (2x) + attention
+    out_bytes = w.batch * w.n_q_heads * (d + 1) * 4
+    meta = G * k * 4 * 8
+    hbm = (lm_bytes + gathered + attended + q_bytes + out_bytes + meta) * L
+    host = gathered * L
+    kv_attended = attended * L
+    return {"hbm": hbm, "host": host, "kv_attended": kv_attended, "gather_per_launch": gathered,
+            "landmark_per_layer": lm_bytes, "attended_per_layer": attended}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", str(dev)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, x: float) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(w, seed, budget_s, layers=1):
+    """Time the fp64 oracle (as it stands) on whole (request, KV head) groups.
+
+    Generates request 0 of layer 0 on the CPU and runs the oracle's per-group
+    step (landmarks, scores, top-k, diff, runs, attention + merge) on its KV
+    heads until ``budget_s`` seconds of oracle time have passed.
+    Returns (seconds per group, groups timed).
+    """
+    import oracle as orc
+    lens = synth.seq_lens(w, seed)
+    q, qs = synth.gen_queries(w, seed, 0)
+    K, V = synth.gen_request_kv(w, seed, 0, 0, lens[0], q[0])
+    r = w.group_size
+    times = []
+    t_start = time.perf_counter()
+    g = 0
+    while time.perf_counter() - t_start < budget_s or not times:
+        gg = g % w.n_kv_heads
+        t0 = time.perf_counter()
+        orc.decode_group(synth.bits(K[gg]), synth.bits(V[gg]), synth.bits(q[0, gg * r:(gg + 1) * r]),
+                         None if qs is None else synth.bits(qs[0, gg * r:(gg + 1) * r]),
+                         block_size=w.block_size, top_k=w.top_k, window=w.window)
+        times.append(time.perf_counter() - t0)
+        g += 1
+    return sum(times) / len(times), len(times)
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    G = w.batch * w.n_kv_heads
+    per_step_groups = G * w.n_layers
+    # each bench step: one bounded sample of groups; the step time is scaled
+    # to the whole workload step (G groups x n_layers layers)
+    import oracle as orc  # noqa: F401  (the reference arm runs the oracle only)
+    for _ in range(args.warmup):
+        oracle_sample(w, args.seed, 0.0)
+    step_s = []
+    sample_budget = max(1.0, 60.0 / max(1, args.steps))
+    n_groups = 0
+    for _ in range(args.steps):
+        t_group, n = oracle_sample(w, args.seed, sample_budget)
+        step_s.append(t_group * per_step_groups)
+        n_groups += n
+    t = statistics.mean(step_s)
+    v = 1.0 / t
+    sample = (f"fp64 numpy oracle on {n_groups} (request, KV head) groups of layer 0 over {args.steps} bench "
+              f"steps, scaled to {per_step_groups} groups per decode step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                   "head_dim": w.head_dim, "context": w.ctx[0], "block": w.block_size, "top_k": w.top_k,
+                   "window": w.window, "layers": w.n_layers},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ GPU path
+def run_ours(args):
+    ws, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    from sparse_kv_cache_landmark_gb300.kvo import Context, lib
+    lib()                                   # fails loudly when the library is not built
+    w = WORKLOADS[args.workload]
+    lens = synth.seq_lens(w, args.seed)
+    n = synth.layer_numel(w, lens)
+    layer_bytes = 2 * n * 2
+    if args.host_layers:
+        n_host = min(args.host_layers, w.n_layers)
+    else:
+        avail = 0
+        try:
+            with open("/proc/meminfo") as f:
+                for line in f:
+                    if line.startswith("MemAvailable"):
+                        avail = int(line.split()[1]) * 1024
+        except OSError:
+            pass
+        fit = int(0.55 * avail / (layer_bytes * ws)) if avail else w.n_layers
+        n_host = max(1, min(w.n_layers, fit))
+    t_gen = time.perf_counter()
+    k_host, v_host, k_win, v_win, qs_l, qspec_l = [], [], [], [], [], []
+    for l in range(w.n_layers):
+        q, qs = synth.gen_queries(w, args.seed, l)
+        qs_l.append(q)
+        qspec_l.append(qs)
+        if l < n_host:
+            kh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+            vh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+            synth.fill_layer(w, args.seed, l, kh, vh, q, lens, device="cuda")
+            k_host.append(kh)
+            v_host.append(vh)
+            kw = torch.empty(w.batch, w.n_kv_heads, w.window, w.head_dim, dtype=torch.bfloat16, device="cuda")
+            vw = torch.empty_like(kw)
+            off = 0
+            for b, nb in enumerate(lens):
+                sz = nb * w.n_kv_heads * w.head_dim
+                kw[b] = kh[off:off + sz].view(w.n_kv_heads, nb, w.head_dim)[:, nb - w.window:].to("cuda")
+                vw[b] = vh[off:off + sz].view(w.n_kv_heads, nb, w.head_dim)[:, nb - w.window:].to("cuda")
+                off += sz
+            k_win.append(kw)
+            v_win.append(vw)
+        else:
+            k_host.append(k_host[l % n_host]); v_host.append(v_host[l % n_host])
+            k_win.append(k_win[l % n_host]); v_win.append(v_win[l % n_host])
+    torch.cuda.synchronize()
+    t_gen = time.perf_counter() - t_gen
+    ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
+                  block_size=w.block_size, top_k=w.top_k, window=w.window, n_layers=w.n_layers, seq_lens=lens,
+                  k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win)
+    q_pin = torch.stack(qs_l).pin_memory()
+    qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
+    q_dev = q_pin.to("cuda")
+    qs_dev = None if qs_pin is None else qs_pin.to("cuda")
+    rows = w.batch * w.n_q_heads
+    o = torch.empty(w.n_layers, rows, w.head_dim, dtype=torch.float32, device="cuda")
+    lse = torch.empty(w.n_layers, rows, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # host->device link bandwidth (pinned copy engine), best of 3
+    probe_h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    probe_d = torch.empty_like(probe_h, device="cuda")
+    link = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        probe_d.copy_(probe_h, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        link = max(link, probe_h.numel() / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del probe_h, probe_d
+
+    for _ in range(max(3, args.warmup)):
+        ctx.decode_step(q_dev, qs_dev, o, lse)
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    time.sleep(0.3)
+    ctx.profile(True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ctx.decode_step(q_dev, qs_dev, o, lse)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    prof = ctx.profile_read()
+    ctx.profile(False)
+    clk = clocks.stop()
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+    t_ms = max_over_ranks(ws, t_ms)
+    value = ws / (t_ms * 1e-3)
+
+    # end to end through the public API with host buffers: q H2D, step, o/lse D2H
+    o_pin = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lse_pin = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        q_dev.copy_(q_pin, non_blocking=True)
+        if qs_pin is not None:
+            qs_dev.copy_(qs_pin, non_blocking=True)
+        ctx.decode_step(q_dev, qs_dev, o, lse)
+        o_pin.copy_(o, non_blocking=True)
+        lse_pin.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1) / args.steps)
+    h2d = q_pin.numel() * 2 + (qs_pin.numel() * 2 if qs_pin is not None else 0)
+    d2h = o_pin.numel() * 4 + lse_pin.numel() * 4
+    assert torch.isfinite(o_pin).all() and torch.isfinite(lse_pin).all()
+    status = ctx.device_status()
+
+    hbm_peak, peak_kind = peaks()
+    by = workload_bytes(w, lens)
+    t_hbm = by["hbm"] / (hbm_peak * 1e9)
+    t_link = by["host"] / (link * 1e9)
+    t_star = max(t_hbm, t_link)
+    g_ms, g_n = prof["gather_prefetch"]
+    gather_avg_s = (g_ms / max(g_n, 1)) * 1e-3
+    achieved = by["gather_per_launch"] / gather_avg_s / 1e9 if g_n else None
+    launches = sum(c for _, c in prof.values())
+    kernels = {}
+    for kind, (ms, cnt) in prof.items():
+        if cnt:
+            kernels[kind] = {"launches_per_step": cnt / args.steps, "avg_us": ms / cnt * 1e3,
+                             "share_of_step": ms / args.steps / t_ms}
+    a_ms, a_n = prof["attention"]
+    if a_n:
+        kernels["attention"]["hbm_gbs"] = by["attended_per_layer"] / (a_ms / a_n * 1e-3) / 1e9
+    s_ms, s_n = prof["select"]
+    if s_n:
+        kernels["select"]["hbm_gbs"] = by["landmark_per_layer"] / (s_ms / s_n * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t_group, n_groups = oracle_sample(w, args.seed, args.cpu_sample_s)
+        G = w.batch * w.n_kv_heads
+        cpu = {"value": 1.0 / (t_group * G * w.n_layers), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"fp64 numpy oracle on {n_groups} (request, KV head) groups of layer 0, "
+                         f"{t_group * 1e3:.1f} ms per group, scaled to {G * w.n_layers} groups per step"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": t_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.ctx[0],
+                       "block": w.block_size, "top_k": w.top_k, "window": w.window, "layers": w.n_layers,
+                       "host_layers_distinct": n_host, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2: every step streams 4.3 GB over the host link and "
+                             "reads 2.1 GB of landmarks + 4.3 GB of gathered KV from HBM"},
+            "effective_kv_gbs": by["kv_attended"] / (t_ms * 1e-3) / 1e9 * ws,
+            "step_roofline": {"t_star_ms": t_star * 1e3, "frac": t_star * 1e3 / t_ms,
+                              "bound": "link" if t_link >= t_hbm else "hbm",
+                              "host_bytes": by["host"], "hbm_bytes": by["hbm"], "link_gbs": link,
+                              "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind},
+            "roofline": {"kernel": "gather_kernel (prefetch)", "bound": "link",
+                         "achieved": achieved, "peak": link, "unit": "GB/s",
+                         "frac": (achieved / link) if achieved else None, "traffic": None,
+                         "peak_kind": "measured in this run: pinned cudaMemcpyAsync host->device, best of 3"},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "e2e": {"value": ws / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "device_status": status,
+            "setup_s": round(t_gen, 1),
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

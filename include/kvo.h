@@ -1,0 +1,239 @@
+/*
+ * kvo.h -- C ABI of the GB300 sparse offloaded-KV decode step.
+ *
+ * One decode step per layer, as described in "DualDecoder: Accelerate Long
+ * Context LLM Inference by Predictive Prefetch" (arXiv 2607.26475):
+ *   1. select_topk       -- score every host-resident block against static
+ *                           GPU-resident K landmarks and keep the exact top-k
+ *                           (the retrieval index, §4.1, Fig. 6, Fig. 8), for the
+ *                           true query and optionally a speculative one;
+ *   2. index_diff        -- compare the true index with the predicted one: the
+ *                           misses go to the urgent stream (§5.2, Fig. 10);
+ *   3. gather_coalesced  -- coalesce an ascending index list into runs of
+ *                           adjacent blocks and copy them host -> HBM into one
+ *                           half of a two-layer ping-pong buffer (§5.4, Fig. 11;
+ *                           "PulseInfer and the I/O Problem Behind Long-Context
+ *                           Decoding" §2: gather-scatter coalescing of
+ *                           fragmented transfers);
+ *   4. sparse_decode_attn -- GQA decode attention over the gathered blocks and
+ *                           over a GPU-resident recent window, the two parts
+ *                           fused by log-sum-exp ("Scaling Attention Beyond GPUs
+ *                           for LLM Inference", abstract); merge_lse exposes
+ *                           the fusion on its own.
+ * kvo_decode_step runs all four for every layer with the stream/event schedule
+ * of §5.3-§5.4 (prefetch for layer l+2 after layer l's attention).
+ *
+ * Conventions
+ *  - Every call returns kvo_status and never aborts, traps or exits.  Host-side
+ *    argument checks come first; on failure nothing is launched and
+ *    kvo_last_error() describes the problem.  Errors the GPU detects (an index
+ *    out of range in a caller-supplied list) are recorded in a device status
+ *    word read by kvo_device_status().
+ *  - All device work is enqueued on the caller's stream (a cudaStream_t passed
+ *    as void*) and is asynchronous.  NULL selects the context's own compute
+ *    stream (for gather_coalesced: its prefetch or urgent stream), which does
+ *    not synchronize with the legacy default stream; pass cudaStreamLegacy
+ *    ((void*)0x1) to order a call on the legacy default stream.
+ *  - bf16 = IEEE bfloat16 bit patterns (uint16).  Sizes are element counts.
+ *  - Notation: b batch, Hq / Hkv query / KV heads, r = Hq / Hkv, d head dim,
+ *    B block size (tokens), k top-k, W window, len_b context of request b,
+ *    C_b = (len_b - W) / B host-resident candidate blocks, G = b * Hkv groups.
+ *    KV head g serves query heads g*r .. g*r + r - 1.
+ *  - No CPU fallback exists: without a CUDA device the calls fail with
+ *    KVO_ERR_CUDA.
+ */
+#ifndef KVO_H
+#define KVO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVO_OK = 0,
+    KVO_ERR_INVALID = 1,   /* bad argument (null pointer, out-of-range size, bad config) */
+    KVO_ERR_CUDA = 2,      /* a CUDA runtime call failed (see kvo_last_error) */
+    KVO_ERR_OOM = 3,       /* device allocation failed */
+    KVO_ERR_TIMEOUT = 4,   /* a bounded device wait gave up */
+    KVO_ERR_STATE = 5,     /* call not valid in the context's current state */
+    KVO_ERR_DEVICE = 6     /* the device status word holds an error */
+} kvo_status;
+
+/* device status word bits (kvo_device_status) */
+#define KVO_DEV_BAD_BLOCK_ID 0x1   /* a block id >= C_b or < 0 in an index list */
+#define KVO_DEV_BAD_SLOT     0x2   /* a slot >= 2k or a run past the buffer */
+#define KVO_DEV_BAD_COUNT    0x4   /* a count outside [0, k] */
+#define KVO_DEV_UNSORTED     0x8   /* an index list that is not strictly ascending */
+
+typedef void* kvo_stream_t;        /* cudaStream_t */
+typedef struct kvo_ctx kvo_ctx;    /* opaque, owned by the library */
+
+typedef struct {
+    int32_t batch;        /* b >= 1 */
+    int32_t n_q_heads;    /* Hq, a multiple of Hkv, r = Hq / Hkv <= 16 */
+    int32_t n_kv_heads;   /* Hkv >= 1 */
+    int32_t head_dim;     /* d: 64 or 128 */
+    int32_t block_size;   /* B >= 1 tokens per landmark block */
+    int32_t top_k;        /* k >= 1, k <= C_b for every request */
+    int32_t window;       /* W >= 0 recent tokens kept on the GPU */
+    int32_t n_layers;     /* >= 1 */
+    const int32_t* seq_lens; /* host [b]; len_b >= W, (len_b - W) % B == 0 */
+} kvo_config;
+
+/*
+ * kv_offload_init -- build a context for one KV cache.
+ *   k_host[l], v_host[l]: page-locked host memory that the device can address
+ *       (cudaHostAlloc / torch pin_memory, or cudaHostRegister'ed), one per
+ *       layer, packed request after request as [b][Hkv][len_b][d] bf16
+ *       (request b starts at element (sum_{b'<b} len_b') * Hkv * d).  Caller-
+ *       owned; must stay valid and unchanged until kv_offload_destroy.
+ *   k_win[l], v_win[l]: device memory [b][Hkv][W][d] bf16 holding tokens
+ *       [len_b - W, len_b) of each request (the recent window).  Caller-owned.
+ *   On success *out owns: the K landmarks of every layer (fp32 block means,
+ *   or the bf16 key itself when B == 1; DualDecoder §4.1, Fig. 8), built here
+ *   synchronously from k_host; the two ping-pong halves of K and V
+ *   ([2][G][2k][B][d] bf16: slots [0,k) take prefetched blocks, [k,2k) misses);
+ *   scratch; and three streams: compute, prefetch (lowest priority) and
+ *   urgent (highest priority; DualDecoder Fig. 10).
+ *   Errors: KVO_ERR_INVALID (config or pointers), KVO_ERR_OOM, KVO_ERR_CUDA.
+ */
+kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* const* v_host,
+                           const void* const* k_win, const void* const* v_win, kvo_ctx** out);
+
+/* kv_offload_destroy -- synchronize and free everything the context owns. NULL is a no-op. */
+kvo_status kv_offload_destroy(kvo_ctx* ctx);
+
+/*
+ * select_topk -- retrieval index of one layer (DualDecoder §4.1, Fig. 6).
+ *   q, q_spec: device [b][Hq][d] bf16; q_spec may be NULL.
+ *   Score of block j of group (b, g): s_j = sum_{h in group g} q_h . L_j
+ *   (fp32).  idx_true[G][k] (device int32) receives the k highest-scoring
+ *   blocks in ascending id order, ties to the lower id.  When q_spec is given,
+ *   idx_pred[G][k] receives the same for q_spec from the same landmark pass
+ *   (the speculative look-ahead query of the dual-token scheme, §5.2).
+ */
+kvo_status select_topk(kvo_ctx* ctx, int layer, const void* q, const void* q_spec,
+                       int32_t* idx_true, int32_t* idx_pred, kvo_stream_t stream);
+
+/*
+ * index_diff -- predicted-vs-needed diff (DualDecoder §5.2, Fig. 10, Fig. 18).
+ *   idx_true[G][k], idx_pred[G][k]: device int32, ascending per group;
+ *   idx_pred NULL means nothing was predicted (every block is a miss).
+ *   Outputs (device int32): miss_idx[G][k] = idx_true minus idx_pred ascending
+ *   (first miss_cnt[g] entries valid), miss_cnt[G], slot_of_true[G][k]:
+ *   the ping-pong slot holding idx_true[g][i] -- its position in idx_pred if
+ *   predicted, else k + its rank among the misses.
+ */
+kvo_status index_diff(kvo_ctx* ctx, const int32_t* idx_true, const int32_t* idx_pred,
+                      int32_t* miss_idx, int32_t* miss_cnt, int32_t* slot_of_true,
+                      kvo_stream_t stream);
+
+/*
+ * gather_coalesced -- coalesced host -> HBM gather into a ping-pong half
+ *   (PulseInfer §2; DualDecoder §5.4, Fig. 11, Fig. 19).
+ *   idx[G][k]: device int32 ascending block ids; cnt[G] valid entries per group
+ *   (NULL: k each).  Each maximal run of adjacent ids becomes one copy of
+ *   n_blocks * B * d bf16 of K and of V from layer `layer`'s host cache into
+ *   buffer half `buf` (0|1), slots slot_base + i.. (slot_base 0 for the
+ *   prefetched prediction, k for urgent misses).  runs_out (device int32
+ *   [G][k][4] = {first block, n blocks, first slot, 0}) and n_runs_out
+ *   (device int32 [G]) are optional.  `urgent` is informational for stream
+ *   choice when stream is NULL: 1 = the urgent stream, 0 = the prefetch
+ *   stream; the caller orders other work after it with events.
+ */
+kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx,
+                            const int32_t* cnt, int slot_base, int urgent, int32_t* runs_out,
+                            int32_t* n_runs_out, kvo_stream_t stream);
+
+/*
+ * sparse_decode_attn -- GQA decode attention of one layer.
+ *   q: device [b][Hq][d] bf16.  slot_of_true: device [G][k] int32 (from
+ *   index_diff).  Keys/values: the B tokens of every slot named in
+ *   slot_of_true of buffer half `buf`, plus the W window tokens of layer
+ *   `layer`.  Softmax scale 1/sqrt(d), natural-log lse, fp32 accumulate.
+ *   fuse_window_merge = 1: o[b][Hq][d], lse[b][Hq] (fp32, device) hold the
+ *   window and sparse parts fused by log-sum-exp.  fuse_window_merge = 0:
+ *   o[2][b][Hq][d], lse[2][b][Hq]: part 0 sparse, part 1 window (an empty
+ *   part has lse = -inf, o = 0).
+ */
+kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q,
+                              const int32_t* slot_of_true, float* o, float* lse,
+                              int fuse_window_merge, kvo_stream_t stream);
+
+/*
+ * merge_lse -- fuse two attention parts over disjoint key sets
+ *   ("Scaling Attention Beyond GPUs for LLM Inference", abstract):
+ *   M = max(lse1, lse2), w_i = exp(lse_i - M), o = (w1 o1 + w2 o2) / (w1 + w2),
+ *   lse = M + ln(w1 + w2); two empty parts (-inf) give o = 0, lse = -inf.
+ *   All pointers device fp32: o*[rows][d], lse*[rows].  o may alias o1 or o2;
+ *   lse must not alias lse1 or lse2.
+ *   No context needed.
+ */
+kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2,
+                     float* o, float* lse, int rows, int d, kvo_stream_t stream);
+
+/*
+ * kvo_decode_step -- one whole decode step over every layer, pipelined.
+ *   q, q_spec: device [n_layers][b][Hq][d] bf16 (q_spec may be NULL: the
+ *   prediction for the next step is then the true index of this step).
+ *   o: device [n_layers][b][Hq][d] fp32, lse: [n_layers][b][Hq] fp32.
+ *   Per layer l: select (true + speculative) -> diff against the prediction
+ *   kept from the previous step -> urgent gather of the misses -> attention;
+ *   the prefetch of layer l+2's prediction is issued on the prefetch stream
+ *   once layer l's attention has released its ping-pong half.  The first
+ *   step after init has no prediction, so every block is a miss.  All work is
+ *   ordered after `stream` and `stream` waits for all of it on return.
+ */
+kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o,
+                           float* lse, kvo_stream_t stream);
+
+/* Forget the predictions kept for the next step (next step starts cold). */
+kvo_status kvo_reset_prediction(kvo_ctx* ctx);
+
+/* kvo_get_stream -- which 0: compute, 1: prefetch, 2: urgent. */
+kvo_status kvo_get_stream(kvo_ctx* ctx, int which, kvo_stream_t* out);
+
+/*
+ * kvo_device_status -- synchronize the context's streams and `stream`, return
+ * and clear the device status word (KVO_DEV_* bits) in *code_out.
+ * Returns KVO_ERR_DEVICE when it was nonzero.
+ */
+kvo_status kvo_device_status(kvo_ctx* ctx, int32_t* code_out, kvo_stream_t stream);
+
+/*
+ * Inspection, for tests and tools.
+ *   kvo_landmarks: copy layer `layer`'s landmarks, in logical layout
+ *   [G][C_max][d], to device memory `dst` (fp32 when B > 1; bf16 when B == 1),
+ *   C_max = max_b C_b; rows past C_b are zero.
+ *   kvo_buffer: device pointers of ping-pong half `buf`, K and V, each
+ *   [G][2k][B][d] bf16 (valid until destroy).
+ *   kvo_info: sizes the context derived: [0] C_max, [1] landmark bytes per
+ *   layer, [2] ping-pong bytes (both halves, K+V), [3] scratch bytes.
+ */
+kvo_status kvo_landmarks(kvo_ctx* ctx, int layer, void* dst, kvo_stream_t stream);
+kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
+kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);
+
+/*
+ * Per-launch timing of kvo_decode_step, for benchmarks.  kvo_profile(ctx, 1)
+ * clears and starts recording a timing event before and after every kernel
+ * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.
+ * kvo_profile_read synchronizes, then writes per kernel kind the summed
+ * launch durations (ms) and launch counts, and clears the record.  Kinds:
+ * 0 select, 1 index diff, 2 run coalescing, 3 prefetch gather, 4 urgent
+ * gather, 5 attention (n_kinds >= 6).
+ */
+kvo_status kvo_profile(kvo_ctx* ctx, int enable);
+kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out, int n_kinds);
+
+/* Human-readable description of the last error of ctx (or of the last
+ * context-free call when ctx is NULL).  Never NULL. */
+const char* kvo_last_error(const kvo_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVO_H */

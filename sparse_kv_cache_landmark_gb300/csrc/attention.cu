@@ -1,0 +1,361 @@
+// GQA decode attention over the gathered sparse blocks plus the GPU-resident
+// recent window, the two parts fused by log-sum-exp ("Scaling Attention Beyond
+// GPUs for LLM Inference", abstract; DualDecoder core claim: attention over the
+// miss-corrected buffer equals attention over the true sparse selection).
+//
+// Decode attention at r = Hq / Hkv <= 16 query rows is bound by the HBM read
+// of K and V (about 4 flop per byte).  The kernel keeps the instruction count
+// per token low with mma.sync m16n8k16 bf16 (the r query rows of a KV group
+// fill the M = 16 rows; rows past r are zero) and loads K and V straight from
+// global memory into fragment registers with 16-byte loads:
+//  * S = Q K^T: the contraction over channels may use any channel order, as
+//    long as Q and K use the same one.  Lane (g, t) loads 16 contiguous bytes
+//    of key row g (channels 32s + 8t .. +8) and uses them as the B fragments
+//    of k-steps 2s and 2s+1; the Q fragments are loaded with the same map.
+//  * O += P V: lane (g, t) needs, for output column g of each n-tile, the
+//    values of tokens 2t, 2t+1, 2t+8, 2t+9.  Output column g of n-tile j is
+//    channel (d/8) g + j, so the lane loads d/8 contiguous channels of those 4
+//    token rows and pairs tokens with byte permutes.
+// Work: a CTA takes up to ATT_TILES_PER_ITEM tiles of 16 tokens of one
+// (request, KV head) group and one part (0 sparse, 1 window); its 4 warps keep
+// online-softmax state over interleaved tiles, merge in shared memory and
+// write one unnormalised partial (m, l, acc).  The last CTA of the group
+// (atomic ticket) merges the partials of each part and fuses the two parts.
+#include <math.h>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2f(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1, float c0, float c1,
+                                               float c2, float c3) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};\n"
+        : "=f"(d0), "=f"(d1), "=f"(d2), "=f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// D: head dim (64|128).  NR: 1 -> query rows 0..7 (r <= 8), 2 -> rows 0..15.
+template <int D, int NR>
+__global__ void __launch_bounds__(ATT_WARPS * 32)
+attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
+            const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot,
+            const int4* __restrict__ items, const int32_t* __restrict__ att_first, const int32_t* __restrict__ att_count,
+            float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* __restrict__ done,
+            float* __restrict__ out_o, float* __restrict__ out_lse, int fuse, int batch, int r, int Hkv, int k,
+            int B, int W, float scale_log2, int32_t* __restrict__ status) {
+    constexpr int KS = D / 16;          // k-steps of the QK^T contraction
+    constexpr int CH = D / 32;          // 16-byte chunks per lane per key row
+    constexpr int NT = D / 8;           // n-tiles of the PV product
+    constexpr int CPT = D / 8;          // channels per lane in PV (== NT)
+
+    __shared__ float sm_m[ATT_WARPS][16];
+    __shared__ float sm_l[ATT_WARPS][16];
+    __shared__ __align__(16) float sm_o[ATT_WARPS][16][D];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int4 it = items[blockIdx.x];
+    const int bg = it.x, part = it.y, tile0 = it.z, ntiles = it.w;
+    const int b = bg / Hkv, gk = bg % Hkv;
+    const int Hq = Hkv * r;
+    const int n_tok = part == 0 ? k * B : W;
+
+    // ---- Q fragments (channel map shared with the K fragments)
+    uint32_t qa0[KS], qa1[KS], qa2[KS], qa3[KS];
+    {
+        const uint16_t* q0 = q + ((int64_t)b * Hq + gk * r + gq) * D;
+        const uint16_t* q1 = q + ((int64_t)b * Hq + gk * r + gq + 8) * D;
+        const bool v0 = gq < r, v1 = NR == 2 && gq + 8 < r;
+#pragma unroll
+        for (int s = 0; s < CH; ++s) {
+            const uint4 w0 = v0 ? ldg16(q0 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 w1 = v1 ? ldg16(q1 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
+            qa0[2 * s] = w0.x; qa2[2 * s] = w0.y; qa0[2 * s + 1] = w0.z; qa2[2 * s + 1] = w0.w;
+            qa1[2 * s] = w1.x; qa3[2 * s] = w1.y; qa1[2 * s + 1] = w1.z; qa3[2 * s + 1] = w1.w;
+        }
+    }
+
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int bad = 0;
+
+    auto row_ptr = [&](const uint16_t* base_buf, const uint16_t* base_win, int tok) -> const uint16_t* {
+        if (part == 0) {
+            const int blk = tok / B;
+            int s = slot[(int64_t)bg * k + blk];
+            if (s < 0 || s >= 2 * k) { bad |= KVO_DEV_BAD_SLOT; s = 0; }
+            return base_buf + (((int64_t)bg * 2 * k + s) * B + (tok - blk * B)) * D;
+        }
+        return base_win + ((int64_t)bg * W + tok) * D;
+    };
+
+    for (int tl = warp; tl < ntiles; tl += ATT_WARPS) {
+        const int tb = (tile0 + tl) * ATT_TILE;
+        // ---- K rows g and 8+g of the tile
+        uint4 kf[2][CH];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tok = min(tb + 8 * nt + gq, n_tok - 1);
+            const uint16_t* kp = row_ptr(bk, wk, tok) + 8 * tq;
+#pragma unroll
+            for (int s = 0; s < CH; ++s) kf[nt][s] = ldg16(kp + 32 * s);
+        }
+        // ---- V rows 2t, 2t+1, 2t+8, 2t+9 (channels CPT*g ..)
+        uint4 vf[4][CPT / 8];
+#pragma unroll
+        for (int vi = 0; vi < 4; ++vi) {
+            const int tok = min(tb + 2 * tq + (vi & 1) + 8 * (vi >> 1), n_tok - 1);
+            const uint16_t* vp = row_ptr(bv, wv, tok) + CPT * gq;
+#pragma unroll
+            for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = ldg16(vp + 8 * c);
+        }
+        // ---- S = Q K^T for the 16 tokens (two n8 tiles)
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const uint4 w = kf[nt][ks >> 1];
+                const uint32_t b0 = (ks & 1) ? w.z : w.x;
+                const uint32_t b1 = (ks & 1) ? w.w : w.y;
+                mma_bf16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa0[ks], qa1[ks], qa2[ks], qa3[ks], b0, b1,
+                               s[nt][0], s[nt][1], s[nt][2], s[nt][3]);
+            }
+        }
+        // ---- online softmax (log2 domain); lane holds tokens 2t, 2t+1 of each n8 tile
+        float x[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int t0 = tb + 8 * nt + 2 * tq;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool ok = t0 + (e & 1) < n_tok;
+                x[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
+            }
+        }
+        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        const float mn0 = fmaxf(m0, mx0);
+        const float al0 = ex2f(m0 - mn0);
+        m0 = mn0;
+        float p[2][4];
+        p[0][0] = ex2f(x[0][0] - mn0); p[0][1] = ex2f(x[0][1] - mn0);
+        p[1][0] = ex2f(x[1][0] - mn0); p[1][1] = ex2f(x[1][1] - mn0);
+        l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        float al1 = 1.f;
+        if (NR == 2) {
+            float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn1 = fmaxf(m1, mx1);
+            al1 = ex2f(m1 - mn1);
+            m1 = mn1;
+            p[0][2] = ex2f(x[0][2] - mn1); p[0][3] = ex2f(x[0][3] - mn1);
+            p[1][2] = ex2f(x[1][2] - mn1); p[1][3] = ex2f(x[1][3] - mn1);
+            l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        } else {
+            p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
+        }
+        const uint32_t pa0 = pack_bf16(p[0][0], p[0][1]);
+        const uint32_t pa1 = pack_bf16(p[0][2], p[0][3]);
+        const uint32_t pa2 = pack_bf16(p[1][0], p[1][1]);
+        const uint32_t pa3 = pack_bf16(p[1][2], p[1][3]);
+        // ---- O = O * alpha + P V
+#pragma unroll
+        for (int c = 0; c < CPT / 8; ++c) {
+            const uint32_t va[4] = {vf[0][c].x, vf[0][c].y, vf[0][c].z, vf[0][c].w};
+            const uint32_t vb[4] = {vf[1][c].x, vf[1][c].y, vf[1][c].z, vf[1][c].w};
+            const uint32_t vc[4] = {vf[2][c].x, vf[2][c].y, vf[2][c].z, vf[2][c].w};
+            const uint32_t vd[4] = {vf[3][c].x, vf[3][c].y, vf[3][c].z, vf[3][c].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                    const int j = 8 * c + 2 * w + hi;   // n-tile == channel offset within the lane's CPT
+                    const uint32_t sel = hi ? 0x7632u : 0x5410u;
+                    const uint32_t b0 = __byte_perm(va[w], vb[w], sel);
+                    const uint32_t b1 = __byte_perm(vc[w], vd[w], sel);
+                    mma_bf16_16816(acc[j][0], acc[j][1], acc[j][2], acc[j][3], pa0, pa1, pa2, pa3, b0, b1,
+                                   acc[j][0] * al0, acc[j][1] * al0, acc[j][2] * al1, acc[j][3] * al1);
+                }
+            }
+        }
+    }
+    if (bad && lane == 0) atomicOr(status, bad);
+
+    // ---- per-warp row sums (quad reduce), then CTA merge in shared memory
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+        sm_m[warp][gq] = m0; sm_l[warp][gq] = l0;
+        sm_m[warp][gq + 8] = NR == 2 ? m1 : -INFINITY; sm_l[warp][gq + 8] = NR == 2 ? l1 : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        // column 2t of n-tile j is channel CPT*2t + j; column 2t+1 is CPT*(2t+1) + j
+        sm_o[warp][gq][CPT * (2 * tq) + j] = acc[j][0];
+        sm_o[warp][gq][CPT * (2 * tq + 1) + j] = acc[j][1];
+        if (NR == 2) {
+            sm_o[warp][gq + 8][CPT * (2 * tq) + j] = acc[j][2];
+            sm_o[warp][gq + 8][CPT * (2 * tq + 1) + j] = acc[j][3];
+        }
+    }
+    __syncthreads();
+    const int64_t item = blockIdx.x;
+    for (int e = tid; e < r * D; e += blockDim.x) {
+        const int row = e / D, c = e - row * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w) M = fmaxf(M, sm_m[w][row]);
+        float a = 0.f, l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < ATT_WARPS; ++w) {
+                const float sc = ex2f(sm_m[w][row] - M);
+                a += sc * sm_o[w][row][c];
+                l += sc * sm_l[w][row];
+            }
+        }
+        part_o[(item * r + row) * D + c] = a;
+        if (c == 0) {
+            part_ml[(item * r + row) * 2 + 0] = M;
+            part_ml[(item * r + row) * 2 + 1] = l;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t prev = atomicAdd(&done[bg], 1u);
+        s_last = prev + 1 == (uint32_t)att_count[bg];
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA of the group: merge each part, then fuse the two parts
+    const int first = att_first[bg], cnt = att_count[bg];
+    const int64_t rows_total = (int64_t)batch * Hq;
+    for (int e = tid; e < r * D; e += blockDim.x) {
+        const int row = e / D, c = e - row * D;
+        float Mp[2] = {-INFINITY, -INFINITY};
+        for (int i = first; i < first + cnt; ++i) {
+            const int pp = items[i].y;
+            Mp[pp] = fmaxf(Mp[pp], __ldcg(part_ml + ((int64_t)i * r + row) * 2));
+        }
+        float Lp[2] = {0.f, 0.f}, Ap[2] = {0.f, 0.f};
+        for (int i = first; i < first + cnt; ++i) {
+            const int pp = items[i].y;
+            const float mi = __ldcg(part_ml + ((int64_t)i * r + row) * 2);
+            if (mi == -INFINITY) continue;
+            const float sc = ex2f(mi - Mp[pp]);
+            Lp[pp] += sc * __ldcg(part_ml + ((int64_t)i * r + row) * 2 + 1);
+            Ap[pp] += sc * __ldcg(part_o + ((int64_t)i * r + row) * D + c);
+        }
+        const int64_t orow = (int64_t)b * Hq + gk * r + row;
+        if (fuse) {
+            const float M = fmaxf(Mp[0], Mp[1]);
+            float o = 0.f, lse = -INFINITY;
+            if (M != -INFINITY) {
+                const float w0 = Mp[0] == -INFINITY ? 0.f : ex2f(Mp[0] - M);
+                const float w1 = Mp[1] == -INFINITY ? 0.f : ex2f(Mp[1] - M);
+                const float L = w0 * Lp[0] + w1 * Lp[1];
+                o = (w0 * Ap[0] + w1 * Ap[1]) / L;
+                lse = (M + lg2f(L)) * kLn2;
+            }
+            out_o[orow * D + c] = o;
+            if (c == 0) out_lse[orow] = lse;
+        } else {
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                float o = 0.f, lse = -INFINITY;
+                if (Mp[pp] != -INFINITY && Lp[pp] > 0.f) {
+                    o = Ap[pp] / Lp[pp];
+                    lse = (Mp[pp] + lg2f(Lp[pp])) * kLn2;
+                }
+                out_o[(pp * rows_total + orow) * D + c] = o;
+                if (c == 0) out_lse[pp * rows_total + orow] = lse;
+            }
+        }
+    }
+    if (tid == 0) done[bg] = 0u;
+}
+
+cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const int32_t* slot, float* o,
+                             float* lse, int fuse, cudaStream_t s) {
+    const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
+    const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
+    const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
+#define KVO_ATT(D_, NR_)                                                                                         \
+    attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
+        (const uint16_t*)q, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items, c.att_first, c.att_count,       \
+        c.att_part_o, c.att_part_ml, c.att_done, o, lse, fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, scale_log2,   \
+        c.status)
+    if (c.d == 128) {
+        if (c.r <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);
+    } else {
+        if (c.r <= 8) KVO_ATT(64, 1); else KVO_ATT(64, 2);
+    }
+#undef KVO_ATT
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- merge_lse
+__global__ void merge_lse_kernel(const float* __restrict__ o1, const float* __restrict__ lse1,
+                                 const float* __restrict__ o2, const float* __restrict__ lse2, float* o, float* lse,
+                                 int rows, int d) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= (int64_t)rows * d) return;
+    const int64_t row = i / d;
+    const float a = lse1[row], bb = lse2[row];
+    const float M = fmaxf(a, bb);
+    float out = 0.f, L = -INFINITY;
+    if (M != -INFINITY) {
+        const float l2e = 1.4426950408889634f;
+        const float w1 = a == -INFINITY ? 0.f : ex2f((a - M) * l2e);
+        const float w2 = bb == -INFINITY ? 0.f : ex2f((bb - M) * l2e);
+        out = (w1 * o1[i] + w2 * o2[i]) / (w1 + w2);
+        L = M + lg2f(w1 + w2) * kLn2;
+    }
+    o[i] = out;
+    if (i % d == 0) lse[row] = L;
+}
+
+cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
+                             float* lse, int rows, int d, cudaStream_t s) {
+    const int64_t n = (int64_t)rows * d;
+    if (n == 0) return cudaSuccess;
+    merge_lse_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(o1, lse1, o2, lse2, o, lse, rows, d);
+    return cudaGetLastError();
+}
+
+}  // namespace kvo

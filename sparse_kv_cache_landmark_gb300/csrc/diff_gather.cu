@@ -1,0 +1,187 @@
+// Predicted-vs-needed diff, run coalescing and the host -> HBM gather.
+//
+// "DualDecoder: Accelerate Long Context LLM Inference by Predictive Prefetch",
+// §5.2 / Fig. 10 / Fig. 18: entries of the true retrieval index that the
+// prediction missed are fetched on an urgent stream before attention;
+// §5.4 / Fig. 11: a two-layer ping-pong sparse KV buffer; Fig. 19: contiguous
+// block prefetch over the host link.  "PulseInfer and the I/O Problem Behind
+// Long-Context Decoding", §2: a gather-scatter engine that coalesces
+// fragmented transfers.
+//
+// Ping-pong half layout (HBM): [G][2k][B][d] bf16 for K and for V; slots
+// [0, k) hold the prefetched prediction in list order, slots [k, 2k) the
+// urgent misses in list order.  A run of n adjacent block ids is one
+// contiguous range of n*B*d bf16 on both the host and the device side.
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+// ------------------------------------------------------------------- diff
+__global__ void __launch_bounds__(256)
+index_diff_kernel(const int32_t* __restrict__ T, const int32_t* __restrict__ P, int32_t* __restrict__ M,
+                  int32_t* __restrict__ M_cnt, int32_t* __restrict__ slot, const int32_t* __restrict__ g_C, int k,
+                  int32_t* __restrict__ status) {
+    extern __shared__ int32_t p_s[];           // prediction of the group, k entries
+    __shared__ uint32_t warp_sums[32];
+    const int bg = blockIdx.x, tid = threadIdx.x;
+    const int C = g_C[bg];
+    const int32_t* Tg = T + (int64_t)bg * k;
+    int bad = 0;
+    if (P) {
+        const int32_t* Pg = P + (int64_t)bg * k;
+        for (int i = tid; i < k; i += blockDim.x) {
+            const int32_t x = Pg[i];
+            p_s[i] = x;
+            if (x < 0 || x >= C) bad |= KVO_DEV_BAD_BLOCK_ID;
+            if (i > 0 && Pg[i - 1] >= x) bad |= KVO_DEV_UNSORTED;
+        }
+    }
+    __syncthreads();
+    uint32_t n_miss = 0;
+    for (int base = 0; base < k; base += blockDim.x) {
+        const int i = base + tid;
+        const bool valid = i < k;
+        const int32_t t = valid ? Tg[i] : 0;
+        if (valid && (t < 0 || t >= C)) bad |= KVO_DEV_BAD_BLOCK_ID;
+        if (valid && i > 0 && Tg[i - 1] >= t) bad |= KVO_DEV_UNSORTED;
+        int pos = -1;
+        if (valid && P) {
+            int lo = 0, hi = k - 1;
+            while (lo <= hi) {
+                const int mid = (lo + hi) >> 1;
+                const int32_t v = p_s[mid];
+                if (v == t) { pos = mid; break; }
+                if (v < t) lo = mid + 1; else hi = mid - 1;
+            }
+        }
+        const bool miss = valid && pos < 0;
+        uint32_t total;
+        const uint32_t excl = block_exclusive_scan(miss ? 1u : 0u, warp_sums, &total);
+        if (miss) {
+            M[(int64_t)bg * k + n_miss + excl] = t;
+            slot[(int64_t)bg * k + i] = k + (int32_t)(n_miss + excl);
+        } else if (valid) {
+            slot[(int64_t)bg * k + i] = pos;
+        }
+        n_miss += total;
+    }
+    if (tid == 0) M_cnt[bg] = (int32_t)n_miss;
+    if (bad) atomicOr(status, bad);
+}
+
+cudaError_t launch_index_diff(const Ctx& c, const int32_t* idx_true, const int32_t* idx_pred, int32_t* miss,
+                              int32_t* miss_cnt, int32_t* slot, cudaStream_t s) {
+    const size_t smem = idx_pred ? (size_t)c.k * sizeof(int32_t) : 0;
+    index_diff_kernel<<<c.G, 256, smem, s>>>(idx_true, idx_pred, miss, miss_cnt, slot, c.g_C, c.k, c.status);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- coalesce
+// runs[G][k] int4 = {first block, n blocks, first slot, 0}; nruns[G].
+__global__ void __launch_bounds__(256)
+coalesce_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int slot_base,
+                int4* __restrict__ runs, int32_t* __restrict__ nruns, const int32_t* __restrict__ g_C, int k,
+                int32_t* __restrict__ status) {
+    __shared__ uint32_t warp_sums[32];
+    const int bg = blockIdx.x, tid = threadIdx.x;
+    const int C = g_C[bg];
+    int n = cnt ? cnt[bg] : k;
+    int bad = 0;
+    if (n < 0 || n > k) { bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
+    const int32_t* S = idx + (int64_t)bg * k;
+    int4* R = runs + (int64_t)bg * k;
+    uint32_t n_start = 0, n_end = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + tid;
+        const bool valid = i < n;
+        const int32_t x = valid ? S[i] : 0;
+        if (valid && (x < 0 || x >= C)) bad |= KVO_DEV_BAD_BLOCK_ID;
+        const bool start = valid && (i == 0 || S[i - 1] + 1 != x);
+        const bool end = valid && (i == n - 1 || S[i + 1] != x + 1);
+        uint32_t ts, te;
+        const uint32_t es = block_exclusive_scan(start ? 1u : 0u, warp_sums, &ts);
+        const uint32_t ee = block_exclusive_scan(end ? 1u : 0u, warp_sums, &te);
+        if (start) { R[n_start + es].x = x; R[n_start + es].y = i; R[n_start + es].z = slot_base + i; }
+        if (end) R[n_end + ee].w = i;
+        n_start += ts;
+        n_end += te;
+    }
+    __syncthreads();
+    for (int j = tid; j < (int)n_start; j += blockDim.x) {
+        int4 v = R[j];
+        v.y = v.w - v.y + 1;
+        v.w = 0;
+        R[j] = v;
+    }
+    if (tid == 0) nruns[bg] = (int32_t)n_start;
+    if (bad) atomicOr(status, bad);
+}
+
+cudaError_t launch_coalesce(const Ctx& c, const int32_t* idx, const int32_t* cnt, int slot_base, int32_t* runs,
+                            int32_t* nruns, cudaStream_t s) {
+    coalesce_kernel<<<c.G, 256, 0, s>>>(idx, cnt, slot_base, (int4*)runs, nruns, c.g_C, c.k, c.status);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ gather
+// One warp per run (grid-stride over the G*k run slots).  The host cache is
+// read in place through its device mapping with 16-byte loads, UNROLL loads
+// of K and of V in flight per lane, and written to the ping-pong half with
+// coalesced 16-byte stores.
+template <int UNROLL>
+__global__ void __launch_bounds__(GATHER_THREADS)
+gather_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh, const int64_t* __restrict__ g_off,
+              const int32_t* __restrict__ g_C, const int4* __restrict__ runs, const int32_t* __restrict__ nruns,
+              uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int G, int k, int B, int D,
+              int32_t* __restrict__ status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t total = (int64_t)G * k;
+    const int64_t blk_elems = (int64_t)B * D;
+    for (int64_t e = warp; e < total; e += n_warps) {
+        const int bg = (int)(e / k);
+        const int ri = (int)(e - (int64_t)bg * k);
+        if (ri >= nruns[bg]) continue;
+        const int4 run = runs[e];
+        if (run.x < 0 || run.y < 1 || run.x + run.y > g_C[bg] || run.z < 0 || run.z + run.y > 2 * k) {
+            if (lane == 0) atomicOr(status, KVO_DEV_BAD_SLOT);
+            continue;
+        }
+        const int64_t src = g_off[bg] + (int64_t)run.x * blk_elems;
+        const int64_t dst = ((int64_t)bg * 2 * k + run.z) * blk_elems;
+        const int64_t n16 = (int64_t)run.y * blk_elems / 8;
+        const uint4* sk = reinterpret_cast<const uint4*>(kh + src);
+        const uint4* sv = reinterpret_cast<const uint4*>(vh + src);
+        uint4* tk = reinterpret_cast<uint4*>(dk + dst);
+        uint4* tv = reinterpret_cast<uint4*>(dv + dst);
+        for (int64_t i0 = lane; i0 < n16; i0 += 32 * UNROLL) {
+            uint4 a[UNROLL], b[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t i = i0 + 32 * u;
+                if (i < n16) { a[u] = sk[i]; b[u] = sv[i]; }
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int64_t i = i0 + 32 * u;
+                if (i < n16) { tk[i] = a[u]; tv[i] = b[u]; }
+            }
+        }
+    }
+}
+
+int gather_default_ctas(const Ctx& c) {
+    (void)c;
+    return 2 * 152;
+}
+
+cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns, int n_ctas,
+                          cudaStream_t s) {
+    gather_kernel<4><<<n_ctas, GATHER_THREADS, 0, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C,
+                                                        (const int4*)runs, nruns, c.pp_k[buf], c.pp_v[buf], c.G, c.k,
+                                                        c.B, c.d, c.status);
+    return cudaGetLastError();
+}
+
+}  // namespace kvo

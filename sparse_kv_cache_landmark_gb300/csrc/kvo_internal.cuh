@@ -1,0 +1,142 @@
+// Internal declarations shared by the CUDA translation units of libkvo.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "kvo.h"
+
+namespace kvo {
+
+// ---------------------------------------------------------------- tunables
+constexpr int SEL_THREADS = 256;          // select: threads per CTA
+constexpr int SEL_RPT = 4;                // select: landmark rows per thread
+constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;   // rows per work item
+constexpr int ATT_WARPS = 4;              // attention: warps per CTA
+constexpr int ATT_TILE = 16;              // attention: tokens per mma tile
+constexpr int ATT_TILES_PER_ITEM = 16;    // attention: tiles per CTA work item
+constexpr int GATHER_THREADS = 256;
+
+// ------------------------------------------------------------------ context
+struct Ctx {
+    kvo_config cfg{};
+    std::vector<int32_t> lens;
+    int G = 0, r = 0, d = 0, B = 0, k = 0, W = 0, L = 0, Hkv = 0, Hq = 0, batch = 0;
+    int Cmax = 0;
+    // per group (device): element offset of the group's rows in the packed host
+    // arrays, candidate blocks C_b, context length len_b
+    int64_t* g_off = nullptr;
+    int32_t* g_C = nullptr;
+    std::vector<const uint16_t*> k_host, v_host;   // device-addressable host pointers
+    std::vector<const uint16_t*> k_win, v_win;
+    std::vector<void*> lm;                          // landmarks per layer
+    size_t lm_bytes = 0;
+    uint16_t* pp_k[2] = {nullptr, nullptr};
+    uint16_t* pp_v[2] = {nullptr, nullptr};
+    size_t pp_bytes = 0;
+    // select scratch
+    uint32_t* sel_keys = nullptr;   // [2][G][Cmax]
+    uint32_t* sel_hist = nullptr;   // [2][G][256]
+    uint32_t* sel_done = nullptr;   // [G]
+    int2* sel_items = nullptr;      // {group, chunk}
+    int32_t* sel_nchunks = nullptr; // [G]
+    int n_sel_items = 0;
+    // coalesce scratch: [2 (prefetch|urgent)][G][k][4], [2][G]
+    int32_t* runs = nullptr;
+    int32_t* nruns = nullptr;
+    // attention scratch
+    int4* att_items = nullptr;      // {group, part, first tile, n tiles}
+    int32_t* att_first = nullptr;   // [G] first item of the group
+    int32_t* att_count = nullptr;   // [G] items of the group
+    int n_att_items = 0;
+    float* att_part_o = nullptr;    // [items][r][d]
+    float* att_part_ml = nullptr;   // [items][r][2]
+    uint32_t* att_done = nullptr;   // [G]
+    int32_t* status = nullptr;      // device status word
+    size_t scratch_bytes = 0;
+    cudaStream_t s_compute = nullptr, s_prefetch = nullptr, s_urgent = nullptr;
+    // decode-step state
+    int32_t* st_true = nullptr;     // [L][G][k]
+    int32_t* st_pred = nullptr;     // [2][L][G][k]  predictions by step parity
+    int32_t* st_miss = nullptr;     // [L][G][k]
+    int32_t* st_miss_cnt = nullptr; // [L][G]
+    int32_t* st_slot = nullptr;     // [L][G][k]
+    int step_parity = 0;
+    bool have_pred = false;
+    std::vector<cudaEvent_t> ev_sel, ev_attn, ev_pref, ev_urg;
+    cudaEvent_t ev_start = nullptr;
+    // optional per-launch timing of the decode step (kvo_profile)
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_pool;
+    struct ProfRec { int kind; int ev; };
+    std::vector<ProfRec> prof_recs;
+    int prof_used = 0;
+    std::string err;
+};
+
+// kernel kinds reported by kvo_profile_read
+enum ProfKind { PK_SELECT = 0, PK_DIFF = 1, PK_COALESCE = 2, PK_GATHER_PREFETCH = 3, PK_GATHER_URGENT = 4,
+                PK_ATTENTION = 5, PK_COUNT = 6 };
+
+// --------------------------------------------------------- device helpers
+__device__ __forceinline__ uint32_t float_to_ordered(float f) {
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Block-wide exclusive scan of one uint32 per thread (blockDim.x multiple of 32, <= 1024).
+// `warp_sums` needs blockDim.x / 32 entries of shared memory.  Returns the
+// exclusive prefix; *total receives the block total.  Contains __syncthreads().
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        uint32_t s = lane < nw ? warp_sums[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < nw) warp_sums[lane] = s;   // inclusive warp prefix
+    }
+    __syncthreads();
+    uint32_t base = wid ? warp_sums[wid - 1] : 0u;
+    *total = warp_sums[nw - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaGetLastError() after the launch.
+cudaError_t launch_landmarks(const Ctx& c, int layer, cudaStream_t s);
+cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
+                          int32_t* idx_pred, cudaStream_t s);
+cudaError_t launch_index_diff(const Ctx& c, const int32_t* idx_true, const int32_t* idx_pred, int32_t* miss,
+                              int32_t* miss_cnt, int32_t* slot, cudaStream_t s);
+cudaError_t launch_coalesce(const Ctx& c, const int32_t* idx, const int32_t* cnt, int slot_base, int32_t* runs,
+                            int32_t* nruns, cudaStream_t s);
+cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
+                          int n_ctas, cudaStream_t s);
+cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const int32_t* slot, float* o,
+                             float* lse, int fuse, cudaStream_t s);
+cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
+                             float* lse, int rows, int d, cudaStream_t s);
+cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s);
+
+int gather_default_ctas(const Ctx& c);
+
+}  // namespace kvo

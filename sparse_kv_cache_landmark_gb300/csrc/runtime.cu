@@ -1,0 +1,537 @@
+// C ABI entry points, context set-up and the pipelined decode step.
+//
+// The decode step follows "DualDecoder: Accelerate Long Context LLM Inference
+// by Predictive Prefetch": the prediction for the next step comes from the
+// speculative query through the same landmarks (§4.1, §5.2); prefetches run on
+// a low-priority stream and misses on a high-priority urgent stream (Fig. 10);
+// two ping-pong halves hold the sparse KV of consecutive layers, reuse ordered
+// by CUDA events (§5.4, Fig. 11); the prefetch for global layer n + 2 is issued
+// once layer n's attention has released its half (§5.3).
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "kvo_internal.cuh"
+
+struct kvo_ctx {
+    kvo::Ctx c;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+kvo_status fail(kvo::Ctx* c, kvo_status st, const std::string& msg) {
+    if (c) c->err = msg; else g_err = msg;
+    return st;
+}
+
+kvo_status cuda_fail(kvo::Ctx* c, cudaError_t e, const char* what) {
+    std::string m = std::string(what) + ": " + cudaGetErrorString(e);
+    if (c) c->err = m; else g_err = m;
+    return e == cudaErrorMemoryAllocation ? KVO_ERR_OOM : KVO_ERR_CUDA;
+}
+
+#define KVO_CUDA(c, expr)                                                   \
+    do {                                                                    \
+        cudaError_t e_ = (expr);                                            \
+        if (e_ != cudaSuccess) return cuda_fail((c), e_, #expr);            \
+    } while (0)
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t bytes, size_t* acc) {
+    *p = nullptr;
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc((void**)p, bytes);
+    if (e == cudaSuccess && acc) *acc += bytes;
+    return e;
+}
+
+void free_ctx(kvo::Ctx& c) {
+    auto F = [](void* p) { if (p) cudaFree(p); };
+    F(c.g_off); F(c.g_C);
+    for (void* p : c.lm) F(p);
+    for (int i = 0; i < 2; ++i) { F(c.pp_k[i]); F(c.pp_v[i]); }
+    F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
+    F(c.runs); F(c.nruns);
+    F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
+    F(c.status);
+    F(c.st_true); F(c.st_pred); F(c.st_miss); F(c.st_miss_cnt); F(c.st_slot);
+    for (auto* v : {&c.ev_sel, &c.ev_attn, &c.ev_pref, &c.ev_urg})
+        for (cudaEvent_t e : *v) if (e) cudaEventDestroy(e);
+    if (c.ev_start) cudaEventDestroy(c.ev_start);
+    for (cudaEvent_t e : c.prof_pool) if (e) cudaEventDestroy(e);
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) if (s) cudaStreamDestroy(s);
+}
+
+// Records a timing event on `s` when profiling is on; returns its pool index or -1.
+cudaError_t prof_mark(kvo::Ctx& c, cudaStream_t s, int* idx) {
+    *idx = -1;
+    if (!c.prof_on) return cudaSuccess;
+    if (c.prof_used == (int)c.prof_pool.size()) {
+        cudaEvent_t e;
+        cudaError_t err = cudaEventCreate(&e);
+        if (err != cudaSuccess) return err;
+        c.prof_pool.push_back(e);
+    }
+    *idx = c.prof_used++;
+    return cudaEventRecord(c.prof_pool[*idx], s);
+}
+
+cudaStream_t pick(const kvo::Ctx& c, kvo_stream_t s) { return s ? (cudaStream_t)s : c.s_compute; }
+
+kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, void* const* v_host,
+                     const void* const* k_win, const void* const* v_win) {
+    if (!cfg || !k_host || !v_host || !cfg->seq_lens) return fail(&c, KVO_ERR_INVALID, "null config, host arrays or seq_lens");
+    c.cfg = *cfg;
+    c.batch = cfg->batch; c.Hq = cfg->n_q_heads; c.Hkv = cfg->n_kv_heads; c.d = cfg->head_dim;
+    c.B = cfg->block_size; c.k = cfg->top_k; c.W = cfg->window; c.L = cfg->n_layers;
+    if (c.batch < 1 || c.Hkv < 1 || c.Hq < c.Hkv || c.Hq % c.Hkv) return fail(&c, KVO_ERR_INVALID, "bad batch or head counts");
+    c.r = c.Hq / c.Hkv;
+    if (c.r > 16) return fail(&c, KVO_ERR_INVALID, "n_q_heads / n_kv_heads must be <= 16");
+    if (c.d != 64 && c.d != 128) return fail(&c, KVO_ERR_INVALID, "head_dim must be 64 or 128");
+    if (c.B < 1 || c.k < 1 || c.k > 8192 || c.W < 0 || c.L < 1)
+        return fail(&c, KVO_ERR_INVALID, "need block_size >= 1, 1 <= top_k <= 8192, window >= 0, n_layers >= 1");
+    if (c.W > 0 && (!k_win || !v_win)) return fail(&c, KVO_ERR_INVALID, "window > 0 needs k_win and v_win");
+    c.G = c.batch * c.Hkv;
+    c.lens.assign(cfg->seq_lens, cfg->seq_lens + c.batch);
+    std::vector<int64_t> off(c.G);
+    std::vector<int32_t> C(c.G);
+    int64_t tok = 0;
+    for (int b = 0; b < c.batch; ++b) {
+        const int64_t n = c.lens[b];
+        if (n < c.W || (n - c.W) % c.B) return fail(&c, KVO_ERR_INVALID, "each len must be >= window with (len - window) % block_size == 0");
+        const int64_t Cb = (n - c.W) / c.B;
+        if (Cb < c.k) return fail(&c, KVO_ERR_INVALID, "top_k exceeds the candidate blocks of a request");
+        if (Cb > (1 << 30)) return fail(&c, KVO_ERR_INVALID, "too many candidate blocks");
+        for (int g = 0; g < c.Hkv; ++g) {
+            off[b * c.Hkv + g] = (tok * c.Hkv + (int64_t)g * n) * c.d;
+            C[b * c.Hkv + g] = (int32_t)Cb;
+        }
+        c.Cmax = std::max<int>(c.Cmax, (int)Cb);
+        tok += n;
+    }
+    // host caches: page-locked and device-addressable
+    for (int l = 0; l < c.L; ++l) {
+        for (int kv = 0; kv < 2; ++kv) {
+            void* hp = kv ? v_host[l] : k_host[l];
+            if (!hp) return fail(&c, KVO_ERR_INVALID, "null host K/V pointer");
+            cudaPointerAttributes a{};
+            cudaError_t e = cudaPointerGetAttributes(&a, hp);
+            if (e != cudaSuccess) return cuda_fail(&c, e, "cudaPointerGetAttributes(host K/V)");
+            if (a.type != cudaMemoryTypeHost || !a.devicePointer)
+                return fail(&c, KVO_ERR_INVALID, "host K/V must be page-locked, device-mapped memory (cudaHostAlloc / cudaHostRegister)");
+            if ((uintptr_t)a.devicePointer % 16) return fail(&c, KVO_ERR_INVALID, "host K/V must be 16-byte aligned");
+            (kv ? c.v_host : c.k_host).push_back((const uint16_t*)a.devicePointer);
+        }
+        if (c.W > 0) {
+            for (int kv = 0; kv < 2; ++kv) {
+                const void* wp = kv ? v_win[l] : k_win[l];
+                if (!wp) return fail(&c, KVO_ERR_INVALID, "null window pointer");
+                cudaPointerAttributes a{};
+                cudaError_t e = cudaPointerGetAttributes(&a, wp);
+                if (e != cudaSuccess) return cuda_fail(&c, e, "cudaPointerGetAttributes(window)");
+                if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+                    return fail(&c, KVO_ERR_INVALID, "window K/V must be device memory");
+                if ((uintptr_t)wp % 16) return fail(&c, KVO_ERR_INVALID, "window K/V must be 16-byte aligned");
+                (kv ? c.v_win : c.k_win).push_back((const uint16_t*)wp);
+            }
+        } else {
+            c.k_win.push_back(nullptr);
+            c.v_win.push_back(nullptr);
+        }
+    }
+    // streams: urgent > compute > prefetch
+    int least = 0, greatest = 0;
+    KVO_CUDA(&c, cudaDeviceGetStreamPriorityRange(&least, &greatest));
+    KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_compute, cudaStreamNonBlocking, (least + greatest) / 2));
+    KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_prefetch, cudaStreamNonBlocking, least));
+    KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_urgent, cudaStreamNonBlocking, greatest));
+    size_t sb = 0;
+    KVO_CUDA(&c, dalloc(&c.g_off, sizeof(int64_t) * c.G, &sb));
+    KVO_CUDA(&c, dalloc(&c.g_C, sizeof(int32_t) * c.G, &sb));
+    KVO_CUDA(&c, cudaMemcpy(c.g_off, off.data(), sizeof(int64_t) * c.G, cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(c.g_C, C.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    // landmarks
+    c.lm_bytes = (size_t)c.G * c.Cmax * c.d * (c.B > 1 ? 4 : 2);
+    c.lm.assign(c.L, nullptr);
+    for (int l = 0; l < c.L; ++l) {
+        KVO_CUDA(&c, dalloc((char**)&c.lm[l], c.lm_bytes, nullptr));
+        KVO_CUDA(&c, cudaMemsetAsync(c.lm[l], 0, c.lm_bytes, c.s_compute));
+        KVO_CUDA(&c, kvo::launch_landmarks(c, l, c.s_compute));
+    }
+    // ping-pong halves
+    const size_t half = (size_t)c.G * 2 * c.k * c.B * c.d * sizeof(uint16_t);
+    for (int i = 0; i < 2; ++i) {
+        KVO_CUDA(&c, dalloc(&c.pp_k[i], half, nullptr));
+        KVO_CUDA(&c, dalloc(&c.pp_v[i], half, nullptr));
+        KVO_CUDA(&c, cudaMemsetAsync(c.pp_k[i], 0, half, c.s_compute));
+        KVO_CUDA(&c, cudaMemsetAsync(c.pp_v[i], 0, half, c.s_compute));
+    }
+    c.pp_bytes = 4 * half;
+    // selection scratch and work items
+    const size_t Cmax4 = (size_t)((c.Cmax + 3) & ~3);
+    KVO_CUDA(&c, dalloc(&c.sel_keys, sizeof(uint32_t) * 2 * c.G * Cmax4, &sb));
+    KVO_CUDA(&c, dalloc(&c.sel_hist, sizeof(uint32_t) * 2 * c.G * 256, &sb));
+    KVO_CUDA(&c, dalloc(&c.sel_done, sizeof(uint32_t) * c.G, &sb));
+    KVO_CUDA(&c, cudaMemsetAsync(c.sel_hist, 0, sizeof(uint32_t) * 2 * c.G * 256, c.s_compute));
+    KVO_CUDA(&c, cudaMemsetAsync(c.sel_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
+    std::vector<int2> sel_items;
+    std::vector<int32_t> nch(c.G);
+    for (int g = 0; g < c.G; ++g) {
+        nch[g] = (C[g] + kvo::SEL_ROWS - 1) / kvo::SEL_ROWS;
+        for (int j = 0; j < nch[g]; ++j) sel_items.push_back(make_int2(g, j));
+    }
+    c.n_sel_items = (int)sel_items.size();
+    KVO_CUDA(&c, dalloc(&c.sel_items, sizeof(int2) * sel_items.size(), &sb));
+    KVO_CUDA(&c, dalloc(&c.sel_nchunks, sizeof(int32_t) * c.G, &sb));
+    KVO_CUDA(&c, cudaMemcpy(c.sel_items, sel_items.data(), sizeof(int2) * sel_items.size(), cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(c.sel_nchunks, nch.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    // run scratch: [2][G][k] int4 + [2][G]
+    KVO_CUDA(&c, dalloc(&c.runs, sizeof(int32_t) * 4 * 2 * (size_t)c.G * c.k, &sb));
+    KVO_CUDA(&c, dalloc(&c.nruns, sizeof(int32_t) * 2 * c.G, &sb));
+    // attention work items
+    std::vector<int4> att;
+    std::vector<int32_t> afirst(c.G), acount(c.G);
+    const int sp_tiles = (c.k * c.B + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    const int w_tiles = (c.W + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    for (int g = 0; g < c.G; ++g) {
+        afirst[g] = (int)att.size();
+        for (int t = 0; t < sp_tiles; t += kvo::ATT_TILES_PER_ITEM)
+            att.push_back(make_int4(g, 0, t, std::min(kvo::ATT_TILES_PER_ITEM, sp_tiles - t)));
+        for (int t = 0; t < w_tiles; t += kvo::ATT_TILES_PER_ITEM)
+            att.push_back(make_int4(g, 1, t, std::min(kvo::ATT_TILES_PER_ITEM, w_tiles - t)));
+        acount[g] = (int)att.size() - afirst[g];
+    }
+    c.n_att_items = (int)att.size();
+    KVO_CUDA(&c, dalloc(&c.att_items, sizeof(int4) * att.size(), &sb));
+    KVO_CUDA(&c, dalloc(&c.att_first, sizeof(int32_t) * c.G, &sb));
+    KVO_CUDA(&c, dalloc(&c.att_count, sizeof(int32_t) * c.G, &sb));
+    KVO_CUDA(&c, cudaMemcpy(c.att_items, att.data(), sizeof(int4) * att.size(), cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(c.att_first, afirst.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(c.att_count, acount.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, dalloc(&c.att_part_o, sizeof(float) * att.size() * c.r * c.d, &sb));
+    KVO_CUDA(&c, dalloc(&c.att_part_ml, sizeof(float) * att.size() * c.r * 2, &sb));
+    KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * c.G, &sb));
+    KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
+    KVO_CUDA(&c, dalloc(&c.status, sizeof(int32_t), &sb));
+    KVO_CUDA(&c, cudaMemsetAsync(c.status, 0, sizeof(int32_t), c.s_compute));
+    // decode-step state
+    const size_t lgk = (size_t)c.L * c.G * c.k;
+    KVO_CUDA(&c, dalloc(&c.st_true, sizeof(int32_t) * lgk, &sb));
+    KVO_CUDA(&c, dalloc(&c.st_pred, sizeof(int32_t) * 2 * lgk, &sb));
+    KVO_CUDA(&c, dalloc(&c.st_miss, sizeof(int32_t) * lgk, &sb));
+    KVO_CUDA(&c, dalloc(&c.st_miss_cnt, sizeof(int32_t) * c.L * c.G, &sb));
+    KVO_CUDA(&c, dalloc(&c.st_slot, sizeof(int32_t) * lgk, &sb));
+    c.scratch_bytes = sb;
+    for (auto* v : {&c.ev_sel, &c.ev_attn, &c.ev_urg}) {
+        v->assign(c.L, nullptr);
+        for (auto& e : *v) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    }
+    c.ev_pref.assign(2, nullptr);
+    for (auto& e : c.ev_pref) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
+    KVO_CUDA(&c, cudaStreamSynchronize(c.s_compute));
+    return KVO_OK;
+}
+
+kvo_status check_ctx(kvo_ctx* ctx) { return ctx ? KVO_OK : fail(nullptr, KVO_ERR_INVALID, "null context"); }
+
+}  // namespace
+
+extern "C" {
+
+kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* const* v_host,
+                           const void* const* k_win, const void* const* v_win, kvo_ctx** out) {
+    if (!out) return fail(nullptr, KVO_ERR_INVALID, "null output pointer");
+    *out = nullptr;
+    kvo_ctx* ctx = new (std::nothrow) kvo_ctx;
+    if (!ctx) return fail(nullptr, KVO_ERR_OOM, "host allocation failed");
+    kvo_status st = init_impl(ctx->c, cfg, k_host, v_host, k_win, v_win);
+    if (st != KVO_OK) {
+        g_err = ctx->c.err;
+        free_ctx(ctx->c);
+        delete ctx;
+        return st;
+    }
+    *out = ctx;
+    return KVO_OK;
+}
+
+kvo_status kv_offload_destroy(kvo_ctx* ctx) {
+    if (!ctx) return KVO_OK;
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent})
+        if (s) cudaStreamSynchronize(s);
+    free_ctx(ctx->c);
+    delete ctx;
+    return KVO_OK;
+}
+
+kvo_status select_topk(kvo_ctx* ctx, int layer, const void* q, const void* q_spec, int32_t* idx_true,
+                       int32_t* idx_pred, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
+    if (!q || !idx_true) return fail(&c, KVO_ERR_INVALID, "null q or idx_true");
+    if (q_spec && !idx_pred) return fail(&c, KVO_ERR_INVALID, "q_spec given without idx_pred");
+    KVO_CUDA(&c, kvo::launch_select(c, layer, q, q_spec, idx_true, q_spec ? idx_pred : nullptr, pick(c, stream)));
+    return KVO_OK;
+}
+
+kvo_status index_diff(kvo_ctx* ctx, const int32_t* idx_true, const int32_t* idx_pred, int32_t* miss_idx,
+                      int32_t* miss_cnt, int32_t* slot_of_true, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!idx_true || !miss_idx || !miss_cnt || !slot_of_true) return fail(&c, KVO_ERR_INVALID, "null pointer argument");
+    KVO_CUDA(&c, kvo::launch_index_diff(c, idx_true, idx_pred, miss_idx, miss_cnt, slot_of_true, pick(c, stream)));
+    return KVO_OK;
+}
+
+kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
+                            int urgent, int32_t* runs_out, int32_t* n_runs_out, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
+    if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
+    if (!idx) return fail(&c, KVO_ERR_INVALID, "null idx");
+    if (slot_base < 0 || slot_base > c.k) return fail(&c, KVO_ERR_INVALID, "slot_base must be in [0, k]");
+    if (runs_out && ((uintptr_t)runs_out % 16)) return fail(&c, KVO_ERR_INVALID, "runs_out must be 16-byte aligned");
+    const int u = urgent ? 1 : 0;
+    cudaStream_t s = stream ? (cudaStream_t)stream : (u ? c.s_urgent : c.s_prefetch);
+    int32_t* runs = runs_out ? runs_out : c.runs + (size_t)u * 4 * c.G * c.k;
+    int32_t* nruns = n_runs_out ? n_runs_out : c.nruns + (size_t)u * c.G;
+    KVO_CUDA(&c, kvo::launch_coalesce(c, idx, cnt, slot_base, runs, nruns, s));
+    KVO_CUDA(&c, kvo::launch_gather(c, layer, buf, runs, nruns, kvo::gather_default_ctas(c), s));
+    return KVO_OK;
+}
+
+kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q, const int32_t* slot_of_true, float* o,
+                              float* lse, int fuse_window_merge, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
+    if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
+    if (!q || !slot_of_true || !o || !lse) return fail(&c, KVO_ERR_INVALID, "null pointer argument");
+    KVO_CUDA(&c, kvo::launch_attention(c, layer, buf, q, slot_of_true, o, lse, fuse_window_merge ? 1 : 0,
+                                       pick(c, stream)));
+    return KVO_OK;
+}
+
+kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o, float* lse,
+                     int rows, int d, kvo_stream_t stream) {
+    if (rows < 0 || d < 1) return fail(nullptr, KVO_ERR_INVALID, "rows must be >= 0 and d >= 1");
+    if (rows > 0 && (!o1 || !lse1 || !o2 || !lse2 || !o || !lse))
+        return fail(nullptr, KVO_ERR_INVALID, "null pointer argument");
+    if (rows > 0 && (lse == lse1 || lse == lse2)) return fail(nullptr, KVO_ERR_INVALID, "lse must not alias lse1 or lse2");
+    cudaError_t e = kvo::launch_merge_lse(o1, lse1, o2, lse2, o, lse, rows, d, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "merge_lse launch");
+    return KVO_OK;
+}
+
+kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                           kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!q || !o || !lse) return fail(&c, KVO_ERR_INVALID, "null q, o or lse");
+    cudaStream_t s_user = pick(c, stream);
+    const size_t gk = (size_t)c.G * c.k;
+    const size_t q_layer = (size_t)c.batch * c.Hq * c.d;
+    const size_t o_layer = q_layer, lse_layer = (size_t)c.batch * c.Hq;
+    const int par = c.step_parity;
+    int32_t* pred_cur = c.st_pred + (size_t)par * c.L * gk;
+    int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
+    const bool have = c.have_pred;
+    const int n_ctas = kvo::gather_default_ctas(c);
+    int32_t* runs_pf = c.runs;
+    int32_t* nruns_pf = c.nruns;
+    int32_t* runs_ur = c.runs + (size_t)4 * gk;
+    int32_t* nruns_ur = c.nruns + c.G;
+
+    KVO_CUDA(&c, cudaEventRecord(c.ev_start, s_user));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, c.ev_start, 0));
+    // launch wrapper: timing events around the launch when profiling is on
+    auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
+        int e0, e1;
+        cudaError_t e = prof_mark(c, s, &e0);
+        if (e != cudaSuccess) return e;
+        e = launch();
+        if (e != cudaSuccess) return e;
+        e = prof_mark(c, s, &e1);
+        if (e != cudaSuccess) return e;
+        if (e0 >= 0) {
+            c.prof_recs.push_back({kind, e0});
+            c.prof_recs.push_back({-1, e1});
+        }
+        return cudaSuccess;
+    };
+
+    // prefetch of a layer: the prediction list into slots [0, k) of its half
+    auto prefetch = [&](int layer, int buf, const int32_t* pred, cudaEvent_t after) -> kvo_status {
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_prefetch, after, 0));
+        KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_prefetch,
+                           [&] { return kvo::launch_coalesce(c, pred, nullptr, 0, runs_pf, nruns_pf, c.s_prefetch); }));
+        KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
+                           [&] { return kvo::launch_gather(c, layer, buf, runs_pf, nruns_pf, n_ctas, c.s_prefetch); }));
+        KVO_CUDA(&c, cudaEventRecord(c.ev_pref[buf], c.s_prefetch));
+        return KVO_OK;
+    };
+    // A prefetch into each half is outstanding at step start when the previous
+    // step issued one (layers 0 and 1, or layer 0 when n_layers == 1).
+    // Half of layer l: parity of the global layer index step * L + l.
+    auto half_of = [&](int l) { return (c.step_parity * (c.L & 1) + l) & 1; };
+    bool pref_ready[2] = {false, false};
+    pref_ready[half_of(0)] = have;
+    if (c.L >= 2) pref_ready[half_of(1)] = have;
+    for (int l = 0; l < c.L; ++l) {
+        const int buf = half_of(l);
+        const void* ql = (const char*)q + l * q_layer * 2;
+        const void* qsl = q_spec ? (const char*)q_spec + l * q_layer * 2 : nullptr;
+        int32_t* T = q_spec ? c.st_true + l * gk : pred_next + l * gk;
+        int32_t* slot = c.st_slot + l * gk;
+        int32_t* miss = c.st_miss + l * gk;
+        int32_t* mcnt = c.st_miss_cnt + (size_t)l * c.G;
+        // 1. retrieval index (true; speculative -> next step's prediction)
+        KVO_CUDA(&c, timed(kvo::PK_SELECT, c.s_compute, [&] {
+            return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, c.s_compute);
+        }));
+        // 2. diff against the prediction made one step earlier
+        KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_compute, [&] {
+            return kvo::launch_index_diff(c, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, slot, c.s_compute);
+        }));
+        KVO_CUDA(&c, cudaEventRecord(c.ev_sel[l], c.s_compute));
+        // single-layer model: the next step's prefetch can start now, into the other half
+        if (c.L == 1) {
+            kvo_status st = prefetch(l, buf ^ 1, pred_next + l * gk, c.ev_sel[l]);
+            if (st) return st;
+        }
+        // 3. urgent gather of the misses into slots [k, 2k)
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, c.ev_sel[l], 0));
+        KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_urgent,
+                           [&] { return kvo::launch_coalesce(c, miss, mcnt, c.k, runs_ur, nruns_ur, c.s_urgent); }));
+        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
+                           [&] { return kvo::launch_gather(c, l, buf, runs_ur, nruns_ur, n_ctas, c.s_urgent); }));
+        KVO_CUDA(&c, cudaEventRecord(c.ev_urg[l], c.s_urgent));
+        // 4. attention once the misses and this half's prefetch have landed
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_urg[l], 0));
+        if (pref_ready[buf]) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_pref[buf], 0));
+        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
+            return kvo::launch_attention(c, l, buf, ql, slot, o + l * o_layer, lse + l * lse_layer, 1, c.s_compute);
+        }));
+        KVO_CUDA(&c, cudaEventRecord(c.ev_attn[l], c.s_compute));
+        pref_ready[buf] = false;
+        // 5. this half is free: prefetch global layer l + 2
+        if (c.L >= 2) {
+            const int t = l + 2;
+            if (t < c.L) {
+                if (have) {
+                    kvo_status st = prefetch(t, buf, pred_cur + t * gk, c.ev_attn[l]);
+                    if (st) return st;
+                    pref_ready[buf] = true;
+                }
+            } else {
+                kvo_status st = prefetch(t - c.L, buf, pred_next + (t - c.L) * gk, c.ev_attn[l]);
+                if (st) return st;
+            }
+        }
+    }
+    // the caller's stream waits for everything, including the next step's prefetches
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) {
+        KVO_CUDA(&c, cudaEventRecord(c.ev_start, s));
+        KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_start, 0));
+    }
+    c.have_pred = true;
+    c.step_parity ^= 1;
+    return KVO_OK;
+}
+
+kvo_status kvo_reset_prediction(kvo_ctx* ctx) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent}) cudaStreamSynchronize(s);
+    ctx->c.have_pred = false;
+    ctx->c.step_parity = 0;
+    return KVO_OK;
+}
+
+kvo_status kvo_get_stream(kvo_ctx* ctx, int which, kvo_stream_t* out) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if (!out || which < 0 || which > 2) return fail(&ctx->c, KVO_ERR_INVALID, "bad stream selector");
+    *out = which == 0 ? ctx->c.s_compute : which == 1 ? ctx->c.s_prefetch : ctx->c.s_urgent;
+    return KVO_OK;
+}
+
+kvo_status kvo_device_status(kvo_ctx* ctx, int32_t* code_out, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (stream) KVO_CUDA(&c, cudaStreamSynchronize((cudaStream_t)stream));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    int32_t v = 0;
+    KVO_CUDA(&c, cudaMemcpy(&v, c.status, sizeof(v), cudaMemcpyDeviceToHost));
+    KVO_CUDA(&c, cudaMemset(c.status, 0, sizeof(int32_t)));
+    if (code_out) *code_out = v;
+    if (v) return fail(&c, KVO_ERR_DEVICE, "device status word " + std::to_string(v));
+    return KVO_OK;
+}
+
+kvo_status kvo_landmarks(kvo_ctx* ctx, int layer, void* dst, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (layer < 0 || layer >= c.L || !dst) return fail(&c, KVO_ERR_INVALID, "bad layer or null dst");
+    KVO_CUDA(&c, kvo::copy_landmarks_logical(c, layer, dst, pick(c, stream)));
+    return KVO_OK;
+}
+
+kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if ((buf != 0 && buf != 1) || !k_out || !v_out) return fail(&ctx->c, KVO_ERR_INVALID, "bad buf or null output");
+    *k_out = ctx->c.pp_k[buf];
+    *v_out = ctx->c.pp_v[buf];
+    return KVO_OK;
+}
+
+kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if (!out4) return fail(&ctx->c, KVO_ERR_INVALID, "null output");
+    out4[0] = ctx->c.Cmax;
+    out4[1] = (int64_t)ctx->c.lm_bytes;
+    out4[2] = (int64_t)ctx->c.pp_bytes;
+    out4[3] = (int64_t)ctx->c.scratch_bytes;
+    return KVO_OK;
+}
+
+kvo_status kvo_profile(kvo_ctx* ctx, int enable) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    c.prof_on = enable != 0;
+    c.prof_recs.clear();
+    c.prof_used = 0;
+    return KVO_OK;
+}
+
+kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out, int n_kinds) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!ms_out || !launches_out || n_kinds < kvo::PK_COUNT) return fail(&c, KVO_ERR_INVALID, "need 6 output slots");
+    for (int i = 0; i < n_kinds; ++i) { ms_out[i] = 0.0; launches_out[i] = 0; }
+    for (size_t i = 0; i + 1 < c.prof_recs.size(); i += 2) {
+        cudaEvent_t a = c.prof_pool[c.prof_recs[i].ev], b = c.prof_pool[c.prof_recs[i + 1].ev];
+        KVO_CUDA(&c, cudaEventSynchronize(b));
+        float ms = 0.f;
+        KVO_CUDA(&c, cudaEventElapsedTime(&ms, a, b));
+        ms_out[c.prof_recs[i].kind] += ms;
+        launches_out[c.prof_recs[i].kind] += 1;
+    }
+    c.prof_recs.clear();
+    c.prof_used = 0;
+    return KVO_OK;
+}
+
+const char* kvo_last_error(const kvo_ctx* ctx) {
+    if (ctx) return ctx->c.err.c_str();
+    return g_err.c_str();
+}
+
+}  // extern "C"

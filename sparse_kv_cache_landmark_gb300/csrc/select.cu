@@ -1,0 +1,336 @@
+// K landmarks and retrieval-index selection.
+//
+// "DualDecoder: Accelerate Long Context LLM Inference by Predictive Prefetch",
+// §4.1 / Fig. 6 / Fig. 8: the retrieval index of a decode step is computed from
+// a (true or speculative) token and static GPU-resident K landmarks.  Landmark
+// of block j = mean key of its B tokens (fp32; for B == 1 the bf16 key itself).
+// Score of block j for KV head g = sum over the group's query heads of q_h . L_j.
+// The index is the exact top-k, ascending, ties to the lower block id.
+//
+// Layout of the landmarks of one layer (HBM, resident):
+//   B > 1 : float4 [G][d/4][Cmax]   (channel-chunk major: thread j reads row j
+//           one 16-byte chunk at a time, a warp reads 512 contiguous bytes)
+//   B == 1: uint4  [G][d/8][Cmax]   (8 bf16 per chunk)
+// Selection is one kernel: CTAs score chunks of landmark rows of one group,
+// write order-preserving uint32 keys and a histogram of their top 8 bits; the
+// last CTA of a group (atomic ticket) finishes a 4-pass MSB radix select on
+// the L2-resident keys and compacts the winners in ascending id order.
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+// ------------------------------------------------------------- landmarks
+template <int D>
+__global__ void landmark_mean_kernel(const uint16_t* __restrict__ kh, const int64_t* __restrict__ g_off,
+                                     const int32_t* __restrict__ g_C, float4* __restrict__ lm, int Cmax, int B) {
+    const int bg = blockIdx.y;
+    const int warps = blockDim.x >> 5;
+    const int j = blockIdx.x * warps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int C = g_C[bg];
+    if (j >= C || lane >= D / 4) return;
+    const uint16_t* src = kh + g_off[bg] + (int64_t)j * B * D + 4 * lane;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int t = 0; t < B; ++t) {
+        uint2 w = *reinterpret_cast<const uint2*>(src + (int64_t)t * D);
+        s0 += bf16lo_to_f32(w.x); s1 += bf16hi_to_f32(w.x);
+        s2 += bf16lo_to_f32(w.y); s3 += bf16hi_to_f32(w.y);
+    }
+    const float fb = (float)B;
+    lm[((int64_t)bg * (D / 4) + lane) * Cmax + j] = make_float4(s0 / fb, s1 / fb, s2 / fb, s3 / fb);
+}
+
+template <int D>
+__global__ void landmark_copy_kernel(const uint16_t* __restrict__ kh, const int64_t* __restrict__ g_off,
+                                     const int32_t* __restrict__ g_C, uint4* __restrict__ lm, int Cmax) {
+    constexpr int LPT = D / 8;              // lanes per token
+    constexpr int TPW = 32 / LPT;           // tokens per warp
+    const int bg = blockIdx.y;
+    const int warps = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int j = (blockIdx.x * warps + (threadIdx.x >> 5)) * TPW + lane / LPT;
+    const int c8 = lane % LPT;
+    if (j >= g_C[bg]) return;
+    const uint4 v = *reinterpret_cast<const uint4*>(kh + g_off[bg] + (int64_t)j * D + 8 * c8);
+    lm[((int64_t)bg * LPT + c8) * Cmax + j] = v;
+}
+
+cudaError_t launch_landmarks(const Ctx& c, int layer, cudaStream_t s) {
+    const int threads = 256, warps = threads / 32;
+    if (c.B > 1) {
+        dim3 grid((c.Cmax + warps - 1) / warps, c.G);
+        if (c.d == 128)
+            landmark_mean_kernel<128><<<grid, threads, 0, s>>>(c.k_host[layer], c.g_off, c.g_C,
+                                                               (float4*)c.lm[layer], c.Cmax, c.B);
+        else
+            landmark_mean_kernel<64><<<grid, threads, 0, s>>>(c.k_host[layer], c.g_off, c.g_C,
+                                                              (float4*)c.lm[layer], c.Cmax, c.B);
+    } else {
+        const int tpw = 32 / (c.d / 8);
+        dim3 grid((c.Cmax + warps * tpw - 1) / (warps * tpw), c.G);
+        if (c.d == 128)
+            landmark_copy_kernel<128><<<grid, threads, 0, s>>>(c.k_host[layer], c.g_off, c.g_C,
+                                                               (uint4*)c.lm[layer], c.Cmax);
+        else
+            landmark_copy_kernel<64><<<grid, threads, 0, s>>>(c.k_host[layer], c.g_off, c.g_C,
+                                                              (uint4*)c.lm[layer], c.Cmax);
+    }
+    return cudaGetLastError();
+}
+
+// logical copy [G][Cmax][d] for inspection
+template <typename T, int CH>
+__global__ void landmark_unpermute_kernel(const T* __restrict__ lm, T* __restrict__ out, int Cmax, int nchunk) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;   // over G*Cmax*nchunk
+    const int64_t per_g = (int64_t)Cmax * nchunk;
+    const int64_t total = per_g * gridDim.y;
+    const int bg = blockIdx.y;
+    if (i >= per_g) return;
+    (void)total;
+    const int j = (int)(i / nchunk), ch = (int)(i % nchunk);
+    out[((int64_t)bg * Cmax + j) * nchunk + ch] = lm[((int64_t)bg * nchunk + ch) * Cmax + j];
+}
+
+cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s) {
+    const int64_t per_g = (int64_t)c.Cmax * (c.B > 1 ? c.d / 4 : c.d / 8);
+    dim3 grid((unsigned)((per_g + 255) / 256), c.G);
+    if (c.B > 1)
+        landmark_unpermute_kernel<float4, 4><<<grid, 256, 0, s>>>((const float4*)c.lm[layer], (float4*)dst, c.Cmax,
+                                                                  c.d / 4);
+    else
+        landmark_unpermute_kernel<uint4, 8><<<grid, 256, 0, s>>>((const uint4*)c.lm[layer], (uint4*)dst, c.Cmax,
+                                                                 c.d / 8);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- selection
+// Thread t of a 256-thread CTA owns radix bin 255 - t (descending).  Given
+// per-bin counts, find the bin holding the k_rem-th largest key.
+__device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, int* s_digit, uint32_t* s_krem,
+                                           uint32_t k_rem) {
+    uint32_t total;
+    const uint32_t excl = block_exclusive_scan(cnt, warp_sums, &total);
+    if (excl < k_rem && excl + cnt >= k_rem) {
+        *s_digit = 255 - (int)threadIdx.x;
+        *s_krem = k_rem - excl;
+    }
+    __syncthreads();
+}
+
+template <int D, bool BF16LM, bool DUAL>
+__global__ void __launch_bounds__(SEL_THREADS)
+select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
+              const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
+              uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
+              int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
+              int Hkv, int k) {
+    constexpr int NQ = DUAL ? 2 : 1;
+    __shared__ __align__(16) float u_s[NQ][D];
+    __shared__ uint32_t h_s[NQ][256];
+    __shared__ uint32_t warp_sums[32];
+    __shared__ int s_last;
+    __shared__ int s_digit;
+    __shared__ uint32_t s_krem;
+
+    const int tid = threadIdx.x;
+    const int2 it = items[blockIdx.x];
+    const int bg = it.x, chunk = it.y;
+    const int b = bg / Hkv, g = bg % Hkv;
+    const int C = g_C[bg];
+    const int Hq = Hkv * r;
+
+    // summed query of the group, fp32
+    for (int c = tid; c < D; c += SEL_THREADS) {
+        const uint16_t* qp = q + ((int64_t)b * Hq + g * r) * D + c;
+        float a = 0.f;
+        for (int h = 0; h < r; ++h) a += __uint_as_float((uint32_t)qp[h * D] << 16);
+        u_s[0][c] = a;
+        if (DUAL) {
+            const uint16_t* sp = qs + ((int64_t)b * Hq + g * r) * D + c;
+            float e = 0.f;
+            for (int h = 0; h < r; ++h) e += __uint_as_float((uint32_t)sp[h * D] << 16);
+            u_s[NQ - 1][c] = e;
+        }
+    }
+    for (int i = tid; i < NQ * 256; i += SEL_THREADS) (&h_s[0][0])[i] = 0u;
+    __syncthreads();
+
+    // ---- score SEL_RPT rows per thread (rows strided by the CTA width)
+    const int row0 = chunk * SEL_ROWS + tid;
+    float acc[NQ][SEL_RPT];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi)
+#pragma unroll
+        for (int i = 0; i < SEL_RPT; ++i) acc[qi][i] = 0.f;
+
+    if (!BF16LM) {
+        const float4* lm = reinterpret_cast<const float4*>(lm_v) + (int64_t)bg * (D / 4) * Cmax;
+#pragma unroll 4
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            float4 v[SEL_RPT];
+#pragma unroll
+            for (int i = 0; i < SEL_RPT; ++i) {
+                const int j = row0 + i * SEL_THREADS;
+                v[i] = j < C ? __ldg(lm + (int64_t)c4 * Cmax + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const float4 u = *reinterpret_cast<const float4*>(&u_s[qi][4 * c4]);
+#pragma unroll
+                for (int i = 0; i < SEL_RPT; ++i) {
+                    float a = acc[qi][i];
+                    a = fmaf(v[i].x, u.x, a);
+                    a = fmaf(v[i].y, u.y, a);
+                    a = fmaf(v[i].z, u.z, a);
+                    a = fmaf(v[i].w, u.w, a);
+                    acc[qi][i] = a;
+                }
+            }
+        }
+    } else {
+        const uint4* lm = reinterpret_cast<const uint4*>(lm_v) + (int64_t)bg * (D / 8) * Cmax;
+#pragma unroll 4
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+            uint4 v[SEL_RPT];
+#pragma unroll
+            for (int i = 0; i < SEL_RPT; ++i) {
+                const int j = row0 + i * SEL_THREADS;
+                v[i] = j < C ? __ldg(lm + (int64_t)c8 * Cmax + j) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                const float4 u0 = *reinterpret_cast<const float4*>(&u_s[qi][8 * c8]);
+                const float4 u1 = *reinterpret_cast<const float4*>(&u_s[qi][8 * c8 + 4]);
+#pragma unroll
+                for (int i = 0; i < SEL_RPT; ++i) {
+                    float a = acc[qi][i];
+                    a = fmaf(bf16lo_to_f32(v[i].x), u0.x, a);
+                    a = fmaf(bf16hi_to_f32(v[i].x), u0.y, a);
+                    a = fmaf(bf16lo_to_f32(v[i].y), u0.z, a);
+                    a = fmaf(bf16hi_to_f32(v[i].y), u0.w, a);
+                    a = fmaf(bf16lo_to_f32(v[i].z), u1.x, a);
+                    a = fmaf(bf16hi_to_f32(v[i].z), u1.y, a);
+                    a = fmaf(bf16lo_to_f32(v[i].w), u1.z, a);
+                    a = fmaf(bf16hi_to_f32(v[i].w), u1.w, a);
+                    acc[qi][i] = a;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+        uint32_t* kq = keys + ((int64_t)qi * G + bg) * Cmax4;
+#pragma unroll
+        for (int i = 0; i < SEL_RPT; ++i) {
+            const int j = row0 + i * SEL_THREADS;
+            if (j < C) {
+                const uint32_t key = float_to_ordered(acc[qi][i]);
+                kq[j] = key;
+                atomicAdd(&h_s[qi][key >> 24], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < NQ * 256; i += SEL_THREADS) {
+        const uint32_t v = (&h_s[0][0])[i];
+        if (v) atomicAdd(&hist[((int64_t)(i / 256) * G + bg) * 256 + (i % 256)], v);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t prev = atomicAdd(&done[bg], 1u);
+        s_last = (prev + 1 == (uint32_t)nchunks[bg]);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA of the group: exact top-k for each query
+    for (int qi = 0; qi < NQ; ++qi) {
+        const uint32_t* kq = keys + ((int64_t)qi * G + bg) * Cmax4;
+        int32_t* out = (qi == 0 ? idx_true : idx_pred) + (int64_t)bg * k;
+        uint32_t* hg = hist + ((int64_t)qi * G + bg) * 256;
+        uint32_t k_rem = (uint32_t)min(k, C);
+        const uint32_t cnt0 = __ldcg(hg + 255 - tid);
+        hg[255 - tid] = 0u;                                  // leave the histogram zeroed
+        pick_digit(cnt0, warp_sums, &s_digit, &s_krem, k_rem);
+        uint32_t prefix = (uint32_t)s_digit << 24, mask = 0xFF000000u;
+        k_rem = s_krem;
+        for (int shift = 16; shift >= 0; shift -= 8) {
+            h_s[0][tid] = 0u;
+            __syncthreads();
+            for (int j = tid; j < C; j += SEL_THREADS) {
+                const uint32_t key = __ldcg(kq + j);
+                if ((key & mask) == prefix) atomicAdd(&h_s[0][(key >> shift) & 0xFFu], 1u);
+            }
+            __syncthreads();
+            const uint32_t cnt = h_s[0][255 - tid];
+            __syncthreads();
+            pick_digit(cnt, warp_sums, &s_digit, &s_krem, k_rem);
+            prefix |= (uint32_t)s_digit << shift;
+            mask |= 0xFFu << shift;
+            k_rem = s_krem;
+        }
+        // prefix == key of the k-th largest; take every larger key and the first
+        // k_rem keys equal to it, in ascending id order.
+        const uint32_t thr = prefix;
+        const uint32_t k_eq = k_rem;
+        const uint32_t k_out = (uint32_t)min(k, C);
+        uint32_t n_out = 0, eq_seen = 0;
+        for (int base = 0; base < C && n_out < k_out; base += 4 * SEL_THREADS) {
+            const int j0 = base + 4 * tid;
+            uint4 kv4 = make_uint4(0u, 0u, 0u, 0u);
+            if (j0 < C) kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
+            const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
+            uint32_t n_eq = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) n_eq += (j0 + e < C && kv[e] == thr);
+            uint32_t eq_total;
+            const uint32_t eq_excl = block_exclusive_scan(n_eq, warp_sums, &eq_total);
+            uint32_t sel = 0, eq_run = eq_seen + eq_excl;
+            bool take[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = j0 + e < C;
+                bool t = valid && kv[e] > thr;
+                if (valid && kv[e] == thr) {
+                    t = eq_run < k_eq;
+                    ++eq_run;
+                }
+                take[e] = t;
+                sel += t;
+            }
+            uint32_t sel_total;
+            uint32_t pos = n_out + block_exclusive_scan(sel, warp_sums, &sel_total);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (take[e]) out[pos++] = j0 + e;
+            n_out += sel_total;
+            eq_seen += eq_total;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) done[bg] = 0u;
+}
+
+cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
+                          int32_t* idx_pred, cudaStream_t s) {
+    const int Cmax4 = (c.Cmax + 3) & ~3;
+    const bool dual = q_spec != nullptr;
+    const bool bf = c.B == 1;
+#define KVO_SEL(D_, BF_, DU_)                                                                                  \
+    select_kernel<D_, BF_, DU_><<<c.n_sel_items, SEL_THREADS, 0, s>>>(                                         \
+        c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C,          \
+        c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k)
+    if (c.d == 128) {
+        if (bf) { if (dual) KVO_SEL(128, true, true); else KVO_SEL(128, true, false); }
+        else    { if (dual) KVO_SEL(128, false, true); else KVO_SEL(128, false, false); }
+    } else {
+        if (bf) { if (dual) KVO_SEL(64, true, true); else KVO_SEL(64, true, false); }
+        else    { if (dual) KVO_SEL(64, false, true); else KVO_SEL(64, false, false); }
+    }
+#undef KVO_SEL
+    return cudaGetLastError();
+}
+
+}  // namespace kvo

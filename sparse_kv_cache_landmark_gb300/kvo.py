@@ -1,0 +1,253 @@
+"""Python binding of libkvo (the C ABI in include/kvo.h): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels; this module
+turns torch tensors into pointers, allocates outputs with torch, and raises
+``KvoError`` on any non-OK status.  There is no fallback: without the built
+library or a CUDA device every call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvo.so")
+
+KVO_OK, KVO_ERR_INVALID, KVO_ERR_CUDA, KVO_ERR_OOM, KVO_ERR_TIMEOUT, KVO_ERR_STATE, KVO_ERR_DEVICE = range(7)
+DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_COUNT, DEV_UNSORTED = 1, 2, 4, 8
+
+EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff", "gather_coalesced",
+           "sparse_decode_attn", "merge_lse", "kvo_decode_step", "kvo_reset_prediction", "kvo_get_stream",
+           "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
+           "kvo_last_error"]
+PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
+
+
+class KvoError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"kvo status {status}: {msg}")
+        self.status = status
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("seq_lens", ctypes.POINTER(ctypes.c_int32))]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvo.so (built by ``build.py``); raises if it is missing."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkvo.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, VP = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+        L.kv_offload_init.argtypes = [ctypes.POINTER(_Config), P, P, P, P, ctypes.POINTER(P)]
+        L.kv_offload_destroy.argtypes = [P]
+        L.select_topk.argtypes = [P, I, VP, VP, VP, VP, VP]
+        L.index_diff.argtypes = [P, VP, VP, VP, VP, VP, VP]
+        L.gather_coalesced.argtypes = [P, I, I, VP, VP, I, I, VP, VP, VP]
+        L.sparse_decode_attn.argtypes = [P, I, I, VP, VP, VP, VP, I, VP]
+        L.merge_lse.argtypes = [VP, VP, VP, VP, VP, VP, I, I, VP]
+        L.kvo_decode_step.argtypes = [P, VP, VP, VP, VP, VP]
+        L.kvo_reset_prediction.argtypes = [P]
+        L.kvo_get_stream.argtypes = [P, I, ctypes.POINTER(P)]
+        L.kvo_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), VP]
+        L.kvo_landmarks.argtypes = [P, I, VP, VP]
+        L.kvo_buffer.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P)]
+        L.kvo_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
+        L.kvo_profile.argtypes = [P, I]
+        L.kvo_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I]
+        L.kvo_last_error.argtypes = [P]
+        L.kvo_last_error.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name != "kvo_last_error":
+                getattr(L, name).restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+CUDA_STREAM_LEGACY = 0x1   # cudaStreamLegacy: the legacy default stream
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    """Handle of ``stream`` (default: torch's current stream) for the C ABI.
+
+    The ABI reads NULL as "the context's own compute stream", so torch's
+    default stream (handle 0) is passed as cudaStreamLegacy instead.
+    """
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    h = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(h or CUDA_STREAM_LEGACY)
+
+
+def _check(st: int, ctx=None):
+    if st != KVO_OK:
+        msg = lib().kvo_last_error(ctx)
+        raise KvoError(st, msg.decode() if msg else "")
+
+
+def merge_lse(o1, lse1, o2, lse2, o=None, lse=None, stream=None):
+    """Fuse two attention parts by log-sum-exp (C: merge_lse). fp32 CUDA tensors [rows][d], [rows]."""
+    rows, d = o1.shape
+    o = torch.empty_like(o1) if o is None else o
+    lse = torch.empty_like(lse1) if lse is None else lse
+    _check(lib().merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(o), _ptr(lse), rows, d, _stream(stream)))
+    return o, lse
+
+
+class Context:
+    """A KV cache in pinned host memory plus the library's device state (C: kv_offload_init).
+
+    ``k_host[l]``/``v_host[l]``: pinned CPU bf16 tensors, packed [b][Hkv][len_b][d];
+    ``k_win[l]``/``v_win[l]``: CUDA bf16 tensors [b][Hkv][W][d] (None when W == 0).
+    The tensors must outlive the context; the context keeps references to them.
+    """
+
+    def __init__(self, *, batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers,
+                 seq_lens: Sequence[int], k_host: List[torch.Tensor], v_host: List[torch.Tensor],
+                 k_win: Optional[List[torch.Tensor]] = None, v_win: Optional[List[torch.Tensor]] = None):
+        L = lib()
+        self._lens = (ctypes.c_int32 * batch)(*[int(x) for x in seq_lens])
+        self.cfg = _Config(batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers, self._lens)
+        self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim = batch, n_q_heads, n_kv_heads, head_dim
+        self.block_size, self.top_k, self.window, self.n_layers = block_size, top_k, window, n_layers
+        self.G = batch * n_kv_heads
+        self._keep = (list(k_host), list(v_host), list(k_win or []), list(v_win or []))
+        arr = lambda ts: (ctypes.c_void_p * n_layers)(*[t.data_ptr() for t in ts]) if ts else None
+        self._kh, self._vh = arr(k_host), arr(v_host)
+        self._kw, self._vw = arr(k_win), arr(v_win)
+        out = ctypes.c_void_p()
+        _check(L.kv_offload_init(ctypes.byref(self.cfg), self._kh, self._vh, self._kw, self._vw, ctypes.byref(out)))
+        self.ctx = out
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lib().kv_offload_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _c(self, st):
+        _check(st, self.ctx)
+
+    def _i32(self, *shape):
+        return torch.empty(*shape, dtype=torch.int32, device="cuda")
+
+    def select_topk(self, layer, q, q_spec=None, idx_true=None, idx_pred=None, stream=None):
+        idx_true = self._i32(self.G, self.top_k) if idx_true is None else idx_true
+        if q_spec is not None and idx_pred is None:
+            idx_pred = self._i32(self.G, self.top_k)
+        self._c(lib().select_topk(self.ctx, layer, _ptr(q), _ptr(q_spec), _ptr(idx_true),
+                                  _ptr(idx_pred) if q_spec is not None else None, _stream(stream)))
+        return idx_true, (idx_pred if q_spec is not None else None)
+
+    def index_diff(self, idx_true, idx_pred=None, stream=None):
+        miss = self._i32(self.G, self.top_k)
+        cnt = self._i32(self.G)
+        slot = self._i32(self.G, self.top_k)
+        self._c(lib().index_diff(self.ctx, _ptr(idx_true), _ptr(idx_pred), _ptr(miss), _ptr(cnt), _ptr(slot),
+                                 _stream(stream)))
+        return miss, cnt, slot
+
+    def gather_coalesced(self, layer, buf, idx, cnt=None, slot_base=0, urgent=False, want_runs=True, stream=None):
+        runs = self._i32(self.G, self.top_k, 4) if want_runs else None
+        nruns = self._i32(self.G) if want_runs else None
+        self._c(lib().gather_coalesced(self.ctx, layer, buf, _ptr(idx), _ptr(cnt), slot_base, int(bool(urgent)),
+                                       _ptr(runs), _ptr(nruns), _stream(stream)))
+        return runs, nruns
+
+    def sparse_decode_attn(self, layer, buf, q, slot_of_true, fuse_window_merge=True, o=None, lse=None, stream=None):
+        rows = self.batch * self.n_q_heads
+        parts = 1 if fuse_window_merge else 2
+        if o is None:
+            o = torch.empty(parts, rows, self.head_dim, dtype=torch.float32, device="cuda")
+        if lse is None:
+            lse = torch.empty(parts, rows, dtype=torch.float32, device="cuda")
+        self._c(lib().sparse_decode_attn(self.ctx, layer, buf, _ptr(q), _ptr(slot_of_true), _ptr(o), _ptr(lse),
+                                         int(bool(fuse_window_merge)), _stream(stream)))
+        return o, lse
+
+    def decode_step(self, q, q_spec=None, o=None, lse=None, stream=None):
+        """One pipelined decode step over every layer (C: kvo_decode_step)."""
+        rows = self.batch * self.n_q_heads
+        if o is None:
+            o = torch.empty(self.n_layers, rows, self.head_dim, dtype=torch.float32, device="cuda")
+        if lse is None:
+            lse = torch.empty(self.n_layers, rows, dtype=torch.float32, device="cuda")
+        self._c(lib().kvo_decode_step(self.ctx, _ptr(q), _ptr(q_spec), _ptr(o), _ptr(lse), _stream(stream)))
+        return o, lse
+
+    def reset_prediction(self):
+        self._c(lib().kvo_reset_prediction(self.ctx))
+
+    def get_stream(self, which: int) -> int:
+        out = ctypes.c_void_p()
+        self._c(lib().kvo_get_stream(self.ctx, which, ctypes.byref(out)))
+        return out.value or 0
+
+    def device_status(self, stream=None) -> int:
+        code = ctypes.c_int32(0)
+        st = lib().kvo_device_status(self.ctx, ctypes.byref(code), _stream(stream))
+        if st not in (KVO_OK, KVO_ERR_DEVICE):
+            self._c(st)
+        return int(code.value)
+
+    def info(self):
+        out = (ctypes.c_int64 * 4)()
+        self._c(lib().kvo_info(self.ctx, out))
+        return {"C_max": out[0], "landmark_bytes": out[1], "pingpong_bytes": out[2], "scratch_bytes": out[3]}
+
+    def profile(self, enable: bool):
+        self._c(lib().kvo_profile(self.ctx, int(bool(enable))))
+
+    def profile_read(self):
+        """{kind: (total ms, launches)} of the decode-step launches recorded since profile(True)."""
+        n = len(PROFILE_KINDS)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        self._c(lib().kvo_profile_read(self.ctx, ms, cnt, n))
+        return {k: (ms[i], cnt[i]) for i, k in enumerate(PROFILE_KINDS)}
+
+    def landmarks(self, layer, stream=None):
+        C = self.info()["C_max"]
+        dt = torch.float32 if self.block_size > 1 else torch.bfloat16
+        dst = torch.empty(self.G, C, self.head_dim, dtype=dt, device="cuda")
+        self._c(lib().kvo_landmarks(self.ctx, layer, _ptr(dst), _stream(stream)))
+        return dst
+
+    def buffer(self, buf):
+        """(K, V) copies of ping-pong half ``buf`` as bf16 CUDA tensors [G][2k][B][d]."""
+        kp, vp = ctypes.c_void_p(), ctypes.c_void_p()
+        self._c(lib().kvo_buffer(self.ctx, buf, ctypes.byref(kp), ctypes.byref(vp)))
+        n = self.G * 2 * self.top_k * self.block_size * self.head_dim
+        torch.cuda.synchronize()
+        return tuple(_device_view(p.value, n).clone().view(self.G, 2 * self.top_k, self.block_size, self.head_dim)
+                     for p in (kp, vp))
+
+
+class _CudaArray:
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i2", "data": (ptr, False), "version": 2}
+
+
+def _device_view(ptr: int, n: int) -> torch.Tensor:
+    """bf16 view of n library-owned device elements (no copy)."""
+    return torch.as_tensor(_CudaArray(ptr, n), device="cuda").view(torch.bfloat16)
