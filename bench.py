@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--host-layers", type=int, default=0, help="distinct host layers (0: all that fit)")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling runs)")
+    ap.add_argument("--gather-ctas", type=int, default=0, help="gather kernel CTAs (0: library default)")
+    ap.add_argument("--gather-threads", type=int, default=0, help="gather threads per CTA (0: library default)")
+    ap.add_argument("--gather-unroll", type=int, default=0, help="gather loads in flight per lane (0: default)")
     return ap.parse_args()
 
 
@@ -211,14 +215,16 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU path
-def run_ours(args):
-    ws, rank, local = dist_setup(args)
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
-    torch.cuda.set_device(local)
+class Built:
+    """A workload resident on the box: pinned host caches, windows, queries, context."""
+
+
+def build_workload(args, ws=1):
     from sparse_kv_cache_landmark_gb300.kvo import Context, lib
     lib()                                   # fails loudly when the library is not built
     w = WORKLOADS[args.workload]
+    if args.layers:
+        w = w.scaled(n_layers=args.layers)
     lens = synth.seq_lens(w, args.seed)
     n = synth.layer_numel(w, lens)
     layer_bytes = 2 * n * 2
@@ -261,17 +267,56 @@ def run_ours(args):
             k_host.append(k_host[l % n_host]); v_host.append(v_host[l % n_host])
             k_win.append(k_win[l % n_host]); v_win.append(v_win[l % n_host])
     torch.cuda.synchronize()
-    t_gen = time.perf_counter() - t_gen
-    ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
-                  block_size=w.block_size, top_k=w.top_k, window=w.window, n_layers=w.n_layers, seq_lens=lens,
-                  k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win)
-    q_pin = torch.stack(qs_l).pin_memory()
-    qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
-    q_dev = q_pin.to("cuda")
-    qs_dev = None if qs_pin is None else qs_pin.to("cuda")
+    B = Built()
+    B.w, B.lens, B.n_host = w, lens, n_host
+    B.setup_s = time.perf_counter() - t_gen
+    B.ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
+                    block_size=w.block_size, top_k=w.top_k, window=w.window, n_layers=w.n_layers, seq_lens=lens,
+                    k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win)
+    if args.gather_ctas or args.gather_threads or args.gather_unroll:
+        B.ctx.set_gather_shape(args.gather_ctas, args.gather_threads or 128, args.gather_unroll or 1)
+    B.keep = (k_host, v_host, k_win, v_win)
+    B.q_pin = torch.stack(qs_l).pin_memory()
+    B.qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
+    B.q_dev = B.q_pin.to("cuda")
+    B.qs_dev = None if B.qs_pin is None else B.qs_pin.to("cuda")
     rows = w.batch * w.n_q_heads
-    o = torch.empty(w.n_layers, rows, w.head_dim, dtype=torch.float32, device="cuda")
-    lse = torch.empty(w.n_layers, rows, dtype=torch.float32, device="cuda")
+    B.o = torch.empty(w.n_layers, rows, w.head_dim, dtype=torch.float32, device="cuda")
+    B.lse = torch.empty(w.n_layers, rows, dtype=torch.float32, device="cuda")
+    return B
+
+
+def time_steps(B, steps, ws=1, profile=True):
+    """(ms per step, per-kind profile) over ``steps`` decode steps on the current stream."""
+    stream = torch.cuda.current_stream()
+    ctx = B.ctx
+    if profile:
+        ctx.profile(True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        ctx.decode_step(B.q_dev, B.qs_dev, B.o, B.lse)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    prof = None
+    if profile:
+        prof = ctx.profile_read()
+        ctx.profile(False)
+    return ev0.elapsed_time(ev1) / steps, prof
+
+
+def run_ours(args):
+    ws, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    Bw = build_workload(args, ws)
+    w, lens, n_host, ctx = Bw.w, Bw.lens, Bw.n_host, Bw.ctx
+    q_pin, qs_pin, q_dev, qs_dev, o, lse = Bw.q_pin, Bw.qs_pin, Bw.q_dev, Bw.qs_dev, Bw.o, Bw.lse
+    t_gen = Bw.setup_s
     stream = torch.cuda.current_stream()
 
     # host->device link bandwidth (pinned copy engine), best of 3
@@ -293,20 +338,8 @@ def run_ours(args):
 
     clocks = Clocks(local)
     time.sleep(0.3)
-    ctx.profile(True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        ctx.decode_step(q_dev, qs_dev, o, lse)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    prof = ctx.profile_read()
-    ctx.profile(False)
+    t_ms, prof = time_steps(Bw, args.steps, ws)
     clk = clocks.stop()
-    t_ms = ev0.elapsed_time(ev1) / args.steps
     t_ms = max_over_ranks(ws, t_ms)
     value = ws / (t_ms * 1e-3)
 
@@ -389,9 +422,12 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "device_status": status,
             "setup_s": round(t_gen, 1),
+            "gather_shape": {"ctas": args.gather_ctas or "default", "threads": args.gather_threads or "default",
+                             "unroll": args.gather_unroll or "default"},
         }
         print(json.dumps(line), flush=True)
     ctx.close()
+    del Bw
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -218,6 +218,16 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
 kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);
 
 /*
+ * kvo_set_gather_shape -- launch shape of the host -> HBM gather kernel:
+ * ctas (0: the default, 2 per SM), threads per CTA (32..256, multiple of 32)
+ * and 16-byte loads of K and of V in flight per lane (1, 2 or 4).  The gather
+ * reads host memory in place; its in-flight loads queue behind the host link,
+ * so a shape that just saturates the link leaves the SMs' memory pipelines to
+ * the HBM-bound kernels running beside it.
+ */
+kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll);
+
+/*
  * Per-launch timing of kvo_decode_step, for benchmarks.  kvo_profile(ctx, 1)
  * clears and starts recording a timing event before and after every kernel
  * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.

@@ -359,3 +359,4 @@ cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2
 }
 
 }  // namespace kvo
+

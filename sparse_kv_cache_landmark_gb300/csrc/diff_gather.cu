@@ -172,15 +172,19 @@ gather_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh, 
 }
 
 int gather_default_ctas(const Ctx& c) {
-    (void)c;
-    return 2 * 152;
+    return c.gather_ctas > 0 ? c.gather_ctas : 2 * 152;
 }
 
-cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns, int n_ctas,
+cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                           cudaStream_t s) {
-    gather_kernel<4><<<n_ctas, GATHER_THREADS, 0, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C,
-                                                        (const int4*)runs, nruns, c.pp_k[buf], c.pp_v[buf], c.G, c.k,
-                                                        c.B, c.d, c.status);
+    const int ctas = gather_default_ctas(c), th = c.gather_threads;
+#define KVO_GATHER(U_)                                                                                          \
+    gather_kernel<U_><<<ctas, th, 0, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, (const int4*)runs, \
+                                          nruns, c.pp_k[buf], c.pp_v[buf], c.G, c.k, c.B, c.d, c.status)
+    if (c.gather_unroll >= 4) KVO_GATHER(4);
+    else if (c.gather_unroll == 2) KVO_GATHER(2);
+    else KVO_GATHER(1);
+#undef KVO_GATHER
     return cudaGetLastError();
 }
 

@@ -57,6 +57,7 @@ struct Ctx {
     float* att_part_ml = nullptr;   // [items][r][2]
     uint32_t* att_done = nullptr;   // [G]
     int32_t* status = nullptr;      // device status word
+    int gather_ctas = 0, gather_threads = 128, gather_unroll = 1;   // gather launch shape (0: default)
     size_t scratch_bytes = 0;
     cudaStream_t s_compute = nullptr, s_prefetch = nullptr, s_urgent = nullptr;
     // decode-step state
@@ -130,7 +131,7 @@ cudaError_t launch_index_diff(const Ctx& c, const int32_t* idx_true, const int32
 cudaError_t launch_coalesce(const Ctx& c, const int32_t* idx, const int32_t* cnt, int slot_base, int32_t* runs,
                             int32_t* nruns, cudaStream_t s);
 cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
-                          int n_ctas, cudaStream_t s);
+                          cudaStream_t s);
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const int32_t* slot, float* o,
                              float* lse, int fuse, cudaStream_t s);
 cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,

@@ -305,7 +305,7 @@ kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx
     int32_t* runs = runs_out ? runs_out : c.runs + (size_t)u * 4 * c.G * c.k;
     int32_t* nruns = n_runs_out ? n_runs_out : c.nruns + (size_t)u * c.G;
     KVO_CUDA(&c, kvo::launch_coalesce(c, idx, cnt, slot_base, runs, nruns, s));
-    KVO_CUDA(&c, kvo::launch_gather(c, layer, buf, runs, nruns, kvo::gather_default_ctas(c), s));
+    KVO_CUDA(&c, kvo::launch_gather(c, layer, buf, runs, nruns, s));
     return KVO_OK;
 }
 
@@ -345,7 +345,6 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
     int32_t* pred_cur = c.st_pred + (size_t)par * c.L * gk;
     int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
     const bool have = c.have_pred;
-    const int n_ctas = kvo::gather_default_ctas(c);
     int32_t* runs_pf = c.runs;
     int32_t* nruns_pf = c.nruns;
     int32_t* runs_ur = c.runs + (size_t)4 * gk;
@@ -375,7 +374,7 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
         KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_prefetch,
                            [&] { return kvo::launch_coalesce(c, pred, nullptr, 0, runs_pf, nruns_pf, c.s_prefetch); }));
         KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
-                           [&] { return kvo::launch_gather(c, layer, buf, runs_pf, nruns_pf, n_ctas, c.s_prefetch); }));
+                           [&] { return kvo::launch_gather(c, layer, buf, runs_pf, nruns_pf, c.s_prefetch); }));
         KVO_CUDA(&c, cudaEventRecord(c.ev_pref[buf], c.s_prefetch));
         return KVO_OK;
     };
@@ -413,7 +412,7 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
         KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_urgent,
                            [&] { return kvo::launch_coalesce(c, miss, mcnt, c.k, runs_ur, nruns_ur, c.s_urgent); }));
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
-                           [&] { return kvo::launch_gather(c, l, buf, runs_ur, nruns_ur, n_ctas, c.s_urgent); }));
+                           [&] { return kvo::launch_gather(c, l, buf, runs_ur, nruns_ur, c.s_urgent); }));
         KVO_CUDA(&c, cudaEventRecord(c.ev_urg[l], c.s_urgent));
         // 4. attention once the misses and this half's prefetch have landed
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_urg[l], 0));
@@ -499,6 +498,17 @@ kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4) {
     out4[1] = (int64_t)ctx->c.lm_bytes;
     out4[2] = (int64_t)ctx->c.pp_bytes;
     out4[3] = (int64_t)ctx->c.scratch_bytes;
+    return KVO_OK;
+}
+
+kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if (ctas < 0 || ctas > 65535 || threads < 32 || threads > kvo::GATHER_THREADS || threads % 32 ||
+        (unroll != 1 && unroll != 2 && unroll != 4))
+        return fail(&ctx->c, KVO_ERR_INVALID, "need 0 <= ctas <= 65535, threads a multiple of 32 in [32, 256], unroll 1|2|4");
+    ctx->c.gather_ctas = ctas;
+    ctx->c.gather_threads = threads;
+    ctx->c.gather_unroll = unroll;
     return KVO_OK;
 }
 

@@ -22,7 +22,7 @@ DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_COUNT, DEV_UNSORTED = 1, 2, 4, 8
 EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff", "gather_coalesced",
            "sparse_decode_attn", "merge_lse", "kvo_decode_step", "kvo_reset_prediction", "kvo_get_stream",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
-           "kvo_last_error"]
+           "kvo_last_error", "kvo_set_gather_shape"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
         L.kvo_profile.argtypes = [P, I]
         L.kvo_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I]
+        L.kvo_set_gather_shape.argtypes = [P, I, I, I]
         L.kvo_last_error.argtypes = [P]
         L.kvo_last_error.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -214,6 +215,9 @@ class Context:
         out = (ctypes.c_int64 * 4)()
         self._c(lib().kvo_info(self.ctx, out))
         return {"C_max": out[0], "landmark_bytes": out[1], "pingpong_bytes": out[2], "scratch_bytes": out[3]}
+
+    def set_gather_shape(self, ctas: int = 0, threads: int = 256, unroll: int = 4):
+        self._c(lib().kvo_set_gather_shape(self.ctx, ctas, threads, unroll))
 
     def profile(self, enable: bool):
         self._c(lib().kvo_profile(self.ctx, int(bool(enable))))
