@@ -218,6 +218,37 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
 kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);
 
 /*
+ * sparse_decode_attn_static -- sparse_decode_attn without a context and
+ * without allocating device memory.  The pages have no counterpart to this
+ * call; it exists for callers that cannot call cudaMalloc: code whose device
+ * memory all belongs to another allocator (a framework arena or a pool sized
+ * once at start-up), and latency-critical callers that cannot afford the
+ * implicit device synchronisation of cudaMalloc / cudaFree in a decode loop.
+ *   Inputs (device): q [b][Hq][d] bf16; k_buf, v_buf [G][2k][B][d] bf16 (the
+ *   layout of a ping-pong half); slot_of_true [G][k] int32; k_win, v_win
+ *   [b][Hkv][W][d] bf16 (may be NULL when W == 0).  Outputs as in
+ *   sparse_decode_attn (fuse_window_merge picks one fused part or two parts);
+ *   status (device int32, optional) receives KVO_DEV_BAD_SLOT for a slot
+ *   outside [0, 2k), which is then not read.
+ *   Scratch: one static device array of 24 MiB, reserved on every GPU that
+ *   loads the library until the process exits.  A call needs
+ *   items * r * (d + 2) * 4 bytes plus small tables, items = G * (ceil(k*B/256)
+ *   + ceil(W/256)); larger calls are rejected with KVO_ERR_INVALID and a message
+ *   giving both sizes.  Every call shares the array and leaves its contents
+ *   behind (the tickets it needs are cleared at the start of each call), so
+ *   calls that overlap on the GPU race: order them on one stream.
+ *   The first call on each device looks up the array's device address with
+ *   that device current (cudaGetSymbolAddress) and caches it; make that first
+ *   call before any stream capture.  No cudaMalloc, cudaFree or allocating
+ *   library routine is called.
+ */
+kvo_status sparse_decode_attn_static(const void* q, const void* k_buf, const void* v_buf,
+                                     const int32_t* slot_of_true, const void* k_win, const void* v_win,
+                                     float* o, float* lse, int32_t* status, int batch, int n_q_heads,
+                                     int n_kv_heads, int head_dim, int block_size, int top_k, int window,
+                                     int fuse_window_merge, kvo_stream_t stream);
+
+/*
  * kvo_set_gather_shape -- launch shape of the host -> HBM gather kernel:
  * ctas (0: the default, 2 per SM), threads per CTA (32..256, multiple of 32)
  * and 16-byte loads of K and of V in flight per lane (1, 2 or 4).  The gather

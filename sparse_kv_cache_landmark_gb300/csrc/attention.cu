@@ -360,3 +360,141 @@ cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2
 
 }  // namespace kvo
 
+// ---------------------------------------------------------------------------
+// sparse_decode_attn_static: the attention kernel above, launched without a
+// context and without allocating, for callers that cannot call cudaMalloc
+// (their device memory belongs to another allocator, or their decode loop
+// cannot afford the implicit synchronisation of cudaMalloc / cudaFree).
+// Its work items, tickets and partial results
+// live in one file-scope device array (kStaticAttnBytes, held by every GPU
+// that loads the library until the process exits).  Host code cannot use the
+// array's name as a device address, so the first call on each device looks
+// the address up with cudaGetSymbolAddress (with that device current) and
+// caches it.  Calls share the array: two calls that overlap on the GPU race.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace kvo {
+
+constexpr size_t kStaticAttnBytes = size_t(24) << 20;
+static __device__ __align__(256) unsigned char g_attn_static[kStaticAttnBytes];
+
+__global__ void static_items_kernel(int4* __restrict__ items, int32_t* __restrict__ first,
+                                    int32_t* __restrict__ count, int G, int sp_tiles, int w_tiles) {
+    const int g = blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= G) return;
+    const int sp_items = (sp_tiles + ATT_TILES_PER_ITEM - 1) / ATT_TILES_PER_ITEM;
+    const int w_items = (w_tiles + ATT_TILES_PER_ITEM - 1) / ATT_TILES_PER_ITEM;
+    const int base = g * (sp_items + w_items);
+    first[g] = base;
+    count[g] = sp_items + w_items;
+    for (int i = 0; i < sp_items; ++i) {
+        const int t = i * ATT_TILES_PER_ITEM;
+        items[base + i] = make_int4(g, 0, t, min(ATT_TILES_PER_ITEM, sp_tiles - t));
+    }
+    for (int i = 0; i < w_items; ++i) {
+        const int t = i * ATT_TILES_PER_ITEM;
+        items[base + sp_items + i] = make_int4(g, 1, t, min(ATT_TILES_PER_ITEM, w_tiles - t));
+    }
+}
+
+namespace {
+std::mutex g_static_mu;
+constexpr int kMaxDevices = 64;
+unsigned char* g_static_addr[kMaxDevices] = {};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+}  // namespace kvo
+
+extern "C" kvo_status sparse_decode_attn_static(const void* q, const void* k_buf, const void* v_buf,
+                                                const int32_t* slot_of_true, const void* k_win, const void* v_win,
+                                                float* o, float* lse, int32_t* status, int batch, int n_q_heads,
+                                                int n_kv_heads, int head_dim, int block_size, int top_k,
+                                                int window, int fuse_window_merge, kvo_stream_t stream) {
+    using namespace kvo;
+    auto bad = [](const char* m) { set_last_error(m); return KVO_ERR_INVALID; };
+    if (batch < 1 || n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads)
+        return bad("bad batch or head counts");
+    const int r = n_q_heads / n_kv_heads;
+    if (r > 16) return bad("n_q_heads / n_kv_heads must be <= 16");
+    if (head_dim != 64 && head_dim != 128) return bad("head_dim must be 64 or 128");
+    if (block_size < 1 || top_k < 1 || window < 0) return bad("need block_size >= 1, top_k >= 1, window >= 0");
+    if (!q || !k_buf || !v_buf || !slot_of_true || !o || !lse) return bad("null pointer argument");
+    if (window > 0 && (!k_win || !v_win)) return bad("window > 0 needs k_win and v_win");
+    for (const void* p : {q, k_buf, v_buf, k_win, v_win})
+        if ((uintptr_t)p % 16) return bad("bf16 inputs must be 16-byte aligned");
+    const int G = batch * n_kv_heads;
+    const int sp_tiles = (int)(((int64_t)top_k * block_size + ATT_TILE - 1) / ATT_TILE);
+    const int w_tiles = (window + ATT_TILE - 1) / ATT_TILE;
+    const int64_t per = (sp_tiles + ATT_TILES_PER_ITEM - 1) / ATT_TILES_PER_ITEM +
+                        (w_tiles + ATT_TILES_PER_ITEM - 1) / ATT_TILES_PER_ITEM;
+    const int64_t n_items = per * G;
+    // layout: status word | tickets [G] | first [G] | count [G] | items | m,l | partial o
+    const size_t off_done = 256;
+    const size_t off_first = align256(off_done + 4 * (size_t)G);
+    const size_t off_count = align256(off_first + 4 * (size_t)G);
+    const size_t off_items = align256(off_count + 4 * (size_t)G);
+    const size_t off_ml = align256(off_items + 16 * (size_t)n_items);
+    const size_t off_o = align256(off_ml + 8 * (size_t)n_items * r);
+    const size_t need = off_o + 4 * (size_t)n_items * r * head_dim;
+    if (n_items > INT32_MAX || need > kStaticAttnBytes) {
+        set_last_error(("sparse_decode_attn_static needs " + std::to_string(need) +
+                        " bytes of static scratch; its capacity is " + std::to_string(kStaticAttnBytes) +
+                        " bytes (reduce batch, KV heads, top_k * block_size or window)").c_str());
+        return KVO_ERR_INVALID;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { set_last_error(cudaGetErrorString(e)); return KVO_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return bad("device ordinal beyond the static scratch table");
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_addr[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_attn_static);
+            if (e != cudaSuccess || !p) {
+                set_last_error(("cudaGetSymbolAddress(static attention scratch): " +
+                                std::string(cudaGetErrorString(e))).c_str());
+                return KVO_ERR_CUDA;
+            }
+            g_static_addr[dev] = (unsigned char*)p;
+        }
+        base = g_static_addr[dev];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t* st = status ? status : (int32_t*)base;
+    uint32_t* done = (uint32_t*)(base + off_done);
+    int32_t* first = (int32_t*)(base + off_first);
+    int32_t* count = (int32_t*)(base + off_count);
+    int4* items = (int4*)(base + off_items);
+    float* part_ml = (float*)(base + off_ml);
+    float* part_o = (float*)(base + off_o);
+    e = cudaMemsetAsync(done, 0, 4 * (size_t)G, s);
+    if (e == cudaSuccess) {
+        static_items_kernel<<<(G + 127) / 128, 128, 0, s>>>(items, first, count, G, sp_tiles, w_tiles);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)head_dim));
+        const uint16_t* wk = window > 0 ? (const uint16_t*)k_win : nullptr;
+        const uint16_t* wv = window > 0 ? (const uint16_t*)v_win : nullptr;
+        const int fuse = fuse_window_merge ? 1 : 0;
+#define KVO_ATT_STATIC(D_, NR_)                                                                                  \
+        attn_kernel<D_, NR_><<<(unsigned)n_items, ATT_WARPS * 32, 0, s>>>(                                        \
+            (const uint16_t*)q, (const uint16_t*)k_buf, (const uint16_t*)v_buf, wk, wv, slot_of_true, items,     \
+            first, count, part_o, part_ml, done, o, lse, fuse, batch, r, n_kv_heads, top_k, block_size, window,  \
+            scale_log2, st)
+        if (head_dim == 128) {
+            if (r <= 8) KVO_ATT_STATIC(128, 1); else KVO_ATT_STATIC(128, 2);
+        } else {
+            if (r <= 8) KVO_ATT_STATIC(64, 1); else KVO_ATT_STATIC(64, 2);
+        }
+#undef KVO_ATT_STATIC
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) { set_last_error(cudaGetErrorString(e)); return KVO_ERR_CUDA; }
+    return KVO_OK;
+}

@@ -140,4 +140,7 @@ cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStrea
 
 int gather_default_ctas(const Ctx& c);
 
+// Sets the message kvo_last_error(NULL) returns (context-free calls).
+void set_last_error(const char* msg);
+
 }  // namespace kvo

@@ -243,6 +243,8 @@ kvo_status check_ctx(kvo_ctx* ctx) { return ctx ? KVO_OK : fail(nullptr, KVO_ERR
 
 }  // namespace
 
+void kvo::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
 extern "C" {
 
 kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* const* v_host,

@@ -22,7 +22,7 @@ DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_COUNT, DEV_UNSORTED = 1, 2, 4, 8
 EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff", "gather_coalesced",
            "sparse_decode_attn", "merge_lse", "kvo_decode_step", "kvo_reset_prediction", "kvo_get_stream",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
-           "kvo_last_error", "kvo_set_gather_shape"]
+           "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
         L.kvo_profile.argtypes = [P, I]
         L.kvo_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I]
+        L.sparse_decode_attn_static.argtypes = [VP, VP, VP, VP, VP, VP, VP, VP, VP] + [I] * 8 + [VP]
         L.kvo_set_gather_shape.argtypes = [P, I, I, I]
         L.kvo_last_error.argtypes = [P]
         L.kvo_last_error.restype = ctypes.c_char_p
@@ -107,6 +108,33 @@ def merge_lse(o1, lse1, o2, lse2, o=None, lse=None, stream=None):
     o = torch.empty_like(o1) if o is None else o
     lse = torch.empty_like(lse1) if lse is None else lse
     _check(lib().merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(o), _ptr(lse), rows, d, _stream(stream)))
+    return o, lse
+
+
+def sparse_decode_attn_static(q, k_buf, v_buf, slot_of_true, k_win, v_win, *, batch, n_q_heads, n_kv_heads,
+                              head_dim, block_size, top_k, window, fuse_window_merge=True, o=None, lse=None,
+                              status=None, stream=None):
+    """Context-free attention that allocates no device memory in the library (C: sparse_decode_attn_static).
+
+    Meant for callers that cannot call cudaMalloc: code whose device memory all
+    belongs to another allocator (a framework arena or a pool sized at start-up)
+    and decode loops that cannot afford the implicit synchronisation of
+    cudaMalloc / cudaFree.  The library's scratch is a fixed 24 MiB static device
+    array shared by every call, so calls must not overlap on the GPU.
+    ``k_buf``/``v_buf`` are bf16 CUDA tensors laid out like a ping-pong half,
+    [G][2k][B][d].  Pass ``o``/``lse`` (and ``status``) to keep this wrapper from
+    allocating its outputs with torch.
+    """
+    rows = batch * n_q_heads
+    parts = 1 if fuse_window_merge else 2
+    if o is None:
+        o = torch.empty(parts, rows, head_dim, dtype=torch.float32, device="cuda")
+    if lse is None:
+        lse = torch.empty(parts, rows, dtype=torch.float32, device="cuda")
+    _check(lib().sparse_decode_attn_static(_ptr(q), _ptr(k_buf), _ptr(v_buf), _ptr(slot_of_true), _ptr(k_win),
+                                           _ptr(v_win), _ptr(o), _ptr(lse), _ptr(status), batch, n_q_heads,
+                                           n_kv_heads, head_dim, block_size, top_k, window,
+                                           int(bool(fuse_window_merge)), _stream(stream)))
     return o, lse
 
 
@@ -236,6 +264,14 @@ class Context:
         dst = torch.empty(self.G, C, self.head_dim, dtype=dt, device="cuda")
         self._c(lib().kvo_landmarks(self.ctx, layer, _ptr(dst), _stream(stream)))
         return dst
+
+    def buffer_views(self, buf):
+        """(K, V) zero-copy views of ping-pong half ``buf`` as bf16 CUDA tensors [G][2k][B][d]."""
+        kp, vp = ctypes.c_void_p(), ctypes.c_void_p()
+        self._c(lib().kvo_buffer(self.ctx, buf, ctypes.byref(kp), ctypes.byref(vp)))
+        n = self.G * 2 * self.top_k * self.block_size * self.head_dim
+        return tuple(_device_view(p.value, n).view(self.G, 2 * self.top_k, self.block_size, self.head_dim)
+                     for p in (kp, vp))
 
     def buffer(self, buf):
         """(K, V) copies of ping-pong half ``buf`` as bf16 CUDA tensors [G][2k][B][d]."""
