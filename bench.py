@@ -52,8 +52,13 @@ def parse():
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling runs)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--gather-ctas", type=int, default=0, help="gather kernel CTAs (0: library default)")
     ap.add_argument("--gather-threads", type=int, default=0, help="gather threads per CTA (0: library default)")
+    ap.add_argument("--gather-engine", type=int, default=-1, help="0 lane loads, 1 TMA bulk copies (-1: default)")
+    ap.add_argument("--gather-drivers", type=int, default=0, help="TMA engine driver warps (0: default)")
+    ap.add_argument("--gather-reserve", type=int, default=-1, help="flat engine smem reservation per CTA (bytes)")
+    ap.add_argument("--graphs", type=int, default=-1, help="1: replay warm steps from CUDA graphs (-1: default)")
     ap.add_argument("--gather-unroll", type=int, default=0, help="gather loads in flight per lane (0: default)")
     return ap.parse_args()
 
@@ -67,8 +72,12 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def workload_bytes(w, lens):
-    """Algorithmic bytes of one step (all layers): HBM and host link."""
+def workload_bytes(w, lens, misses_per_step=0):
+    """Algorithmic bytes of one step (all layers): HBM and host link.
+
+    ``misses_per_step``: blocks fetched by the urgent stream per step (summed
+    over layers and groups) on top of the k prefetched blocks per group.
+    """
     G, d, k, B, W, L = w.batch * w.n_kv_heads, w.head_dim, w.top_k, w.block_size, w.window, w.n_layers
     tok = 4 * d                                             # K+V bf16 bytes per token per KV head
     C = [(n - W) // B for n in lens]
@@ -78,10 +87,11 @@ def workload_bytes(w, lens):
     q_bytes = w.batch * w.n_q_heads * d * 2 * 3             # select (2x) + attention
     out_bytes = w.batch * w.n_q_heads * (d + 1) * 4
     meta = G * k * 4 * 8
-    hbm = (lm_bytes + gathered + attended + q_bytes + out_bytes + meta) * L
-    host = gathered * L
+    urgent = misses_per_step * B * tok
+    hbm = (lm_bytes + gathered + attended + q_bytes + out_bytes + meta) * L + urgent
+    host = gathered * L + urgent
     kv_attended = attended * L
-    return {"hbm": hbm, "host": host, "kv_attended": kv_attended, "gather_per_launch": gathered,
+    return {"hbm": hbm, "host": host, "kv_attended": kv_attended, "gather_per_launch": gathered, "urgent": urgent,
             "landmark_per_layer": lm_bytes, "attended_per_layer": attended}
 
 
@@ -184,6 +194,10 @@ def run_reference(args):
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
+    if args.layers:
+        w = w.scaled(n_layers=args.layers)
+    if args.batch:
+        w = w.scaled(batch=args.batch)
     G = w.batch * w.n_kv_heads
     per_step_groups = G * w.n_layers
     # each bench step: one bounded sample of groups; the step time is scaled
@@ -225,6 +239,8 @@ def build_workload(args, ws=1):
     w = WORKLOADS[args.workload]
     if args.layers:
         w = w.scaled(n_layers=args.layers)
+    if args.batch:
+        w = w.scaled(batch=args.batch)
     lens = synth.seq_lens(w, args.seed)
     n = synth.layer_numel(w, lens)
     layer_bytes = 2 * n * 2
@@ -275,6 +291,12 @@ def build_workload(args, ws=1):
                     k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win)
     if args.gather_ctas or args.gather_threads or args.gather_unroll:
         B.ctx.set_gather_shape(args.gather_ctas, args.gather_threads or 128, args.gather_unroll or 1)
+    if args.gather_engine >= 0:
+        B.ctx.set_gather_engine(args.gather_engine, args.gather_drivers)
+    if args.gather_reserve >= 0:
+        B.ctx.set_gather_reserve(args.gather_reserve)
+    if args.graphs >= 0:
+        B.ctx.set_graphs(bool(args.graphs))
     B.keep = (k_host, v_host, k_win, v_win)
     B.q_pin = torch.stack(qs_l).pin_memory()
     B.qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
@@ -366,8 +388,14 @@ def run_ours(args):
     assert torch.isfinite(o_pin).all() and torch.isfinite(lse_pin).all()
     status = ctx.device_status()
 
+    # steady-state misses per step: each layer's true index against the prediction of the previous step
+    misses = 0
+    for l in range(w.n_layers):
+        T, P = ctx.select_topk(l, q_dev[l], None if qs_dev is None else qs_dev[l])
+        _, cnt, _ = ctx.index_diff(T, P if P is not None else T)
+        misses += int(cnt.sum().item())
     hbm_peak, peak_kind = peaks()
-    by = workload_bytes(w, lens)
+    by = workload_bytes(w, lens, misses)
     t_hbm = by["hbm"] / (hbm_peak * 1e9)
     t_link = by["host"] / (link * 1e9)
     t_star = max(t_hbm, t_link)
@@ -403,9 +431,10 @@ def run_ours(args):
                        "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.ctx[0],
                        "block": w.block_size, "top_k": w.top_k, "window": w.window, "layers": w.n_layers,
                        "host_layers_distinct": n_host, "parallelism": f"replicas x{ws}",
-                       "l2": "inputs larger than L2: every step streams 4.3 GB over the host link and "
-                             "reads 2.1 GB of landmarks + 4.3 GB of gathered KV from HBM"},
+                       "l2": f"inputs larger than L2 (129 MB): every step moves {by['host'] / 1e9:.2f} GB over "
+                             f"the host link and {by['hbm'] / 1e9:.2f} GB through HBM"},
             "effective_kv_gbs": by["kv_attended"] / (t_ms * 1e-3) / 1e9 * ws,
+            "urgent_misses_per_step": misses,
             "step_roofline": {"t_star_ms": t_star * 1e3, "frac": t_star * 1e3 / t_ms,
                               "bound": "link" if t_link >= t_hbm else "hbm",
                               "host_bytes": by["host"], "hbm_bytes": by["hbm"], "link_gbs": link,
@@ -423,7 +452,9 @@ def run_ours(args):
             "device_status": status,
             "setup_s": round(t_gen, 1),
             "gather_shape": {"ctas": args.gather_ctas or "default", "threads": args.gather_threads or "default",
-                             "unroll": args.gather_unroll or "default"},
+                             "unroll": args.gather_unroll or "default",
+                             "engine": "default" if args.gather_engine < 0 else args.gather_engine,
+                             "drivers": args.gather_drivers or "default"},
         }
         print(json.dumps(line), flush=True)
     ctx.close()

@@ -67,6 +67,7 @@ typedef enum {
 #define KVO_DEV_BAD_SLOT     0x2   /* a slot >= 2k or a run past the buffer */
 #define KVO_DEV_BAD_COUNT    0x4   /* a count outside [0, k] */
 #define KVO_DEV_UNSORTED     0x8   /* an index list that is not strictly ascending */
+#define KVO_DEV_TIMEOUT      0x10  /* a bounded device wait gave up */
 
 typedef void* kvo_stream_t;        /* cudaStream_t */
 typedef struct kvo_ctx kvo_ctx;    /* opaque, owned by the library */
@@ -164,6 +165,20 @@ kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q,
                               int fuse_window_merge, kvo_stream_t stream);
 
 /*
+ * sparse_decode_attn_cobatch -- co-batched attention of the true and the
+ * speculative query (DualDecoder §5.2, Fig. 18: the real and the speculative
+ * token attend in one batched pass).  Both queries of a KV group attend, in
+ * one kernel pass over the same K/V bytes, to the blocks named by
+ * slot_of_true plus the window; the speculative query's r rows fill M rows
+ * r..2r-1 of the tensor-core tiles, so 2r <= 16 is required.
+ *   q, q_spec: device [b][Hq][d] bf16.  o, lse as in sparse_decode_attn;
+ *   o_spec, lse_spec: the same layouts for the speculative query.
+ */
+kvo_status sparse_decode_attn_cobatch(kvo_ctx* ctx, int layer, int buf, const void* q, const void* q_spec,
+                                      const int32_t* slot_of_true, float* o, float* lse, float* o_spec,
+                                      float* lse_spec, int fuse_window_merge, kvo_stream_t stream);
+
+/*
  * merge_lse -- fuse two attention parts over disjoint key sets
  *   ("Scaling Attention Beyond GPUs for LLM Inference", abstract):
  *   M = max(lse1, lse2), w_i = exp(lse_i - M), o = (w1 o1 + w2 o2) / (w1 + w2),
@@ -189,6 +204,26 @@ kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const 
  */
 kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o,
                            float* lse, kvo_stream_t stream);
+
+/*
+ * kvo_decode_step_dual -- kvo_decode_step whose attention is co-batched: each
+ * layer's attention pass also produces the speculative query's output over the
+ * same key set (o_spec [n_layers][b][Hq][d], lse_spec [n_layers][b][Hq] fp32),
+ * as the dual-token pipeline needs it (DualDecoder §5.2).  q_spec is required;
+ * 2r <= 16.
+ */
+kvo_status kvo_decode_step_dual(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                                float* o_spec, float* lse_spec, kvo_stream_t stream);
+
+/*
+ * kvo_set_graphs -- 1: warm decode steps (every step after the first) are
+ * captured once per step parity into a CUDA graph and replayed, which removes
+ * the host launch work and shortens the gaps between dependent kernels; a
+ * graph is re-captured when the q/o/lse pointers of the call change or a
+ * gather tuning call is made.  Profiling (kvo_profile) bypasses the graphs.
+ * 0 (default): every step is launched stream by stream.
+ */
+kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable);
 
 /* Forget the predictions kept for the next step (next step starts cold). */
 kvo_status kvo_reset_prediction(kvo_ctx* ctx);
@@ -259,6 +294,29 @@ kvo_status sparse_decode_attn_static(const void* q, const void* k_buf, const voi
 kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll);
 
 /*
+ * kvo_set_gather_engine -- how the gather moves bytes.  engine 0: lane loads
+ * (the kernel shaped by kvo_set_gather_shape).  engines 1 and 2: TMA bulk
+ * copies, host -> shared memory -> HBM, driven by `drivers` warps (0: default
+ * 32), each with 3 (engine 1) or 7 (engine 2) batches of up to 16 KiB in
+ * flight; the SMs' load/store pipelines stay free for the HBM-bound kernels
+ * running beside it.  Every TMA wait is bounded (2 s); on expiry the driver
+ * sets KVO_DEV_TIMEOUT and stops.  engine 3: lane loads over the index list
+ * itself, a flat stream of 16-byte words per group (entry j of a list goes to
+ * slot base + j, so adjacent ids are read and written as contiguous ranges);
+ * the decode step then skips building run lists.
+ */
+kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers);
+
+/*
+ * kvo_set_gather_reserve -- engine 3 only: shared memory each gather CTA
+ * reserves without using it (0..227 KiB).  A reservation near the SM's
+ * capacity gives each gather CTA an SM of its own, so HBM-bound kernels never
+ * share an SM (and its load/store pipeline) with loads waiting on the link.
+ * Set the engine before kvo_set_gather_shape when asking for > 256 threads.
+ */
+kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes);
+
+/*
  * Per-launch timing of kvo_decode_step, for benchmarks.  kvo_profile(ctx, 1)
  * clears and starts recording a timing event before and after every kernel
  * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.
@@ -269,6 +327,12 @@ kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll)
  */
 kvo_status kvo_profile(kvo_ctx* ctx, int enable);
 kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out, int n_kinds);
+/* kvo_profile_trace: the recorded launches in issue order (call before
+ * kvo_profile_read, which clears them): start and end (ms, relative to the
+ * first recorded launch), kind and layer.  Writes min(cap, count) entries and
+ * the count to *n_out. */
+kvo_status kvo_profile_trace(kvo_ctx* ctx, double* start_ms, double* end_ms, int32_t* kind, int32_t* layer,
+                             int cap, int* n_out);
 
 /* Human-readable description of the last error of ctx (or of the last
  * context-free call when ctx is NULL).  Never NULL. */

@@ -230,6 +230,8 @@ class GroupResult:
     lse_window: np.ndarray
     o: np.ndarray                      # merged
     lse: np.ndarray
+    o_spec: np.ndarray = None          # speculative query over the same key set (co-batched)
+    lse_spec: np.ndarray = None
     extra: dict = field(default_factory=dict)
 
 
@@ -271,9 +273,21 @@ def decode_group(k_rows_bits, v_rows_bits, q_group_bits, q_spec_group_bits, *,
         o_s[h], l_s[h] = attention_part(Q[h], K[sel], V[sel])
         o_w[h], l_w[h] = attention_part(Q[h], K[win], V[win])
         o[h], lse[h] = merge_lse(o_s[h], l_s[h], o_w[h], l_w[h])
+    # Co-batched speculative rows (DualDecoder §5.2, Fig. 18: the real and the
+    # speculative token attend in one batched pass).  Reading: the speculative
+    # query attends to the same key set as the true one (the true selection plus
+    # the window), each part merged by log-sum-exp like the true query's.
+    o_sp = l_sp = None
+    if q_spec_group_bits is not None:
+        Qs = bf16_bits_to_f64(q_spec_group_bits)
+        o_sp = np.zeros((r, d)); l_sp = np.zeros(r)
+        for h in range(r):
+            a = attention_part(Qs[h], K[sel], V[sel])
+            b_ = attention_part(Qs[h], K[win], V[win])
+            o_sp[h], l_sp[h] = merge_lse(a[0], a[1], b_[0], b_[1])
     return GroupResult(T=T, P=P, scores_true=s_true, scores_pred=s_pred, M=M, slot_of_true=slot,
                        runs_prefetch=runs_p, runs_urgent=runs_m, o_sparse=o_s, lse_sparse=l_s,
-                       o_window=o_w, lse_window=l_w, o=o, lse=lse)
+                       o_window=o_w, lse_window=l_w, o=o, lse=lse, o_spec=o_sp, lse_spec=l_sp)
 
 
 def decode_layer(k_packed, v_packed, q_bits, q_spec_bits, seq_lens, *, n_kv_heads: int,

@@ -58,13 +58,19 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return __ldg(reinter
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // D: head dim (64|128).  NR: 1 -> query rows 0..7 (r <= 8), 2 -> rows 0..15.
+#ifndef KVO_ATT_MINB_NR1
+#define KVO_ATT_MINB_NR1 4   // resident CTAs per SM requested for r <= 8 (caps registers at 128)
+#endif
+
 template <int D, int NR>
-__global__ void __launch_bounds__(ATT_WARPS * 32)
-attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
+__global__ void __launch_bounds__(ATT_WARPS * 32, NR == 1 ? KVO_ATT_MINB_NR1 : 2)
+attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec, const uint16_t* __restrict__ bk,
+            const uint16_t* __restrict__ bv,
             const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot,
             const int4* __restrict__ items, const int32_t* __restrict__ att_first, const int32_t* __restrict__ att_count,
             float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* __restrict__ done,
-            float* __restrict__ out_o, float* __restrict__ out_lse, int fuse, int batch, int r, int Hkv, int k,
+            float* __restrict__ out_o, float* __restrict__ out_lse, float* __restrict__ out_o_spec,
+            float* __restrict__ out_lse_spec, int fuse, int batch, int r, int Hkv, int k,
             int B, int W, float scale_log2, int32_t* __restrict__ status) {
     constexpr int KS = D / 16;          // k-steps of the QK^T contraction
     constexpr int CH = D / 32;          // 16-byte chunks per lane per key row
@@ -73,7 +79,7 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
 
     __shared__ float sm_m[ATT_WARPS][16];
     __shared__ float sm_l[ATT_WARPS][16];
-    __shared__ __align__(16) float sm_o[ATT_WARPS][16][D];
+    __shared__ __align__(16) float sm_o[ATT_WARPS][8 * NR][D];
     __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -83,13 +89,18 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
     const int b = bg / Hkv, gk = bg % Hkv;
     const int Hq = Hkv * r;
     const int n_tok = part == 0 ? k * B : W;
+    // query rows: the r heads of the group, then (co-batched) the r heads of the speculative query
+    const int nrows = q_spec ? 2 * r : r;
+    auto qrow = [&](int row) -> const uint16_t* {
+        return row < r ? q + ((int64_t)b * Hq + gk * r + row) * D : q_spec + ((int64_t)b * Hq + gk * r + row - r) * D;
+    };
 
     // ---- Q fragments (channel map shared with the K fragments)
     uint32_t qa0[KS], qa1[KS], qa2[KS], qa3[KS];
     {
-        const uint16_t* q0 = q + ((int64_t)b * Hq + gk * r + gq) * D;
-        const uint16_t* q1 = q + ((int64_t)b * Hq + gk * r + gq + 8) * D;
-        const bool v0 = gq < r, v1 = NR == 2 && gq + 8 < r;
+        const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
+        const uint16_t* q0 = v0 ? qrow(gq) : q;
+        const uint16_t* q1 = v1 ? qrow(gq + 8) : q;
 #pragma unroll
         for (int s = 0; s < CH; ++s) {
             const uint4 w0 = v0 ? ldg16(q0 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
@@ -99,9 +110,12 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
         }
     }
 
-    float acc[NT][4];
+    // NR == 1: only rows 0..7 exist, so only the c0/c1 accumulators are kept
+    float acc[NT][2 * NR];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2 * NR; ++e) acc[j][e] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     int bad = 0;
 
@@ -145,8 +159,14 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
                 const uint4 w = kf[nt][ks >> 1];
                 const uint32_t b0 = (ks & 1) ? w.z : w.x;
                 const uint32_t b1 = (ks & 1) ? w.w : w.y;
-                mma_bf16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa0[ks], qa1[ks], qa2[ks], qa3[ks], b0, b1,
-                               s[nt][0], s[nt][1], s[nt][2], s[nt][3]);
+                if constexpr (NR == 2) {
+                    mma_bf16_16816(s[nt][0], s[nt][1], s[nt][2], s[nt][3], qa0[ks], qa1[ks], qa2[ks], qa3[ks], b0,
+                                   b1, s[nt][0], s[nt][1], s[nt][2], s[nt][3]);
+                } else {
+                    float d2, d3;
+                    mma_bf16_16816(s[nt][0], s[nt][1], d2, d3, qa0[ks], 0u, qa2[ks], 0u, b0, b1, s[nt][0], s[nt][1],
+                                   0.f, 0.f);
+                }
             }
         }
         // ---- online softmax (log2 domain); lane holds tokens 2t, 2t+1 of each n8 tile
@@ -203,8 +223,14 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
                     const uint32_t sel = hi ? 0x7632u : 0x5410u;
                     const uint32_t b0 = __byte_perm(va[w], vb[w], sel);
                     const uint32_t b1 = __byte_perm(vc[w], vd[w], sel);
-                    mma_bf16_16816(acc[j][0], acc[j][1], acc[j][2], acc[j][3], pa0, pa1, pa2, pa3, b0, b1,
-                                   acc[j][0] * al0, acc[j][1] * al0, acc[j][2] * al1, acc[j][3] * al1);
+                    if constexpr (NR == 2) {
+                        mma_bf16_16816(acc[j][0], acc[j][1], acc[j][2], acc[j][3], pa0, pa1, pa2, pa3, b0, b1,
+                                       acc[j][0] * al0, acc[j][1] * al0, acc[j][2] * al1, acc[j][3] * al1);
+                    } else {
+                        float d2, d3;
+                        mma_bf16_16816(acc[j][0], acc[j][1], d2, d3, pa0, 0u, pa2, 0u, b0, b1, acc[j][0] * al0,
+                                       acc[j][1] * al0, 0.f, 0.f);
+                    }
                 }
             }
         }
@@ -225,14 +251,14 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
         // column 2t of n-tile j is channel CPT*2t + j; column 2t+1 is CPT*(2t+1) + j
         sm_o[warp][gq][CPT * (2 * tq) + j] = acc[j][0];
         sm_o[warp][gq][CPT * (2 * tq + 1) + j] = acc[j][1];
-        if (NR == 2) {
+        if constexpr (NR == 2) {
             sm_o[warp][gq + 8][CPT * (2 * tq) + j] = acc[j][2];
             sm_o[warp][gq + 8][CPT * (2 * tq + 1) + j] = acc[j][3];
         }
     }
     __syncthreads();
     const int64_t item = blockIdx.x;
-    for (int e = tid; e < r * D; e += blockDim.x) {
+    for (int e = tid; e < nrows * D; e += blockDim.x) {
         const int row = e / D, c = e - row * D;
         float M = -INFINITY;
 #pragma unroll
@@ -246,10 +272,10 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
                 l += sc * sm_l[w][row];
             }
         }
-        part_o[(item * r + row) * D + c] = a;
+        part_o[(item * nrows + row) * D + c] = a;
         if (c == 0) {
-            part_ml[(item * r + row) * 2 + 0] = M;
-            part_ml[(item * r + row) * 2 + 1] = l;
+            part_ml[(item * nrows + row) * 2 + 0] = M;
+            part_ml[(item * nrows + row) * 2 + 1] = l;
         }
     }
     __threadfence();
@@ -265,23 +291,26 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
     // ---- last CTA of the group: merge each part, then fuse the two parts
     const int first = att_first[bg], cnt = att_count[bg];
     const int64_t rows_total = (int64_t)batch * Hq;
-    for (int e = tid; e < r * D; e += blockDim.x) {
+    for (int e = tid; e < nrows * D; e += blockDim.x) {
         const int row = e / D, c = e - row * D;
         float Mp[2] = {-INFINITY, -INFINITY};
         for (int i = first; i < first + cnt; ++i) {
             const int pp = items[i].y;
-            Mp[pp] = fmaxf(Mp[pp], __ldcg(part_ml + ((int64_t)i * r + row) * 2));
+            Mp[pp] = fmaxf(Mp[pp], __ldcg(part_ml + ((int64_t)i * nrows + row) * 2));
         }
         float Lp[2] = {0.f, 0.f}, Ap[2] = {0.f, 0.f};
         for (int i = first; i < first + cnt; ++i) {
             const int pp = items[i].y;
-            const float mi = __ldcg(part_ml + ((int64_t)i * r + row) * 2);
+            const float mi = __ldcg(part_ml + ((int64_t)i * nrows + row) * 2);
             if (mi == -INFINITY) continue;
             const float sc = ex2f(mi - Mp[pp]);
-            Lp[pp] += sc * __ldcg(part_ml + ((int64_t)i * r + row) * 2 + 1);
-            Ap[pp] += sc * __ldcg(part_o + ((int64_t)i * r + row) * D + c);
+            Lp[pp] += sc * __ldcg(part_ml + ((int64_t)i * nrows + row) * 2 + 1);
+            Ap[pp] += sc * __ldcg(part_o + ((int64_t)i * nrows + row) * D + c);
         }
-        const int64_t orow = (int64_t)b * Hq + gk * r + row;
+        const bool spec_row = row >= r;
+        const int64_t orow = (int64_t)b * Hq + gk * r + (spec_row ? row - r : row);
+        float* dst_o = spec_row ? out_o_spec : out_o;
+        float* dst_lse = spec_row ? out_lse_spec : out_lse;
         if (fuse) {
             const float M = fmaxf(Mp[0], Mp[1]);
             float o = 0.f, lse = -INFINITY;
@@ -292,8 +321,8 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
                 o = (w0 * Ap[0] + w1 * Ap[1]) / L;
                 lse = (M + lg2f(L)) * kLn2;
             }
-            out_o[orow * D + c] = o;
-            if (c == 0) out_lse[orow] = lse;
+            dst_o[orow * D + c] = o;
+            if (c == 0) dst_lse[orow] = lse;
         } else {
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp) {
@@ -302,28 +331,29 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk, con
                     o = Ap[pp] / Lp[pp];
                     lse = (Mp[pp] + lg2f(Lp[pp])) * kLn2;
                 }
-                out_o[(pp * rows_total + orow) * D + c] = o;
-                if (c == 0) out_lse[pp * rows_total + orow] = lse;
+                dst_o[(pp * rows_total + orow) * D + c] = o;
+                if (c == 0) dst_lse[pp * rows_total + orow] = lse;
             }
         }
     }
     if (tid == 0) done[bg] = 0u;
 }
 
-cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const int32_t* slot, float* o,
-                             float* lse, int fuse, cudaStream_t s) {
+cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
+                             float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
+    const int nrows = q_spec ? 2 * c.r : c.r;
 #define KVO_ATT(D_, NR_)                                                                                         \
     attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
-        (const uint16_t*)q, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items, c.att_first, c.att_count,       \
-        c.att_part_o, c.att_part_ml, c.att_done, o, lse, fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, scale_log2,   \
-        c.status)
+        (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items,       \
+        c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,      \
+        c.batch, c.r, c.Hkv, c.k, c.B, c.W, scale_log2, c.status)
     if (c.d == 128) {
-        if (c.r <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);
+        if (nrows <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);
     } else {
-        if (c.r <= 8) KVO_ATT(64, 1); else KVO_ATT(64, 2);
+        if (nrows <= 8) KVO_ATT(64, 1); else KVO_ATT(64, 2);
     }
 #undef KVO_ATT
     return cudaGetLastError();
@@ -484,9 +514,9 @@ extern "C" kvo_status sparse_decode_attn_static(const void* q, const void* k_buf
         const int fuse = fuse_window_merge ? 1 : 0;
 #define KVO_ATT_STATIC(D_, NR_)                                                                                  \
         attn_kernel<D_, NR_><<<(unsigned)n_items, ATT_WARPS * 32, 0, s>>>(                                        \
-            (const uint16_t*)q, (const uint16_t*)k_buf, (const uint16_t*)v_buf, wk, wv, slot_of_true, items,     \
-            first, count, part_o, part_ml, done, o, lse, fuse, batch, r, n_kv_heads, top_k, block_size, window,  \
-            scale_log2, st)
+            (const uint16_t*)q, nullptr, (const uint16_t*)k_buf, (const uint16_t*)v_buf, wk, wv, slot_of_true,  \
+            items, first, count, part_o, part_ml, done, o, lse, nullptr, nullptr, fuse, batch, r, n_kv_heads,    \
+            top_k, block_size, window, scale_log2, st)
         if (head_dim == 128) {
             if (r <= 8) KVO_ATT_STATIC(128, 1); else KVO_ATT_STATIC(128, 2);
         } else {

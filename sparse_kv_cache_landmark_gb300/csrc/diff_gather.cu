@@ -12,6 +12,8 @@
 // [0, k) hold the prefetched prediction in list order, slots [k, 2k) the
 // urgent misses in list order.  A run of n adjacent block ids is one
 // contiguous range of n*B*d bf16 on both the host and the device side.
+#include <algorithm>
+
 #include "kvo_internal.cuh"
 
 namespace kvo {
@@ -171,12 +173,110 @@ gather_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh, 
     }
 }
 
+// Flat variant: the index list itself is the copy plan.  Entry j of group bg
+// (block idx[bg][j], j < cnt[bg]) goes to slot slot_base + j, so a run of
+// adjacent block ids is one contiguous source range and one contiguous
+// destination range.  Persistent warps walk chunks of 32*U 16-byte words of
+// one group's entry stream (K and V): no per-run dependency chain, and a
+// warp's metadata loads hit one or two cache lines.  The launch may reserve
+// shared memory it never uses so that each gather CTA has its SM to itself:
+// the other kernels then never queue their HBM loads behind zero-copy loads
+// waiting on the host link in the same SM's load/store pipeline.
+template <int U, bool POW2>
+__global__ void __launch_bounds__(1024)
+gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh,
+                   const int64_t* __restrict__ g_off, const int32_t* __restrict__ g_C,
+                   const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int slot_base,
+                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int G, int k, int B, int D, int words_log2,
+                   int32_t* __restrict__ status) {
+    constexpr uint32_t CHUNK = 32 * U;                       // words per warp iteration
+    const uint32_t words = (uint32_t)B * D / 8;             // 16-byte words per block
+    const uint32_t per_group = ((uint32_t)k * words + CHUNK - 1) / CHUNK;   // chunks per group
+    const int64_t total = (int64_t)G * per_group;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    int bad = 0;
+    for (int64_t ch = warp; ch < total; ch += n_warps) {
+        const int bg = (int)(ch / per_group);
+        const uint32_t c0 = (uint32_t)(ch - (int64_t)bg * per_group) * CHUNK;
+        int n = cnt ? cnt[bg] : k;
+        if (n < 0 || n > k) { bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
+        const uint32_t lim = (uint32_t)n * words;
+        if (c0 >= lim) continue;
+        const int C = g_C[bg];
+        const int64_t src0 = g_off[bg];
+        const int64_t dst0 = ((int64_t)bg * 2 * k + slot_base) * B * D;
+        const int32_t* ig = idx + (int64_t)bg * k;
+        uint4 a[U], b[U];
+        int64_t to[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t i = c0 + u * 32 + lane;
+            ok[u] = false;
+            if (i < lim) {
+                const uint32_t j = POW2 ? (i >> words_log2) : (i / words);
+                const uint32_t w = i - j * words;
+                const int32_t blk = __ldg(ig + j);
+                if (blk >= 0 && blk < C) {
+                    const int64_t off = (int64_t)blk * B * D + 8 * (int64_t)w;
+                    a[u] = *reinterpret_cast<const uint4*>(kh + src0 + off);
+                    b[u] = *reinterpret_cast<const uint4*>(vh + src0 + off);
+                    to[u] = dst0 + (int64_t)j * B * D + 8 * (int64_t)w;
+                    ok[u] = true;
+                } else {
+                    bad |= KVO_DEV_BAD_BLOCK_ID;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (ok[u]) {
+                *reinterpret_cast<uint4*>(dk + to[u]) = a[u];
+                *reinterpret_cast<uint4*>(dv + to[u]) = b[u];
+            }
+    }
+    if (bad) atomicOr(status, bad);
+}
+
+cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
+                               cudaStream_t s) {
+    const uint32_t words = (uint32_t)c.B * c.d / 8;
+    int lg = -1;
+    if ((words & (words - 1)) == 0) { lg = 0; while ((1u << lg) < words) ++lg; }
+    const int ctas = c.gather_ctas > 0 ? c.gather_ctas : 2 * 152;
+    const int th = c.gather_threads;
+    const size_t smem = (size_t)c.gather_reserve_smem;
+#define KVO_FLAT(U_, P_)                                                                                          \
+    gather_flat_kernel<U_, P_><<<ctas, th, smem, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, idx, cnt, \
+                                                      slot_base, c.pp_k[buf], c.pp_v[buf], c.G, c.k, c.B, c.d, lg, \
+                                                      c.status)
+    if (lg >= 0) { if (c.gather_unroll >= 2) KVO_FLAT(2, true); else KVO_FLAT(1, true); }
+    else { if (c.gather_unroll >= 2) KVO_FLAT(2, false); else KVO_FLAT(1, false); }
+#undef KVO_FLAT
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_gather_flat() {
+    const int mx = 227 * 1024;
+    cudaError_t e = cudaFuncSetAttribute(gather_flat_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gather_flat_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gather_flat_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gather_flat_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    return e;
+}
+
 int gather_default_ctas(const Ctx& c) {
     return c.gather_ctas > 0 ? c.gather_ctas : 2 * 152;
 }
 
 cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                           cudaStream_t s) {
+    if (c.gather_engine == 1) return launch_gather_tma(c, layer, buf, runs, nruns, s);
     const int ctas = gather_default_ctas(c), th = c.gather_threads;
 #define KVO_GATHER(U_)                                                                                          \
     gather_kernel<U_><<<ctas, th, 0, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, (const int4*)runs, \

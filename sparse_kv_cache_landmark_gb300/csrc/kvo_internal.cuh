@@ -14,12 +14,16 @@ namespace kvo {
 
 // ---------------------------------------------------------------- tunables
 constexpr int SEL_THREADS = 256;          // select: threads per CTA
-constexpr int SEL_RPT = 4;                // select: landmark rows per thread
-constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;   // rows per work item
+constexpr int SEL_RPT_MAX = 4;            // select: landmark rows per thread (1 or 4, chosen at init)
 constexpr int ATT_WARPS = 4;              // attention: warps per CTA
 constexpr int ATT_TILE = 16;              // attention: tokens per mma tile
 constexpr int ATT_TILES_PER_ITEM = 16;    // attention: tiles per CTA work item
 constexpr int GATHER_THREADS = 256;
+constexpr int TMA_STAGE_BYTES = 16384;    // TMA gather: bytes per batch
+constexpr int TMA_MAX_PIECES = 64;        // TMA gather: pieces per batch
+__host__ __device__ constexpr size_t tma_driver_smem(int stages) {
+    return (size_t)stages * TMA_STAGE_BYTES + (size_t)stages * TMA_MAX_PIECES * 24 + (size_t)stages * 12 + 16;
+}
 
 // ------------------------------------------------------------------ context
 struct Ctx {
@@ -45,6 +49,7 @@ struct Ctx {
     int2* sel_items = nullptr;      // {group, chunk}
     int32_t* sel_nchunks = nullptr; // [G]
     int n_sel_items = 0;
+    int sel_rpt = 4;                // rows per thread of the selection kernel
     // coalesce scratch: [2 (prefetch|urgent)][G][k][4], [2][G]
     int32_t* runs = nullptr;
     int32_t* nruns = nullptr;
@@ -58,6 +63,10 @@ struct Ctx {
     uint32_t* att_done = nullptr;   // [G]
     int32_t* status = nullptr;      // device status word
     int gather_ctas = 0, gather_threads = 128, gather_unroll = 1;   // gather launch shape (0: default)
+    int gather_engine = 0;          // 0: lane loads over runs, 1: TMA bulk copies, 3: flat lane loads over entries
+    int gather_drivers = 0;         // TMA engine: driver warps (0: default)
+    int gather_stages = 4;          // TMA engine: batches per driver (4 or 8)
+    int gather_reserve_smem = 0;    // flat engine: shared memory reserved per CTA (0: none)
     size_t scratch_bytes = 0;
     cudaStream_t s_compute = nullptr, s_prefetch = nullptr, s_urgent = nullptr;
     // decode-step state
@@ -73,9 +82,15 @@ struct Ctx {
     // optional per-launch timing of the decode step (kvo_profile)
     bool prof_on = false;
     std::vector<cudaEvent_t> prof_pool;
-    struct ProfRec { int kind; int ev; };
+    struct ProfRec { int kind; int ev; int layer; };
     std::vector<ProfRec> prof_recs;
     int prof_used = 0;
+    // CUDA-graph replay of warm decode steps (one executable graph per step parity)
+    bool use_graphs = false;
+    cudaStream_t s_graph = nullptr;
+    cudaEvent_t ev_gin = nullptr, ev_gout = nullptr;
+    cudaGraphExec_t gexec[2] = {nullptr, nullptr};
+    const void* gkey[2][6] = {};
     std::string err;
 };
 
@@ -132,13 +147,20 @@ cudaError_t launch_coalesce(const Ctx& c, const int32_t* idx, const int32_t* cnt
                             int32_t* nruns, cudaStream_t s);
 cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                           cudaStream_t s);
-cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const int32_t* slot, float* o,
-                             float* lse, int fuse, cudaStream_t s);
+cudaError_t launch_gather_tma(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
+                              cudaStream_t s);
+cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
+                               cudaStream_t s);
+cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
+                             float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s);
 cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
                              float* lse, int rows, int d, cudaStream_t s);
 cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s);
 
 int gather_default_ctas(const Ctx& c);
+// Raise the dynamic shared memory limits of the gather kernels (host call; done at init, never during capture).
+cudaError_t prepare_gather_tma();
+cudaError_t prepare_gather_flat();
 
 // Sets the message kvo_last_error(NULL) returns (context-free calls).
 void set_last_error(const char* msg);

@@ -64,8 +64,11 @@ void free_ctx(kvo::Ctx& c) {
     for (auto* v : {&c.ev_sel, &c.ev_attn, &c.ev_pref, &c.ev_urg})
         for (cudaEvent_t e : *v) if (e) cudaEventDestroy(e);
     if (c.ev_start) cudaEventDestroy(c.ev_start);
+    if (c.ev_gin) cudaEventDestroy(c.ev_gin);
+    if (c.ev_gout) cudaEventDestroy(c.ev_gout);
+    for (cudaGraphExec_t g : c.gexec) if (g) cudaGraphExecDestroy(g);
     for (cudaEvent_t e : c.prof_pool) if (e) cudaEventDestroy(e);
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) if (s) cudaStreamDestroy(s);
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph}) if (s) cudaStreamDestroy(s);
 }
 
 // Records a timing event on `s` when profiling is on; returns its pool index or -1.
@@ -182,8 +185,15 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaMemsetAsync(c.sel_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
     std::vector<int2> sel_items;
     std::vector<int32_t> nch(c.G);
+    // 1024 rows per CTA, or 256 when that leaves fewer than ~8 CTAs per SM
+    {
+        int64_t n4 = 0;
+        for (int g = 0; g < c.G; ++g) n4 += (C[g] + kvo::SEL_THREADS * 4 - 1) / (kvo::SEL_THREADS * 4);
+        c.sel_rpt = n4 < 8 * 152 ? 1 : 4;
+    }
+    const int sel_rows = kvo::SEL_THREADS * c.sel_rpt;
     for (int g = 0; g < c.G; ++g) {
-        nch[g] = (C[g] + kvo::SEL_ROWS - 1) / kvo::SEL_ROWS;
+        nch[g] = (C[g] + sel_rows - 1) / sel_rows;
         for (int j = 0; j < nch[g]; ++j) sel_items.push_back(make_int2(g, j));
     }
     c.n_sel_items = (int)sel_items.size();
@@ -214,8 +224,9 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaMemcpy(c.att_items, att.data(), sizeof(int4) * att.size(), cudaMemcpyHostToDevice));
     KVO_CUDA(&c, cudaMemcpy(c.att_first, afirst.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
     KVO_CUDA(&c, cudaMemcpy(c.att_count, acount.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
-    KVO_CUDA(&c, dalloc(&c.att_part_o, sizeof(float) * att.size() * c.r * c.d, &sb));
-    KVO_CUDA(&c, dalloc(&c.att_part_ml, sizeof(float) * att.size() * c.r * 2, &sb));
+    const int att_rows = 2 * c.r <= 16 ? 2 * c.r : c.r;   // room for co-batched speculative rows
+    KVO_CUDA(&c, dalloc(&c.att_part_o, sizeof(float) * att.size() * att_rows * c.d, &sb));
+    KVO_CUDA(&c, dalloc(&c.att_part_ml, sizeof(float) * att.size() * att_rows * 2, &sb));
     KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * c.G, &sb));
     KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
     KVO_CUDA(&c, dalloc(&c.status, sizeof(int32_t), &sb));
@@ -235,6 +246,11 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     c.ev_pref.assign(2, nullptr);
     for (auto& e : c.ev_pref) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
+    KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_gin, cudaEventDisableTiming));
+    KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_gout, cudaEventDisableTiming));
+    KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_graph, cudaStreamNonBlocking, (least + greatest) / 2));
+    KVO_CUDA(&c, kvo::prepare_gather_tma());
+    KVO_CUDA(&c, kvo::prepare_gather_flat());
     KVO_CUDA(&c, cudaStreamSynchronize(c.s_compute));
     return KVO_OK;
 }
@@ -266,7 +282,7 @@ kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* con
 
 kvo_status kv_offload_destroy(kvo_ctx* ctx) {
     if (!ctx) return KVO_OK;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent})
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph})
         if (s) cudaStreamSynchronize(s);
     free_ctx(ctx->c);
     delete ctx;
@@ -307,7 +323,10 @@ kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx
     int32_t* runs = runs_out ? runs_out : c.runs + (size_t)u * 4 * c.G * c.k;
     int32_t* nruns = n_runs_out ? n_runs_out : c.nruns + (size_t)u * c.G;
     KVO_CUDA(&c, kvo::launch_coalesce(c, idx, cnt, slot_base, runs, nruns, s));
-    KVO_CUDA(&c, kvo::launch_gather(c, layer, buf, runs, nruns, s));
+    if (c.gather_engine == 3)
+        KVO_CUDA(&c, kvo::launch_gather_flat(c, layer, buf, idx, cnt, slot_base, s));
+    else
+        KVO_CUDA(&c, kvo::launch_gather(c, layer, buf, runs, nruns, s));
     return KVO_OK;
 }
 
@@ -318,8 +337,8 @@ kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q, c
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
     if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
     if (!q || !slot_of_true || !o || !lse) return fail(&c, KVO_ERR_INVALID, "null pointer argument");
-    KVO_CUDA(&c, kvo::launch_attention(c, layer, buf, q, slot_of_true, o, lse, fuse_window_merge ? 1 : 0,
-                                       pick(c, stream)));
+    KVO_CUDA(&c, kvo::launch_attention(c, layer, buf, q, nullptr, slot_of_true, o, lse, nullptr, nullptr,
+                                       fuse_window_merge ? 1 : 0, pick(c, stream)));
     return KVO_OK;
 }
 
@@ -334,12 +353,11 @@ kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const 
     return KVO_OK;
 }
 
-kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
-                           kvo_stream_t stream) {
-    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+// Enqueues one decode step ordered after `s_user` (which waits for all of it).
+// Host state (parity, prediction) is not changed here.
+static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                                   float* o_spec, float* lse_spec, cudaStream_t s_user) {
     kvo::Ctx& c = ctx->c;
-    if (!q || !o || !lse) return fail(&c, KVO_ERR_INVALID, "null q, o or lse");
-    cudaStream_t s_user = pick(c, stream);
     const size_t gk = (size_t)c.G * c.k;
     const size_t q_layer = (size_t)c.batch * c.Hq * c.d;
     const size_t o_layer = q_layer, lse_layer = (size_t)c.batch * c.Hq;
@@ -355,6 +373,7 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
     KVO_CUDA(&c, cudaEventRecord(c.ev_start, s_user));
     for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, c.ev_start, 0));
     // launch wrapper: timing events around the launch when profiling is on
+    int cur_layer = -1;
     auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
         int e0, e1;
         cudaError_t e = prof_mark(c, s, &e0);
@@ -364,19 +383,27 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
         e = prof_mark(c, s, &e1);
         if (e != cudaSuccess) return e;
         if (e0 >= 0) {
-            c.prof_recs.push_back({kind, e0});
-            c.prof_recs.push_back({-1, e1});
+            c.prof_recs.push_back({kind, e0, cur_layer});
+            c.prof_recs.push_back({-1, e1, cur_layer});
         }
         return cudaSuccess;
     };
 
     // prefetch of a layer: the prediction list into slots [0, k) of its half
     auto prefetch = [&](int layer, int buf, const int32_t* pred, cudaEvent_t after) -> kvo_status {
+        cur_layer = layer;
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_prefetch, after, 0));
-        KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_prefetch,
-                           [&] { return kvo::launch_coalesce(c, pred, nullptr, 0, runs_pf, nruns_pf, c.s_prefetch); }));
-        KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
-                           [&] { return kvo::launch_gather(c, layer, buf, runs_pf, nruns_pf, c.s_prefetch); }));
+        if (c.gather_engine == 3) {
+            KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch, [&] {
+                return kvo::launch_gather_flat(c, layer, buf, pred, nullptr, 0, c.s_prefetch);
+            }));
+        } else {
+            KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_prefetch, [&] {
+                return kvo::launch_coalesce(c, pred, nullptr, 0, runs_pf, nruns_pf, c.s_prefetch);
+            }));
+            KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
+                               [&] { return kvo::launch_gather(c, layer, buf, runs_pf, nruns_pf, c.s_prefetch); }));
+        }
         KVO_CUDA(&c, cudaEventRecord(c.ev_pref[buf], c.s_prefetch));
         return KVO_OK;
     };
@@ -388,6 +415,7 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
     pref_ready[half_of(0)] = have;
     if (c.L >= 2) pref_ready[half_of(1)] = have;
     for (int l = 0; l < c.L; ++l) {
+        cur_layer = l;
         const int buf = half_of(l);
         const void* ql = (const char*)q + l * q_layer * 2;
         const void* qsl = q_spec ? (const char*)q_spec + l * q_layer * 2 : nullptr;
@@ -410,17 +438,26 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
             if (st) return st;
         }
         // 3. urgent gather of the misses into slots [k, 2k)
+        cur_layer = l;
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, c.ev_sel[l], 0));
-        KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_urgent,
-                           [&] { return kvo::launch_coalesce(c, miss, mcnt, c.k, runs_ur, nruns_ur, c.s_urgent); }));
-        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
-                           [&] { return kvo::launch_gather(c, l, buf, runs_ur, nruns_ur, c.s_urgent); }));
+        if (c.gather_engine == 3) {
+            KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
+                               [&] { return kvo::launch_gather_flat(c, l, buf, miss, mcnt, c.k, c.s_urgent); }));
+        } else {
+            KVO_CUDA(&c, timed(kvo::PK_COALESCE, c.s_urgent, [&] {
+                return kvo::launch_coalesce(c, miss, mcnt, c.k, runs_ur, nruns_ur, c.s_urgent);
+            }));
+            KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
+                               [&] { return kvo::launch_gather(c, l, buf, runs_ur, nruns_ur, c.s_urgent); }));
+        }
         KVO_CUDA(&c, cudaEventRecord(c.ev_urg[l], c.s_urgent));
         // 4. attention once the misses and this half's prefetch have landed
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_urg[l], 0));
         if (pref_ready[buf]) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_pref[buf], 0));
         KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
-            return kvo::launch_attention(c, l, buf, ql, slot, o + l * o_layer, lse + l * lse_layer, 1, c.s_compute);
+            return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
+                                         lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute);
         }));
         KVO_CUDA(&c, cudaEventRecord(c.ev_attn[l], c.s_compute));
         pref_ready[buf] = false;
@@ -444,14 +481,93 @@ kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, floa
         KVO_CUDA(&c, cudaEventRecord(c.ev_start, s));
         KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_start, 0));
     }
+    return KVO_OK;
+}
+
+static void drop_graphs(kvo::Ctx& c) {
+    for (auto& g : c.gexec)
+        if (g) { cudaGraphExecDestroy(g); g = nullptr; }
+}
+
+static kvo_status decode_step_impl(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                                   float* o_spec, float* lse_spec, kvo_stream_t stream) {
+    kvo::Ctx& c = ctx->c;
+    cudaStream_t s_user = pick(c, stream);
+    if (c.use_graphs && c.have_pred && !c.prof_on) {
+        const int par = c.step_parity;
+        const void* key[6] = {q, q_spec, o, lse, o_spec, lse_spec};
+        bool same = c.gexec[par] != nullptr;
+        for (int i = 0; i < 6 && same; ++i) same = c.gkey[par][i] == key[i];
+        if (!same) {
+            if (c.gexec[par]) { cudaGraphExecDestroy(c.gexec[par]); c.gexec[par] = nullptr; }
+            KVO_CUDA(&c, cudaStreamBeginCapture(c.s_graph, cudaStreamCaptureModeThreadLocal));
+            kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, c.s_graph);
+            cudaGraph_t g = nullptr;
+            cudaError_t e = cudaStreamEndCapture(c.s_graph, &g);
+            if (st != KVO_OK) { if (g) cudaGraphDestroy(g); return st; }
+            if (e != cudaSuccess) return cuda_fail(&c, e, "cudaStreamEndCapture(decode step)");
+            e = cudaGraphInstantiate(&c.gexec[par], g, 0);
+            cudaGraphDestroy(g);
+            if (e != cudaSuccess) { c.gexec[par] = nullptr; return cuda_fail(&c, e, "cudaGraphInstantiate(decode step)"); }
+            for (int i = 0; i < 6; ++i) c.gkey[par][i] = key[i];
+        }
+        KVO_CUDA(&c, cudaEventRecord(c.ev_gin, s_user));
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
+        KVO_CUDA(&c, cudaGraphLaunch(c.gexec[par], c.s_graph));
+        KVO_CUDA(&c, cudaEventRecord(c.ev_gout, c.s_graph));
+        KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_gout, 0));
+    } else {
+        kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, s_user);
+        if (st != KVO_OK) return st;
+    }
     c.have_pred = true;
     c.step_parity ^= 1;
     return KVO_OK;
 }
 
+kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph})
+        cudaStreamSynchronize(s);
+    drop_graphs(ctx->c);
+    ctx->c.use_graphs = enable != 0;
+    return KVO_OK;
+}
+
+kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                           kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if (!q || !o || !lse) return fail(&ctx->c, KVO_ERR_INVALID, "null q, o or lse");
+    return decode_step_impl(ctx, q, q_spec, o, lse, nullptr, nullptr, stream);
+}
+
+kvo_status kvo_decode_step_dual(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                                float* o_spec, float* lse_spec, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!q || !q_spec || !o || !lse || !o_spec || !lse_spec) return fail(&c, KVO_ERR_INVALID, "null pointer argument");
+    if (2 * c.r > 16) return fail(&c, KVO_ERR_INVALID, "co-batching needs 2 * n_q_heads / n_kv_heads <= 16");
+    return decode_step_impl(ctx, q, q_spec, o, lse, o_spec, lse_spec, stream);
+}
+
+kvo_status sparse_decode_attn_cobatch(kvo_ctx* ctx, int layer, int buf, const void* q, const void* q_spec,
+                                      const int32_t* slot_of_true, float* o, float* lse, float* o_spec,
+                                      float* lse_spec, int fuse_window_merge, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
+    if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
+    if (!q || !q_spec || !slot_of_true || !o || !lse || !o_spec || !lse_spec)
+        return fail(&c, KVO_ERR_INVALID, "null pointer argument");
+    if (2 * c.r > 16) return fail(&c, KVO_ERR_INVALID, "co-batching needs 2 * n_q_heads / n_kv_heads <= 16");
+    KVO_CUDA(&c, kvo::launch_attention(c, layer, buf, q, q_spec, slot_of_true, o, lse, o_spec, lse_spec,
+                                       fuse_window_merge ? 1 : 0, pick(c, stream)));
+    return KVO_OK;
+}
+
 kvo_status kvo_reset_prediction(kvo_ctx* ctx) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
     ctx->c.have_pred = false;
     ctx->c.step_parity = 0;
     return KVO_OK;
@@ -505,12 +621,38 @@ kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4) {
 
 kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    if (ctas < 0 || ctas > 65535 || threads < 32 || threads > kvo::GATHER_THREADS || threads % 32 ||
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    drop_graphs(ctx->c);
+    const int max_threads = ctx->c.gather_engine == 3 ? 1024 : kvo::GATHER_THREADS;
+    if (ctas < 0 || ctas > 65535 || threads < 32 || threads > max_threads || threads % 32 ||
         (unroll != 1 && unroll != 2 && unroll != 4))
-        return fail(&ctx->c, KVO_ERR_INVALID, "need 0 <= ctas <= 65535, threads a multiple of 32 in [32, 256], unroll 1|2|4");
+        return fail(&ctx->c, KVO_ERR_INVALID,
+                    "need 0 <= ctas <= 65535, threads a multiple of 32 (<= 256; <= 1024 for engine 3), unroll 1|2|4");
     ctx->c.gather_ctas = ctas;
     ctx->c.gather_threads = threads;
     ctx->c.gather_unroll = unroll;
+    return KVO_OK;
+}
+
+kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    drop_graphs(ctx->c);
+    if (smem_bytes < 0 || smem_bytes > 227 * 1024) return fail(&ctx->c, KVO_ERR_INVALID, "0 <= smem_bytes <= 227 KiB");
+    ctx->c.gather_reserve_smem = smem_bytes;
+    return KVO_OK;
+}
+
+kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    drop_graphs(ctx->c);
+    // engine 1: 4 batches per driver; engine 2: 8 batches per driver (one driver per CTA)
+    if (engine < 0 || engine > 3 || drivers < 0 || drivers > 4096)
+        return fail(&ctx->c, KVO_ERR_INVALID, "engine must be 0..3 and 0 <= drivers <= 4096");
+    ctx->c.gather_engine = engine == 0 ? 0 : engine == 3 ? 3 : 1;
+    ctx->c.gather_stages = engine == 2 ? 8 : 4;
+    ctx->c.gather_drivers = drivers;
     return KVO_OK;
 }
 
@@ -538,6 +680,30 @@ kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out,
     }
     c.prof_recs.clear();
     c.prof_used = 0;
+    return KVO_OK;
+}
+
+kvo_status kvo_profile_trace(kvo_ctx* ctx, double* start_ms, double* end_ms, int32_t* kind, int32_t* layer,
+                             int cap, int* n_out) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!n_out || cap < 0 || (cap > 0 && (!start_ms || !end_ms || !kind || !layer)))
+        return fail(&c, KVO_ERR_INVALID, "bad trace output arguments");
+    const int n = (int)(c.prof_recs.size() / 2);
+    *n_out = n;
+    if (n == 0) return KVO_OK;
+    cudaEvent_t base = c.prof_pool[c.prof_recs[0].ev];
+    for (int i = 0; i < n && i < cap; ++i) {
+        cudaEvent_t a = c.prof_pool[c.prof_recs[2 * i].ev], b = c.prof_pool[c.prof_recs[2 * i + 1].ev];
+        KVO_CUDA(&c, cudaEventSynchronize(b));
+        float t0 = 0.f, t1 = 0.f;
+        KVO_CUDA(&c, cudaEventElapsedTime(&t0, base, a));
+        KVO_CUDA(&c, cudaEventElapsedTime(&t1, base, b));
+        start_ms[i] = t0;
+        end_ms[i] = t1;
+        kind[i] = c.prof_recs[2 * i].kind;
+        layer[i] = c.prof_recs[2 * i].layer;
+    }
     return KVO_OK;
 }
 

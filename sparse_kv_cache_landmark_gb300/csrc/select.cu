@@ -117,7 +117,7 @@ __device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, in
     __syncthreads();
 }
 
-template <int D, bool BF16LM, bool DUAL>
+template <int D, bool BF16LM, bool DUAL, int SEL_RPT>
 __global__ void __launch_bounds__(SEL_THREADS)
 select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
               const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
@@ -156,6 +156,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     __syncthreads();
 
     // ---- score SEL_RPT rows per thread (rows strided by the CTA width)
+    constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;
     const int row0 = chunk * SEL_ROWS + tid;
     float acc[NQ][SEL_RPT];
 #pragma unroll
@@ -319,9 +320,16 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
     const bool dual = q_spec != nullptr;
     const bool bf = c.B == 1;
 #define KVO_SEL(D_, BF_, DU_)                                                                                  \
-    select_kernel<D_, BF_, DU_><<<c.n_sel_items, SEL_THREADS, 0, s>>>(                                         \
-        c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C,          \
-        c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k)
+    do {                                                                                                       \
+        if (c.sel_rpt == 1)                                                                                    \
+            select_kernel<D_, BF_, DU_, 1><<<c.n_sel_items, SEL_THREADS, 0, s>>>(                              \
+                c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C,   \
+                c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k);  \
+        else                                                                                                   \
+            select_kernel<D_, BF_, DU_, 4><<<c.n_sel_items, SEL_THREADS, 0, s>>>(                              \
+                c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C,   \
+                c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k);  \
+    } while (0)
     if (c.d == 128) {
         if (bf) { if (dual) KVO_SEL(128, true, true); else KVO_SEL(128, true, false); }
         else    { if (dual) KVO_SEL(128, false, true); else KVO_SEL(128, false, false); }

@@ -17,12 +17,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvo.so")
 
 KVO_OK, KVO_ERR_INVALID, KVO_ERR_CUDA, KVO_ERR_OOM, KVO_ERR_TIMEOUT, KVO_ERR_STATE, KVO_ERR_DEVICE = range(7)
-DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_COUNT, DEV_UNSORTED = 1, 2, 4, 8
+DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_COUNT, DEV_UNSORTED, DEV_TIMEOUT = 1, 2, 4, 8, 16
 
 EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff", "gather_coalesced",
            "sparse_decode_attn", "merge_lse", "kvo_decode_step", "kvo_reset_prediction", "kvo_get_stream",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
-           "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape"]
+           "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
+           "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -58,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.sparse_decode_attn.argtypes = [P, I, I, VP, VP, VP, VP, I, VP]
         L.merge_lse.argtypes = [VP, VP, VP, VP, VP, VP, I, I, VP]
         L.kvo_decode_step.argtypes = [P, VP, VP, VP, VP, VP]
+        L.kvo_decode_step_dual.argtypes = [P, VP, VP, VP, VP, VP, VP, VP]
+        L.sparse_decode_attn_cobatch.argtypes = [P, I, I, VP, VP, VP, VP, VP, VP, VP, I, VP]
         L.kvo_reset_prediction.argtypes = [P]
         L.kvo_get_stream.argtypes = [P, I, ctypes.POINTER(P)]
         L.kvo_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), VP]
@@ -68,6 +71,11 @@ def lib() -> ctypes.CDLL:
         L.kvo_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I]
         L.sparse_decode_attn_static.argtypes = [VP, VP, VP, VP, VP, VP, VP, VP, VP] + [I] * 8 + [VP]
         L.kvo_set_gather_shape.argtypes = [P, I, I, I]
+        L.kvo_set_gather_engine.argtypes = [P, I, I]
+        L.kvo_set_gather_reserve.argtypes = [P, I]
+        L.kvo_set_graphs.argtypes = [P, I]
+        DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
+        L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
         L.kvo_last_error.argtypes = [P]
         L.kvo_last_error.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -214,6 +222,27 @@ class Context:
                                          int(bool(fuse_window_merge)), _stream(stream)))
         return o, lse
 
+    def sparse_decode_attn_cobatch(self, layer, buf, q, q_spec, slot_of_true, fuse_window_merge=True, stream=None):
+        """Co-batched attention of q and q_spec over the same blocks (C: sparse_decode_attn_cobatch)."""
+        rows = self.batch * self.n_q_heads
+        parts = 1 if fuse_window_merge else 2
+        mk = lambda *sh: torch.empty(*sh, dtype=torch.float32, device="cuda")
+        o, lse, os_, ls_ = mk(parts, rows, self.head_dim), mk(parts, rows), mk(parts, rows, self.head_dim), mk(parts, rows)
+        self._c(lib().sparse_decode_attn_cobatch(self.ctx, layer, buf, _ptr(q), _ptr(q_spec), _ptr(slot_of_true),
+                                                 _ptr(o), _ptr(lse), _ptr(os_), _ptr(ls_),
+                                                 int(bool(fuse_window_merge)), _stream(stream)))
+        return o, lse, os_, ls_
+
+    def decode_step_dual(self, q, q_spec, stream=None):
+        """Pipelined step with co-batched attention (C: kvo_decode_step_dual) -> (o, lse, o_spec, lse_spec)."""
+        rows = self.batch * self.n_q_heads
+        mk = lambda *sh: torch.empty(*sh, dtype=torch.float32, device="cuda")
+        o, lse = mk(self.n_layers, rows, self.head_dim), mk(self.n_layers, rows)
+        os_, ls_ = mk(self.n_layers, rows, self.head_dim), mk(self.n_layers, rows)
+        self._c(lib().kvo_decode_step_dual(self.ctx, _ptr(q), _ptr(q_spec), _ptr(o), _ptr(lse), _ptr(os_),
+                                           _ptr(ls_), _stream(stream)))
+        return o, lse, os_, ls_
+
     def decode_step(self, q, q_spec=None, o=None, lse=None, stream=None):
         """One pipelined decode step over every layer (C: kvo_decode_step)."""
         rows = self.batch * self.n_q_heads
@@ -247,6 +276,17 @@ class Context:
     def set_gather_shape(self, ctas: int = 0, threads: int = 256, unroll: int = 4):
         self._c(lib().kvo_set_gather_shape(self.ctx, ctas, threads, unroll))
 
+    def set_gather_engine(self, engine: int, drivers: int = 0):
+        """0: lane-load gather, 1: TMA bulk-copy gather with ``drivers`` driver warps."""
+        self._c(lib().kvo_set_gather_engine(self.ctx, engine, drivers))
+
+    def set_graphs(self, enable: bool):
+        """Replay warm decode steps from captured CUDA graphs (C: kvo_set_graphs)."""
+        self._c(lib().kvo_set_graphs(self.ctx, int(bool(enable))))
+
+    def set_gather_reserve(self, smem_bytes: int):
+        self._c(lib().kvo_set_gather_reserve(self.ctx, smem_bytes))
+
     def profile(self, enable: bool):
         self._c(lib().kvo_profile(self.ctx, int(bool(enable))))
 
@@ -257,6 +297,16 @@ class Context:
         cnt = (ctypes.c_int64 * n)()
         self._c(lib().kvo_profile_read(self.ctx, ms, cnt, n))
         return {k: (ms[i], cnt[i]) for i, k in enumerate(PROFILE_KINDS)}
+
+    def profile_trace(self):
+        """[(kind, layer, start_ms, end_ms)] of the recorded launches (before profile_read)."""
+        n = ctypes.c_int(0)
+        self._c(lib().kvo_profile_trace(self.ctx, None, None, None, None, 0, ctypes.byref(n)))
+        m = n.value
+        t0, t1 = (ctypes.c_double * m)(), (ctypes.c_double * m)()
+        kd, ly = (ctypes.c_int32 * m)(), (ctypes.c_int32 * m)()
+        self._c(lib().kvo_profile_trace(self.ctx, t0, t1, kd, ly, m, ctypes.byref(n)))
+        return [(PROFILE_KINDS[kd[i]], ly[i], t0[i], t1[i]) for i in range(m)]
 
     def landmarks(self, layer, stream=None):
         C = self.info()["C_max"]

@@ -124,6 +124,67 @@ def test_diff_gather_attention_chain(case):
             assert np.all(lse2[1, rows] == -np.inf) and not o2[1, rows].any()
 
 
+@pytest.mark.parametrize("engine,drivers", [(1, 1), (1, 3), (1, 32), (2, 5), (3, 0)])
+def test_gather_engines_bit_exact(case, engine, drivers):
+    """TMA bulk copies (engines 1, 2) and the flat lane-load gather (engine 3)
+    write the same bytes as the oracle's gather."""
+    c, refs = case
+    w = c.w
+    k = w.top_k
+    T, P = c.ctx.select_topk(0, c.q_dev(0), c.q_dev(0, spec=True))
+    if P is None:
+        P = T.clone()
+    miss, cnt, slot = c.ctx.index_diff(T, P)
+    c.ctx.set_gather_engine(engine, drivers)
+    try:
+        c.ctx.gather_coalesced(0, 0, P, None, slot_base=0)
+        c.ctx.gather_coalesced(0, 0, miss, cnt, slot_base=k, urgent=True)
+        torch.cuda.synchronize()
+        assert c.ctx.device_status() == 0
+    finally:
+        c.ctx.set_gather_engine(0, 0)
+    bufK, bufV = c.ctx.buffer(0)
+    bufK, bufV = synth.bits(bufK.cpu()), synth.bits(bufV.cpu())
+    for (b, g), ref in refs.items():
+        i = b * w.n_kv_heads + g
+        for kv, buf in (("k", bufK), ("v", bufV)):
+            exp, written = orc.gather_slots(synth.bits(c.rows(0, b, g, kv)), w.block_size,
+                                            ref.runs_prefetch + ref.runs_urgent, 2 * k)
+            assert np.array_equal(buf[i][written], exp[written]), (b, g, kv)
+
+
+def test_cobatched_attention(case):
+    """True and speculative queries in one attention pass (2r <= 16)."""
+    c, refs = case
+    w = c.w
+    if 2 * w.group_size > 16:
+        pytest.skip("co-batching needs 2r <= 16")
+    q = c.q_dev(0)
+    qs = c.q_dev(0, spec=True)
+    if qs is None:
+        qs = (q.float() * 0.5).to(torch.bfloat16)     # any second query works
+    T, _ = c.ctx.select_topk(0, q)
+    miss, cnt, slot = c.ctx.index_diff(T, None)
+    c.ctx.gather_coalesced(0, 0, miss, cnt, slot_base=w.top_k, urgent=True)
+    o1, l1 = c.ctx.sparse_decode_attn(0, 0, q, slot)
+    o2, l2 = c.ctx.sparse_decode_attn(0, 0, qs, slot)
+    o, lse, os_, ls_ = c.ctx.sparse_decode_attn_cobatch(0, 0, q, qs, slot)
+    torch.cuda.synchronize()
+    assert c.ctx.device_status() == 0
+    np.testing.assert_allclose(o.cpu().numpy(), o1.cpu().numpy(), rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(os_.cpu().numpy(), o2.cpu().numpy(), rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(ls_.cpu().numpy(), l2.cpu().numpy(), rtol=1e-5, atol=1e-5)
+    r = w.group_size
+    qs_bits = synth.bits(qs.cpu())
+    for (b, g), ref in refs.items():
+        rr = orc.decode_group(synth.bits(c.rows(0, b, g, "k")), synth.bits(c.rows(0, b, g, "v")),
+                              synth.bits(c.q[0][b, g * r:(g + 1) * r]), qs_bits[b, g * r:(g + 1) * r],
+                              block_size=w.block_size, top_k=w.top_k, window=w.window)
+        rows = slice(b * w.n_q_heads + g * r, b * w.n_q_heads + (g + 1) * r)
+        assert_attn_close(os_[0, rows].cpu().numpy(), rr.o_spec, what="o_spec")
+        assert_attn_close(ls_[0, rows].cpu().numpy(), rr.lse_spec, what="lse_spec")
+
+
 def test_merge_lse_matches_fused(case):
     from sparse_kv_cache_landmark_gb300.kvo import merge_lse
     c, refs = case

@@ -36,10 +36,13 @@ def _check(c, o, lse):
                 assert_attn_close(lse[l, rows], ref.lse, what=f"lse layer {l}")
 
 
-@pytest.mark.parametrize("L,spec", [(1, True), (4, True), (5, True), (3, False), (2, False)])
-def test_decode_step_cold_and_warm(L, spec):
+@pytest.mark.parametrize("L,spec,engine", [(1, True, 0), (4, True, 0), (5, True, 0), (3, False, 0), (2, False, 0),
+                                           (4, True, 1), (1, True, 1), (4, True, 3), (1, True, 3),
+                                           (3, False, 3)])
+def test_decode_step_cold_and_warm(L, spec, engine):
     c = _case(L, spec)
     try:
+        c.ctx.set_gather_engine(engine, 4 if engine else 0)
         q = c.q_stack()
         qs = c.q_stack(spec=True)
         outs = []
@@ -75,5 +78,54 @@ def test_decode_step_profile_counts_launches():
         assert prof["gather_urgent"][1] == L and prof["gather_prefetch"][1] == L
         assert prof["coalesce"][1] == 2 * L
         assert all(ms >= 0 for ms, _ in prof.values())
+    finally:
+        c.close()
+
+
+def test_decode_step_dual_cobatched():
+    c = _case(4, True)
+    try:
+        q, qs = c.q_stack(), c.q_stack(spec=True)
+        for step in range(2):
+            o, lse, os_, ls_ = c.ctx.decode_step_dual(q, qs)
+            torch.cuda.synchronize()
+            assert c.ctx.device_status() == 0
+            _check(c, o, lse)
+            w = c.w
+            r = w.group_size
+            on, ln = os_.cpu().numpy(), ls_.cpu().numpy()
+            for l in range(c.L):
+                for b in range(w.batch):
+                    for g in range(w.n_kv_heads):
+                        ref = c.oracle_group(l, b, g)
+                        rows = slice(b * w.n_q_heads + g * r, b * w.n_q_heads + (g + 1) * r)
+                        assert_attn_close(on[l, rows], ref.o_spec, what="o_spec")
+                        assert_attn_close(ln[l, rows], ref.lse_spec, what="lse_spec")
+    finally:
+        c.close()
+
+
+@pytest.mark.parametrize("L,spec,engine", [(4, True, 0), (1, True, 3), (3, False, 3)])
+def test_decode_step_graph_replay(L, spec, engine):
+    """Graph-replayed warm steps give the same outputs as stream-launched ones."""
+    c = _case(L, spec)
+    try:
+        c.ctx.set_gather_engine(engine, 0)
+        q, qs = c.q_stack(), c.q_stack(spec=True)
+        o0, l0 = c.ctx.decode_step(q, qs)
+        o1, l1 = c.ctx.decode_step(q, qs)
+        ref_o, ref_l = o1.clone(), l1.clone()
+        c.ctx.set_graphs(True)
+        o = torch.empty_like(o1)
+        lse = torch.empty_like(l1)
+        for step in range(5):                 # captures parity 0 and 1, then replays
+            o.fill_(float("nan"))
+            c.ctx.decode_step(q, qs, o, lse)
+            torch.cuda.synchronize()
+            assert c.ctx.device_status() == 0
+            np.testing.assert_allclose(o.cpu().numpy(), ref_o.cpu().numpy(), rtol=1e-5, atol=1e-5)
+            np.testing.assert_allclose(lse.cpu().numpy(), ref_l.cpu().numpy(), rtol=1e-5, atol=1e-5)
+        _check(c, o, lse)
+        c.ctx.set_graphs(False)
     finally:
         c.close()

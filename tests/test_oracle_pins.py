@@ -278,3 +278,23 @@ def test_prediction_never_changes_output():
         assert res.T.tolist() == base.T.tolist()
         np.testing.assert_array_equal(res.o, base.o)
         assert len(res.M) == len(set(base.T.tolist()) - set(pred))
+
+
+def test_cobatched_speculative_rows():
+    # the speculative query attends to the true selection plus the window
+    rng = np.random.default_rng(11)
+    B, C, W, d, r, k = 2, 10, 3, 8, 2, 4
+    n = C * B + W
+    K = rng.integers(-20, 20, size=(n, d)) / 8.0
+    V = rng.integers(-20, 20, size=(n, d)) / 8.0
+    q = rng.integers(-20, 20, size=(r, d)) / 8.0
+    qs = rng.integers(-20, 20, size=(r, d)) / 8.0
+    res = orc.decode_group(_bits(K), _bits(V), _bits(q), _bits(qs), block_size=B, top_k=k, window=W)
+    toks = np.concatenate([np.arange(x * B, (x + 1) * B) for x in res.T] + [np.arange(n - W, n)])
+    for h in range(r):
+        z = K[toks] @ qs[h] / math.sqrt(d)
+        np.testing.assert_allclose(res.o_spec[h], softmax(z) @ V[toks], atol=1e-12)
+        assert res.lse_spec[h] == pytest.approx(logsumexp(z), abs=1e-12)
+    same = orc.decode_group(_bits(K), _bits(V), _bits(q), _bits(q), block_size=B, top_k=k, window=W)
+    np.testing.assert_array_equal(same.o_spec, same.o)
+    assert orc.decode_group(_bits(K), _bits(V), _bits(q), None, block_size=B, top_k=k, window=W).o_spec is None
