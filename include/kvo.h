@@ -200,7 +200,10 @@ kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const 
  *   the prefetch of layer l+2's prediction is issued on the prefetch stream
  *   once layer l's attention has released its ping-pong half.  The first
  *   step after init has no prediction, so every block is a miss.  All work is
- *   ordered after `stream` and `stream` waits for all of it on return.
+ *   ordered after `stream`, and `stream` waits for the outputs; the prefetches
+ *   this step issues for the next step may still be in flight on return (the
+ *   next step orders itself after them; kvo_device_status, kvo_reset_prediction
+ *   and kv_offload_destroy synchronize them).
  */
 kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o,
                            float* lse, kvo_stream_t stream);
@@ -303,7 +306,10 @@ kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll)
  * sets KVO_DEV_TIMEOUT and stops.  engine 3: lane loads over the index list
  * itself, a flat stream of 16-byte words per group (entry j of a list goes to
  * slot base + j, so adjacent ids are read and written as contiguous ranges);
- * the decode step then skips building run lists.
+ * the decode step then skips building run lists.  Engine 3 is the default:
+ * 38 CTAs x 1024 threads, 2 loads of K and of V in flight per lane, 200 KiB of
+ * shared memory reserved per CTA so each gather CTA has an SM to itself.
+ * Selecting an engine resets the launch shape to that engine's default.
  */
 kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers);
 

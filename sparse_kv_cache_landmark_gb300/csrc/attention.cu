@@ -58,6 +58,9 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return __ldg(reinter
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // D: head dim (64|128).  NR: 1 -> query rows 0..7 (r <= 8), 2 -> rows 0..15.
+#ifndef KVO_ATT_PREFETCH
+#define KVO_ATT_PREFETCH 1   // prefetch each warp's next tile into L2
+#endif
 #ifndef KVO_ATT_MINB_NR1
 #define KVO_ATT_MINB_NR1 4   // resident CTAs per SM requested for r <= 8 (caps registers at 128)
 #endif
@@ -131,6 +134,17 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
 
     for (int tl = warp; tl < ntiles; tl += ATT_WARPS) {
         const int tb = (tile0 + tl) * ATT_TILE;
+        // pull this warp's next tile into L2 while the current one is computed:
+        // lane l takes token l & 15, K rows for l < 16 and V rows otherwise (2 lines each)
+        if (KVO_ATT_PREFETCH && tl + ATT_WARPS < ntiles) {
+            const int ntok = (tile0 + tl + ATT_WARPS) * ATT_TILE + (lane & 15);
+            if (ntok < n_tok) {
+                const uint16_t* p = row_ptr(lane < 16 ? bk : bv, lane < 16 ? wk : wv, ntok);
+#pragma unroll
+                for (int off = 0; off < D * 2; off += 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"((const char*)p + off));
+            }
+        }
         // ---- K rows g and 8+g of the tile
         uint4 kf[2][CH];
 #pragma unroll

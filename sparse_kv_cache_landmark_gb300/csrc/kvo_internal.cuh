@@ -62,11 +62,13 @@ struct Ctx {
     float* att_part_ml = nullptr;   // [items][r][2]
     uint32_t* att_done = nullptr;   // [G]
     int32_t* status = nullptr;      // device status word
-    int gather_ctas = 0, gather_threads = 128, gather_unroll = 1;   // gather launch shape (0: default)
-    int gather_engine = 0;          // 0: lane loads over runs, 1: TMA bulk copies, 3: flat lane loads over entries
+    // Gather launch shape and engine.  Default: the flat lane-load engine on 38
+    // SM-exclusive CTAs of 1024 threads, 2 loads of K and of V in flight per lane.
+    int gather_ctas = 38, gather_threads = 1024, gather_unroll = 2;
+    int gather_engine = 3;          // 0: lane loads over runs, 1: TMA bulk copies, 3: flat lane loads over entries
     int gather_drivers = 0;         // TMA engine: driver warps (0: default)
     int gather_stages = 4;          // TMA engine: batches per driver (4 or 8)
-    int gather_reserve_smem = 0;    // flat engine: shared memory reserved per CTA (0: none)
+    int gather_reserve_smem = 200 * 1024;   // flat engine: shared memory reserved per CTA (SM exclusivity)
     size_t scratch_bytes = 0;
     cudaStream_t s_compute = nullptr, s_prefetch = nullptr, s_urgent = nullptr;
     // decode-step state
@@ -77,8 +79,12 @@ struct Ctx {
     int32_t* st_slot = nullptr;     // [L][G][k]
     int step_parity = 0;
     bool have_pred = false;
-    std::vector<cudaEvent_t> ev_sel, ev_attn, ev_pref, ev_urg;
-    cudaEvent_t ev_start = nullptr;
+    // ordering events of the decode step; captured steps use their own set (an
+    // event recorded inside a capture cannot be waited on outside it)
+    struct EvSet {
+        std::vector<cudaEvent_t> sel, attn, pref, urg;
+        cudaEvent_t start = nullptr;
+    } ev_eager, ev_graph;
     // optional per-launch timing of the decode step (kvo_profile)
     bool prof_on = false;
     std::vector<cudaEvent_t> prof_pool;

@@ -61,9 +61,11 @@ void free_ctx(kvo::Ctx& c) {
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
     F(c.status);
     F(c.st_true); F(c.st_pred); F(c.st_miss); F(c.st_miss_cnt); F(c.st_slot);
-    for (auto* v : {&c.ev_sel, &c.ev_attn, &c.ev_pref, &c.ev_urg})
-        for (cudaEvent_t e : *v) if (e) cudaEventDestroy(e);
-    if (c.ev_start) cudaEventDestroy(c.ev_start);
+    for (auto* E : {&c.ev_eager, &c.ev_graph}) {
+        for (auto* v : {&E->sel, &E->attn, &E->pref, &E->urg})
+            for (cudaEvent_t e : *v) if (e) cudaEventDestroy(e);
+        if (E->start) cudaEventDestroy(E->start);
+    }
     if (c.ev_gin) cudaEventDestroy(c.ev_gin);
     if (c.ev_gout) cudaEventDestroy(c.ev_gout);
     for (cudaGraphExec_t g : c.gexec) if (g) cudaGraphExecDestroy(g);
@@ -239,13 +241,15 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, dalloc(&c.st_miss_cnt, sizeof(int32_t) * c.L * c.G, &sb));
     KVO_CUDA(&c, dalloc(&c.st_slot, sizeof(int32_t) * lgk, &sb));
     c.scratch_bytes = sb;
-    for (auto* v : {&c.ev_sel, &c.ev_attn, &c.ev_urg}) {
-        v->assign(c.L, nullptr);
-        for (auto& e : *v) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    for (auto* E : {&c.ev_eager, &c.ev_graph}) {
+        for (auto* v : {&E->sel, &E->attn, &E->urg}) {
+            v->assign(c.L, nullptr);
+            for (auto& e : *v) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        }
+        E->pref.assign(2, nullptr);
+        for (auto& e : E->pref) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        KVO_CUDA(&c, cudaEventCreateWithFlags(&E->start, cudaEventDisableTiming));
     }
-    c.ev_pref.assign(2, nullptr);
-    for (auto& e : c.ev_pref) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
-    KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_start, cudaEventDisableTiming));
     KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_gin, cudaEventDisableTiming));
     KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_gout, cudaEventDisableTiming));
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_graph, cudaStreamNonBlocking, (least + greatest) / 2));
@@ -356,8 +360,9 @@ kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const 
 // Enqueues one decode step ordered after `s_user` (which waits for all of it).
 // Host state (parity, prediction) is not changed here.
 static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
-                                   float* o_spec, float* lse_spec, cudaStream_t s_user) {
+                                   float* o_spec, float* lse_spec, cudaStream_t s_user, bool join_prefetch) {
     kvo::Ctx& c = ctx->c;
+    kvo::Ctx::EvSet& E = join_prefetch ? c.ev_graph : c.ev_eager;
     const size_t gk = (size_t)c.G * c.k;
     const size_t q_layer = (size_t)c.batch * c.Hq * c.d;
     const size_t o_layer = q_layer, lse_layer = (size_t)c.batch * c.Hq;
@@ -370,8 +375,8 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
     int32_t* runs_ur = c.runs + (size_t)4 * gk;
     int32_t* nruns_ur = c.nruns + c.G;
 
-    KVO_CUDA(&c, cudaEventRecord(c.ev_start, s_user));
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, c.ev_start, 0));
+    KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
     // launch wrapper: timing events around the launch when profiling is on
     int cur_layer = -1;
     auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
@@ -404,16 +409,20 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
             KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
                                [&] { return kvo::launch_gather(c, layer, buf, runs_pf, nruns_pf, c.s_prefetch); }));
         }
-        KVO_CUDA(&c, cudaEventRecord(c.ev_pref[buf], c.s_prefetch));
+        KVO_CUDA(&c, cudaEventRecord(E.pref[buf], c.s_prefetch));
         return KVO_OK;
     };
     // A prefetch into each half is outstanding at step start when the previous
     // step issued one (layers 0 and 1, or layer 0 when n_layers == 1).
     // Half of layer l: parity of the global layer index step * L + l.
     auto half_of = [&](int l) { return (c.step_parity * (c.L & 1) + l) & 1; };
+    // Inside a graph capture the previous step's prefetches are complete before
+    // the graph starts (the launch waits for the prefetch stream), and waiting
+    // on their events would tie the graph to work outside it.
+    const bool prior_pref = have && !join_prefetch;
     bool pref_ready[2] = {false, false};
-    pref_ready[half_of(0)] = have;
-    if (c.L >= 2) pref_ready[half_of(1)] = have;
+    pref_ready[half_of(0)] = prior_pref;
+    if (c.L >= 2) pref_ready[half_of(1)] = prior_pref;
     for (int l = 0; l < c.L; ++l) {
         cur_layer = l;
         const int buf = half_of(l);
@@ -431,15 +440,15 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
         KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_compute, [&] {
             return kvo::launch_index_diff(c, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, slot, c.s_compute);
         }));
-        KVO_CUDA(&c, cudaEventRecord(c.ev_sel[l], c.s_compute));
+        KVO_CUDA(&c, cudaEventRecord(E.sel[l], c.s_compute));
         // single-layer model: the next step's prefetch can start now, into the other half
         if (c.L == 1) {
-            kvo_status st = prefetch(l, buf ^ 1, pred_next + l * gk, c.ev_sel[l]);
+            kvo_status st = prefetch(l, buf ^ 1, pred_next + l * gk, E.sel[l]);
             if (st) return st;
         }
         // 3. urgent gather of the misses into slots [k, 2k)
         cur_layer = l;
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, c.ev_sel[l], 0));
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.sel[l], 0));
         if (c.gather_engine == 3) {
             KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
                                [&] { return kvo::launch_gather_flat(c, l, buf, miss, mcnt, c.k, c.s_urgent); }));
@@ -450,36 +459,40 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
             KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
                                [&] { return kvo::launch_gather(c, l, buf, runs_ur, nruns_ur, c.s_urgent); }));
         }
-        KVO_CUDA(&c, cudaEventRecord(c.ev_urg[l], c.s_urgent));
+        KVO_CUDA(&c, cudaEventRecord(E.urg[l], c.s_urgent));
         // 4. attention once the misses and this half's prefetch have landed
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_urg[l], 0));
-        if (pref_ready[buf]) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_pref[buf], 0));
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
+        if (pref_ready[buf]) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.pref[buf], 0));
         KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
             return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
                                          lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
                                          lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute);
         }));
-        KVO_CUDA(&c, cudaEventRecord(c.ev_attn[l], c.s_compute));
+        KVO_CUDA(&c, cudaEventRecord(E.attn[l], c.s_compute));
         pref_ready[buf] = false;
         // 5. this half is free: prefetch global layer l + 2
         if (c.L >= 2) {
             const int t = l + 2;
             if (t < c.L) {
                 if (have) {
-                    kvo_status st = prefetch(t, buf, pred_cur + t * gk, c.ev_attn[l]);
+                    kvo_status st = prefetch(t, buf, pred_cur + t * gk, E.attn[l]);
                     if (st) return st;
                     pref_ready[buf] = true;
                 }
             } else {
-                kvo_status st = prefetch(t - c.L, buf, pred_next + (t - c.L) * gk, c.ev_attn[l]);
+                kvo_status st = prefetch(t - c.L, buf, pred_next + (t - c.L) * gk, E.attn[l]);
                 if (st) return st;
             }
         }
     }
-    // the caller's stream waits for everything, including the next step's prefetches
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) {
-        KVO_CUDA(&c, cudaEventRecord(c.ev_start, s));
-        KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_start, 0));
+    // The caller's stream waits for the outputs (compute and urgent streams).
+    // The prefetches issued for the next step stay in flight: the next step's
+    // attention waits for them through ev_pref, and nothing before it reads or
+    // overwrites what they touch.  A graph capture joins them too.
+    for (cudaStream_t s : {c.s_compute, c.s_urgent, c.s_prefetch}) {
+        if (s == c.s_prefetch && !join_prefetch) break;
+        KVO_CUDA(&c, cudaEventRecord(E.start, s));
+        KVO_CUDA(&c, cudaStreamWaitEvent(s_user, E.start, 0));
     }
     return KVO_OK;
 }
@@ -501,7 +514,7 @@ static kvo_status decode_step_impl(kvo_ctx* ctx, const void* q, const void* q_sp
         if (!same) {
             if (c.gexec[par]) { cudaGraphExecDestroy(c.gexec[par]); c.gexec[par] = nullptr; }
             KVO_CUDA(&c, cudaStreamBeginCapture(c.s_graph, cudaStreamCaptureModeThreadLocal));
-            kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, c.s_graph);
+            kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, c.s_graph, true);
             cudaGraph_t g = nullptr;
             cudaError_t e = cudaStreamEndCapture(c.s_graph, &g);
             if (st != KVO_OK) { if (g) cudaGraphDestroy(g); return st; }
@@ -513,11 +526,14 @@ static kvo_status decode_step_impl(kvo_ctx* ctx, const void* q, const void* q_sp
         }
         KVO_CUDA(&c, cudaEventRecord(c.ev_gin, s_user));
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
+        // prefetches an earlier stream-launched step left in flight finish first
+        KVO_CUDA(&c, cudaEventRecord(c.ev_gin, c.s_prefetch));
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
         KVO_CUDA(&c, cudaGraphLaunch(c.gexec[par], c.s_graph));
         KVO_CUDA(&c, cudaEventRecord(c.ev_gout, c.s_graph));
         KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_gout, 0));
     } else {
-        kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, s_user);
+        kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, s_user, false);
         if (st != KVO_OK) return st;
     }
     c.have_pred = true;
@@ -651,6 +667,14 @@ kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
     if (engine < 0 || engine > 3 || drivers < 0 || drivers > 4096)
         return fail(&ctx->c, KVO_ERR_INVALID, "engine must be 0..3 and 0 <= drivers <= 4096");
     ctx->c.gather_engine = engine == 0 ? 0 : engine == 3 ? 3 : 1;
+    // each engine starts from its own default launch shape
+    if (engine == 3) {
+        ctx->c.gather_ctas = 38; ctx->c.gather_threads = 1024; ctx->c.gather_unroll = 2;
+        ctx->c.gather_reserve_smem = 200 * 1024;
+    } else {
+        ctx->c.gather_ctas = 0; ctx->c.gather_threads = 128; ctx->c.gather_unroll = 1;
+        ctx->c.gather_reserve_smem = 0;
+    }
     ctx->c.gather_stages = engine == 2 ? 8 : 4;
     ctx->c.gather_drivers = drivers;
     return KVO_OK;

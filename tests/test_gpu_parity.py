@@ -142,7 +142,7 @@ def test_gather_engines_bit_exact(case, engine, drivers):
         torch.cuda.synchronize()
         assert c.ctx.device_status() == 0
     finally:
-        c.ctx.set_gather_engine(0, 0)
+        c.ctx.set_gather_engine(3, 0)          # back to the default engine
     bufK, bufV = c.ctx.buffer(0)
     bufK, bufV = synth.bits(bufK.cpu()), synth.bits(bufV.cpu())
     for (b, g), ref in refs.items():
@@ -249,7 +249,12 @@ def test_bad_index_lists_set_the_status_word():
         c.ctx.index_diff(bad, None)
         assert c.ctx.device_status() & 1
         c.ctx.gather_coalesced(0, 0, bad, None, slot_base=0)
+        # the flat engine rejects the ids themselves, the run-walking engines the runs past C_b
+        assert c.ctx.device_status() & (1 | 2)
+        c.ctx.set_gather_engine(0, 0)
+        c.ctx.gather_coalesced(0, 0, bad, None, slot_base=0)
         assert c.ctx.device_status() & 2
+        c.ctx.set_gather_engine(3, 0)
         # descending ids: flagged as unsorted
         desc = torch.arange(k - 1, -1, -1, dtype=torch.int32, device="cuda").repeat(G, 1).contiguous()
         c.ctx.index_diff(desc, None)

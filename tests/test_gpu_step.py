@@ -36,13 +36,13 @@ def _check(c, o, lse):
                 assert_attn_close(lse[l, rows], ref.lse, what=f"lse layer {l}")
 
 
-@pytest.mark.parametrize("L,spec,engine", [(1, True, 0), (4, True, 0), (5, True, 0), (3, False, 0), (2, False, 0),
-                                           (4, True, 1), (1, True, 1), (4, True, 3), (1, True, 3),
-                                           (3, False, 3)])
+@pytest.mark.parametrize("L,spec,engine", [(1, True, 3), (4, True, 3), (5, True, 3), (3, False, 3), (2, False, 3),
+                                           (4, True, 0), (1, True, 0), (3, False, 0),
+                                           (4, True, 1), (1, True, 1)])
 def test_decode_step_cold_and_warm(L, spec, engine):
     c = _case(L, spec)
     try:
-        c.ctx.set_gather_engine(engine, 4 if engine else 0)
+        c.ctx.set_gather_engine(engine, 4 if engine == 1 else 0)
         q = c.q_stack()
         qs = c.q_stack(spec=True)
         outs = []
@@ -64,20 +64,27 @@ def test_decode_step_cold_and_warm(L, spec, engine):
         c.close()
 
 
-def test_decode_step_profile_counts_launches():
+@pytest.mark.parametrize("engine", [3, 0])
+def test_decode_step_profile_counts_launches(engine):
     c = _case(4, True)
     try:
+        c.ctx.set_gather_engine(engine, 0)
         q, qs = c.q_stack(), c.q_stack(spec=True)
         c.ctx.decode_step(q, qs)
         c.ctx.profile(True)
         c.ctx.decode_step(q, qs)
+        trace = c.ctx.profile_trace()
         prof = c.ctx.profile_read()
         c.ctx.profile(False)
         L = c.L
         assert prof["select"][1] == L and prof["diff"][1] == L and prof["attention"][1] == L
         assert prof["gather_urgent"][1] == L and prof["gather_prefetch"][1] == L
-        assert prof["coalesce"][1] == 2 * L
+        # the flat engine copies straight from the index lists; the others walk run lists
+        assert prof["coalesce"][1] == (0 if engine == 3 else 2 * L)
         assert all(ms >= 0 for ms, _ in prof.values())
+        assert len(trace) == sum(n for _, n in prof.values())
+        assert all(t1 >= t0 for _, _, t0, t1 in trace)
+        assert sorted({l for k, l, _, _ in trace if k == "attention"}) == list(range(L))
     finally:
         c.close()
 
@@ -127,5 +134,15 @@ def test_decode_step_graph_replay(L, spec, engine):
             np.testing.assert_allclose(lse.cpu().numpy(), ref_l.cpu().numpy(), rtol=1e-5, atol=1e-5)
         _check(c, o, lse)
         c.ctx.set_graphs(False)
+        for step in range(2):                 # stream-launched steps after graph steps
+            o2, l2 = c.ctx.decode_step(q, qs)
+            torch.cuda.synchronize()
+            np.testing.assert_allclose(o2.cpu().numpy(), ref_o.cpu().numpy(), rtol=1e-5, atol=1e-5)
+        c.ctx.set_graphs(True)                # and back to graphs with new output pointers
+        o3, l3 = c.ctx.decode_step(q, qs)
+        o3, l3 = c.ctx.decode_step(q, qs)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(o3.cpu().numpy(), ref_o.cpu().numpy(), rtol=1e-5, atol=1e-5)
+        assert c.ctx.device_status() == 0
     finally:
         c.close()
