@@ -74,6 +74,12 @@ def peaks():
     return 6800.0, "fallback"
 
 
+# DRAM bytes per launch of the default gather kernel from one ncu capture of a
+# 134.2 MB launch (profiles/gather_flat_kernel_llama3_8b_decode.md); reported
+# only for the launch shape and workload it was taken on.
+NCU_TRAFFIC = {("llama3_8b_decode", "gather_flat_kernel"): 72.669952e6 + 43.264e3}
+
+
 def workload_bytes(w, lens, misses_per_step=0):
     """Algorithmic bytes of one step (all layers): HBM and host link.
 
@@ -337,6 +343,9 @@ def run_ours(args):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
     torch.cuda.set_device(local)
+    # weak scaling: every rank serves its own batch of requests (its own seed),
+    # no data crosses ranks; only the timing is reduced (max over ranks)
+    args.seed = args.seed + 7919 * rank
     Bw = build_workload(args, ws)
     w, lens, n_host, ctx = Bw.w, Bw.lens, Bw.n_host, Bw.ctx
     q_pin, qs_pin, q_dev, qs_dev, o, lse = Bw.q_pin, Bw.qs_pin, Bw.q_dev, Bw.qs_dev, Bw.o, Bw.lse
@@ -427,6 +436,10 @@ def run_ours(args):
     if s_n:
         kernels["select"]["hbm_gbs"] = by["landmark_per_layer"] / (s_ms / s_n * 1e-3) / 1e9
 
+    gkern = ("gather_flat_kernel" if args.gather_engine in (-1, 3) else
+             "gather_tma_kernel" if args.gather_engine in (1, 2) else "gather_kernel")
+    default_shape = not (args.gather_ctas or args.gather_threads or args.gather_unroll or args.gather_reserve >= 0)
+    traffic = NCU_TRAFFIC.get((w.name, gkern)) if (default_shape and not args.layers and not args.batch) else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         t_group, n_groups = oracle_sample(w, args.seed, args.cpu_sample_s)
@@ -442,7 +455,8 @@ def run_ours(args):
             "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
                        "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.ctx[0],
                        "block": w.block_size, "top_k": w.top_k, "window": w.window, "layers": w.n_layers,
-                       "host_layers_distinct": n_host, "parallelism": f"replicas x{ws}",
+                       "host_layers_distinct": n_host,
+                       "parallelism": f"request-sharded x{ws}, each rank its own batch, no collective on the data path",
                        "l2": f"inputs larger than L2 (129 MB): every step moves {by['host'] / 1e9:.2f} GB over "
                              f"the host link and {by['hbm'] / 1e9:.2f} GB through HBM"},
             "effective_kv_gbs": by["kv_attended"] / (t_ms * 1e-3) / 1e9 * ws,
@@ -451,11 +465,13 @@ def run_ours(args):
                               "bound": "link" if t_link >= t_hbm else "hbm",
                               "host_bytes": by["host"], "hbm_bytes": by["hbm"], "link_gbs": link,
                               "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind},
-            "roofline": {"kernel": ("gather_flat_kernel" if args.gather_engine in (-1, 3) else
-                                    "gather_tma_kernel" if args.gather_engine in (1, 2) else "gather_kernel")
-                                   + " (prefetch)", "bound": "link",
+            "roofline": {"kernel": gkern + " (prefetch)", "bound": "link",
                          "achieved": achieved, "peak": link, "unit": "GB/s",
-                         "frac": (achieved / link) if achieved else None, "traffic": None,
+                         "frac": (achieved / link) if achieved else None,
+                         "traffic": traffic,
+                         "traffic_note": ("DRAM read+write bytes per launch from one ncu capture "
+                                          "(writes still in L2 at kernel end are not counted)") if traffic else
+                                         "no ncu capture of this kernel, shape and workload",
                          "peak_kind": "measured in this run: pinned cudaMemcpyAsync host->device, best of 3"},
             "kernels": kernels,
             "kernel_timing": ("CUDA events around each launch on its own stream, in a second timed pass "
