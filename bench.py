@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--gather-drivers", type=int, default=0, help="TMA engine driver warps (0: default)")
     ap.add_argument("--gather-reserve", type=int, default=-1, help="flat engine smem reservation per CTA (bytes)")
     ap.add_argument("--graphs", type=int, default=-1, help="1: replay warm steps from CUDA graphs (-1: default)")
+    ap.add_argument("--append", type=int, default=0,
+                    help="grow the cache: one kvo_append before every decode step (reserves this many tokens)")
     ap.add_argument("--gather-unroll", type=int, default=0, help="gather loads in flight per lane (0: default)")
     return ap.parse_args()
 
@@ -250,7 +252,11 @@ def build_workload(args, ws=1):
     if args.batch:
         w = w.scaled(batch=args.batch)
     lens = synth.seq_lens(w, args.seed)
-    n = synth.layer_numel(w, lens)
+    # with --append the host rows reserve `append` more tokens per group; the
+    # generator draws them too (the appended tokens), and they start zeroed
+    app = max(0, args.append)
+    gen_lens = [x + app for x in lens]
+    n = synth.layer_numel(w, gen_lens)
     layer_bytes = 2 * n * 2
     if args.host_layers:
         n_host = min(args.host_layers, w.n_layers)
@@ -267,6 +273,7 @@ def build_workload(args, ws=1):
         n_host = max(1, min(w.n_layers, fit))
     t_gen = time.perf_counter()
     k_host, v_host, k_win, v_win, qs_l, qspec_l = [], [], [], [], [], []
+    fut_k, fut_v = [], []
     for l in range(w.n_layers):
         q, qs = synth.gen_queries(w, args.seed, l)
         qs_l.append(q)
@@ -274,16 +281,24 @@ def build_workload(args, ws=1):
         if l < n_host:
             kh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
             vh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
-            synth.fill_layer(w, args.seed, l, kh, vh, q, lens, device="cuda")
+            synth.fill_layer(w, args.seed, l, kh, vh, q, gen_lens, device="cuda")
             k_host.append(kh)
             v_host.append(vh)
             kw = torch.empty(w.batch, w.n_kv_heads, w.window, w.head_dim, dtype=torch.bfloat16, device="cuda")
             vw = torch.empty_like(kw)
             off = 0
             for b, nb in enumerate(lens):
-                sz = nb * w.n_kv_heads * w.head_dim
-                kw[b] = kh[off:off + sz].view(w.n_kv_heads, nb, w.head_dim)[:, nb - w.window:].to("cuda")
-                vw[b] = vh[off:off + sz].view(w.n_kv_heads, nb, w.head_dim)[:, nb - w.window:].to("cuda")
+                cap = nb + app
+                sz = cap * w.n_kv_heads * w.head_dim
+                kr = kh[off:off + sz].view(w.n_kv_heads, cap, w.head_dim)
+                vr = vh[off:off + sz].view(w.n_kv_heads, cap, w.head_dim)
+                kw[b] = kr[:, nb - w.window:nb].to("cuda")
+                vw[b] = vr[:, nb - w.window:nb].to("cuda")
+                if app:
+                    fut_k.append((l, b, kr[:, nb:].to("cuda")))
+                    fut_v.append((l, b, vr[:, nb:].to("cuda")))
+                    kr[:, nb:] = 0
+                    vr[:, nb:] = 0
                 off += sz
             k_win.append(kw)
             v_win.append(vw)
@@ -296,7 +311,18 @@ def build_workload(args, ws=1):
     B.setup_s = time.perf_counter() - t_gen
     B.ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
                     block_size=w.block_size, top_k=w.top_k, window=w.window, n_layers=w.n_layers, seq_lens=lens,
-                    k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win)
+                    k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win, max_append=app)
+    B.app = app
+    B.app_used = 0
+    if app:
+        # future tokens as [append][L][b][Hkv][d]; layers past n_host reuse layer l % n_host
+        fk = torch.empty(app, w.n_layers, w.batch, w.n_kv_heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+        fv = torch.empty_like(fk)
+        for (l, b, t), (_, _, tv) in zip(fut_k, fut_v):
+            for ll in range(l, w.n_layers, n_host):
+                fk[:, ll, b] = t.permute(1, 0, 2)
+                fv[:, ll, b] = tv.permute(1, 0, 2)
+        B.fut_k, B.fut_v = fk, fv
     if args.gather_ctas or args.gather_threads or args.gather_unroll:
         B.ctx.set_gather_shape(args.gather_ctas, args.gather_threads or 128, args.gather_unroll or 1)
     if args.gather_engine >= 0:
@@ -327,6 +353,9 @@ def time_steps(B, steps, ws=1, profile=True):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(steps):
+        if B.app:
+            ctx.append(B.fut_k[B.app_used], B.fut_v[B.app_used])
+            B.app_used += 1
         ctx.decode_step(B.q_dev, B.qs_dev, B.o, B.lse)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -415,6 +444,33 @@ def run_ours(args):
         T, P = ctx.select_topk(l, q_dev[l], None if qs_dev is None else qs_dev[l])
         _, cnt, _ = ctx.index_diff(T, P if P is not None else T)
         misses += int(cnt.sum().item())
+    # co-batched dual-query attention (DualDecoder Fig. 18): the true and the
+    # speculative query in one pass vs two separate passes, layer 0's ping-pong half
+    cob = None
+    if 2 * w.group_size <= 16:
+        q0 = q_dev[0]
+        qs0 = qs_dev[0] if qs_dev is not None else (q0.float() * 0.5).to(torch.bfloat16)
+        T, _ = ctx.select_topk(0, q0)
+        miss, cnt, slot = ctx.index_diff(T, None)
+        ctx.gather_coalesced(0, 0, miss, cnt, slot_base=w.top_k, urgent=True)
+        torch.cuda.synchronize()
+
+        def _t(fn, n=20):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            b.record(stream)
+            b.synchronize()
+            return a.elapsed_time(b) / n * 1e3
+        two = _t(lambda: (ctx.sparse_decode_attn(0, 0, q0, slot), ctx.sparse_decode_attn(0, 0, qs0, slot)))
+        one = _t(lambda: ctx.sparse_decode_attn(0, 0, q0, slot))
+        co = _t(lambda: ctx.sparse_decode_attn_cobatch(0, 0, q0, qs0, slot))
+        cob = {"single_us": round(one, 2), "two_launches_us": round(two, 2), "cobatched_us": round(co, 2),
+               "cobatched_over_two": round(co / two, 3),
+               "note": "one layer's attention, isolated (no gather running), 20 back-to-back calls"}
     hbm_peak, peak_kind = peaks()
     by = workload_bytes(w, lens, misses)
     t_hbm = by["hbm"] / (hbm_peak * 1e9)
@@ -461,6 +517,7 @@ def run_ours(args):
                              f"the host link and {by['hbm'] / 1e9:.2f} GB through HBM"},
             "effective_kv_gbs": by["kv_attended"] / (t_ms * 1e-3) / 1e9 * ws,
             "urgent_misses_per_step": misses,
+            "cobatched_attention": cob,
             "step_roofline": {"t_star_ms": t_star * 1e3, "frac": t_star * 1e3 / t_ms,
                               "bound": "link" if t_link >= t_hbm else "hbm",
                               "host_bytes": by["host"], "hbm_bytes": by["hbm"], "link_gbs": link,
@@ -484,6 +541,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "device_status": status,
             "setup_s": round(t_gen, 1),
+            "append_per_step": bool(args.append),
             "gather_shape": {"ctas": args.gather_ctas or "default", "threads": args.gather_threads or "default",
                              "unroll": args.gather_unroll or "default",
                              "engine": "default" if args.gather_engine < 0 else args.gather_engine,

@@ -82,17 +82,24 @@ typedef struct {
     int32_t window;       /* W >= 0 recent tokens kept on the GPU */
     int32_t n_layers;     /* >= 1 */
     const int32_t* seq_lens; /* host [b]; len_b >= W, (len_b - W) % B == 0 */
+    int32_t max_append;   /* tokens each request may grow by through kvo_append (0: fixed cache).
+                             > 0 needs W > 0 and W % B == 0; the host arrays then reserve
+                             len_b + max_append rows per (request, KV head). */
 } kvo_config;
 
 /*
  * kv_offload_init -- build a context for one KV cache.
  *   k_host[l], v_host[l]: page-locked host memory that the device can address
  *       (cudaHostAlloc / torch pin_memory, or cudaHostRegister'ed), one per
- *       layer, packed request after request as [b][Hkv][len_b][d] bf16
- *       (request b starts at element (sum_{b'<b} len_b') * Hkv * d).  Caller-
- *       owned; must stay valid and unchanged until kv_offload_destroy.
+ *       layer, packed request after request as [b][Hkv][cap_b][d] bf16 with
+ *       cap_b = len_b + max_append (request b starts at element
+ *       (sum_{b'<b} cap_b') * Hkv * d; rows >= len_b are spare capacity that
+ *       kvo_append fills).  Caller-owned; must stay valid and unchanged (apart
+ *       from what kvo_append writes) until kv_offload_destroy.
  *   k_win[l], v_win[l]: device memory [b][Hkv][W][d] bf16 holding tokens
- *       [len_b - W, len_b) of each request (the recent window).  Caller-owned.
+ *       [len_b - W, len_b) of each request (the recent window).  Caller-owned;
+ *       with max_append > 0 they are copied into the library's window ring at
+ *       init and not read again.
  *   On success *out owns: the K landmarks of every layer (fp32 block means,
  *   or the bf16 key itself when B == 1; DualDecoder §4.1, Fig. 8), built here
  *   synchronously from k_host; the two ping-pong halves of K and V
@@ -227,6 +234,22 @@ kvo_status kvo_decode_step_dual(kvo_ctx* ctx, const void* q, const void* q_spec,
  * 0 (default): every step is launched stream by stream.
  */
 kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable);
+
+/*
+ * kvo_append -- grow every request by one decode token (needs max_append > 0).
+ *   k_new, v_new: device [n_layers][b][Hkv][d] bf16, the new token's key and
+ *   value per layer and KV head.  The token joins the GPU-resident recent
+ *   window (a library-owned ring of W + B tokens per layer and group, filled
+ *   from k_win / v_win at init).  When the window reaches W + B tokens its
+ *   oldest block leaves it: the B rows are written to the host cache (rows
+ *   C_b*B .. of the group) and the block's landmark (mean key; the key itself
+ *   for B == 1) becomes candidate block C_b, so C_b grows by one.  The
+ *   attended set of later calls is the candidates' top-k plus the whole
+ *   window (W to W + B - 1 tokens).  Ordered on `stream` like the other calls.
+ *   Errors: KVO_ERR_STATE when the context was built with max_append == 0 or
+ *   the reserved capacity is used up.
+ */
+kvo_status kvo_append(kvo_ctx* ctx, const void* k_new, const void* v_new, kvo_stream_t stream);
 
 /* Forget the predictions kept for the next step (next step starts cold). */
 kvo_status kvo_reset_prediction(kvo_ctx* ctx);

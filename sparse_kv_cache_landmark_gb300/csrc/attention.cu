@@ -74,7 +74,8 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
             float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* __restrict__ done,
             float* __restrict__ out_o, float* __restrict__ out_lse, float* __restrict__ out_o_spec,
             float* __restrict__ out_lse_spec, int fuse, int batch, int r, int Hkv, int k,
-            int B, int W, float scale_log2, int32_t* __restrict__ status) {
+            int B, int W, int Wcap, const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len,
+            float scale_log2, int32_t* __restrict__ status) {
     constexpr int KS = D / 16;          // k-steps of the QK^T contraction
     constexpr int CH = D / 32;          // 16-byte chunks per lane per key row
     constexpr int NT = D / 8;           // n-tiles of the PV product
@@ -91,7 +92,10 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
     const int bg = it.x, part = it.y, tile0 = it.z, ntiles = it.w;
     const int b = bg / Hkv, gk = bg % Hkv;
     const int Hq = Hkv * r;
-    const int n_tok = part == 0 ? k * B : W;
+    // window: W tokens from slot 0 of [Wcap] rows, or (appendable cache) w_len[bg]
+    // tokens of a ring of Wcap rows starting at slot w_start[bg]
+    const int ws = w_start ? w_start[bg] : 0;
+    const int n_tok = part == 0 ? k * B : (w_len ? w_len[bg] : W);
     // query rows: the r heads of the group, then (co-batched) the r heads of the speculative query
     const int nrows = q_spec ? 2 * r : r;
     auto qrow = [&](int row) -> const uint16_t* {
@@ -129,11 +133,14 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
             if (s < 0 || s >= 2 * k) { bad |= KVO_DEV_BAD_SLOT; s = 0; }
             return base_buf + (((int64_t)bg * 2 * k + s) * B + (tok - blk * B)) * D;
         }
-        return base_win + ((int64_t)bg * W + tok) * D;
+        int slot_w = ws + tok;
+        if (slot_w >= Wcap) slot_w -= Wcap;
+        return base_win + ((int64_t)bg * Wcap + slot_w) * D;
     };
 
     for (int tl = warp; tl < ntiles; tl += ATT_WARPS) {
         const int tb = (tile0 + tl) * ATT_TILE;
+        if (tb >= n_tok) break;                 // a shorter window than the items cover
         // pull this warp's next tile into L2 while the current one is computed:
         // lane l takes token l & 15, K rows for l < 16 and V rows otherwise (2 lines each)
         if (KVO_ATT_PREFETCH && tl + ATT_WARPS < ntiles) {
@@ -363,7 +370,7 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
         (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items,       \
         c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,      \
-        c.batch, c.r, c.Hkv, c.k, c.B, c.W, scale_log2, c.status)
+        c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
     if (c.d == 128) {
         if (nrows <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);
     } else {
@@ -530,7 +537,7 @@ extern "C" kvo_status sparse_decode_attn_static(const void* q, const void* k_buf
         attn_kernel<D_, NR_><<<(unsigned)n_items, ATT_WARPS * 32, 0, s>>>(                                        \
             (const uint16_t*)q, nullptr, (const uint16_t*)k_buf, (const uint16_t*)v_buf, wk, wv, slot_of_true,  \
             items, first, count, part_o, part_ml, done, o, lse, nullptr, nullptr, fuse, batch, r, n_kv_heads,    \
-            top_k, block_size, window, scale_log2, st)
+            top_k, block_size, window, window, nullptr, nullptr, scale_log2, st)
         if (head_dim == 128) {
             if (r <= 8) KVO_ATT_STATIC(128, 1); else KVO_ATT_STATIC(128, 2);
         } else {

@@ -36,7 +36,18 @@ struct Ctx {
     int64_t* g_off = nullptr;
     int32_t* g_C = nullptr;
     std::vector<const uint16_t*> k_host, v_host;   // device-addressable host pointers
-    std::vector<const uint16_t*> k_win, v_win;
+    std::vector<const uint16_t*> k_win, v_win;     // window per layer ([G][Wcap][d]; the ring in append mode)
+    int Wcap = 0;                   // window storage per group: W, or W + B in append mode
+    int max_append = 0, appended = 0;
+    int32_t* g_len = nullptr;       // [G] current context length (append mode)
+    int32_t* g_wstart = nullptr;    // [G] ring slot of the window's first token (append mode)
+    int32_t* g_wlen = nullptr;      // [G] window length (append mode)
+    std::vector<uint16_t*> ring_k, ring_v;   // library-owned window rings (append mode)
+    uint16_t** d_ring_k = nullptr;  // device copies of the per-layer pointer tables
+    uint16_t** d_ring_v = nullptr;
+    uint16_t** d_host_k = nullptr;
+    uint16_t** d_host_v = nullptr;
+    void** d_lm = nullptr;
     std::vector<void*> lm;                          // landmarks per layer
     size_t lm_bytes = 0;
     uint16_t* pp_k[2] = {nullptr, nullptr};
@@ -162,6 +173,8 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
 cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
                              float* lse, int rows, int d, cudaStream_t s);
 cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s);
+cudaError_t launch_ring_fill(const Ctx& c, int layer, const uint16_t* k_win, const uint16_t* v_win, cudaStream_t s);
+cudaError_t launch_append(const Ctx& c, const void* k_new, const void* v_new, cudaStream_t s);
 
 int gather_default_ctas(const Ctx& c);
 // Raise the dynamic shared memory limits of the gather kernels (host call; done at init, never during capture).

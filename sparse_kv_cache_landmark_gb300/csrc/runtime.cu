@@ -53,7 +53,10 @@ cudaError_t dalloc(T** p, size_t bytes, size_t* acc) {
 
 void free_ctx(kvo::Ctx& c) {
     auto F = [](void* p) { if (p) cudaFree(p); };
-    F(c.g_off); F(c.g_C);
+    F(c.g_off); F(c.g_C); F(c.g_len); F(c.g_wstart); F(c.g_wlen);
+    for (void* p : c.ring_k) F(p);
+    for (void* p : c.ring_v) F(p);
+    F(c.d_ring_k); F(c.d_ring_v); F(c.d_host_k); F(c.d_host_v); F(c.d_lm);
     for (void* p : c.lm) F(p);
     for (int i = 0; i < 2; ++i) { F(c.pp_k[i]); F(c.pp_v[i]); }
     F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
@@ -102,23 +105,35 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     if (c.B < 1 || c.k < 1 || c.k > 8192 || c.W < 0 || c.L < 1)
         return fail(&c, KVO_ERR_INVALID, "need block_size >= 1, 1 <= top_k <= 8192, window >= 0, n_layers >= 1");
     if (c.W > 0 && (!k_win || !v_win)) return fail(&c, KVO_ERR_INVALID, "window > 0 needs k_win and v_win");
+    c.max_append = cfg->max_append;
+    if (c.max_append < 0) return fail(&c, KVO_ERR_INVALID, "max_append must be >= 0");
+    if (c.max_append > 0 && (c.W == 0 || c.W % c.B))
+        return fail(&c, KVO_ERR_INVALID, "max_append > 0 needs window > 0 and window % block_size == 0");
+    c.Wcap = c.max_append > 0 ? c.W + c.B : c.W;
     c.G = c.batch * c.Hkv;
     c.lens.assign(cfg->seq_lens, cfg->seq_lens + c.batch);
     std::vector<int64_t> off(c.G);
-    std::vector<int32_t> C(c.G);
+    std::vector<int32_t> C(c.G), Ccap(c.G), glen(c.G), gws(c.G), gwl(c.G);
     int64_t tok = 0;
     for (int b = 0; b < c.batch; ++b) {
         const int64_t n = c.lens[b];
         if (n < c.W || (n - c.W) % c.B) return fail(&c, KVO_ERR_INVALID, "each len must be >= window with (len - window) % block_size == 0");
         const int64_t Cb = (n - c.W) / c.B;
+        const int64_t cap = n + c.max_append;            // rows reserved per (request, KV head)
+        const int64_t Cc = (cap - c.W) / c.B;            // most candidate blocks the request can reach
         if (Cb < c.k) return fail(&c, KVO_ERR_INVALID, "top_k exceeds the candidate blocks of a request");
-        if (Cb > (1 << 30)) return fail(&c, KVO_ERR_INVALID, "too many candidate blocks");
+        if (Cc > (1 << 30)) return fail(&c, KVO_ERR_INVALID, "too many candidate blocks");
         for (int g = 0; g < c.Hkv; ++g) {
-            off[b * c.Hkv + g] = (tok * c.Hkv + (int64_t)g * n) * c.d;
-            C[b * c.Hkv + g] = (int32_t)Cb;
+            const int i = b * c.Hkv + g;
+            off[i] = (tok * c.Hkv + (int64_t)g * cap) * c.d;
+            C[i] = (int32_t)Cb;
+            Ccap[i] = (int32_t)Cc;
+            glen[i] = (int32_t)n;
+            gws[i] = c.Wcap ? (int32_t)((Cb * c.B) % c.Wcap) : 0;
+            gwl[i] = c.W;
         }
-        c.Cmax = std::max<int>(c.Cmax, (int)Cb);
-        tok += n;
+        c.Cmax = std::max<int>(c.Cmax, (int)Cc);
+        tok += cap;
     }
     // host caches: page-locked and device-addressable
     for (int l = 0; l < c.L; ++l) {
@@ -161,6 +176,34 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, dalloc(&c.g_C, sizeof(int32_t) * c.G, &sb));
     KVO_CUDA(&c, cudaMemcpy(c.g_off, off.data(), sizeof(int64_t) * c.G, cudaMemcpyHostToDevice));
     KVO_CUDA(&c, cudaMemcpy(c.g_C, C.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    if (c.max_append > 0) {
+        KVO_CUDA(&c, dalloc(&c.g_len, sizeof(int32_t) * c.G, &sb));
+        KVO_CUDA(&c, dalloc(&c.g_wstart, sizeof(int32_t) * c.G, &sb));
+        KVO_CUDA(&c, dalloc(&c.g_wlen, sizeof(int32_t) * c.G, &sb));
+        KVO_CUDA(&c, cudaMemcpy(c.g_len, glen.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+        KVO_CUDA(&c, cudaMemcpy(c.g_wstart, gws.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+        KVO_CUDA(&c, cudaMemcpy(c.g_wlen, gwl.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+        // window rings, filled from the caller's windows
+        const size_t ring_bytes = (size_t)c.G * c.Wcap * c.d * sizeof(uint16_t);
+        c.ring_k.assign(c.L, nullptr);
+        c.ring_v.assign(c.L, nullptr);
+        for (int l = 0; l < c.L; ++l) {
+            KVO_CUDA(&c, dalloc(&c.ring_k[l], ring_bytes, &sb));
+            KVO_CUDA(&c, dalloc(&c.ring_v[l], ring_bytes, &sb));
+            KVO_CUDA(&c, kvo::launch_ring_fill(c, l, c.k_win[l], c.v_win[l], c.s_compute));
+            c.k_win[l] = c.ring_k[l];
+            c.v_win[l] = c.ring_v[l];
+        }
+        KVO_CUDA(&c, dalloc(&c.d_ring_k, sizeof(void*) * c.L, &sb));
+        KVO_CUDA(&c, dalloc(&c.d_ring_v, sizeof(void*) * c.L, &sb));
+        KVO_CUDA(&c, dalloc(&c.d_host_k, sizeof(void*) * c.L, &sb));
+        KVO_CUDA(&c, dalloc(&c.d_host_v, sizeof(void*) * c.L, &sb));
+        KVO_CUDA(&c, dalloc(&c.d_lm, sizeof(void*) * c.L, &sb));
+        KVO_CUDA(&c, cudaMemcpy(c.d_ring_k, c.ring_k.data(), sizeof(void*) * c.L, cudaMemcpyHostToDevice));
+        KVO_CUDA(&c, cudaMemcpy(c.d_ring_v, c.ring_v.data(), sizeof(void*) * c.L, cudaMemcpyHostToDevice));
+        KVO_CUDA(&c, cudaMemcpy(c.d_host_k, c.k_host.data(), sizeof(void*) * c.L, cudaMemcpyHostToDevice));
+        KVO_CUDA(&c, cudaMemcpy(c.d_host_v, c.v_host.data(), sizeof(void*) * c.L, cudaMemcpyHostToDevice));
+    }
     // landmarks
     c.lm_bytes = (size_t)c.G * c.Cmax * c.d * (c.B > 1 ? 4 : 2);
     c.lm.assign(c.L, nullptr);
@@ -169,6 +212,8 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, cudaMemsetAsync(c.lm[l], 0, c.lm_bytes, c.s_compute));
         KVO_CUDA(&c, kvo::launch_landmarks(c, l, c.s_compute));
     }
+    if (c.max_append > 0)
+        KVO_CUDA(&c, cudaMemcpy(c.d_lm, c.lm.data(), sizeof(void*) * c.L, cudaMemcpyHostToDevice));
     // ping-pong halves
     const size_t half = (size_t)c.G * 2 * c.k * c.B * c.d * sizeof(uint16_t);
     for (int i = 0; i < 2; ++i) {
@@ -190,12 +235,12 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     // 1024 rows per CTA, or 256 when that leaves fewer than ~8 CTAs per SM
     {
         int64_t n4 = 0;
-        for (int g = 0; g < c.G; ++g) n4 += (C[g] + kvo::SEL_THREADS * 4 - 1) / (kvo::SEL_THREADS * 4);
+        for (int g = 0; g < c.G; ++g) n4 += (Ccap[g] + kvo::SEL_THREADS * 4 - 1) / (kvo::SEL_THREADS * 4);
         c.sel_rpt = n4 < 8 * 152 ? 1 : 4;
     }
     const int sel_rows = kvo::SEL_THREADS * c.sel_rpt;
     for (int g = 0; g < c.G; ++g) {
-        nch[g] = (C[g] + sel_rows - 1) / sel_rows;
+        nch[g] = (Ccap[g] + sel_rows - 1) / sel_rows;     // rows past the current C_b are skipped
         for (int j = 0; j < nch[g]; ++j) sel_items.push_back(make_int2(g, j));
     }
     c.n_sel_items = (int)sel_items.size();
@@ -210,7 +255,8 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     std::vector<int4> att;
     std::vector<int32_t> afirst(c.G), acount(c.G);
     const int sp_tiles = (c.k * c.B + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
-    const int w_tiles = (c.W + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;   // the window may grow to W + B - 1
+    const int w_tiles = (w_max + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
     for (int g = 0; g < c.G; ++g) {
         afirst[g] = (int)att.size();
         for (int t = 0; t < sp_tiles; t += kvo::ATT_TILES_PER_ITEM)
@@ -578,6 +624,17 @@ kvo_status sparse_decode_attn_cobatch(kvo_ctx* ctx, int layer, int buf, const vo
     if (2 * c.r > 16) return fail(&c, KVO_ERR_INVALID, "co-batching needs 2 * n_q_heads / n_kv_heads <= 16");
     KVO_CUDA(&c, kvo::launch_attention(c, layer, buf, q, q_spec, slot_of_true, o, lse, o_spec, lse_spec,
                                        fuse_window_merge ? 1 : 0, pick(c, stream)));
+    return KVO_OK;
+}
+
+kvo_status kvo_append(kvo_ctx* ctx, const void* k_new, const void* v_new, kvo_stream_t stream) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!k_new || !v_new) return fail(&c, KVO_ERR_INVALID, "null k_new or v_new");
+    if (c.max_append == 0) return fail(&c, KVO_ERR_STATE, "context built with max_append == 0");
+    if (c.appended >= c.max_append) return fail(&c, KVO_ERR_STATE, "append capacity used up");
+    KVO_CUDA(&c, kvo::launch_append(c, k_new, v_new, pick(c, stream)));
+    ++c.appended;
     return KVO_OK;
 }
 

@@ -23,7 +23,7 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "sparse_decode_attn", "merge_lse", "kvo_decode_step", "kvo_reset_prediction", "kvo_get_stream",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
-           "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs"]
+           "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -37,7 +37,7 @@ class _Config(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("n_layers", ctypes.c_int32),
-                ("seq_lens", ctypes.POINTER(ctypes.c_int32))]
+                ("seq_lens", ctypes.POINTER(ctypes.c_int32)), ("max_append", ctypes.c_int32)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_gather_engine.argtypes = [P, I, I]
         L.kvo_set_gather_reserve.argtypes = [P, I]
         L.kvo_set_graphs.argtypes = [P, I]
+        L.kvo_append.argtypes = [P, VP, VP, VP]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
         L.kvo_last_error.argtypes = [P]
@@ -156,10 +157,12 @@ class Context:
 
     def __init__(self, *, batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers,
                  seq_lens: Sequence[int], k_host: List[torch.Tensor], v_host: List[torch.Tensor],
-                 k_win: Optional[List[torch.Tensor]] = None, v_win: Optional[List[torch.Tensor]] = None):
+                 k_win: Optional[List[torch.Tensor]] = None, v_win: Optional[List[torch.Tensor]] = None,
+                 max_append: int = 0):
         L = lib()
         self._lens = (ctypes.c_int32 * batch)(*[int(x) for x in seq_lens])
-        self.cfg = _Config(batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers, self._lens)
+        self.cfg = _Config(batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers, self._lens,
+                           max_append)
         self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim = batch, n_q_heads, n_kv_heads, head_dim
         self.block_size, self.top_k, self.window, self.n_layers = block_size, top_k, window, n_layers
         self.G = batch * n_kv_heads
@@ -252,6 +255,10 @@ class Context:
             lse = torch.empty(self.n_layers, rows, dtype=torch.float32, device="cuda")
         self._c(lib().kvo_decode_step(self.ctx, _ptr(q), _ptr(q_spec), _ptr(o), _ptr(lse), _stream(stream)))
         return o, lse
+
+    def append(self, k_new, v_new, stream=None):
+        """Grow every request by one token (C: kvo_append); k_new, v_new: CUDA bf16 [L][b][Hkv][d]."""
+        self._c(lib().kvo_append(self.ctx, _ptr(k_new), _ptr(v_new), _stream(stream)))
 
     def reset_prediction(self):
         self._c(lib().kvo_reset_prediction(self.ctx))

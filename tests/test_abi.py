@@ -43,7 +43,7 @@ def _cfg(kvo, **kw):
     base.update(kw)
     lens = (ctypes.c_int32 * max(base["batch"], 1))(*([16 * 20 + 16] * max(base["batch"], 1)))
     return kvo._Config(base["batch"], base["n_q_heads"], base["n_kv_heads"], base["head_dim"], base["block_size"],
-                       base["top_k"], base["window"], base["n_layers"], lens), lens
+                       base["top_k"], base["window"], base["n_layers"], lens, base.get("max_append", 0)), lens
 
 
 @pytest.mark.parametrize("kw,frag", [
@@ -54,6 +54,8 @@ def _cfg(kvo, **kw):
     (dict(top_k=0), "top_k"),
     (dict(top_k=21), "top_k exceeds"),
     (dict(block_size=7), "block_size == 0"),
+    (dict(max_append=-1), "max_append"),
+    (dict(max_append=8, window=24), "window % block_size"),
 ])
 def test_init_rejects_bad_configs_on_the_host(lib, kw, frag):
     from sparse_kv_cache_landmark_gb300 import kvo
