@@ -24,6 +24,7 @@
 #include <math.h>
 
 #include "kvo_internal.cuh"
+#include "tma_ptx.cuh"
 
 namespace kvo {
 
@@ -65,49 +66,18 @@ constexpr float kLn2 = 0.69314718055994530942f;
 #define KVO_ATT_MINB_NR1 4   // resident CTAs per SM requested for r <= 8 (caps registers at 128)
 #endif
 
+// One warp's online-softmax state over 16-token tiles, and the tile math shared
+// by both attention kernels.  Lane (g, t): K fragments are 16-byte chunks of key
+// rows g and 8+g at channels 32s + 8t; V fragments are d/8 channels (d/8)g ..
+// of value rows 2t, 2t+1, 2t+8, 2t+9 of the tile.
 template <int D, int NR>
-__global__ void __launch_bounds__(ATT_WARPS * 32, NR == 1 ? KVO_ATT_MINB_NR1 : 2)
-attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec, const uint16_t* __restrict__ bk,
-            const uint16_t* __restrict__ bv,
-            const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot,
-            const int4* __restrict__ items, const int32_t* __restrict__ att_first, const int32_t* __restrict__ att_count,
-            float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* __restrict__ done,
-            float* __restrict__ out_o, float* __restrict__ out_lse, float* __restrict__ out_o_spec,
-            float* __restrict__ out_lse_spec, int fuse, int batch, int r, int Hkv, int k,
-            int B, int W, int Wcap, const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len,
-            float scale_log2, int32_t* __restrict__ status) {
-    constexpr int KS = D / 16;          // k-steps of the QK^T contraction
-    constexpr int CH = D / 32;          // 16-byte chunks per lane per key row
-    constexpr int NT = D / 8;           // n-tiles of the PV product
-    constexpr int CPT = D / 8;          // channels per lane in PV (== NT)
-
-    __shared__ float sm_m[ATT_WARPS][16];
-    __shared__ float sm_l[ATT_WARPS][16];
-    __shared__ __align__(16) float sm_o[ATT_WARPS][8 * NR][D];
-    __shared__ int s_last;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, tq = lane & 3;
-    const int4 it = items[blockIdx.x];
-    const int bg = it.x, part = it.y, tile0 = it.z, ntiles = it.w;
-    const int b = bg / Hkv, gk = bg % Hkv;
-    const int Hq = Hkv * r;
-    // window: W tokens from slot 0 of [Wcap] rows, or (appendable cache) w_len[bg]
-    // tokens of a ring of Wcap rows starting at slot w_start[bg]
-    const int ws = w_start ? w_start[bg] : 0;
-    const int n_tok = part == 0 ? k * B : (w_len ? w_len[bg] : W);
-    // query rows: the r heads of the group, then (co-batched) the r heads of the speculative query
-    const int nrows = q_spec ? 2 * r : r;
-    auto qrow = [&](int row) -> const uint16_t* {
-        return row < r ? q + ((int64_t)b * Hq + gk * r + row) * D : q_spec + ((int64_t)b * Hq + gk * r + row - r) * D;
-    };
-
-    // ---- Q fragments (channel map shared with the K fragments)
+struct WarpAttn {
+    static constexpr int KS = D / 16, CH = D / 32, NT = D / 8, CPT = D / 8;
     uint32_t qa0[KS], qa1[KS], qa2[KS], qa3[KS];
-    {
-        const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
-        const uint16_t* q0 = v0 ? qrow(gq) : q;
-        const uint16_t* q1 = v1 ? qrow(gq + 8) : q;
+    float acc[NT][2 * NR];   // NR == 1: only rows 0..7 exist, so only c0/c1 are kept
+    float m0, m1, l0, l1;
+
+    __device__ __forceinline__ void init(const uint16_t* q0, const uint16_t* q1, bool v0, bool v1, int tq) {
 #pragma unroll
         for (int s = 0; s < CH; ++s) {
             const uint4 w0 = v0 ? ldg16(q0 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
@@ -115,63 +85,16 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
             qa0[2 * s] = w0.x; qa2[2 * s] = w0.y; qa0[2 * s + 1] = w0.z; qa2[2 * s + 1] = w0.w;
             qa1[2 * s] = w1.x; qa3[2 * s] = w1.y; qa1[2 * s + 1] = w1.z; qa3[2 * s + 1] = w1.w;
         }
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2 * NR; ++e) acc[j][e] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
     }
 
-    // NR == 1: only rows 0..7 exist, so only the c0/c1 accumulators are kept
-    float acc[NT][2 * NR];
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2 * NR; ++e) acc[j][e] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    int bad = 0;
-
-    auto row_ptr = [&](const uint16_t* base_buf, const uint16_t* base_win, int tok) -> const uint16_t* {
-        if (part == 0) {
-            const int blk = tok / B;
-            int s = slot[(int64_t)bg * k + blk];
-            if (s < 0 || s >= 2 * k) { bad |= KVO_DEV_BAD_SLOT; s = 0; }
-            return base_buf + (((int64_t)bg * 2 * k + s) * B + (tok - blk * B)) * D;
-        }
-        int slot_w = ws + tok;
-        if (slot_w >= Wcap) slot_w -= Wcap;
-        return base_win + ((int64_t)bg * Wcap + slot_w) * D;
-    };
-
-    for (int tl = warp; tl < ntiles; tl += ATT_WARPS) {
-        const int tb = (tile0 + tl) * ATT_TILE;
-        if (tb >= n_tok) break;                 // a shorter window than the items cover
-        // pull this warp's next tile into L2 while the current one is computed:
-        // lane l takes token l & 15, K rows for l < 16 and V rows otherwise (2 lines each)
-        if (KVO_ATT_PREFETCH && tl + ATT_WARPS < ntiles) {
-            const int ntok = (tile0 + tl + ATT_WARPS) * ATT_TILE + (lane & 15);
-            if (ntok < n_tok) {
-                const uint16_t* p = row_ptr(lane < 16 ? bk : bv, lane < 16 ? wk : wv, ntok);
-#pragma unroll
-                for (int off = 0; off < D * 2; off += 128)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"((const char*)p + off));
-            }
-        }
-        // ---- K rows g and 8+g of the tile
-        uint4 kf[2][CH];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int tok = min(tb + 8 * nt + gq, n_tok - 1);
-            const uint16_t* kp = row_ptr(bk, wk, tok) + 8 * tq;
-#pragma unroll
-            for (int s = 0; s < CH; ++s) kf[nt][s] = ldg16(kp + 32 * s);
-        }
-        // ---- V rows 2t, 2t+1, 2t+8, 2t+9 (channels CPT*g ..)
-        uint4 vf[4][CPT / 8];
-#pragma unroll
-        for (int vi = 0; vi < 4; ++vi) {
-            const int tok = min(tb + 2 * tq + (vi & 1) + 8 * (vi >> 1), n_tok - 1);
-            const uint16_t* vp = row_ptr(bv, wv, tok) + CPT * gq;
-#pragma unroll
-            for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = ldg16(vp + 8 * c);
-        }
-        // ---- S = Q K^T for the 16 tokens (two n8 tiles)
-        float s[2][4];
+    // S = Q K^T for the 16 tokens of a tile (two n8 tiles)
+    __device__ __forceinline__ void qk(const uint4 (&kf)[2][CH], float (&s)[2][4]) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -190,28 +113,31 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
                 }
             }
         }
-        // ---- online softmax (log2 domain); lane holds tokens 2t, 2t+1 of each n8 tile
+    }
+
+    // online softmax of tokens tb .. tb+15 (valid below n_tok), log2 domain;
+    // gives the bf16 P fragments and the rescale factors of the old state
+    __device__ __forceinline__ void softmax(const float (&s)[2][4], int tb, int n_tok, float scale_log2, int tq,
+                                            uint32_t (&pa)[4], float& al0, float& al1) {
+        // lane holds tokens 2t, 2t+1 of each n8 tile
         float x[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int t0 = tb + 8 * nt + 2 * tq;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool ok = t0 + (e & 1) < n_tok;
-                x[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
-            }
+            for (int e = 0; e < 4; ++e) x[nt][e] = (t0 + (e & 1) < n_tok) ? s[nt][e] * scale_log2 : -INFINITY;
         }
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         const float mn0 = fmaxf(m0, mx0);
-        const float al0 = ex2f(m0 - mn0);
+        al0 = ex2f(m0 - mn0);
         m0 = mn0;
         float p[2][4];
         p[0][0] = ex2f(x[0][0] - mn0); p[0][1] = ex2f(x[0][1] - mn0);
         p[1][0] = ex2f(x[1][0] - mn0); p[1][1] = ex2f(x[1][1] - mn0);
         l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        float al1 = 1.f;
+        al1 = 1.f;
         if (NR == 2) {
             float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
@@ -225,11 +151,15 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
         } else {
             p[0][2] = p[0][3] = p[1][2] = p[1][3] = 0.f;
         }
-        const uint32_t pa0 = pack_bf16(p[0][0], p[0][1]);
-        const uint32_t pa1 = pack_bf16(p[0][2], p[0][3]);
-        const uint32_t pa2 = pack_bf16(p[1][0], p[1][1]);
-        const uint32_t pa3 = pack_bf16(p[1][2], p[1][3]);
-        // ---- O = O * alpha + P V
+        pa[0] = pack_bf16(p[0][0], p[0][1]);
+        pa[1] = pack_bf16(p[0][2], p[0][3]);
+        pa[2] = pack_bf16(p[1][0], p[1][1]);
+        pa[3] = pack_bf16(p[1][2], p[1][3]);
+    }
+
+    // O = O * alpha + P V
+    __device__ __forceinline__ void pv(const uint4 (&vf)[4][CPT / 8], const uint32_t (&pa)[4], float al0, float al1) {
+        const uint32_t pa0 = pa[0], pa1 = pa[1], pa2 = pa[2], pa3 = pa[3];
 #pragma unroll
         for (int c = 0; c < CPT / 8; ++c) {
             const uint32_t va[4] = {vf[0][c].x, vf[0][c].y, vf[0][c].z, vf[0][c].w};
@@ -256,30 +186,60 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
             }
         }
     }
-    if (bad && lane == 0) atomicOr(status, bad);
 
-    // ---- per-warp row sums (quad reduce), then CTA merge in shared memory
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (tq == 0) {
-        sm_m[warp][gq] = m0; sm_l[warp][gq] = l0;
-        sm_m[warp][gq + 8] = NR == 2 ? m1 : -INFINITY; sm_l[warp][gq + 8] = NR == 2 ? l1 : 0.f;
+    __device__ __forceinline__ void tile(const uint4 (&kf)[2][CH], const uint4 (&vf)[4][CPT / 8], int tb, int n_tok,
+                                         float scale_log2, int tq) {
+        float s[2][4];
+        qk(kf, s);
+        uint32_t pa[4];
+        float al0, al1;
+        softmax(s, tb, n_tok, scale_log2, tq, pa, al0, al1);
+        pv(vf, pa, al0, al1);
     }
+
+    // warp state -> shared memory (row sums reduced over the lane quad)
+    __device__ __forceinline__ void to_smem(float (*sm_m)[16], float (*sm_l)[16], float* sm_o_w, int warp, int gq,
+                                            int tq) {
+        float a0 = l0, a1 = l1;
+        a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
+        a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+        if (tq == 0) {
+            sm_m[warp][gq] = m0; sm_l[warp][gq] = a0;
+            sm_m[warp][gq + 8] = NR == 2 ? m1 : -INFINITY; sm_l[warp][gq + 8] = NR == 2 ? a1 : 0.f;
+        }
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        // column 2t of n-tile j is channel CPT*2t + j; column 2t+1 is CPT*(2t+1) + j
-        sm_o[warp][gq][CPT * (2 * tq) + j] = acc[j][0];
-        sm_o[warp][gq][CPT * (2 * tq + 1) + j] = acc[j][1];
-        if constexpr (NR == 2) {
-            sm_o[warp][gq + 8][CPT * (2 * tq) + j] = acc[j][2];
-            sm_o[warp][gq + 8][CPT * (2 * tq + 1) + j] = acc[j][3];
+        for (int j = 0; j < NT; ++j) {
+            // column 2t of n-tile j is channel CPT*2t + j; column 2t+1 is CPT*(2t+1) + j
+            sm_o_w[gq * D + CPT * (2 * tq) + j] = acc[j][0];
+            sm_o_w[gq * D + CPT * (2 * tq + 1) + j] = acc[j][1];
+            if constexpr (NR == 2) {
+                sm_o_w[(gq + 8) * D + CPT * (2 * tq) + j] = acc[j][2];
+                sm_o_w[(gq + 8) * D + CPT * (2 * tq + 1) + j] = acc[j][3];
+            }
         }
     }
-    __syncthreads();
-    const int64_t item = blockIdx.x;
-    for (int e = tid; e < nrows * D; e += blockDim.x) {
+};
+
+// Work-item epilogue shared by both kernels: merge the warps' states (already
+// in shared memory), write one unnormalised partial for the item, and let the
+// CTA that finishes a group's last item (atomic ticket) merge each part and
+// fuse the two parts by log-sum-exp.  Called by the nthr compute threads of the
+// CTA (threads 0 .. nthr-1), which synchronise on named barrier 1.
+template <int D, int NR>
+__device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[16], const float* sm_o, int* s_last,
+                                              const int4* __restrict__ items, const int32_t* __restrict__ att_first,
+                                              const int32_t* __restrict__ att_count, float* __restrict__ part_o,
+                                              float* __restrict__ part_ml, uint32_t* __restrict__ done,
+                                              float* __restrict__ out_o, float* __restrict__ out_lse,
+                                              float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec,
+                                              int fuse, int batch, int r, int Hkv, int bg, int nrows,
+                                              int64_t item, int nthr) {
+    const int tid = threadIdx.x;
+    const int b = bg / Hkv, gk = bg % Hkv;
+    const int Hq = Hkv * r;
+    for (int e = tid; e < nrows * D; e += nthr) {
         const int row = e / D, c = e - row * D;
         float M = -INFINITY;
 #pragma unroll
@@ -289,7 +249,7 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
 #pragma unroll
             for (int w = 0; w < ATT_WARPS; ++w) {
                 const float sc = ex2f(sm_m[w][row] - M);
-                a += sc * sm_o[w][row][c];
+                a += sc * sm_o[(w * 8 * NR + row) * D + c];
                 l += sc * sm_l[w][row];
             }
         }
@@ -300,19 +260,18 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
         }
     }
     __threadfence();
-    __syncthreads();
+    bar_named(1, nthr);
     if (tid == 0) {
         const uint32_t prev = atomicAdd(&done[bg], 1u);
-        s_last = prev + 1 == (uint32_t)att_count[bg];
+        *s_last = prev + 1 == (uint32_t)att_count[bg];
     }
-    __syncthreads();
-    if (!s_last) return;
+    bar_named(1, nthr);
+    if (!*s_last) return;
     __threadfence();
 
-    // ---- last CTA of the group: merge each part, then fuse the two parts
     const int first = att_first[bg], cnt = att_count[bg];
     const int64_t rows_total = (int64_t)batch * Hq;
-    for (int e = tid; e < nrows * D; e += blockDim.x) {
+    for (int e = tid; e < nrows * D; e += nthr) {
         const int row = e / D, c = e - row * D;
         float Mp[2] = {-INFINITY, -INFINITY};
         for (int i = first; i < first + cnt; ++i) {
@@ -358,6 +317,103 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
         }
     }
     if (tid == 0) done[bg] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Register-direct kernel: one CTA per work item; each warp loads its tiles'
+// K/V fragments straight from global memory with 16-byte loads (next tile
+// prefetched into L2).
+template <int D, int NR>
+__global__ void __launch_bounds__(ATT_WARPS * 32, NR == 1 ? KVO_ATT_MINB_NR1 : 2)
+attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec, const uint16_t* __restrict__ bk,
+            const uint16_t* __restrict__ bv,
+            const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot,
+            const int4* __restrict__ items, const int32_t* __restrict__ att_first, const int32_t* __restrict__ att_count,
+            float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* __restrict__ done,
+            float* __restrict__ out_o, float* __restrict__ out_lse, float* __restrict__ out_o_spec,
+            float* __restrict__ out_lse_spec, int fuse, int batch, int r, int Hkv, int k,
+            int B, int W, int Wcap, const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len,
+            float scale_log2, int32_t* __restrict__ status) {
+    using WA = WarpAttn<D, NR>;
+    constexpr int CH = WA::CH, CPT = WA::CPT;
+    __shared__ float sm_m[ATT_WARPS][16];
+    __shared__ float sm_l[ATT_WARPS][16];
+    __shared__ __align__(16) float sm_o[ATT_WARPS * 8 * NR * D];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int4 it = items[blockIdx.x];
+    const int bg = it.x, part = it.y, tile0 = it.z, ntiles = it.w;
+    const int b = bg / Hkv, gk = bg % Hkv;
+    const int Hq = Hkv * r;
+    // window: W tokens from slot 0 of [Wcap] rows, or (appendable cache) w_len[bg]
+    // tokens of a ring of Wcap rows starting at slot w_start[bg]
+    const int ws = w_start ? w_start[bg] : 0;
+    const int n_tok = part == 0 ? k * B : (w_len ? w_len[bg] : W);
+    // query rows: the r heads of the group, then (co-batched) the r heads of the speculative query
+    const int nrows = q_spec ? 2 * r : r;
+    auto qrow = [&](int row) -> const uint16_t* {
+        return row < r ? q + ((int64_t)b * Hq + gk * r + row) * D : q_spec + ((int64_t)b * Hq + gk * r + row - r) * D;
+    };
+    WA st;
+    {
+        const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
+        st.init(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq);
+    }
+    int bad = 0;
+    auto row_ptr = [&](const uint16_t* base_buf, const uint16_t* base_win, int tok) -> const uint16_t* {
+        if (part == 0) {
+            const int blk = tok / B;
+            int s = slot[(int64_t)bg * k + blk];
+            if (s < 0 || s >= 2 * k) { bad |= KVO_DEV_BAD_SLOT; s = 0; }
+            return base_buf + (((int64_t)bg * 2 * k + s) * B + (tok - blk * B)) * D;
+        }
+        int slot_w = ws + tok;
+        if (slot_w >= Wcap) slot_w -= Wcap;
+        return base_win + ((int64_t)bg * Wcap + slot_w) * D;
+    };
+
+    for (int tl = warp; tl < ntiles; tl += ATT_WARPS) {
+        const int tb = (tile0 + tl) * ATT_TILE;
+        if (tb >= n_tok) break;                 // a shorter window than the items cover
+        // pull this warp's next tile into L2 while the current one is computed:
+        // lane l takes token l & 15, K rows for l < 16 and V rows otherwise (2 lines each)
+        if (KVO_ATT_PREFETCH && tl + ATT_WARPS < ntiles) {
+            const int ntok = (tile0 + tl + ATT_WARPS) * ATT_TILE + (lane & 15);
+            if (ntok < n_tok) {
+                const uint16_t* p = row_ptr(lane < 16 ? bk : bv, lane < 16 ? wk : wv, ntok);
+#pragma unroll
+                for (int off = 0; off < D * 2; off += 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"((const char*)p + off));
+            }
+        }
+        // K rows g and 8+g of the tile
+        uint4 kf[2][CH];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tok = min(tb + 8 * nt + gq, n_tok - 1);
+            const uint16_t* kp = row_ptr(bk, wk, tok) + 8 * tq;
+#pragma unroll
+            for (int s = 0; s < CH; ++s) kf[nt][s] = ldg16(kp + 32 * s);
+        }
+        // V rows 2t, 2t+1, 2t+8, 2t+9 (channels CPT*g ..)
+        uint4 vf[4][CPT / 8];
+#pragma unroll
+        for (int vi = 0; vi < 4; ++vi) {
+            const int tok = min(tb + 2 * tq + (vi & 1) + 8 * (vi >> 1), n_tok - 1);
+            const uint16_t* vp = row_ptr(bv, wv, tok) + CPT * gq;
+#pragma unroll
+            for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = ldg16(vp + 8 * c);
+        }
+        st.tile(kf, vf, tb, n_tok, scale_log2, tq);
+    }
+    if (bad && lane == 0) atomicOr(status, bad);
+    st.to_smem(sm_m, sm_l, sm_o + warp * 8 * NR * D, warp, gq, tq);
+    __syncthreads();
+    attn_epilogue<D, NR>(sm_m, sm_l, sm_o, &s_last, items, att_first, att_count, part_o, part_ml, done, out_o,
+                         out_lse, out_o_spec, out_lse_spec, fuse, batch, r, Hkv, bg, nrows, blockIdx.x,
+                         ATT_WARPS * 32);
 }
 
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
