@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--append", type=int, default=0,
                     help="grow the cache: one kvo_append before every decode step (reserves this many tokens)")
     ap.add_argument("--gather-unroll", type=int, default=0, help="gather loads in flight per lane (0: default)")
+    ap.add_argument("--attn-impl", type=int, default=-1,
+                    help="attention kernel: 0 register-direct, 1 TMA-staged persistent (-1: default)")
+    ap.add_argument("--attn-ctas", type=int, default=0, help="TMA-staged attention grid (0: fill the SMs)")
     return ap.parse_args()
 
 
@@ -331,6 +334,8 @@ def build_workload(args, ws=1):
         B.ctx.set_gather_reserve(args.gather_reserve)
     if args.graphs >= 0:
         B.ctx.set_graphs(bool(args.graphs))
+    if args.attn_impl >= 0:
+        B.ctx.set_attn_impl(args.attn_impl, args.attn_ctas)
     B.keep = (k_host, v_host, k_win, v_win)
     B.q_pin = torch.stack(qs_l).pin_memory()
     B.qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
@@ -546,6 +551,8 @@ def run_ours(args):
                              "unroll": args.gather_unroll or "default",
                              "engine": "default" if args.gather_engine < 0 else args.gather_engine,
                              "drivers": args.gather_drivers or "default"},
+            "attention_kernel": {"impl": "default" if args.attn_impl < 0 else args.attn_impl,
+                                 "ctas": args.attn_ctas or "default"},
         }
         print(json.dumps(line), flush=True)
     ctx.close()

@@ -346,6 +346,25 @@ kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers);
 kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes);
 
 /*
+ * kvo_set_attn_impl -- which kernel computes the attention of
+ * sparse_decode_attn, sparse_decode_attn_cobatch and the decode step.  Both
+ * do the same arithmetic but split a group's tiles into work items
+ * differently, so their results agree up to float rounding, not bit for bit.
+ * impl 0: register-direct, one CTA per 256-token work item, each warp loading
+ * its tiles' K/V fragments from HBM with 16-byte loads.  impl 1 (default):
+ * TMA-staged persistent kernel; one producer warp per CTA streams the tiles
+ * into an 8-stage shared-memory ring with bulk copies while four warps
+ * compute, and the tiles of all groups are split into one equal contiguous
+ * range per CTA, over as many CTAs as are resident on the device at once (in
+ * the decode step: on the SMs the flat gather leaves free), or over `ctas`
+ * CTAs when ctas > 0.  Waits inside impl 1 are bounded (2 s); on expiry the
+ * kernel sets KVO_DEV_TIMEOUT.  Synchronises the context's streams and drops
+ * captured graphs.  Errors: KVO_ERR_INVALID for a null context, impl outside
+ * 0..1 or ctas < 0; KVO_ERR_CUDA if the work lists cannot be allocated.
+ */
+kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
+
+/*
  * Per-launch timing of kvo_decode_step, for benchmarks.  kvo_profile(ctx, 1)
  * clears and starts recording a timing event before and after every kernel
  * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.

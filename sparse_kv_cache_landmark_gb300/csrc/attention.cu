@@ -416,17 +416,278 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
                          ATT_WARPS * 32);
 }
 
+// ---------------------------------------------------------------------------
+// TMA-staged persistent kernel.  The host splits the tiles of all groups
+// (sparse part, then window part, group after group) into one contiguous range
+// per CTA; the range is cut into work items at part boundaries, so a CTA runs
+// one to a few long items and pays the item epilogue (partial write, ticket)
+// that rarely.  One producer warp streams every 16-token tile of its items, K
+// rows then V rows, into a ring of ATT_STAGES shared-memory stages with
+// cp.async.bulk, one copy per run of contiguous source rows (a run breaks where
+// a block's slot does not follow the previous row's, and at the window ring's
+// wrap), completing on the stage's "full" mbarrier; it reads the slots of its
+// rows' blocks ATT_PF tiles ahead, so slot loads never stall the copies.  Four
+// compute warps take tiles round-robin, read their mma fragments from shared
+// memory with the lane mapping of the register-direct kernel, and release the
+// stage on its "empty" mbarrier.  Every mbarrier wait is bounded by the global
+// timer: on expiry the CTA records KVO_DEV_TIMEOUT and stops waiting (its
+// results are then invalid; the host sees the status bit).
+template <int D>
+struct AttnTmaSmem {
+    static constexpr int TILE_BYTES = ATT_TILE * D * 2;                  // one K (or V) tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int RING = ATT_STAGES * STAGE_BYTES;
+    static constexpr int O_OFF = RING;                                    // float [ATT_WARPS * 8 * NR][D]
+    static constexpr size_t bytes(int NR) {
+        return (size_t)RING + sizeof(float) * (ATT_WARPS * 8 * NR * D + 2 * ATT_WARPS * 16) +
+               sizeof(uint64_t) * 2 * ATT_STAGES + 16;
+    }
+};
+
+constexpr long long kAttWaitNs = 2000000000LL;   // 2 s per mbarrier wait
+constexpr int ATT_PF = 4;                        // producer: tiles of slot lookahead
+
+// Bounded wait; false (and the CTA's abort flag set) when the limit passed.
+__device__ __forceinline__ bool att_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t* status) {
+    if (mbar_try_wait(mbar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (int it = 0;; ++it) {
+        if (mbar_try_wait(mbar, parity)) return true;
+        if ((it & 63) == 63) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > (uint64_t)kAttWaitNs) {
+                *abort_flag = 1;
+                atomicOr(status, KVO_DEV_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Producer warp: copy the nt tiles of one work item into the ring.  Lane j
+// handles row j & 15 of the K tile (j < 16) or of the V tile (j >= 16).
+template <int D>
+__device__ __forceinline__ void attn_produce(unsigned char* smem, uint64_t* full, uint64_t* empty,
+                                             volatile int* s_abort, int64_t qseq, int nt, int part, int bg,
+                                             int tile0, int n_tok, int ws, const uint16_t* __restrict__ bk,
+                                             const uint16_t* __restrict__ bv, const uint16_t* __restrict__ wk,
+                                             const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot,
+                                             int k, int B, int Wcap, int32_t* status) {
+    using SM = AttnTmaSmem<D>;
+    const int lane = threadIdx.x & 31, kv = lane >> 4, row = lane & 15;
+    int bad = 0;
+    // slot of the gathered block that holds this lane's row of tile tl
+    auto slot_of = [&](int tl) -> int {
+        const int tok = (tile0 + tl) * ATT_TILE + row;
+        if (part != 0 || tl >= nt || tok >= n_tok) return 0;
+        return __ldg(slot + (int64_t)bg * k + tok / B);
+    };
+    int pf[ATT_PF];
+#pragma unroll
+    for (int i = 0; i < ATT_PF; ++i) pf[i] = slot_of(i);
+    for (int t0 = 0; t0 < nt; t0 += ATT_PF) {
+#pragma unroll
+        for (int i = 0; i < ATT_PF; ++i) {
+            const int tl = t0 + i;
+            if (tl >= nt) break;
+            const int64_t qi = qseq + tl;
+            const int st = (int)(qi % ATT_STAGES);
+            const uint32_t fb = smem_u32(&full[st]);
+            if (lane == 0 && qi >= ATT_STAGES && !*s_abort)
+                att_wait(smem_u32(&empty[st]), (uint32_t)((qi / ATT_STAGES - 1) & 1), s_abort, status);
+            __syncwarp();
+            const int tb = (tile0 + tl) * ATT_TILE;
+            const int rows = min(ATT_TILE, n_tok - tb);
+            if (lane == 0) mbar_expect_tx(fb, (uint32_t)(rows * D * 2 * 2));
+            __syncwarp();
+            const int tok = tb + row;
+            const bool valid = row < rows;
+            const uint16_t* src;
+            bool start;
+            if (part == 0) {
+                const int blk = tok / B, off = tok - blk * B;
+                int sl = pf[i];
+                if (valid && (sl < 0 || sl >= 2 * k)) { bad |= KVO_DEV_BAD_SLOT; sl = 0; }
+                const int sl_prev = __shfl_up_sync(0xffffffffu, sl, 1);
+                src = (kv ? bv : bk) + (((int64_t)bg * 2 * k + sl) * B + off) * D;
+                start = valid && (row == 0 || (off == 0 && sl != sl_prev + 1));
+            } else {
+                int sw = ws + tok;
+                if (sw >= Wcap) sw -= Wcap;
+                src = (kv ? wv : wk) + ((int64_t)bg * Wcap + sw) * D;
+                start = valid && (row == 0 || sw == 0);
+            }
+            const unsigned starts = (__ballot_sync(0xffffffffu, start) >> (kv * 16)) & 0xffffu;
+            if (start) {
+                const unsigned later = starts & ~((2u << row) - 1u);
+                const int next = later ? __ffs(later) - 1 : rows;
+                const uint32_t dst = smem_u32(smem + st * SM::STAGE_BYTES + kv * SM::TILE_BYTES + row * D * 2);
+                bulk_load(dst, src, (uint32_t)((next - row) * D * 2), fb);
+            }
+            pf[i] = slot_of(tl + ATT_PF);
+        }
+    }
+    if (bad) atomicOr(status, bad);
+}
+
+template <int D, int NR>
+__global__ void __launch_bounds__((ATT_WARPS + 1) * 32, 2)
+attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
+                const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv, const uint16_t* __restrict__ wk,
+                const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot, const int4* __restrict__ items,
+                const int32_t* __restrict__ cta_first, const int32_t* __restrict__ att_first,
+                const int32_t* __restrict__ att_count, float* __restrict__ part_o, float* __restrict__ part_ml,
+                uint32_t* __restrict__ done, float* __restrict__ out_o, float* __restrict__ out_lse,
+                float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec, int fuse, int batch, int r,
+                int Hkv, int k, int B, int W, int Wcap, const int32_t* __restrict__ w_start,
+                const int32_t* __restrict__ w_len, float scale_log2, int32_t* __restrict__ status) {
+    using WA = WarpAttn<D, NR>;
+    using SM = AttnTmaSmem<D>;
+    constexpr int CH = WA::CH, CPT = WA::CPT;
+    constexpr int NTHR = ATT_WARPS * 32;              // compute threads
+    extern __shared__ __align__(128) unsigned char smem[];
+    float* sm_o = reinterpret_cast<float*>(smem + SM::O_OFF);
+    float (*sm_m)[16] = reinterpret_cast<float (*)[16]>(sm_o + ATT_WARPS * 8 * NR * D);
+    float (*sm_l)[16] = sm_m + ATT_WARPS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm_l + ATT_WARPS);
+    uint64_t* empty = full + ATT_STAGES;
+    int* s_last = reinterpret_cast<int*>(empty + ATT_STAGES);
+    volatile int* s_abort = s_last + 1;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    if (tid == 0) {
+        for (int i = 0; i < ATT_STAGES; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 1);
+        }
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int Hq = Hkv * r;
+    const int nrows = q_spec ? 2 * r : r;
+    const int item_lo = cta_first[blockIdx.x], item_hi = cta_first[blockIdx.x + 1];
+    int64_t qseq = 0;                                 // tiles issued / consumed so far by this CTA
+    for (int item = item_lo; item < item_hi; ++item) {
+        const int4 it = items[item];
+        const int bg = it.x, part = it.y, tile0 = it.z;
+        const int b = bg / Hkv, gk = bg % Hkv;
+        const int ws = w_start ? w_start[bg] : 0;
+        const int n_tok = part == 0 ? k * B : (w_len ? w_len[bg] : W);
+        // tiles of this item that hold tokens (a window may be shorter than its items cover)
+        const int nt = max(0, min(it.w, (n_tok - tile0 * ATT_TILE + ATT_TILE - 1) / ATT_TILE));
+
+        if (warp == ATT_WARPS) {
+            attn_produce<D>(smem, full, empty, s_abort, qseq, nt, part, bg, tile0, n_tok, ws, bk, bv, wk, wv, slot,
+                            k, B, Wcap, status);
+        } else {
+            auto qrow = [&](int rr) -> const uint16_t* {
+                return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D
+                              : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
+            };
+            WA stt;
+            {
+                const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
+                stt.init(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq);
+            }
+            for (int tl = warp; tl < nt; tl += ATT_WARPS) {
+                const int64_t qi = qseq + tl;
+                const int st = (int)(qi % ATT_STAGES);
+                if (!*s_abort) att_wait(smem_u32(&full[st]), (uint32_t)((qi / ATT_STAGES) & 1), s_abort, status);
+                const int tb = (tile0 + tl) * ATT_TILE;
+                const int rows = min(ATT_TILE, n_tok - tb);
+                const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem + st * SM::STAGE_BYTES);
+                const uint16_t* vs = ks + ATT_TILE * D;
+                // rows past the tile's end hold stale data: read the last valid row instead
+                float sc[2][4];
+                {
+                    uint4 kf[2][CH];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
+#pragma unroll
+                        for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
+                    }
+                    stt.qk(kf, sc);
+                }
+                uint4 vf[4][CPT / 8];
+#pragma unroll
+                for (int vi = 0; vi < 4; ++vi) {
+                    const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
+#pragma unroll
+                    for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
+                uint32_t pa[4];
+                float al0, al1;
+                stt.softmax(sc, tb, n_tok, scale_log2, tq, pa, al0, al1);
+                stt.pv(vf, pa, al0, al1);
+            }
+            stt.to_smem(sm_m, sm_l, sm_o + warp * 8 * NR * D, warp, gq, tq);
+            bar_named(1, NTHR);
+            attn_epilogue<D, NR>(sm_m, sm_l, sm_o, s_last, items, att_first, att_count, part_o, part_ml, done,
+                                 out_o, out_lse, out_o_spec, out_lse_spec, fuse, batch, r, Hkv, bg, nrows, item,
+                                 NTHR);
+        }
+        qseq += nt;
+    }
+    // no copy may still target this CTA's shared memory when it exits: the
+    // producer waits (bounded) for the last fills of the ring
+    if (warp == ATT_WARPS && lane == 0 && !*s_abort) {
+        for (int64_t qi = max((int64_t)0, qseq - ATT_STAGES); qi < qseq; ++qi)
+            att_wait(smem_u32(&full[qi % ATT_STAGES]), (uint32_t)((qi / ATT_STAGES) & 1), s_abort, status);
+    }
+}
+
+template <int D, int NR>
+static cudaError_t tma_attr(int* per_sm) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tma_kernel<D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)AttnTmaSmem<D>::bytes(NR));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, attn_tma_kernel<D, NR>, (ATT_WARPS + 1) * 32,
+                                                         AttnTmaSmem<D>::bytes(NR));
+}
+
+// Shared-memory attribute of the TMA-staged kernel; SMs of the device and
+// CTAs of the kernel per SM (the smaller count of its two query-row variants).
+cudaError_t prepare_attention(Ctx& c) {
+    int dev = 0, sms = 0, p1 = 0, p2 = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (c.d == 128) {
+        if ((e = tma_attr<128, 1>(&p1)) != cudaSuccess || (e = tma_attr<128, 2>(&p2)) != cudaSuccess) return e;
+    } else {
+        if ((e = tma_attr<64, 1>(&p1)) != cudaSuccess || (e = tma_attr<64, 2>(&p2)) != cudaSuccess) return e;
+    }
+    c.tma_per_sm = std::max(1, std::min(p1, p2));
+    c.n_sms = std::max(1, sms);
+    return cudaSuccess;
+}
+
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
-                             float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s) {
+                             float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
+                             bool in_step) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
     const int nrows = q_spec ? 2 * c.r : c.r;
+    const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
 #define KVO_ATT(D_, NR_)                                                                                         \
-    attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
-        (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items,       \
-        c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,      \
-        c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
+    if (c.att_impl == 1)                                                                                        \
+        attn_tma_kernel<D_, NR_><<<pl.grid, (ATT_WARPS + 1) * 32, AttnTmaSmem<D_>::bytes(NR_), s>>>(            \
+            (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, pl.items,      \
+            pl.cta, pl.first, pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec,     \
+            fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status);      \
+    else                                                                                                        \
+        attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                           \
+            (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items,   \
+            c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,  \
+            c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
     if (c.d == 128) {
         if (nrows <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);
     } else {

@@ -18,6 +18,7 @@ constexpr int SEL_RPT_MAX = 4;            // select: landmark rows per thread (1
 constexpr int ATT_WARPS = 4;              // attention: warps per CTA
 constexpr int ATT_TILE = 16;              // attention: tokens per mma tile
 constexpr int ATT_TILES_PER_ITEM = 16;    // attention: tiles per CTA work item
+constexpr int ATT_STAGES = 8;             // TMA-staged attention: shared-memory ring stages (K + V tile each)
 constexpr int GATHER_THREADS = 256;
 constexpr int TMA_STAGE_BYTES = 16384;    // TMA gather: bytes per batch
 constexpr int TMA_MAX_PIECES = 64;        // TMA gather: pieces per batch
@@ -69,6 +70,21 @@ struct Ctx {
     int32_t* att_first = nullptr;   // [G] first item of the group
     int32_t* att_count = nullptr;   // [G] items of the group
     int n_att_items = 0;
+    int att_impl = 1;               // attention kernel: 0 register-direct loads, 1 TMA-staged persistent
+    int att_part_cap = 0;           // work items the partial-result buffers hold
+    // TMA-staged kernel: balanced per-CTA tile ranges cut into work items, one
+    // plan for the whole device (standalone calls) and one for the decode step,
+    // whose attention shares the device with a gather holding SMs of its own
+    int tma_per_sm = 1;             // CTAs of the kernel resident per SM
+    int n_sms = 1;
+    int tma_ctas = 0;               // requested grid (0: fill the available SMs)
+    struct TmaPlan {
+        int grid = 0, n_items = 0;
+        int4* items = nullptr;      // {group, part, first tile, tiles}
+        int32_t* cta = nullptr;     // [grid + 1] first item of each CTA
+        int32_t* first = nullptr;   // [G] first item of each group
+        int32_t* count = nullptr;   // [G] items of each group
+    } tma[2];
     float* att_part_o = nullptr;    // [items][r][d]
     float* att_part_ml = nullptr;   // [items][r][2]
     uint32_t* att_done = nullptr;   // [G]
@@ -169,7 +185,8 @@ cudaError_t launch_gather_tma(const Ctx& c, int layer, int buf, const int32_t* r
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
                                cudaStream_t s);
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
-                             float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s);
+                             float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
+                             bool in_step = false);
 cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
                              float* lse, int rows, int d, cudaStream_t s);
 cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s);
@@ -180,6 +197,7 @@ int gather_default_ctas(const Ctx& c);
 // Raise the dynamic shared memory limits of the gather kernels (host call; done at init, never during capture).
 cudaError_t prepare_gather_tma();
 cudaError_t prepare_gather_flat();
+cudaError_t prepare_attention(Ctx& c);
 
 // Sets the message kvo_last_error(NULL) returns (context-free calls).
 void set_last_error(const char* msg);

@@ -51,6 +51,83 @@ cudaError_t dalloc(T** p, size_t bytes, size_t* acc) {
     return e;
 }
 
+// Partial-result buffers of the attention kernels, for `items` work items.
+cudaError_t part_alloc(kvo::Ctx& c, int items) {
+    if (items <= c.att_part_cap) return cudaSuccess;
+    if (c.att_part_o) cudaFree(c.att_part_o);
+    if (c.att_part_ml) cudaFree(c.att_part_ml);
+    c.att_part_o = nullptr;
+    c.att_part_ml = nullptr;
+    c.att_part_cap = 0;
+    const size_t rows = 2 * c.r <= 16 ? 2 * c.r : c.r;   // room for co-batched speculative rows
+    cudaError_t e = dalloc(&c.att_part_o, sizeof(float) * items * rows * c.d, nullptr);
+    if (e == cudaSuccess) e = dalloc(&c.att_part_ml, sizeof(float) * items * rows * 2, nullptr);
+    if (e == cudaSuccess) c.att_part_cap = items;
+    return e;
+}
+
+// Work items of the TMA-staged attention kernel: the tiles of every group
+// (sparse part, then window part; window tiles up to the largest window the
+// context can hold), group after group, split into `grid` equal contiguous
+// ranges, each range cut at part boundaries.
+kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
+    const int64_t sp_tiles = (c.k * c.B + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;
+    const int64_t w_tiles = (w_max + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    const int64_t per_g = sp_tiles + w_tiles, T = per_g * c.G;
+    grid = std::max<int64_t>(1, std::min<int64_t>(grid, T));
+    std::vector<int4> items;
+    std::vector<int32_t> cta(grid + 1), first(c.G, 0), count(c.G, 0);
+    for (int64_t j = 0; j < grid; ++j) {
+        cta[j] = (int32_t)items.size();
+        int64_t t = T * j / grid;
+        const int64_t hi = T * (j + 1) / grid;
+        while (t < hi) {
+            const int g = (int)(t / per_g);
+            const int64_t off = t - g * per_g;
+            const bool sparse = off < sp_tiles;
+            const int64_t n = std::min(hi - t, sparse ? sp_tiles - off : per_g - off);
+            items.push_back(make_int4(g, sparse ? 0 : 1, (int)(sparse ? off : off - sp_tiles), (int)n));
+            t += n;
+        }
+    }
+    cta[grid] = (int32_t)items.size();
+    for (size_t i = 0; i < items.size(); ++i) {
+        const int g = items[i].x;
+        if (count[g] == 0) first[g] = (int32_t)i;
+        ++count[g];
+    }
+    auto F = [](void* p) { if (p) cudaFree(p); };
+    F(pl.items); F(pl.cta); F(pl.first); F(pl.count);
+    pl = kvo::Ctx::TmaPlan{};
+    KVO_CUDA(&c, part_alloc(c, (int)items.size()));
+    KVO_CUDA(&c, dalloc(&pl.items, sizeof(int4) * items.size(), nullptr));
+    KVO_CUDA(&c, dalloc(&pl.cta, sizeof(int32_t) * cta.size(), nullptr));
+    KVO_CUDA(&c, dalloc(&pl.first, sizeof(int32_t) * c.G, nullptr));
+    KVO_CUDA(&c, dalloc(&pl.count, sizeof(int32_t) * c.G, nullptr));
+    KVO_CUDA(&c, cudaMemcpy(pl.items, items.data(), sizeof(int4) * items.size(), cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(pl.cta, cta.data(), sizeof(int32_t) * cta.size(), cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(pl.first, first.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    KVO_CUDA(&c, cudaMemcpy(pl.count, count.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
+    pl.grid = (int)grid;
+    pl.n_items = (int)items.size();
+    return KVO_OK;
+}
+
+// Both plans: the whole device, and the decode step's share of it (each flat
+// gather CTA reserves most of its SM's shared memory, so no attention CTA
+// lands on those SMs while a prefetch runs beside the attention).  An explicit
+// grid (tma_ctas > 0) applies to both.  Callers synchronise first.
+kvo_status build_tma_plans(kvo::Ctx& c) {
+    const int64_t dev = (int64_t)c.tma_per_sm * c.n_sms;
+    int held = 0;
+    if (c.gather_engine == 3 && c.gather_reserve_smem >= 64 * 1024)
+        held = std::min(c.gather_ctas > 0 ? c.gather_ctas : 2 * c.n_sms, c.n_sms - 1);
+    const int64_t step = (int64_t)c.tma_per_sm * (c.n_sms - held);
+    if (kvo_status st = build_tma_plan(c, c.tma[0], c.tma_ctas > 0 ? c.tma_ctas : dev)) return st;
+    return build_tma_plan(c, c.tma[1], c.tma_ctas > 0 ? c.tma_ctas : step);
+}
+
 void free_ctx(kvo::Ctx& c) {
     auto F = [](void* p) { if (p) cudaFree(p); };
     F(c.g_off); F(c.g_C); F(c.g_len); F(c.g_wstart); F(c.g_wlen);
@@ -62,6 +139,7 @@ void free_ctx(kvo::Ctx& c) {
     F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
     F(c.runs); F(c.nruns);
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
+    for (auto& pl : c.tma) { F(pl.items); F(pl.cta); F(pl.first); F(pl.count); }
     F(c.status);
     F(c.st_true); F(c.st_pred); F(c.st_miss); F(c.st_miss_cnt); F(c.st_slot);
     for (auto* E : {&c.ev_eager, &c.ev_graph}) {
@@ -272,11 +350,10 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaMemcpy(c.att_items, att.data(), sizeof(int4) * att.size(), cudaMemcpyHostToDevice));
     KVO_CUDA(&c, cudaMemcpy(c.att_first, afirst.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
     KVO_CUDA(&c, cudaMemcpy(c.att_count, acount.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
-    const int att_rows = 2 * c.r <= 16 ? 2 * c.r : c.r;   // room for co-batched speculative rows
-    KVO_CUDA(&c, dalloc(&c.att_part_o, sizeof(float) * att.size() * att_rows * c.d, &sb));
-    KVO_CUDA(&c, dalloc(&c.att_part_ml, sizeof(float) * att.size() * att_rows * 2, &sb));
+    KVO_CUDA(&c, part_alloc(c, (int)att.size()));
     KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * c.G, &sb));
     KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
+    KVO_CUDA(&c, kvo::prepare_attention(c));
     KVO_CUDA(&c, dalloc(&c.status, sizeof(int32_t), &sb));
     KVO_CUDA(&c, cudaMemsetAsync(c.status, 0, sizeof(int32_t), c.s_compute));
     // decode-step state
@@ -302,7 +379,7 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, kvo::prepare_gather_tma());
     KVO_CUDA(&c, kvo::prepare_gather_flat());
     KVO_CUDA(&c, cudaStreamSynchronize(c.s_compute));
-    return KVO_OK;
+    return build_tma_plans(c);
 }
 
 kvo_status check_ctx(kvo_ctx* ctx) { return ctx ? KVO_OK : fail(nullptr, KVO_ERR_INVALID, "null context"); }
@@ -512,7 +589,7 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
         KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
             return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
                                          lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
-                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute);
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute, true);
         }));
         KVO_CUDA(&c, cudaEventRecord(E.attn[l], c.s_compute));
         pref_ready[buf] = false;
@@ -704,7 +781,7 @@ kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll)
     ctx->c.gather_ctas = ctas;
     ctx->c.gather_threads = threads;
     ctx->c.gather_unroll = unroll;
-    return KVO_OK;
+    return build_tma_plans(ctx->c);   // the step's attention plan depends on the gather's SMs
 }
 
 kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
@@ -713,7 +790,7 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
     drop_graphs(ctx->c);
     if (smem_bytes < 0 || smem_bytes > 227 * 1024) return fail(&ctx->c, KVO_ERR_INVALID, "0 <= smem_bytes <= 227 KiB");
     ctx->c.gather_reserve_smem = smem_bytes;
-    return KVO_OK;
+    return build_tma_plans(ctx->c);   // the step's attention plan depends on the gather's SMs
 }
 
 kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
@@ -734,7 +811,18 @@ kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
     }
     ctx->c.gather_stages = engine == 2 ? 8 : 4;
     ctx->c.gather_drivers = drivers;
-    return KVO_OK;
+    return build_tma_plans(ctx->c);   // the step's attention plan depends on the gather's SMs
+}
+
+kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if (impl < 0 || impl > 1 || ctas < 0)
+        return fail(&ctx->c, KVO_ERR_INVALID, "attention implementation must be 0 or 1 and ctas >= 0");
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    drop_graphs(ctx->c);
+    ctx->c.att_impl = impl;
+    ctx->c.tma_ctas = ctas;
+    return build_tma_plans(ctx->c);
 }
 
 kvo_status kvo_profile(kvo_ctx* ctx, int enable) {

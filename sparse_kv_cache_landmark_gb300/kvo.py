@@ -23,7 +23,8 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "sparse_decode_attn", "merge_lse", "kvo_decode_step", "kvo_reset_prediction", "kvo_get_stream",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
-           "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append"]
+           "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
+           "kvo_set_attn_impl"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -74,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_gather_engine.argtypes = [P, I, I]
         L.kvo_set_gather_reserve.argtypes = [P, I]
         L.kvo_set_graphs.argtypes = [P, I]
+        L.kvo_set_attn_impl.argtypes = [P, I, I]
         L.kvo_append.argtypes = [P, VP, VP, VP]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
@@ -290,6 +292,11 @@ class Context:
     def set_graphs(self, enable: bool):
         """Replay warm decode steps from captured CUDA graphs (C: kvo_set_graphs)."""
         self._c(lib().kvo_set_graphs(self.ctx, int(bool(enable))))
+
+    def set_attn_impl(self, impl: int, ctas: int = 0):
+        """Attention kernel: 0 register-direct loads, 1 TMA-staged persistent with
+        ``ctas`` CTAs (0: as many as fit) (C: kvo_set_attn_impl)."""
+        self._c(lib().kvo_set_attn_impl(self.ctx, impl, ctas))
 
     def set_gather_reserve(self, smem_bytes: int):
         self._c(lib().kvo_set_gather_reserve(self.ctx, smem_bytes))

@@ -16,8 +16,9 @@ from tests.margins import MARGIN
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,spec,L", [(16, True, 2), (1, False, 1), (32, False, 3)])
-def test_append_grows_the_cache(B, spec, L):
+@pytest.mark.parametrize("B,spec,L,att", [(16, True, 2, (1, 0)), (1, False, 1, (1, 0)), (32, False, 3, (1, 0)),
+                                          (16, False, 1, (0, 0)), (16, False, 1, (1, 2))])
+def test_append_grows_the_cache(B, spec, L, att):
     W, n_app, d = 32, 40 if B > 1 else 12, 128
     len0 = W + B * 20 if B > 1 else W + 400
     cap = len0 + n_app
@@ -41,6 +42,7 @@ def test_append_grows_the_cache(B, spec, L):
                   top_k=w.top_k, window=W, n_layers=L, seq_lens=[len0] * w.batch, k_host=k_host, v_host=v_host,
                   k_win=k_win, v_win=v_win, max_append=n_app)
     try:
+        ctx.set_attn_impl(*att)        # the window ring wraps inside and across attention tiles
         q = torch.stack([full[l].q for l in range(L)]).cuda()
         qs = torch.stack([full[l].q_spec for l in range(L)]).cuda() if spec else None
         checked = skipped = 0

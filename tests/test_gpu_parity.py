@@ -153,6 +153,49 @@ def test_gather_engines_bit_exact(case, engine, drivers):
             assert np.array_equal(buf[i][written], exp[written]), (b, g, kv)
 
 
+@pytest.mark.parametrize("ctas", [0, 1, 3])
+def test_attention_kernels_agree(case, ctas):
+    """The register-direct kernel (impl 0) and the TMA-staged persistent kernel
+    (impl 1; ctas > 0 gives each CTA a longer tile range, several work items
+    and stage-ring reuse across them) both match the oracle.  They split the
+    tiles differently, so they agree to rounding, not bit for bit."""
+    c, refs = case
+    w = c.w
+    r = w.group_size
+    q = c.q_dev(0)
+    qs = c.q_dev(0, spec=True)
+    T, _ = c.ctx.select_topk(0, q)
+    miss, cnt, slot = c.ctx.index_diff(T, None)
+    c.ctx.gather_coalesced(0, 0, miss, cnt, slot_base=w.top_k, urgent=True)
+    out = {}
+    try:
+        for impl in (0, 1):
+            c.ctx.set_attn_impl(impl, ctas if impl == 1 else 0)
+            res = [t.cpu() for t in c.ctx.sparse_decode_attn(0, 0, q, slot, fuse_window_merge=True)]
+            res += [t.cpu() for t in c.ctx.sparse_decode_attn(0, 0, q, slot, fuse_window_merge=False)]
+            if qs is not None and 2 * r <= 16:
+                res += [t.cpu() for t in c.ctx.sparse_decode_attn_cobatch(0, 0, q, qs, slot)]
+            torch.cuda.synchronize()
+            assert c.ctx.device_status() == 0
+            out[impl] = res
+    finally:
+        c.ctx.set_attn_impl(1, 0)
+    for a, b in zip(out[0], out[1]):
+        assert a.shape == b.shape
+        np.testing.assert_allclose(b.numpy(), a.numpy(), rtol=1e-2, atol=2e-3)
+    for impl in (0, 1):
+        o, lse, o2, lse2 = (t.numpy() for t in out[impl][:4])
+        for (b, g), ref in refs.items():
+            rows = slice(b * w.n_q_heads + g * r, b * w.n_q_heads + (g + 1) * r)
+            assert_attn_close(o[0, rows], ref.o)
+            assert_attn_close(lse[0, rows], ref.lse, what="lse")
+            assert_attn_close(o2[0, rows], ref.o_sparse, what="o_sparse")
+            assert_attn_close(lse2[0, rows], ref.lse_sparse, what="lse_sparse")
+            if w.window:
+                assert_attn_close(o2[1, rows], ref.o_window, what="o_window")
+                assert_attn_close(lse2[1, rows], ref.lse_window, what="lse_window")
+
+
 def test_cobatched_attention(case):
     """True and speculative queries in one attention pass (2r <= 16)."""
     c, refs = case

@@ -64,6 +64,27 @@ def test_decode_step_cold_and_warm(L, spec, engine):
         c.close()
 
 
+def test_decode_step_attention_kernels_agree():
+    """The decode step matches the oracle with either attention kernel and any
+    TMA grid (the kernels split tiles differently: equal up to rounding)."""
+    c = _case(4, True)
+    try:
+        q, qs = c.q_stack(), c.q_stack(spec=True)
+        res = []
+        for impl, ctas in ((1, 0), (0, 0), (1, 2)):
+            c.ctx.set_attn_impl(impl, ctas)
+            for _ in range(2):
+                o, lse = c.ctx.decode_step(q, qs)
+            torch.cuda.synchronize()
+            assert c.ctx.device_status() == 0
+            res.append((o.cpu(), lse.cpu()))
+        for o, lse in res:
+            _check(c, o, lse)
+            np.testing.assert_allclose(o.numpy(), res[0][0].numpy(), rtol=1e-2, atol=2e-3)
+    finally:
+        c.close()
+
+
 @pytest.mark.parametrize("engine", [3, 0])
 def test_decode_step_profile_counts_launches(engine):
     c = _case(4, True)
