@@ -352,12 +352,11 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes);
  * differently, so their results agree up to float rounding, not bit for bit.
  * impl 0: register-direct, one CTA per 256-token work item, each warp loading
  * its tiles' K/V fragments from HBM with 16-byte loads.  impl 1 (default):
- * TMA-staged persistent kernel; one producer warp per CTA streams the tiles
- * into an 8-stage shared-memory ring with bulk copies while four warps
- * compute, and the tiles of all groups are split into one equal contiguous
- * range per CTA, over as many CTAs as are resident on the device at once (in
- * the decode step: on the SMs the flat gather leaves free), or over `ctas`
- * CTAs when ctas > 0.  Waits inside impl 1 are bounded (2 s); on expiry the
+ * TMA-staged persistent kernel; each of a CTA's four warps keeps its next 2-4
+ * tiles in flight in shared-memory stages filled by bulk copies, and the tiles
+ * of all groups are split into one equal contiguous range per CTA, over as
+ * many CTAs as are resident on the device at once (in the decode step: on the
+ * SMs the flat gather leaves free), or over `ctas` CTAs when ctas > 0.  Waits inside impl 1 are bounded (2 s); on expiry the
  * kernel sets KVO_DEV_TIMEOUT.  Synchronises the context's streams and drops
  * captured graphs.  Errors: KVO_ERR_INVALID for a null context, impl outside
  * 0..1 or ctas < 0; KVO_ERR_CUDA if the work lists cannot be allocated.

@@ -16,11 +16,15 @@
 //    values of tokens 2t, 2t+1, 2t+8, 2t+9.  Output column g of n-tile j is
 //    channel (d/8) g + j, so the lane loads d/8 contiguous channels of those 4
 //    token rows and pairs tokens with byte permutes.
-// Work: a CTA takes up to ATT_TILES_PER_ITEM tiles of 16 tokens of one
-// (request, KV head) group and one part (0 sparse, 1 window); its 4 warps keep
-// online-softmax state over interleaved tiles, merge in shared memory and
-// write one unnormalised partial (m, l, acc).  The last CTA of the group
+// Work: a work item is a run of 16-token tiles of one (request, KV head)
+// group and one part (0 sparse, 1 window); a CTA's 4 warps keep online-softmax
+// state over interleaved tiles of the item, merge in shared memory and write
+// one unnormalised partial (m, l, acc).  The CTA finishing a group's last item
 // (atomic ticket) merges the partials of each part and fuses the two parts.
+// Two kernels share this math: the register-direct kernel (one CTA per item of
+// up to ATT_TILES_PER_ITEM tiles; fragments loaded from global memory) and the
+// TMA-staged persistent kernel (one balanced tile range per CTA; tiles copied
+// into shared memory by bulk copies ahead of the math).
 #include <math.h>
 
 #include "kvo_internal.cuh"
@@ -273,19 +277,34 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
     const int64_t rows_total = (int64_t)batch * Hq;
     for (int e = tid; e < nrows * D; e += nthr) {
         const int row = e / D, c = e - row * D;
-        float Mp[2] = {-INFINITY, -INFINITY};
-        for (int i = first; i < first + cnt; ++i) {
-            const int pp = items[i].y;
-            Mp[pp] = fmaxf(Mp[pp], __ldcg(part_ml + ((int64_t)i * nrows + row) * 2));
-        }
-        float Lp[2] = {0.f, 0.f}, Ap[2] = {0.f, 0.f};
-        for (int i = first; i < first + cnt; ++i) {
-            const int pp = items[i].y;
-            const float mi = __ldcg(part_ml + ((int64_t)i * nrows + row) * 2);
-            if (mi == -INFINITY) continue;
-            const float sc = ex2f(mi - Mp[pp]);
-            Lp[pp] += sc * __ldcg(part_ml + ((int64_t)i * nrows + row) * 2 + 1);
-            Ap[pp] += sc * __ldcg(part_o + ((int64_t)i * nrows + row) * D + c);
+        // online log-sum-exp merge of the group's partials, per part; the loads
+        // of four partials are issued together
+        float Mp[2] = {-INFINITY, -INFINITY}, Lp[2] = {0.f, 0.f}, Ap[2] = {0.f, 0.f};
+        for (int i0 = first; i0 < first + cnt; i0 += 4) {
+            float mi[4], li[4], ai[4];
+            int pi[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = i0 + j < first + cnt;
+                const int64_t base = (int64_t)(ok ? i0 + j : first) * nrows + row;
+                mi[j] = ok ? __ldcg(part_ml + base * 2) : -INFINITY;
+                li[j] = ok ? __ldcg(part_ml + base * 2 + 1) : 0.f;
+                ai[j] = ok ? __ldcg(part_o + base * D + c) : 0.f;
+                pi[j] = ok ? __ldg(&items[i0 + j].y) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (mi[j] == -INFINITY) continue;
+                const int pp = pi[j];
+                const float Mo = pp ? Mp[1] : Mp[0];
+                const float Mn = fmaxf(Mo, mi[j]);
+                const float so = ex2f(Mo - Mn), sn = ex2f(mi[j] - Mn);
+                if (pp) {
+                    Lp[1] = Lp[1] * so + li[j] * sn; Ap[1] = Ap[1] * so + ai[j] * sn; Mp[1] = Mn;
+                } else {
+                    Lp[0] = Lp[0] * so + li[j] * sn; Ap[0] = Ap[0] * so + ai[j] * sn; Mp[0] = Mn;
+                }
+            }
         }
         const bool spec_row = row >= r;
         const int64_t orow = (int64_t)b * Hq + gk * r + (spec_row ? row - r : row);
@@ -421,31 +440,32 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
 // (sparse part, then window part, group after group) into one contiguous range
 // per CTA; the range is cut into work items at part boundaries, so a CTA runs
 // one to a few long items and pays the item epilogue (partial write, ticket)
-// that rarely.  One producer warp streams every 16-token tile of its items, K
-// rows then V rows, into a ring of ATT_STAGES shared-memory stages with
-// cp.async.bulk, one copy per run of contiguous source rows (a run breaks where
-// a block's slot does not follow the previous row's, and at the window ring's
-// wrap), completing on the stage's "full" mbarrier; it reads the slots of its
-// rows' blocks ATT_PF tiles ahead, so slot loads never stall the copies.  Four
-// compute warps take tiles round-robin, read their mma fragments from shared
-// memory with the lane mapping of the register-direct kernel, and release the
-// stage on its "empty" mbarrier.  Every mbarrier wait is bounded by the global
-// timer: on expiry the CTA records KVO_DEV_TIMEOUT and stops waiting (its
-// results are then invalid; the host sees the status bit).
-template <int D>
-struct AttnTmaSmem {
+// that rarely.  Within an item warp w takes tiles w, w+4, ..., and every warp
+// feeds itself: it keeps its next STG tiles in flight in a private ring of
+// shared-memory stages, each filled by cp.async.bulk copies (K rows and V
+// rows; one copy per run of contiguous source rows: a run breaks where a
+// block's slot does not follow the previous row's, and at the window ring's
+// wrap) completing on the stage's mbarrier.  After computing a tile from its
+// stage, the warp refills that stage with the tile STG places further down
+// its own tile stream, across work items, so copy issue is spread over all
+// warps and the loads stay STG tiles ahead of the math.  The fragments are
+// read from shared memory with the lane mapping of the register-direct kernel.
+// Every mbarrier wait is bounded by the global timer: on expiry the CTA
+// records KVO_DEV_TIMEOUT and stops waiting (its results are then invalid;
+// the host sees the status bit).
+template <int D, int NR>
+struct AttnTmaCfg {
+    // stages per warp: as deep as lets two CTAs share an SM
+    static constexpr int STG = D == 128 ? (NR == 1 ? 3 : 2) : 4;
     static constexpr int TILE_BYTES = ATT_TILE * D * 2;                  // one K (or V) tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int RING = ATT_STAGES * STAGE_BYTES;
-    static constexpr int O_OFF = RING;                                    // float [ATT_WARPS * 8 * NR][D]
-    static constexpr size_t bytes(int NR) {
-        return (size_t)RING + sizeof(float) * (ATT_WARPS * 8 * NR * D + 2 * ATT_WARPS * 16) +
-               sizeof(uint64_t) * 2 * ATT_STAGES + 16;
-    }
+    static constexpr int RING = ATT_WARPS * STG * STAGE_BYTES;
+    static constexpr int O_FLOATS = ATT_WARPS * 8 * NR * D;
+    static constexpr size_t BYTES = (size_t)RING + sizeof(float) * (O_FLOATS + 2 * ATT_WARPS * 16) +
+                                    sizeof(uint64_t) * ATT_WARPS * STG + 16;
 };
 
 constexpr long long kAttWaitNs = 2000000000LL;   // 2 s per mbarrier wait
-constexpr int ATT_PF = 4;                        // producer: tiles of slot lookahead
 
 // Bounded wait; false (and the CTA's abort flag set) when the limit passed.
 __device__ __forceinline__ bool att_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag,
@@ -465,74 +485,96 @@ __device__ __forceinline__ bool att_wait(uint32_t mbar, uint32_t parity, volatil
     }
 }
 
-// Producer warp: copy the nt tiles of one work item into the ring.  Lane j
-// handles row j & 15 of the K tile (j < 16) or of the V tile (j >= 16).
-template <int D>
-__device__ __forceinline__ void attn_produce(unsigned char* smem, uint64_t* full, uint64_t* empty,
-                                             volatile int* s_abort, int64_t qseq, int nt, int part, int bg,
-                                             int tile0, int n_tok, int ws, const uint16_t* __restrict__ bk,
-                                             const uint16_t* __restrict__ bv, const uint16_t* __restrict__ wk,
-                                             const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot,
-                                             int k, int B, int Wcap, int32_t* status) {
-    using SM = AttnTmaSmem<D>;
-    const int lane = threadIdx.x & 31, kv = lane >> 4, row = lane & 15;
-    int bad = 0;
-    // slot of the gathered block that holds this lane's row of tile tl
-    auto slot_of = [&](int tl) -> int {
-        const int tok = (tile0 + tl) * ATT_TILE + row;
-        if (part != 0 || tl >= nt || tok >= n_tok) return 0;
-        return __ldg(slot + (int64_t)bg * k + tok / B);
-    };
-    int pf[ATT_PF];
-#pragma unroll
-    for (int i = 0; i < ATT_PF; ++i) pf[i] = slot_of(i);
-    for (int t0 = 0; t0 < nt; t0 += ATT_PF) {
-#pragma unroll
-        for (int i = 0; i < ATT_PF; ++i) {
-            const int tl = t0 + i;
-            if (tl >= nt) break;
-            const int64_t qi = qseq + tl;
-            const int st = (int)(qi % ATT_STAGES);
-            const uint32_t fb = smem_u32(&full[st]);
-            if (lane == 0 && qi >= ATT_STAGES && !*s_abort)
-                att_wait(smem_u32(&empty[st]), (uint32_t)((qi / ATT_STAGES - 1) & 1), s_abort, status);
-            __syncwarp();
-            const int tb = (tile0 + tl) * ATT_TILE;
-            const int rows = min(ATT_TILE, n_tok - tb);
-            if (lane == 0) mbar_expect_tx(fb, (uint32_t)(rows * D * 2 * 2));
-            __syncwarp();
-            const int tok = tb + row;
-            const bool valid = row < rows;
-            const uint16_t* src;
-            bool start;
-            if (part == 0) {
-                const int blk = tok / B, off = tok - blk * B;
-                int sl = pf[i];
-                if (valid && (sl < 0 || sl >= 2 * k)) { bad |= KVO_DEV_BAD_SLOT; sl = 0; }
-                const int sl_prev = __shfl_up_sync(0xffffffffu, sl, 1);
-                src = (kv ? bv : bk) + (((int64_t)bg * 2 * k + sl) * B + off) * D;
-                start = valid && (row == 0 || (off == 0 && sl != sl_prev + 1));
-            } else {
-                int sw = ws + tok;
-                if (sw >= Wcap) sw -= Wcap;
-                src = (kv ? wv : wk) + ((int64_t)bg * Wcap + sw) * D;
-                start = valid && (row == 0 || sw == 0);
-            }
-            const unsigned starts = (__ballot_sync(0xffffffffu, start) >> (kv * 16)) & 0xffffu;
-            if (start) {
-                const unsigned later = starts & ~((2u << row) - 1u);
-                const int next = later ? __ffs(later) - 1 : rows;
-                const uint32_t dst = smem_u32(smem + st * SM::STAGE_BYTES + kv * SM::TILE_BYTES + row * D * 2);
-                bulk_load(dst, src, (uint32_t)((next - row) * D * 2), fb);
-            }
-            pf[i] = slot_of(tl + ATT_PF);
-        }
+// Where one warp stands in its tile stream: work item, tile of the item, and
+// the item's fields.  `item == hi` once the stream is exhausted.
+struct AttnCursor {
+    int item, hi, tl;
+    int bg, part, tile0, nt, n_tok, ws;
+};
+
+__device__ __forceinline__ void cursor_load(AttnCursor& c, const int4* __restrict__ items, int k, int B, int W,
+                                            const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len) {
+    const int4 it = items[c.item];
+    c.bg = it.x; c.part = it.y; c.tile0 = it.z;
+    c.ws = w_start ? w_start[c.bg] : 0;
+    c.n_tok = c.part == 0 ? k * B : (w_len ? w_len[c.bg] : W);
+    // tiles of the item that hold tokens (a window may be shorter than its items cover)
+    c.nt = max(0, min(it.w, (c.n_tok - c.tile0 * ATT_TILE + ATT_TILE - 1) / ATT_TILE));
+}
+
+// Move to the warp's next tile (tl += ATT_WARPS), into later items when needed.
+__device__ __forceinline__ void cursor_next(AttnCursor& c, int warp, const int4* __restrict__ items, int k, int B,
+                                            int W, const int32_t* __restrict__ w_start,
+                                            const int32_t* __restrict__ w_len) {
+    c.tl += ATT_WARPS;
+    while (c.tl >= c.nt && c.item < c.hi) {
+        if (++c.item == c.hi) break;
+        cursor_load(c, items, k, B, W, w_start, w_len);
+        c.tl = warp;
     }
-    if (bad) atomicOr(status, bad);
+}
+
+// Slot of the gathered block holding this lane's row (lane & 15) of the
+// cursor's tile (0 where the row does not exist or lies in the window).
+__device__ __forceinline__ int cursor_slot(const AttnCursor& c, const int32_t* __restrict__ slot, int k, int B,
+                                           int row) {
+    if (c.item >= c.hi || c.part != 0) return 0;
+    const int tok = (c.tile0 + c.tl) * ATT_TILE + row;
+    if (tok >= c.n_tok) return 0;
+    return __ldg(slot + (int64_t)c.bg * k + tok / B);
+}
+
+// Copy the cursor's tile into a stage: lane j copies row j & 15 of the K tile
+// (j < 16) or of the V tile (j >= 16); `sl` is the lane's cursor_slot.
+template <int D>
+__device__ __forceinline__ void tile_copy(const AttnCursor& c, int sl, unsigned char* stage, uint32_t fb,
+                                          const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
+                                          const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, int k,
+                                          int B, int Wcap, int& bad) {
+    const int lane = threadIdx.x & 31, kv = lane >> 4, row = lane & 15;
+    const int tb = (c.tile0 + c.tl) * ATT_TILE;
+    const int rows = min(ATT_TILE, c.n_tok - tb);
+    if (lane == 0) mbar_expect_tx(fb, (uint32_t)(rows * D * 2 * 2));
+    __syncwarp();
+    const int tok = tb + row;
+    const bool valid = row < rows;
+    const uint16_t* src;
+    bool start;
+    if (c.part == 0) {
+        const int blk = tok / B, off = tok - blk * B;
+        if (valid && (sl < 0 || sl >= 2 * k)) { bad |= KVO_DEV_BAD_SLOT; sl = 0; }
+        const int sl_prev = __shfl_up_sync(0xffffffffu, sl, 1);
+        src = (kv ? bv : bk) + (((int64_t)c.bg * 2 * k + sl) * B + off) * D;
+        start = valid && (row == 0 || (off == 0 && sl != sl_prev + 1));
+    } else {
+        int sw = c.ws + tok;
+        if (sw >= Wcap) sw -= Wcap;
+        src = (kv ? wv : wk) + ((int64_t)c.bg * Wcap + sw) * D;
+        start = valid && (row == 0 || sw == 0);
+    }
+    const unsigned starts = (__ballot_sync(0xffffffffu, start) >> (kv * 16)) & 0xffffu;
+    if (start) {
+        const unsigned later = starts & ~((2u << row) - 1u);
+        const int next = later ? __ffs(later) - 1 : rows;
+        bulk_load(smem_u32(stage + kv * (ATT_TILE * D * 2) + row * D * 2), src, (uint32_t)((next - row) * D * 2),
+                  fb);
+    }
+}
+
+__device__ __forceinline__ void cursor_first(AttnCursor& c, int lo, int hi, int warp, const int4* __restrict__ items,
+                                             int k, int B, int W, const int32_t* __restrict__ w_start,
+                                             const int32_t* __restrict__ w_len) {
+    c.item = lo; c.hi = hi; c.tl = warp; c.nt = 0;
+    if (c.item >= c.hi) return;
+    cursor_load(c, items, k, B, W, w_start, w_len);
+    while (c.tl >= c.nt) {
+        if (++c.item == c.hi) break;
+        cursor_load(c, items, k, B, W, w_start, w_len);
+    }
 }
 
 template <int D, int NR>
-__global__ void __launch_bounds__((ATT_WARPS + 1) * 32, 2)
+__global__ void __launch_bounds__(ATT_WARPS * 32, 2)
 attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
                 const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv, const uint16_t* __restrict__ wk,
                 const uint16_t* __restrict__ wv, const int32_t* __restrict__ slot, const int4* __restrict__ items,
@@ -543,113 +585,105 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
                 int Hkv, int k, int B, int W, int Wcap, const int32_t* __restrict__ w_start,
                 const int32_t* __restrict__ w_len, float scale_log2, int32_t* __restrict__ status) {
     using WA = WarpAttn<D, NR>;
-    using SM = AttnTmaSmem<D>;
-    constexpr int CH = WA::CH, CPT = WA::CPT;
-    constexpr int NTHR = ATT_WARPS * 32;              // compute threads
+    using CF = AttnTmaCfg<D, NR>;
+    constexpr int CH = WA::CH, CPT = WA::CPT, STG = CF::STG;
+    constexpr int NTHR = ATT_WARPS * 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    float* sm_o = reinterpret_cast<float*>(smem + SM::O_OFF);
-    float (*sm_m)[16] = reinterpret_cast<float (*)[16]>(sm_o + ATT_WARPS * 8 * NR * D);
+    float* sm_o = reinterpret_cast<float*>(smem + CF::RING);
+    float (*sm_m)[16] = reinterpret_cast<float (*)[16]>(sm_o + CF::O_FLOATS);
     float (*sm_l)[16] = sm_m + ATT_WARPS;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm_l + ATT_WARPS);
-    uint64_t* empty = full + ATT_STAGES;
-    int* s_last = reinterpret_cast<int*>(empty + ATT_STAGES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm_l + ATT_WARPS);   // [ATT_WARPS][STG]
+    int* s_last = reinterpret_cast<int*>(full + ATT_WARPS * STG);
     volatile int* s_abort = s_last + 1;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, tq = lane & 3;
-    if (tid == 0) {
-        for (int i = 0; i < ATT_STAGES; ++i) {
-            mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), 1);
-        }
-        *s_abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    const int gq = lane >> 2, tq = lane & 3, row = lane & 15;
+    if (tid < ATT_WARPS * STG) mbar_init(smem_u32(&full[tid]), 1);
+    if (tid == 0) *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
 
     const int Hq = Hkv * r;
     const int nrows = q_spec ? 2 * r : r;
-    const int item_lo = cta_first[blockIdx.x], item_hi = cta_first[blockIdx.x + 1];
-    int64_t qseq = 0;                                 // tiles issued / consumed so far by this CTA
-    for (int item = item_lo; item < item_hi; ++item) {
-        const int4 it = items[item];
-        const int bg = it.x, part = it.y, tile0 = it.z;
-        const int b = bg / Hkv, gk = bg % Hkv;
-        const int ws = w_start ? w_start[bg] : 0;
-        const int n_tok = part == 0 ? k * B : (w_len ? w_len[bg] : W);
-        // tiles of this item that hold tokens (a window may be shorter than its items cover)
-        const int nt = max(0, min(it.w, (n_tok - tile0 * ATT_TILE + ATT_TILE - 1) / ATT_TILE));
+    const int lo = cta_first[blockIdx.x], hi = cta_first[blockIdx.x + 1];
+    unsigned char* ring = smem + warp * STG * CF::STAGE_BYTES;
+    uint64_t* wfull = full + warp * STG;
+    int bad = 0;
 
-        if (warp == ATT_WARPS) {
-            attn_produce<D>(smem, full, empty, s_abort, qseq, nt, part, bg, tile0, n_tok, ws, bk, bv, wk, wv, slot,
-                            k, B, Wcap, status);
-        } else {
-            auto qrow = [&](int rr) -> const uint16_t* {
-                return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D
-                              : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
-            };
-            WA stt;
-            {
-                const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
-                stt.init(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq);
-            }
-            for (int tl = warp; tl < nt; tl += ATT_WARPS) {
-                const int64_t qi = qseq + tl;
-                const int st = (int)(qi % ATT_STAGES);
-                if (!*s_abort) att_wait(smem_u32(&full[st]), (uint32_t)((qi / ATT_STAGES) & 1), s_abort, status);
-                const int tb = (tile0 + tl) * ATT_TILE;
-                const int rows = min(ATT_TILE, n_tok - tb);
-                const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem + st * SM::STAGE_BYTES);
-                const uint16_t* vs = ks + ATT_TILE * D;
-                // rows past the tile's end hold stale data: read the last valid row instead
-                float sc[2][4];
-                {
-                    uint4 kf[2][CH];
+    // issue cursor: STG tiles ahead of the math in this warp's tile stream
+    AttnCursor ic;
+    cursor_first(ic, lo, hi, warp, items, k, B, W, w_start, w_len);
+    int isl = cursor_slot(ic, slot, k, B, row);
+    int64_t nissue = 0, ncons = 0;
+    auto issue = [&]() {
+        if (ic.item >= ic.hi) return;
+        const int st = (int)(nissue % STG);
+        tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad);
+        ++nissue;
+        cursor_next(ic, warp, items, k, B, W, w_start, w_len);
+        isl = cursor_slot(ic, slot, k, B, row);
+    };
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
-#pragma unroll
-                        for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
-                    }
-                    stt.qk(kf, sc);
-                }
-                uint4 vf[4][CPT / 8];
-#pragma unroll
-                for (int vi = 0; vi < 4; ++vi) {
-                    const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
-#pragma unroll
-                    for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
-                uint32_t pa[4];
-                float al0, al1;
-                stt.softmax(sc, tb, n_tok, scale_log2, tq, pa, al0, al1);
-                stt.pv(vf, pa, al0, al1);
-            }
-            stt.to_smem(sm_m, sm_l, sm_o + warp * 8 * NR * D, warp, gq, tq);
-            bar_named(1, NTHR);
-            attn_epilogue<D, NR>(sm_m, sm_l, sm_o, s_last, items, att_first, att_count, part_o, part_ml, done,
-                                 out_o, out_lse, out_o_spec, out_lse_spec, fuse, batch, r, Hkv, bg, nrows, item,
-                                 NTHR);
+    for (int i = 0; i < STG; ++i) issue();
+
+    for (int item = lo; item < hi; ++item) {
+        AttnCursor cc;                       // this item, from this warp's view
+        cc.item = item; cc.hi = hi;
+        cursor_load(cc, items, k, B, W, w_start, w_len);
+        const int b = cc.bg / Hkv, gk = cc.bg % Hkv;
+        auto qrow = [&](int rr) -> const uint16_t* {
+            return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
+        };
+        WA stt;
+        {
+            const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
+            stt.init(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq);
         }
-        qseq += nt;
+        for (int tl = warp; tl < cc.nt; tl += ATT_WARPS) {
+            const int st = (int)(ncons % STG);
+            if (!*s_abort) att_wait(smem_u32(&wfull[st]), (uint32_t)((ncons / STG) & 1), s_abort, status);
+            ++ncons;
+            const int tb = (cc.tile0 + tl) * ATT_TILE;
+            const int rows = min(ATT_TILE, cc.n_tok - tb);
+            const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * CF::STAGE_BYTES);
+            const uint16_t* vs = ks + ATT_TILE * D;
+            // rows past the tile's end hold stale data: read the last valid row instead
+            uint4 kf[2][CH];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
+#pragma unroll
+                for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
+            }
+            uint4 vf[4][CPT / 8];
+#pragma unroll
+            for (int vi = 0; vi < 4; ++vi) {
+                const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
+#pragma unroll
+                for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
+            }
+            stt.tile(kf, vf, tb, cc.n_tok, scale_log2, tq);
+            // the stage's shared-memory reads are done (their values fed the mma):
+            // order them before the async-proxy refill of the same stage
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue();
+        }
+        stt.to_smem(sm_m, sm_l, sm_o + warp * 8 * NR * D, warp, gq, tq);
+        bar_named(1, NTHR);
+        attn_epilogue<D, NR>(sm_m, sm_l, sm_o, s_last, items, att_first, att_count, part_o, part_ml, done, out_o,
+                             out_lse, out_o_spec, out_lse_spec, fuse, batch, r, Hkv, cc.bg, nrows, item, NTHR);
     }
-    // no copy may still target this CTA's shared memory when it exits: the
-    // producer waits (bounded) for the last fills of the ring
-    if (warp == ATT_WARPS && lane == 0 && !*s_abort) {
-        for (int64_t qi = max((int64_t)0, qseq - ATT_STAGES); qi < qseq; ++qi)
-            att_wait(smem_u32(&full[qi % ATT_STAGES]), (uint32_t)((qi / ATT_STAGES) & 1), s_abort, status);
-    }
+    if (bad) atomicOr(status, bad);
 }
 
 template <int D, int NR>
 static cudaError_t tma_attr(int* per_sm) {
     cudaError_t e = cudaFuncSetAttribute(attn_tma_kernel<D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)AttnTmaSmem<D>::bytes(NR));
+                                         (int)AttnTmaCfg<D, NR>::BYTES);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, attn_tma_kernel<D, NR>, (ATT_WARPS + 1) * 32,
-                                                         AttnTmaSmem<D>::bytes(NR));
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, attn_tma_kernel<D, NR>, ATT_WARPS * 32,
+                                                         AttnTmaCfg<D, NR>::BYTES);
 }
 
 // Shared-memory attribute of the TMA-staged kernel; SMs of the device and
@@ -679,7 +713,7 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
 #define KVO_ATT(D_, NR_)                                                                                         \
     if (c.att_impl == 1)                                                                                        \
-        attn_tma_kernel<D_, NR_><<<pl.grid, (ATT_WARPS + 1) * 32, AttnTmaSmem<D_>::bytes(NR_), s>>>(            \
+        attn_tma_kernel<D_, NR_><<<pl.grid, ATT_WARPS * 32, AttnTmaCfg<D_, NR_>::BYTES, s>>>(                   \
             (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, pl.items,      \
             pl.cta, pl.first, pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec,     \
             fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status);      \

@@ -18,7 +18,6 @@ constexpr int SEL_RPT_MAX = 4;            // select: landmark rows per thread (1
 constexpr int ATT_WARPS = 4;              // attention: warps per CTA
 constexpr int ATT_TILE = 16;              // attention: tokens per mma tile
 constexpr int ATT_TILES_PER_ITEM = 16;    // attention: tiles per CTA work item
-constexpr int ATT_STAGES = 8;             // TMA-staged attention: shared-memory ring stages (K + V tile each)
 constexpr int GATHER_THREADS = 256;
 constexpr int TMA_STAGE_BYTES = 16384;    // TMA gather: bytes per batch
 constexpr int TMA_MAX_PIECES = 64;        // TMA gather: pieces per batch
