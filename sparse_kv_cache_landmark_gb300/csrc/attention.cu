@@ -81,13 +81,27 @@ struct WarpAttn {
     float acc[NT][2 * NR];   // NR == 1: only rows 0..7 exist, so only c0/c1 are kept
     float m0, m1, l0, l1;
 
-    __device__ __forceinline__ void init(const uint16_t* q0, const uint16_t* q1, bool v0, bool v1, int tq) {
+    // the lane's Q words: rows g (w0) and 8+g (w1), channels 32s + 8t .. +8
+    static __device__ __forceinline__ void load_q(const uint16_t* q0, const uint16_t* q1, bool v0, bool v1, int tq,
+                                                  uint4 (&w0)[CH], uint4 (&w1)[CH]) {
 #pragma unroll
         for (int s = 0; s < CH; ++s) {
-            const uint4 w0 = v0 ? ldg16(q0 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
-            const uint4 w1 = v1 ? ldg16(q1 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
-            qa0[2 * s] = w0.x; qa2[2 * s] = w0.y; qa0[2 * s + 1] = w0.z; qa2[2 * s + 1] = w0.w;
-            qa1[2 * s] = w1.x; qa3[2 * s] = w1.y; qa1[2 * s + 1] = w1.z; qa3[2 * s + 1] = w1.w;
+            w0[s] = v0 ? ldg16(q0 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
+            w1[s] = (NR == 2 && v1) ? ldg16(q1 + 32 * s + 8 * tq) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+    __device__ __forceinline__ void init(const uint16_t* q0, const uint16_t* q1, bool v0, bool v1, int tq) {
+        uint4 w0[CH], w1[CH];
+        load_q(q0, q1, v0, v1, tq, w0, w1);
+        init_from(w0, w1);
+    }
+
+    __device__ __forceinline__ void init_from(const uint4 (&w0)[CH], const uint4 (&w1)[CH]) {
+#pragma unroll
+        for (int s = 0; s < CH; ++s) {
+            qa0[2 * s] = w0[s].x; qa2[2 * s] = w0[s].y; qa0[2 * s + 1] = w0[s].z; qa2[2 * s + 1] = w0[s].w;
+            qa1[2 * s] = w1[s].x; qa3[2 * s] = w1[s].y; qa1[2 * s + 1] = w1[s].z; qa3[2 * s + 1] = w1[s].w;
         }
 #pragma unroll
         for (int j = 0; j < NT; ++j)
@@ -263,15 +277,18 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
             part_ml[(item * nrows + row) * 2 + 1] = l;
         }
     }
-    __threadfence();
+    // the barrier makes the CTA's partial stores visible to thread 0, whose
+    // device-scope fence (cumulative) orders them before its ticket; the last
+    // CTA's fence after the ticket orders the merge's loads after it
     bar_named(1, nthr);
     if (tid == 0) {
-        const uint32_t prev = atomicAdd(&done[bg], 1u);
-        *s_last = prev + 1 == (uint32_t)att_count[bg];
+        __threadfence();
+        const bool last = atomicAdd(&done[bg], 1u) + 1 == (uint32_t)att_count[bg];
+        if (last) __threadfence();
+        *s_last = last;
     }
     bar_named(1, nthr);
     if (!*s_last) return;
-    __threadfence();
 
     const int first = att_first[bg], cnt = att_count[bg];
     const int64_t rows_total = (int64_t)batch * Hq;
@@ -453,6 +470,8 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
 // Every mbarrier wait is bounded by the global timer: on expiry the CTA
 // records KVO_DEV_TIMEOUT and stops waiting (its results are then invalid;
 // the host sees the status bit).
+constexpr int ATT_ITEMS_SMEM = 32;   // work-item headers a CTA keeps in shared memory
+
 template <int D, int NR>
 struct AttnTmaCfg {
     // stages per warp: as deep as lets two CTAs share an SM
@@ -462,7 +481,7 @@ struct AttnTmaCfg {
     static constexpr int RING = ATT_WARPS * STG * STAGE_BYTES;
     static constexpr int O_FLOATS = ATT_WARPS * 8 * NR * D;
     static constexpr size_t BYTES = (size_t)RING + sizeof(float) * (O_FLOATS + 2 * ATT_WARPS * 16) +
-                                    sizeof(uint64_t) * ATT_WARPS * STG + 16;
+                                    sizeof(uint64_t) * ATT_WARPS * STG + sizeof(int4) * ATT_ITEMS_SMEM + 16;
 };
 
 constexpr long long kAttWaitNs = 2000000000LL;   // 2 s per mbarrier wait
@@ -489,28 +508,59 @@ __device__ __forceinline__ bool att_wait(uint32_t mbar, uint32_t parity, volatil
 // the item's fields.  `item == hi` once the stream is exhausted.
 struct AttnCursor {
     int item, hi, tl;
-    int bg, part, tile0, nt, n_tok, ws;
+    int bg, part, tile0, ntiles, nt, n_tok, ws;
 };
 
-__device__ __forceinline__ void cursor_load(AttnCursor& c, const int4* __restrict__ items, int k, int B, int W,
-                                            const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len) {
-    const int4 it = items[c.item];
-    c.bg = it.x; c.part = it.y; c.tile0 = it.z;
-    c.ws = w_start ? w_start[c.bg] : 0;
-    c.n_tok = c.part == 0 ? k * B : (w_len ? w_len[c.bg] : W);
-    // tiles of the item that hold tokens (a window may be shorter than its items cover)
-    c.nt = max(0, min(it.w, (c.n_tok - c.tile0 * ATT_TILE + ATT_TILE - 1) / ATT_TILE));
+// Header of a work item: from the CTA's shared-memory copy of its first
+// ATT_ITEMS_SMEM items, else from global memory.
+__device__ __forceinline__ int4 item_hdr(const int4* s_items, const int4* __restrict__ items, int lo, int item) {
+    return item - lo < ATT_ITEMS_SMEM ? s_items[item - lo] : __ldg(items + item);
 }
 
+// Item fields from its header; the window start and length are read only for
+// the window part.  `nt` (tiles that hold tokens) is left to cursor_nt, so a
+// prefetching caller does not wait for the window length here.
+__device__ __forceinline__ void cursor_fields(AttnCursor& c, int4 it, int k, int B, int W,
+                                              const int32_t* __restrict__ w_start,
+                                              const int32_t* __restrict__ w_len) {
+    c.bg = it.x; c.part = it.y; c.tile0 = it.z; c.ntiles = it.w;
+    c.ws = (c.part == 1 && w_start) ? __ldg(w_start + c.bg) : 0;
+    c.n_tok = c.part == 0 ? k * B : (w_len ? __ldg(w_len + c.bg) : W);
+}
+// tiles of the item that hold tokens (a window may be shorter than its items cover)
+__device__ __forceinline__ void cursor_nt(AttnCursor& c) {
+    c.nt = max(0, min(c.ntiles, (c.n_tok - c.tile0 * ATT_TILE + ATT_TILE - 1) / ATT_TILE));
+}
+
+struct ItemSrc {
+    const int4* s_items;
+    const int4* items;
+    int lo, k, B, W;
+    const int32_t* w_start;
+    const int32_t* w_len;
+    __device__ __forceinline__ void load(AttnCursor& c) const {
+        cursor_fields(c, item_hdr(s_items, items, lo, c.item), k, B, W, w_start, w_len);
+        cursor_nt(c);
+    }
+};
+
 // Move to the warp's next tile (tl += ATT_WARPS), into later items when needed.
-__device__ __forceinline__ void cursor_next(AttnCursor& c, int warp, const int4* __restrict__ items, int k, int B,
-                                            int W, const int32_t* __restrict__ w_start,
-                                            const int32_t* __restrict__ w_len) {
+__device__ __forceinline__ void cursor_next(AttnCursor& c, int warp, const ItemSrc& src) {
     c.tl += ATT_WARPS;
     while (c.tl >= c.nt && c.item < c.hi) {
         if (++c.item == c.hi) break;
-        cursor_load(c, items, k, B, W, w_start, w_len);
+        src.load(c);
         c.tl = warp;
+    }
+}
+
+__device__ __forceinline__ void cursor_first(AttnCursor& c, int lo, int hi, int warp, const ItemSrc& src) {
+    c.item = lo; c.hi = hi; c.tl = warp; c.nt = 0;
+    if (c.item >= c.hi) return;
+    src.load(c);
+    while (c.tl >= c.nt) {
+        if (++c.item == c.hi) break;
+        src.load(c);
     }
 }
 
@@ -561,18 +611,6 @@ __device__ __forceinline__ void tile_copy(const AttnCursor& c, int sl, unsigned 
     }
 }
 
-__device__ __forceinline__ void cursor_first(AttnCursor& c, int lo, int hi, int warp, const int4* __restrict__ items,
-                                             int k, int B, int W, const int32_t* __restrict__ w_start,
-                                             const int32_t* __restrict__ w_len) {
-    c.item = lo; c.hi = hi; c.tl = warp; c.nt = 0;
-    if (c.item >= c.hi) return;
-    cursor_load(c, items, k, B, W, w_start, w_len);
-    while (c.tl >= c.nt) {
-        if (++c.item == c.hi) break;
-        cursor_load(c, items, k, B, W, w_start, w_len);
-    }
-}
-
 template <int D, int NR>
 __global__ void __launch_bounds__(ATT_WARPS * 32, 2)
 attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
@@ -593,26 +631,29 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     float (*sm_m)[16] = reinterpret_cast<float (*)[16]>(sm_o + CF::O_FLOATS);
     float (*sm_l)[16] = sm_m + ATT_WARPS;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm_l + ATT_WARPS);   // [ATT_WARPS][STG]
-    int* s_last = reinterpret_cast<int*>(full + ATT_WARPS * STG);
+    int4* s_items = reinterpret_cast<int4*>(full + ATT_WARPS * STG);  // [ATT_ITEMS_SMEM]
+    int* s_last = reinterpret_cast<int*>(s_items + ATT_ITEMS_SMEM);
     volatile int* s_abort = s_last + 1;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3, row = lane & 15;
+    const int lo = cta_first[blockIdx.x], hi = cta_first[blockIdx.x + 1];
     if (tid < ATT_WARPS * STG) mbar_init(smem_u32(&full[tid]), 1);
+    if (tid < ATT_ITEMS_SMEM && lo + tid < hi) s_items[tid] = items[lo + tid];
     if (tid == 0) *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
 
     const int Hq = Hkv * r;
     const int nrows = q_spec ? 2 * r : r;
-    const int lo = cta_first[blockIdx.x], hi = cta_first[blockIdx.x + 1];
+    const ItemSrc src{s_items, items, lo, k, B, W, w_start, w_len};
     unsigned char* ring = smem + warp * STG * CF::STAGE_BYTES;
     uint64_t* wfull = full + warp * STG;
     int bad = 0;
 
     // issue cursor: STG tiles ahead of the math in this warp's tile stream
     AttnCursor ic;
-    cursor_first(ic, lo, hi, warp, items, k, B, W, w_start, w_len);
+    cursor_first(ic, lo, hi, warp, src);
     int isl = cursor_slot(ic, slot, k, B, row);
     int64_t nissue = 0, ncons = 0;
     auto issue = [&]() {
@@ -620,25 +661,33 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
         const int st = (int)(nissue % STG);
         tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad);
         ++nissue;
-        cursor_next(ic, warp, items, k, B, W, w_start, w_len);
+        cursor_next(ic, warp, src);
         isl = cursor_slot(ic, slot, k, B, row);
     };
 #pragma unroll
     for (int i = 0; i < STG; ++i) issue();
 
-    for (int item = lo; item < hi; ++item) {
-        AttnCursor cc;                       // this item, from this warp's view
-        cc.item = item; cc.hi = hi;
-        cursor_load(cc, items, k, B, W, w_start, w_len);
-        const int b = cc.bg / Hkv, gk = cc.bg % Hkv;
+    // the next item's fields and Q words, fetched one item ahead
+    const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
+    AttnCursor nc;
+    uint4 nq0[CH], nq1[CH];
+    auto fetch = [&](int item) {
+        nc.item = item; nc.hi = hi; nc.tl = warp;
+        cursor_fields(nc, item_hdr(s_items, items, lo, item), k, B, W, w_start, w_len);
+        const int b = nc.bg / Hkv, gk = nc.bg % Hkv;
         auto qrow = [&](int rr) -> const uint16_t* {
             return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
         };
+        WA::load_q(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq, nq0, nq1);
+    };
+    if (lo < hi) fetch(lo);
+
+    for (int item = lo; item < hi; ++item) {
+        AttnCursor cc = nc;                  // this item, from this warp's view
+        cursor_nt(cc);
         WA stt;
-        {
-            const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
-            stt.init(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq);
-        }
+        stt.init_from(nq0, nq1);
+        if (item + 1 < hi) fetch(item + 1);
         for (int tl = warp; tl < cc.nt; tl += ATT_WARPS) {
             const int st = (int)(ncons % STG);
             if (!*s_abort) att_wait(smem_u32(&wfull[st]), (uint32_t)((ncons / STG) & 1), s_abort, status);
