@@ -470,7 +470,7 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
 // Every mbarrier wait is bounded by the global timer: on expiry the CTA
 // records KVO_DEV_TIMEOUT and stops waiting (its results are then invalid;
 // the host sees the status bit).
-constexpr int ATT_ITEMS_SMEM = 32;   // work-item headers a CTA keeps in shared memory
+constexpr int ATT_ITEMS_SMEM = 8;    // work-item headers a CTA keeps in shared memory
 
 template <int D, int NR>
 struct AttnTmaCfg {

@@ -69,7 +69,8 @@ cudaError_t part_alloc(kvo::Ctx& c, int items) {
 // Work items of the TMA-staged attention kernel: the tiles of every group
 // (sparse part, then window part; window tiles up to the largest window the
 // context can hold), group after group, split into `grid` equal contiguous
-// ranges, each range cut at part boundaries.
+// ranges (their bounds rounded to a multiple of the CTA's warps, so the warps
+// of an item get equal tile counts), each range cut at part boundaries.
 kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
     const int64_t sp_tiles = (c.k * c.B + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
     const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;
@@ -78,10 +79,14 @@ kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
     grid = std::max<int64_t>(1, std::min<int64_t>(grid, T));
     std::vector<int4> items;
     std::vector<int32_t> cta(grid + 1), first(c.G, 0), count(c.G, 0);
+    auto bound = [&](int64_t j) {
+        const int64_t b = T * j / grid;
+        return j == grid ? T : std::min(T, b - b % kvo::ATT_WARPS);
+    };
     for (int64_t j = 0; j < grid; ++j) {
         cta[j] = (int32_t)items.size();
-        int64_t t = T * j / grid;
-        const int64_t hi = T * (j + 1) / grid;
+        int64_t t = bound(j);
+        const int64_t hi = bound(j + 1);
         while (t < hi) {
             const int g = (int)(t / per_g);
             const int64_t off = t - g * per_g;
