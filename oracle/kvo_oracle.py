@@ -43,7 +43,7 @@ import numpy as np
 
 __all__ = [
     "bf16_bits_to_f64", "group_tokens", "landmarks", "block_scores", "topk_blocks",
-    "kth_relative_gap", "index_diff", "coalesce_runs", "gather_slots",
+    "kth_relative_gap", "index_diff", "coalesce_runs", "gather_slots", "resident_assign", "resident_step",
     "attention_part", "merge_lse", "GroupResult", "decode_group", "decode_layer",
 ]
 
@@ -172,6 +172,64 @@ def gather_slots(rows_bits, block_size: int, runs, n_slots: int):
             buf[dst + m] = rows[blk * block_size:(blk + 1) * block_size]
             written[dst + m] = True
     return buf, written
+
+
+# ----------------------------------------------------------------------------
+# cross-step residency: delta prefetch
+#   ("NeuroPrefetcher: Storage-Aware Sparse LLM Inference via Delta
+#   Prefetching", title: fetch only what the previous step did not bring;
+#   DualDecoder §5.2 / Fig. 18: misses of the true index are fetched urgently)
+# ----------------------------------------------------------------------------
+def resident_assign(slots, need, keep=None):
+    """Make every block of ``need`` resident in one (layer, group)'s slot table.
+
+    ``slots``: sequence of length cap, the block id held by each slot (-1:
+    empty).  ``need``: ascending block ids that must be resident afterwards.
+    ``keep``: ascending block ids (or None) whose slots must not be reused.
+
+    Reading (the pages name delta prefetching but give no rule): blocks of
+    ``need`` already resident stay in their slots; the missing ones, in
+    ascending id order, take the reusable slots in ascending slot order, a slot
+    being reusable when it is empty or holds a block in neither ``need`` nor
+    ``keep``.
+
+    Returns (new slot table as a list, fetched [(block id, slot)] in ascending
+    id order, slot of each entry of ``need``).  Raises ValueError when the
+    reusable slots are too few.
+    """
+    new = [int(x) for x in slots]
+    where = {b: s for s, b in enumerate(new) if b >= 0}
+    need = [int(x) for x in need]
+    protect = set(need) | (set(int(x) for x in keep) if keep is not None else set())
+    missing = [x for x in need if x not in where]
+    reusable = [s for s, b in enumerate(new) if b < 0 or b not in protect]
+    if len(missing) > len(reusable):
+        raise ValueError("not enough reusable slots")
+    fetched = []
+    for x, s in zip(missing, reusable):
+        new[s] = x
+        fetched.append((x, s))
+    where = {b: s for s, b in enumerate(new) if b >= 0}
+    return new, fetched, [where[x] for x in need]
+
+
+def resident_step(slots, T, P_cur, P_next):
+    """One decode step of one (layer, group) with a resident block set.
+
+    Urgent phase: the true index T becomes resident, sparing the blocks of the
+    prediction P_cur made one step earlier (None on a cold start).  Prefetch
+    phase (after attention): the prediction P_next for the next step becomes
+    resident, sparing the blocks of T.  With a slot table of 2k entries neither
+    phase runs out of slots (k blocks needed, at most k more protected).
+
+    Returns (table after both phases, urgent fetches, slot of each T entry,
+    prefetch fetches); with P_next None the prefetch phase is skipped.
+    """
+    slots, urgent, slot_of_true = resident_assign(slots, T, P_cur)
+    pref = []
+    if P_next is not None:
+        slots, pref, _ = resident_assign(slots, P_next, T)
+    return slots, urgent, slot_of_true, pref
 
 
 # ----------------------------------------------------------------------------

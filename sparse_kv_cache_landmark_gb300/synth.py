@@ -22,6 +22,10 @@ Recipe per workload (see ``workloads.py``)
   "token_runs" places 60% of the planted tokens as isolated tokens and 40% in
   runs of U{2..64}, every segment separated by at least one unplanted token.
 * speculative query: q_spec = q + sigma * N(0,1) (sigma set per workload).
+* decode steps (cross-step runs): step s has q_s = n + delta * e_s and
+  q_spec_s = n + delta * e_{s+1} + sigma * f_s, with n, e_s, f_s ~ N(0,1)
+  drawn per step, so the speculative query is a noisy draw of the next step's
+  query; step 0 with delta = 0 is the single-step draw above.
 * ``attempts[b, g]`` re-seeds the query streams of one (request, KV head) group,
   so a caller can redraw a group whose selection margin is too thin.
 """
@@ -39,7 +43,7 @@ from .workloads import Workload
 MASK32 = 0xFFFFFFFF
 
 # stream ids
-_Q, _QS, _K, _V, _KS, _MU, _ASSIGN, _PLANT, _LEN, _SEG = range(1, 11)
+_Q, _QS, _K, _V, _KS, _MU, _ASSIGN, _PLANT, _LEN, _SEG, _QD = range(1, 12)
 
 
 # ---------------------------------------------------------------------------
@@ -169,6 +173,46 @@ def gen_group_query(w: Workload, seed: int, layer: int, b: int, g: int, attempt:
     e = normal_from_hash(hash_stream(idx, stream_key(seed, _QS, layer, b, g, attempt)))
     sig = torch.tensor(w.spec_sigma, dtype=torch.float32)
     return q, _bf16(n + sig * e).view(r, d)
+
+
+def gen_group_query_step(w: Workload, seed: int, layer: int, b: int, g: int, step: int, drift: float,
+                         attempt: int = 0):
+    """(q, q_spec) of one group at decode step ``step`` (bf16 ``[r][d]``; q_spec may be None).
+
+    q = bf16(n + drift * e_step), q_spec = bf16(n + drift * e_{step+1} + sigma * f_step):
+    the speculative query is a noisy estimate of the next step's query.
+    """
+    r, d = w.group_size, w.head_dim
+    idx = torch.arange(r * d, dtype=torch.int64)
+    n = normal_from_hash(hash_stream(idx, stream_key(seed, _Q, layer, b, g, attempt)))
+    dr = torch.tensor(drift, dtype=torch.float32)
+
+    def e(s):
+        return normal_from_hash(hash_stream(idx, stream_key(seed, _QD, layer, b, g, attempt, s)))
+    x = n if drift == 0 else n + dr * e(step)
+    q = _bf16(x).view(r, d)
+    if w.spec_sigma is None:
+        return q, None
+    key = (seed, _QS, layer, b, g, attempt) + ((step,) if step else ())
+    f = normal_from_hash(hash_stream(idx, stream_key(*key)))
+    y = n if drift == 0 else n + dr * e(step + 1)
+    sig = torch.tensor(w.spec_sigma, dtype=torch.float32)
+    return q, _bf16(y + sig * f).view(r, d)
+
+
+def gen_queries_step(w: Workload, seed: int, layer: int, step: int, drift: float, attempts=None):
+    """(q, q_spec) bf16 CPU tensors ``[b][Hq][d]`` of decode step ``step``."""
+    a = _attempts(w, attempts)
+    r, d = w.group_size, w.head_dim
+    q = torch.empty(w.batch, w.n_q_heads, d, dtype=torch.bfloat16)
+    qs = None if w.spec_sigma is None else torch.empty_like(q)
+    for b in range(w.batch):
+        for g in range(w.n_kv_heads):
+            qg, qsg = gen_group_query_step(w, seed, layer, b, g, step, drift, int(a[b, g]))
+            q[b, g * r:(g + 1) * r] = qg
+            if qs is not None:
+                qs[b, g * r:(g + 1) * r] = qsg
+    return q, qs
 
 
 def gen_queries(w: Workload, seed: int, layer: int, attempts=None):

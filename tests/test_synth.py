@@ -77,3 +77,21 @@ def test_channel_scale_and_clusters():
     blk = K[0].float().view(40, 64, 128)
     # tokens of one block scatter around one centroid with sigma ~0.3
     assert 0.2 < (blk - blk.mean(dim=1, keepdim=True)).std() < 0.4
+
+
+def test_step_queries_reduce_to_single_step_and_drift_as_stated():
+    from sparse_kv_cache_landmark_gb300.workloads import WORKLOADS
+    w = WORKLOADS["long_ctx_predict"].scaled(batch=2)
+    q0, qs0 = synth.gen_queries(w, 5, 0)
+    q, qs = synth.gen_queries_step(w, 5, 0, 0, 0.0)
+    assert torch.equal(q, q0) and torch.equal(qs, qs0)
+    # q_s - q_0(drift 0) ~ drift * N(0,1); q_spec_s - q_{s+1} ~ sigma * N(0,1)
+    drift = 0.1
+    qa, qsa = synth.gen_queries_step(w, 5, 0, 3, drift)
+    qb, _ = synth.gen_queries_step(w, 5, 0, 4, drift)
+    assert abs((qa.float() - q0.float()).std().item() - drift) < 0.01
+    assert abs((qsa.float() - qb.float()).std().item() - w.spec_sigma) < 0.01
+    # without speculation there is no q_spec; steps differ only through the drift
+    w2 = WORKLOADS["llama3_8b_decode"].scaled(batch=1)
+    qc, qsc = synth.gen_queries_step(w2, 5, 0, 2, 0.0)
+    assert qsc is None and torch.equal(qc, synth.gen_queries(w2, 5, 0)[0])
