@@ -85,6 +85,10 @@ typedef struct {
     int32_t max_append;   /* tokens each request may grow by through kvo_append (0: fixed cache).
                              > 0 needs W > 0 and W % B == 0; the host arrays then reserve
                              len_b + max_append rows per (request, KV head). */
+    int32_t resident;     /* 0: two-layer ping-pong buffer (DualDecoder §5.4).  1: cross-step delta
+                             prefetch -- every layer keeps a GPU-resident set of 2k block slots per
+                             (request, KV head) across decode steps, and kvo_decode_step fetches
+                             only the blocks the set lacks (see kvo_resident_slots). */
 } kvo_config;
 
 /*
@@ -269,13 +273,41 @@ kvo_status kvo_device_status(kvo_ctx* ctx, int32_t* code_out, kvo_stream_t strea
  *   kvo_landmarks: copy layer `layer`'s landmarks, in logical layout
  *   [G][C_max][d], to device memory `dst` (fp32 when B > 1; bf16 when B == 1),
  *   C_max = max_b C_b; rows past C_b are zero.
- *   kvo_buffer: device pointers of ping-pong half `buf`, K and V, each
- *   [G][2k][B][d] bf16 (valid until destroy).
+ *   kvo_buffer: device pointers of ping-pong half `buf` (0, 1) or, with
+ *   resident = 1, of layer l's resident block set (buf = 2 + l), K and V, each
+ *   [G][2k][B][d] bf16 (valid until destroy).  gather_coalesced,
+ *   sparse_decode_attn and sparse_decode_attn_cobatch accept the same ids.
  *   kvo_info: sizes the context derived: [0] C_max, [1] landmark bytes per
  *   layer, [2] ping-pong bytes (both halves, K+V), [3] scratch bytes.
  */
 kvo_status kvo_landmarks(kvo_ctx* ctx, int layer, void* dst, kvo_stream_t stream);
 kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
+
+/*
+ * Cross-step delta prefetch (resident = 1; "NeuroPrefetcher: Storage-Aware
+ * Sparse LLM Inference via Delta Prefetching", title; DualDecoder §5.2 /
+ * Fig. 18).  Per layer and (request, KV head) a table of 2k slots names the
+ * block each slot of the layer's resident set holds (-1: empty).  In every
+ * kvo_decode_step, per layer: (urgent) the true index T becomes resident --
+ * blocks already resident stay in their slots, the missing ones in ascending
+ * id order take the reusable slots in ascending slot order, a slot being
+ * reusable when empty or holding a block neither in T nor in the prediction P
+ * fetched for this step -- and only those blocks cross the host link, on the
+ * urgent stream; attention reads T through its slots; then (prefetch, with a
+ * speculative query) the prediction for the next step becomes resident the
+ * same way, sparing the blocks of T, on the low-priority stream.  Without a
+ * speculative query only the urgent phase runs (the previous step's T is
+ * spared).  CUDA-graph replay is not used in this mode.
+ *   kvo_resident_slots: synchronize, copy layer `layer`'s slot table
+ *   [G][2k] int32 to host memory `slots_out`.
+ *   kvo_resident_fetched: synchronize, write the blocks fetched since init (or
+ *   the last reset) to host out2[0] (urgent) and out2[1] (prefetch); reset != 0
+ *   zeroes the counters afterwards.
+ *   Errors: KVO_ERR_STATE when the context was built with resident = 0;
+ *   KVO_ERR_INVALID for a bad layer or a null pointer.
+ */
+kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out);
+kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset);
 kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);
 
 /*

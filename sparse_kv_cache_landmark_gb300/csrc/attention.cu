@@ -763,12 +763,12 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
 #define KVO_ATT(D_, NR_)                                                                                         \
     if (c.att_impl == 1)                                                                                        \
         attn_tma_kernel<D_, NR_><<<pl.grid, ATT_WARPS * 32, AttnTmaCfg<D_, NR_>::BYTES, s>>>(                   \
-            (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, pl.items,      \
+            (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, pl.items,      \
             pl.cta, pl.first, pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec,     \
             fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status);      \
     else                                                                                                        \
         attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                           \
-            (const uint16_t*)q, (const uint16_t*)q_spec, c.pp_k[buf], c.pp_v[buf], wk, wv, slot, c.att_items,   \
+            (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, c.att_items,   \
             c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,  \
             c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
     if (c.d == 128) {

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(1024)
 gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh,
                    const int64_t* __restrict__ g_off, const int32_t* __restrict__ g_C,
                    const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int slot_base,
+                   const int32_t* __restrict__ dslot,
                    uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int G, int k, int B, int D, int words_log2,
                    int32_t* __restrict__ status) {
     constexpr uint32_t CHUNK = 32 * U;                       // words per warp iteration
@@ -206,8 +207,8 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
         if (c0 >= lim) continue;
         const int C = g_C[bg];
         const int64_t src0 = g_off[bg];
-        const int64_t dst0 = ((int64_t)bg * 2 * k + slot_base) * B * D;
         const int32_t* ig = idx + (int64_t)bg * k;
+        const int32_t* sg = dslot ? dslot + (int64_t)bg * k : nullptr;
         uint4 a[U], b[U];
         int64_t to[U];
         bool ok[U];
@@ -219,14 +220,16 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
                 const uint32_t j = POW2 ? (i >> words_log2) : (i / words);
                 const uint32_t w = i - j * words;
                 const int32_t blk = __ldg(ig + j);
-                if (blk >= 0 && blk < C) {
+                // destination: slot slot_base + j, or the entry's own slot when a slot list is given
+                const int32_t sl = sg ? __ldg(sg + j) : slot_base + (int32_t)j;
+                if (blk >= 0 && blk < C && sl >= 0 && sl < 2 * k) {
                     const int64_t off = (int64_t)blk * B * D + 8 * (int64_t)w;
                     a[u] = *reinterpret_cast<const uint4*>(kh + src0 + off);
                     b[u] = *reinterpret_cast<const uint4*>(vh + src0 + off);
-                    to[u] = dst0 + (int64_t)j * B * D + 8 * (int64_t)w;
+                    to[u] = ((int64_t)bg * 2 * k + sl) * B * D + 8 * (int64_t)w;
                     ok[u] = true;
                 } else {
-                    bad |= KVO_DEV_BAD_BLOCK_ID;
+                    bad |= (blk >= 0 && blk < C) ? KVO_DEV_BAD_SLOT : KVO_DEV_BAD_BLOCK_ID;
                 }
             }
         }
@@ -241,7 +244,7 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
 }
 
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int32_t* dslot) {
     const uint32_t words = (uint32_t)c.B * c.d / 8;
     int lg = -1;
     if ((words & (words - 1)) == 0) { lg = 0; while ((1u << lg) < words) ++lg; }
@@ -250,7 +253,8 @@ cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* 
     const size_t smem = (size_t)c.gather_reserve_smem;
 #define KVO_FLAT(U_, P_)                                                                                          \
     gather_flat_kernel<U_, P_><<<ctas, th, smem, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, idx, cnt, \
-                                                      slot_base, c.pp_k[buf], c.pp_v[buf], c.G, c.k, c.B, c.d, lg, \
+                                                      slot_base, dslot, c.buf_k(buf), c.buf_v(buf), c.G, c.k,     \
+                                                      c.B, c.d, lg,                                               \
                                                       c.status)
     if (lg >= 0) { if (c.gather_unroll >= 2) KVO_FLAT(2, true); else KVO_FLAT(1, true); }
     else { if (c.gather_unroll >= 2) KVO_FLAT(2, false); else KVO_FLAT(1, false); }
@@ -280,7 +284,7 @@ cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs,
     const int ctas = gather_default_ctas(c), th = c.gather_threads;
 #define KVO_GATHER(U_)                                                                                          \
     gather_kernel<U_><<<ctas, th, 0, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, (const int4*)runs, \
-                                          nruns, c.pp_k[buf], c.pp_v[buf], c.G, c.k, c.B, c.d, c.status)
+                                          nruns, c.buf_k(buf), c.buf_v(buf), c.G, c.k, c.B, c.d, c.status)
     if (c.gather_unroll >= 4) KVO_GATHER(4);
     else if (c.gather_unroll == 2) KVO_GATHER(2);
     else KVO_GATHER(1);

@@ -186,7 +186,7 @@ static cudaError_t launch_tma_stages(const Ctx& c, int layer, int buf, const int
     const int per_cta = STAGES >= 8 ? 1 : 2;
     const size_t smem = (size_t)per_cta * tma_driver_smem(STAGES);
     gather_tma_kernel<STAGES><<<(drivers + per_cta - 1) / per_cta, per_cta * 32, smem, s>>>(
-        c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, (const int4*)runs, nruns, c.pp_k[buf], c.pp_v[buf], c.G,
+        c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, (const int4*)runs, nruns, c.buf_k(buf), c.buf_v(buf), c.G,
         c.k, c.B, c.d, drivers, c.status);
     return cudaGetLastError();
 }

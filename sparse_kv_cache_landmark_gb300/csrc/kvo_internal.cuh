@@ -53,6 +53,21 @@ struct Ctx {
     uint16_t* pp_k[2] = {nullptr, nullptr};
     uint16_t* pp_v[2] = {nullptr, nullptr};
     size_t pp_bytes = 0;
+    // Resident mode (cross-step delta prefetch): one persistent block set of 2k
+    // slots per layer and group, laid out like a ping-pong half.
+    bool resident = false;
+    std::vector<uint16_t*> res_k, res_v;   // [L] -> [G][2k][B][d]
+    int32_t* res_map = nullptr;     // [L][G][Ccap] slot of each block, -1 when not resident
+    int32_t* res_slots = nullptr;   // [L][G][2k] block held by each slot, -1 when empty
+    int32_t* res_dslot = nullptr;   // [L][G][k] urgent fetches: destination slots
+    int32_t* res_pf_ids = nullptr;  // [L][G][k] prefetch fetches: block ids
+    int32_t* res_pf_cnt = nullptr;  // [L][G]
+    int32_t* res_pf_dslot = nullptr;// [L][G][k]
+    unsigned long long* res_fetched = nullptr;   // [2] blocks fetched: urgent, prefetch
+    std::vector<char> res_pending;  // [L] a prefetch into the layer's set was issued and not yet waited for
+    // K / V buffer by id: 0, 1 ping-pong halves; 2 + l resident set of layer l
+    uint16_t* buf_k(int buf) const { return buf < 2 ? pp_k[buf] : res_k[buf - 2]; }
+    uint16_t* buf_v(int buf) const { return buf < 2 ? pp_v[buf] : res_v[buf - 2]; }
     // select scratch
     uint32_t* sel_keys = nullptr;   // [2][G][Cmax]
     uint32_t* sel_hist = nullptr;   // [2][G][256]
@@ -109,6 +124,7 @@ struct Ctx {
     // event recorded inside a capture cannot be waited on outside it)
     struct EvSet {
         std::vector<cudaEvent_t> sel, attn, pref, urg;
+        std::vector<cudaEvent_t> rassign, rpref;   // resident mode, per layer: prefetch assigned / landed
         cudaEvent_t start = nullptr;
     } ev_eager, ev_graph;
     // optional per-launch timing of the decode step (kvo_profile)
@@ -182,7 +198,11 @@ cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs,
 cudaError_t launch_gather_tma(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                               cudaStream_t s);
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
-                               cudaStream_t s);
+                               cudaStream_t s, const int32_t* dslot = nullptr);
+cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
+                                   int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
+                                   int phase, cudaStream_t s);
+cudaError_t prepare_resident(const Ctx& c);
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
                              bool in_step = false);

@@ -1,0 +1,141 @@
+// Cross-step delta prefetch: per (layer, group) a GPU-resident block set of 2k
+// slots outlives the decode step, and each step fetches only the blocks it
+// does not already hold ("NeuroPrefetcher: Storage-Aware Sparse LLM Inference
+// via Delta Prefetching", title; "DualDecoder: Accelerate Long Context LLM
+// Inference by Predictive Prefetch", §5.2 / Fig. 18: the true index's misses
+// are fetched urgently before attention).
+//
+// Rule (the pages give none; the plainest one that keeps every copy
+// destination decided before the copy starts): the blocks of the `need` list
+// already resident stay in their slots; the missing ones, in ascending id
+// order, take the reusable slots in ascending slot order, a slot being
+// reusable when it is empty or holds a block in neither `need` nor `keep`.
+// The decode step calls it twice per layer: urgent (need = true index, keep =
+// the prediction fetched for this step) and, after attention, prefetch (need
+// = the prediction for the next step, keep = the true index).  With 2k slots
+// neither call runs out of reusable slots.
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+constexpr int RES_THREADS = 512;
+
+__device__ __forceinline__ bool sorted_contains(const int32_t* a, int n, int32_t x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < x) lo = mid + 1; else hi = mid;
+    }
+    return lo < n && a[lo] == x;
+}
+
+// One CTA per group.  map [G][Ccap] and slots [G][cap] are this layer's tables.
+// Outputs: the fetched blocks (ascending ids) with their destination slots and
+// count, and (optional) the slot of every need entry after the update.
+__global__ void __launch_bounds__(RES_THREADS)
+resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restrict__ keep,
+                       int32_t* __restrict__ map, int32_t* __restrict__ slots, const int32_t* __restrict__ g_C,
+                       int32_t* __restrict__ out_ids, int32_t* __restrict__ out_cnt, int32_t* __restrict__ out_dslot,
+                       int32_t* __restrict__ slot_of, unsigned long long* __restrict__ fetched, int k, int cap,
+                       int Ccap, int32_t* __restrict__ status) {
+    extern __shared__ __align__(16) int32_t rs[];
+    int32_t* s_need = rs;                  // [k]
+    int32_t* s_keep = s_need + k;          // [k]
+    int32_t* s_ev = s_keep + k;            // [cap] reusable slots in ascending order
+    int32_t* s_mid = s_ev + cap;           // [k] missing ids, ascending
+    __shared__ uint32_t warp_sums[RES_THREADS / 32];
+    __shared__ uint32_t s_tot;
+    const int g = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const int C = min(g_C[g], Ccap);
+    int32_t* mg = map + (int64_t)g * Ccap;
+    int32_t* sg = slots + (int64_t)g * cap;
+    int bad = 0;
+    for (int i = tid; i < k; i += nt) {
+        s_need[i] = need[(int64_t)g * k + i];
+        s_keep[i] = keep ? keep[(int64_t)g * k + i] : -1;
+    }
+    __syncthreads();
+    const int nk = keep ? k : 0;
+
+    // 1. reusable slots (each thread scans a contiguous chunk)
+    const int per = (cap + nt - 1) / nt;
+    const int s0 = min(cap, tid * per), s1 = min(cap, s0 + per);
+    uint32_t nev = 0;
+    for (int s = s0; s < s1; ++s) {
+        const int32_t b = sg[s];
+        nev += (b < 0 || (!sorted_contains(s_need, k, b) && !sorted_contains(s_keep, nk, b))) ? 1u : 0u;
+    }
+    uint32_t base = block_exclusive_scan(nev, warp_sums, &s_tot);
+    const uint32_t n_ev = s_tot;
+    for (int s = s0; s < s1; ++s) {
+        const int32_t b = sg[s];
+        if (b < 0 || (!sorted_contains(s_need, k, b) && !sorted_contains(s_keep, nk, b))) s_ev[base++] = s;
+    }
+
+    // 2. missing need entries (contiguous chunks keep the ascending order)
+    const int pk = (k + nt - 1) / nt;
+    const int i0 = min(k, tid * pk), i1 = min(k, i0 + pk);
+    uint32_t nm = 0;
+    for (int i = i0; i < i1; ++i) {
+        const int32_t x = s_need[i];
+        if (x < 0 || x >= C) { bad |= KVO_DEV_BAD_BLOCK_ID; continue; }
+        nm += mg[x] < 0 ? 1u : 0u;
+    }
+    base = block_exclusive_scan(nm, warp_sums, &s_tot);
+    const uint32_t n_miss = s_tot;
+    for (int i = i0; i < i1; ++i) {
+        const int32_t x = s_need[i];
+        if (x >= 0 && x < C && mg[x] < 0) s_mid[base++] = x;
+    }
+    __syncthreads();
+    const int n_fetch = (int)min(n_miss, n_ev);
+    if (n_miss > n_ev && tid == 0) bad |= KVO_DEV_BAD_COUNT;
+
+    // 3. evict the old occupants, then map the fetched blocks
+    for (int j = tid; j < n_fetch; j += nt) {
+        const int32_t old = sg[s_ev[j]];
+        if (old >= 0 && old < Ccap) mg[old] = -1;
+    }
+    __syncthreads();
+    for (int j = tid; j < n_fetch; j += nt) {
+        const int32_t x = s_mid[j], s = s_ev[j];
+        mg[x] = s;
+        sg[s] = x;
+        out_ids[(int64_t)g * k + j] = x;
+        out_dslot[(int64_t)g * k + j] = s;
+    }
+    __syncthreads();
+    if (slot_of) {
+        for (int i = tid; i < k; i += nt) {
+            const int32_t x = s_need[i];
+            int32_t s = (x >= 0 && x < C) ? mg[x] : -1;
+            if (s < 0) s = 0;                      // only after a reported error
+            slot_of[(int64_t)g * k + i] = s;
+        }
+    }
+    if (tid == 0) {
+        out_cnt[g] = n_fetch;
+        if (fetched && n_fetch) atomicAdd(fetched, (unsigned long long)n_fetch);
+    }
+    if (bad) atomicOr(status, bad);
+}
+
+static size_t res_smem(const Ctx& c) { return sizeof(int32_t) * (3 * (size_t)c.k + 2 * (size_t)c.k); }
+
+cudaError_t prepare_resident(const Ctx& c) {
+    return cudaFuncSetAttribute(resident_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)res_smem(c));
+}
+
+// phase 0: urgent (counts into res_fetched[0]), 1: prefetch (res_fetched[1])
+cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
+                                   int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
+                                   int phase, cudaStream_t s) {
+    const int cap = 2 * c.k;
+    resident_assign_kernel<<<c.G, RES_THREADS, res_smem(c), s>>>(
+        need, keep, c.res_map + (size_t)layer * c.G * c.Cmax, c.res_slots + (size_t)layer * c.G * cap, c.g_C,
+        out_ids, out_cnt, out_dslot, slot_of, c.res_fetched + phase, c.k, cap, c.Cmax, c.status);
+    return cudaGetLastError();
+}
+
+}  // namespace kvo

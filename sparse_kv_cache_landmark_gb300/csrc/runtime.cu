@@ -141,6 +141,10 @@ void free_ctx(kvo::Ctx& c) {
     F(c.d_ring_k); F(c.d_ring_v); F(c.d_host_k); F(c.d_host_v); F(c.d_lm);
     for (void* p : c.lm) F(p);
     for (int i = 0; i < 2; ++i) { F(c.pp_k[i]); F(c.pp_v[i]); }
+    for (void* p : c.res_k) F(p);
+    for (void* p : c.res_v) F(p);
+    F(c.res_map); F(c.res_slots); F(c.res_dslot); F(c.res_pf_ids); F(c.res_pf_cnt); F(c.res_pf_dslot);
+    F(c.res_fetched);
     F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
     F(c.runs); F(c.nruns);
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
@@ -148,7 +152,7 @@ void free_ctx(kvo::Ctx& c) {
     F(c.status);
     F(c.st_true); F(c.st_pred); F(c.st_miss); F(c.st_miss_cnt); F(c.st_slot);
     for (auto* E : {&c.ev_eager, &c.ev_graph}) {
-        for (auto* v : {&E->sel, &E->attn, &E->pref, &E->urg})
+        for (auto* v : {&E->sel, &E->attn, &E->pref, &E->urg, &E->rassign, &E->rpref})
             for (cudaEvent_t e : *v) if (e) cudaEventDestroy(e);
         if (E->start) cudaEventDestroy(E->start);
     }
@@ -193,6 +197,8 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     if (c.max_append > 0 && (c.W == 0 || c.W % c.B))
         return fail(&c, KVO_ERR_INVALID, "max_append > 0 needs window > 0 and window % block_size == 0");
     c.Wcap = c.max_append > 0 ? c.W + c.B : c.W;
+    if (cfg->resident < 0 || cfg->resident > 1) return fail(&c, KVO_ERR_INVALID, "resident must be 0 or 1");
+    c.resident = cfg->resident == 1;
     c.G = c.batch * c.Hkv;
     c.lens.assign(cfg->seq_lens, cfg->seq_lens + c.batch);
     std::vector<int64_t> off(c.G);
@@ -306,6 +312,30 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, cudaMemsetAsync(c.pp_v[i], 0, half, c.s_compute));
     }
     c.pp_bytes = 4 * half;
+    if (c.resident) {
+        // per-layer resident block sets and their slot tables (every slot empty)
+        c.res_k.assign(c.L, nullptr);
+        c.res_v.assign(c.L, nullptr);
+        for (int l = 0; l < c.L; ++l) {
+            KVO_CUDA(&c, dalloc(&c.res_k[l], half, nullptr));
+            KVO_CUDA(&c, dalloc(&c.res_v[l], half, nullptr));
+            KVO_CUDA(&c, cudaMemsetAsync(c.res_k[l], 0, half, c.s_compute));
+            KVO_CUDA(&c, cudaMemsetAsync(c.res_v[l], 0, half, c.s_compute));
+        }
+        const size_t lg = (size_t)c.L * c.G;
+        KVO_CUDA(&c, dalloc(&c.res_map, sizeof(int32_t) * lg * c.Cmax, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_slots, sizeof(int32_t) * lg * 2 * c.k, &sb));
+        KVO_CUDA(&c, cudaMemsetAsync(c.res_map, 0xff, sizeof(int32_t) * lg * c.Cmax, c.s_compute));
+        KVO_CUDA(&c, cudaMemsetAsync(c.res_slots, 0xff, sizeof(int32_t) * lg * 2 * c.k, c.s_compute));
+        KVO_CUDA(&c, dalloc(&c.res_dslot, sizeof(int32_t) * lg * c.k, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_pf_ids, sizeof(int32_t) * lg * c.k, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_pf_cnt, sizeof(int32_t) * lg, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_pf_dslot, sizeof(int32_t) * lg * c.k, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_fetched, sizeof(unsigned long long) * 2, &sb));
+        KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
+        c.res_pending.assign(c.L, 0);
+        KVO_CUDA(&c, kvo::prepare_resident(c));
+    }
     // selection scratch and work items
     const size_t Cmax4 = (size_t)((c.Cmax + 3) & ~3);
     KVO_CUDA(&c, dalloc(&c.sel_keys, sizeof(uint32_t) * 2 * c.G * Cmax4, &sb));
@@ -376,6 +406,10 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         }
         E->pref.assign(2, nullptr);
         for (auto& e : E->pref) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        for (auto* v : {&E->rassign, &E->rpref}) {
+            v->assign(c.resident ? c.L : 0, nullptr);
+            for (auto& e : *v) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        }
         KVO_CUDA(&c, cudaEventCreateWithFlags(&E->start, cudaEventDisableTiming));
     }
     KVO_CUDA(&c, cudaEventCreateWithFlags(&c.ev_gin, cudaEventDisableTiming));
@@ -388,6 +422,9 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
 }
 
 kvo_status check_ctx(kvo_ctx* ctx) { return ctx ? KVO_OK : fail(nullptr, KVO_ERR_INVALID, "null context"); }
+
+// buffer ids: 0, 1 ping-pong halves; 2 + l the resident set of layer l (resident mode)
+bool buf_ok(const kvo::Ctx& c, int buf) { return buf == 0 || buf == 1 || (c.resident && buf >= 2 && buf < 2 + c.L); }
 
 }  // namespace
 
@@ -446,7 +483,7 @@ kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
-    if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
+    if (!buf_ok(c, buf)) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1 (or 2 + layer with resident = 1)");
     if (!idx) return fail(&c, KVO_ERR_INVALID, "null idx");
     if (slot_base < 0 || slot_base > c.k) return fail(&c, KVO_ERR_INVALID, "slot_base must be in [0, k]");
     if (runs_out && ((uintptr_t)runs_out % 16)) return fail(&c, KVO_ERR_INVALID, "runs_out must be 16-byte aligned");
@@ -467,7 +504,7 @@ kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q, c
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
-    if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
+    if (!buf_ok(c, buf)) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1 (or 2 + layer with resident = 1)");
     if (!q || !slot_of_true || !o || !lse) return fail(&c, KVO_ERR_INVALID, "null pointer argument");
     KVO_CUDA(&c, kvo::launch_attention(c, layer, buf, q, nullptr, slot_of_true, o, lse, nullptr, nullptr,
                                        fuse_window_merge ? 1 : 0, pick(c, stream)));
@@ -625,6 +662,110 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
     return KVO_OK;
 }
 
+// Decode step with per-layer resident block sets (cross-step delta prefetch).
+// Per layer l: select (true index, and with q_spec the prediction for the next
+// step); urgent assign (T resident, sparing the prediction fetched for this
+// step) and urgent gather of just the blocks that were missing; attention over
+// the layer's resident set; then, with q_spec, prefetch assign (next step's
+// prediction resident, sparing T) and its gather on the low-priority stream.
+// Ordering: the next step's select of layer l waits for this step's prefetch
+// assign of l (it reads T and the slot table), and its attention for the
+// prefetch gather; urgent copies never touch slots of the prediction being
+// prefetched, because the urgent assign spares them.
+static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
+                                       float* o_spec, float* lse_spec, cudaStream_t s_user) {
+    kvo::Ctx& c = ctx->c;
+    kvo::Ctx::EvSet& E = c.ev_eager;
+    const size_t gk = (size_t)c.G * c.k;
+    const size_t q_layer = (size_t)c.batch * c.Hq * c.d;
+    const size_t o_layer = q_layer, lse_layer = (size_t)c.batch * c.Hq;
+    const int par = c.step_parity;
+    int32_t* pred_cur = c.st_pred + (size_t)par * c.L * gk;
+    int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
+    const bool have = c.have_pred;
+
+    KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
+    int cur_layer = -1;
+    auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
+        int e0, e1;
+        cudaError_t e = prof_mark(c, s, &e0);
+        if (e != cudaSuccess) return e;
+        e = launch();
+        if (e != cudaSuccess) return e;
+        e = prof_mark(c, s, &e1);
+        if (e != cudaSuccess) return e;
+        if (e0 >= 0) {
+            c.prof_recs.push_back({kind, e0, cur_layer});
+            c.prof_recs.push_back({-1, e1, cur_layer});
+        }
+        return cudaSuccess;
+    };
+    for (int l = 0; l < c.L; ++l) {
+        cur_layer = l;
+        const int buf = 2 + l;
+        const void* ql = (const char*)q + l * q_layer * 2;
+        const void* qsl = q_spec ? (const char*)q_spec + l * q_layer * 2 : nullptr;
+        int32_t* T = q_spec ? c.st_true + l * gk : pred_next + l * gk;
+        int32_t* slot = c.st_slot + l * gk;
+        int32_t* miss = c.st_miss + l * gk;
+        int32_t* mcnt = c.st_miss_cnt + (size_t)l * c.G;
+        int32_t* dsl = c.res_dslot + l * gk;
+        const bool pending = c.res_pending[l] != 0;
+        // the previous step's prefetch of this layer has read T and written the slot table
+        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.rassign[l], 0));
+        // 1. retrieval index (true; speculative -> next step's prediction)
+        KVO_CUDA(&c, timed(kvo::PK_SELECT, c.s_compute, [&] {
+            return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, c.s_compute);
+        }));
+        // 2. urgent assign: T resident, sparing the prediction fetched for this step
+        KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_compute, [&] {
+            return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
+                                               c.s_compute);
+        }));
+        KVO_CUDA(&c, cudaEventRecord(E.sel[l], c.s_compute));
+        // 3. urgent gather of the blocks that were missing
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.sel[l], 0));
+        // without a prediction nothing is spared: in-flight prefetch copies must land first
+        if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.rpref[l], 0));
+        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
+                           [&] { return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl); }));
+        KVO_CUDA(&c, cudaEventRecord(E.urg[l], c.s_urgent));
+        // 4. attention over the resident set once the urgent and prefetched blocks have landed
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
+        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.rpref[l], 0));
+        c.res_pending[l] = 0;
+        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
+            return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
+                                         lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute, true);
+        }));
+        KVO_CUDA(&c, cudaEventRecord(E.attn[l], c.s_compute));
+        // 5. prefetch of the next step's prediction, sparing T
+        if (q_spec) {
+            int32_t* pids = c.res_pf_ids + l * gk;
+            int32_t* pcnt = c.res_pf_cnt + (size_t)l * c.G;
+            int32_t* pdsl = c.res_pf_dslot + l * gk;
+            KVO_CUDA(&c, cudaStreamWaitEvent(c.s_prefetch, E.attn[l], 0));
+            KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_prefetch, [&] {
+                return kvo::launch_resident_assign(c, l, pred_next + l * gk, T, pids, pcnt, pdsl, nullptr, 1,
+                                                   c.s_prefetch);
+            }));
+            KVO_CUDA(&c, cudaEventRecord(E.rassign[l], c.s_prefetch));
+            KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
+                               [&] { return kvo::launch_gather_flat(c, l, buf, pids, pcnt, 0, c.s_prefetch, pdsl); }));
+            KVO_CUDA(&c, cudaEventRecord(E.rpref[l], c.s_prefetch));
+            c.res_pending[l] = 1;
+        }
+    }
+    // the caller's stream waits for the outputs; prefetches stay in flight
+    for (cudaStream_t s : {c.s_compute, c.s_urgent}) {
+        KVO_CUDA(&c, cudaEventRecord(E.start, s));
+        KVO_CUDA(&c, cudaStreamWaitEvent(s_user, E.start, 0));
+    }
+    return KVO_OK;
+}
+
 static void drop_graphs(kvo::Ctx& c) {
     for (auto& g : c.gexec)
         if (g) { cudaGraphExecDestroy(g); g = nullptr; }
@@ -634,7 +775,10 @@ static kvo_status decode_step_impl(kvo_ctx* ctx, const void* q, const void* q_sp
                                    float* o_spec, float* lse_spec, kvo_stream_t stream) {
     kvo::Ctx& c = ctx->c;
     cudaStream_t s_user = pick(c, stream);
-    if (c.use_graphs && c.have_pred && !c.prof_on) {
+    if (c.resident) {
+        kvo_status st = decode_step_resident(ctx, q, q_spec, o, lse, o_spec, lse_spec, s_user);
+        if (st != KVO_OK) return st;
+    } else if (c.use_graphs && c.have_pred && !c.prof_on) {
         const int par = c.step_parity;
         const void* key[6] = {q, q_spec, o, lse, o_spec, lse_spec};
         bool same = c.gexec[par] != nullptr;
@@ -700,7 +844,7 @@ kvo_status sparse_decode_attn_cobatch(kvo_ctx* ctx, int layer, int buf, const vo
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
-    if (buf != 0 && buf != 1) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1");
+    if (!buf_ok(c, buf)) return fail(&c, KVO_ERR_INVALID, "buf must be 0 or 1 (or 2 + layer with resident = 1)");
     if (!q || !q_spec || !slot_of_true || !o || !lse || !o_spec || !lse_spec)
         return fail(&c, KVO_ERR_INVALID, "null pointer argument");
     if (2 * c.r > 16) return fail(&c, KVO_ERR_INVALID, "co-batching needs 2 * n_q_heads / n_kv_heads <= 16");
@@ -758,9 +902,9 @@ kvo_status kvo_landmarks(kvo_ctx* ctx, int layer, void* dst, kvo_stream_t stream
 
 kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    if ((buf != 0 && buf != 1) || !k_out || !v_out) return fail(&ctx->c, KVO_ERR_INVALID, "bad buf or null output");
-    *k_out = ctx->c.pp_k[buf];
-    *v_out = ctx->c.pp_v[buf];
+    if (!buf_ok(ctx->c, buf) || !k_out || !v_out) return fail(&ctx->c, KVO_ERR_INVALID, "bad buf or null output");
+    *k_out = ctx->c.buf_k(buf);
+    *v_out = ctx->c.buf_v(buf);
     return KVO_OK;
 }
 
@@ -771,6 +915,31 @@ kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4) {
     out4[1] = (int64_t)ctx->c.lm_bytes;
     out4[2] = (int64_t)ctx->c.pp_bytes;
     out4[3] = (int64_t)ctx->c.scratch_bytes;
+    return KVO_OK;
+}
+
+kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
+    if (layer < 0 || layer >= c.L || !slots_out) return fail(&c, KVO_ERR_INVALID, "bad layer or null output");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    const size_t n = (size_t)c.G * 2 * c.k;
+    KVO_CUDA(&c, cudaMemcpy(slots_out, c.res_slots + (size_t)layer * n, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
+    return KVO_OK;
+}
+
+kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
+    if (!out2) return fail(&c, KVO_ERR_INVALID, "null output");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    unsigned long long h[2];
+    KVO_CUDA(&c, cudaMemcpy(h, c.res_fetched, sizeof(h), cudaMemcpyDeviceToHost));
+    out2[0] = (int64_t)h[0];
+    out2[1] = (int64_t)h[1];
+    if (reset) KVO_CUDA(&c, cudaMemset(c.res_fetched, 0, sizeof(h)));
     return KVO_OK;
 }
 

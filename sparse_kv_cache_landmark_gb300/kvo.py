@@ -24,7 +24,7 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
-           "kvo_set_attn_impl"]
+           "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -38,7 +38,8 @@ class _Config(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("n_layers", ctypes.c_int32),
-                ("seq_lens", ctypes.POINTER(ctypes.c_int32)), ("max_append", ctypes.c_int32)]
+                ("seq_lens", ctypes.POINTER(ctypes.c_int32)), ("max_append", ctypes.c_int32),
+                ("resident", ctypes.c_int32)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -76,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_gather_reserve.argtypes = [P, I]
         L.kvo_set_graphs.argtypes = [P, I]
         L.kvo_set_attn_impl.argtypes = [P, I, I]
+        L.kvo_resident_slots.argtypes = [P, I, ctypes.POINTER(ctypes.c_int32)]
+        L.kvo_resident_fetched.argtypes = [P, ctypes.POINTER(ctypes.c_int64), I]
         L.kvo_append.argtypes = [P, VP, VP, VP]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
@@ -160,11 +163,11 @@ class Context:
     def __init__(self, *, batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers,
                  seq_lens: Sequence[int], k_host: List[torch.Tensor], v_host: List[torch.Tensor],
                  k_win: Optional[List[torch.Tensor]] = None, v_win: Optional[List[torch.Tensor]] = None,
-                 max_append: int = 0):
+                 max_append: int = 0, resident: bool = False):
         L = lib()
         self._lens = (ctypes.c_int32 * batch)(*[int(x) for x in seq_lens])
         self.cfg = _Config(batch, n_q_heads, n_kv_heads, head_dim, block_size, top_k, window, n_layers, self._lens,
-                           max_append)
+                           max_append, int(bool(resident)))
         self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim = batch, n_q_heads, n_kv_heads, head_dim
         self.block_size, self.top_k, self.window, self.n_layers = block_size, top_k, window, n_layers
         self.G = batch * n_kv_heads
@@ -292,6 +295,19 @@ class Context:
     def set_graphs(self, enable: bool):
         """Replay warm decode steps from captured CUDA graphs (C: kvo_set_graphs)."""
         self._c(lib().kvo_set_graphs(self.ctx, int(bool(enable))))
+
+    def resident_slots(self, layer: int) -> torch.Tensor:
+        """Slot table of layer ``layer``'s resident set, int32 ``[G][2k]`` (-1 empty) (C: kvo_resident_slots)."""
+        out = torch.empty(self.G, 2 * self.top_k, dtype=torch.int32)
+        self._c(lib().kvo_resident_slots(self.ctx, layer,
+                                         ctypes.cast(out.data_ptr(), ctypes.POINTER(ctypes.c_int32))))
+        return out
+
+    def resident_fetched(self, reset: bool = False):
+        """(urgent, prefetch) blocks fetched since init or the last reset (C: kvo_resident_fetched)."""
+        out = (ctypes.c_int64 * 2)()
+        self._c(lib().kvo_resident_fetched(self.ctx, out, int(bool(reset))))
+        return int(out[0]), int(out[1])
 
     def set_attn_impl(self, impl: int, ctas: int = 0):
         """Attention kernel: 0 register-direct loads, 1 TMA-staged persistent with

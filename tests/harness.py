@@ -11,7 +11,7 @@ from sparse_kv_cache_landmark_gb300.kvo import Context
 class Case:
     """Host caches (pinned), windows (device), queries and a library context."""
 
-    def __init__(self, w, seed, attempts=None, n_layers=None, gen_device="cuda"):
+    def __init__(self, w, seed, attempts=None, n_layers=None, gen_device="cuda", resident=False):
         self.w, self.seed = w, seed
         self.L = n_layers or w.n_layers
         self.lens = synth.seq_lens(w, seed)
@@ -32,7 +32,8 @@ class Case:
         self.ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
                            block_size=w.block_size, top_k=w.top_k, window=w.window, n_layers=self.L,
                            seq_lens=self.lens, k_host=self.k_host, v_host=self.v_host,
-                           k_win=self.k_win if w.window > 0 else None, v_win=self.v_win if w.window > 0 else None)
+                           k_win=self.k_win if w.window > 0 else None, v_win=self.v_win if w.window > 0 else None,
+                           resident=resident)
 
     def _window(self, host):
         w = self.w

@@ -1,0 +1,125 @@
+"""Cross-step delta prefetch (resident block sets, kv_offload_init resident = 1)
+against the oracle over several decode steps with drifting queries: the slot
+tables and the fetch counts are bit-exact, attention is within the tolerance,
+and every occupied slot holds its block's bytes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from sparse_kv_cache_landmark_gb300 import synth
+from sparse_kv_cache_landmark_gb300.workloads import Workload
+from tests.harness import Case, assert_attn_close
+from tests.margins import MARGIN
+
+pytestmark = pytest.mark.gpu
+
+
+def _attempts(c, steps, drift):
+    """Per layer, attempts [b][Hkv] giving every group its selection margin at every step."""
+    w = c.w
+    r = w.group_size
+    out = []
+    for l in range(c.L):
+        a = np.zeros((w.batch, w.n_kv_heads), dtype=np.int64)
+        for b in range(w.batch):
+            for g in range(w.n_kv_heads):
+                C = (c.lens[b] - w.window) // w.block_size
+                lm = orc.landmarks(synth.bits(c.rows(l, b, g)), w.block_size, C)
+                for att in range(300):
+                    ok = True
+                    for s in range(steps):
+                        qg, qsg = synth.gen_group_query_step(w, c.seed, l, b, g, s, drift, att)
+                        gaps = [orc.kth_relative_gap(orc.block_scores(synth.bits(qg), lm), w.top_k)]
+                        if qsg is not None:
+                            gaps.append(orc.kth_relative_gap(orc.block_scores(synth.bits(qsg), lm), w.top_k))
+                        if min(gaps) < MARGIN:
+                            ok = False
+                            break
+                    if ok:
+                        a[b, g] = att
+                        break
+                else:
+                    raise AssertionError("no attempt with margins at every step")
+        out.append(a)
+    return out
+
+
+@pytest.mark.parametrize("spec,L,B,k,dual", [(True, 2, 16, 16, True), (False, 1, 16, 16, False),
+                                             (True, 1, 1, 64, False), (True, 3, 32, 8, False)])
+def test_resident_steps_match_the_oracle(spec, L, B, k, dual):
+    W, drift, steps, seed = 32, 0.15, 6, 321
+    n = W + B * 64 if B > 1 else W + 600
+    w = Workload(f"resident_B{B}", 2, 8, 2, 128, B, k, W, L, (n, n), spec_sigma=0.3 if spec else None)
+    c = Case(w, seed, gen_device="cpu", resident=True)
+    try:
+        att = _attempts(c, steps, drift)
+        G, r = w.batch * w.n_kv_heads, w.group_size
+        state = [[[-1] * (2 * k) for _ in range(G)] for _ in range(L)]
+        p_cur = [[None] * G for _ in range(L)]
+        n_urg = n_pref = 0
+        churn = []
+        for s in range(steps):
+            qq = [synth.gen_queries_step(w, seed, l, s, drift, att[l]) for l in range(L)]
+            q = torch.stack([x[0] for x in qq]).cuda().contiguous()
+            qs = torch.stack([x[1] for x in qq]).cuda().contiguous() if spec else None
+            if dual:
+                o, lse, o_sp, lse_sp = c.ctx.decode_step_dual(q, qs)
+            else:
+                o, lse = c.ctx.decode_step(q, qs)
+            torch.cuda.synchronize()
+            assert c.ctx.device_status() == 0
+            o, lse = o.cpu().numpy(), lse.cpu().numpy()
+            fetched_step = 0
+            for l in range(L):
+                table = c.ctx.resident_slots(l).numpy()
+                for b in range(w.batch):
+                    for g in range(w.n_kv_heads):
+                        i = b * w.n_kv_heads + g
+                        qg = synth.bits(qq[l][0][b, g * r:(g + 1) * r])
+                        qsg = synth.bits(qq[l][1][b, g * r:(g + 1) * r]) if spec else None
+                        ref = orc.decode_group(synth.bits(c.rows(l, b, g, "k")), synth.bits(c.rows(l, b, g, "v")),
+                                               qg, qsg, block_size=B, top_k=k, window=W)
+                        new, urg, _, pref = orc.resident_step(state[l][i], ref.T.tolist(), p_cur[l][i],
+                                                              ref.P.tolist() if spec else None)
+                        state[l][i] = new
+                        p_cur[l][i] = ref.P.tolist() if spec else ref.T.tolist()
+                        n_urg += len(urg)
+                        n_pref += len(pref)
+                        fetched_step += len(urg) + len(pref)
+                        assert table[i].tolist() == new, (s, l, b, g)
+                        rows = slice(b * w.n_q_heads + g * r, b * w.n_q_heads + (g + 1) * r)
+                        assert_attn_close(o[l, rows], ref.o, what=f"o step {s} layer {l}")
+                        assert_attn_close(lse[l, rows], ref.lse, what=f"lse step {s} layer {l}")
+                        if dual:
+                            assert_attn_close(o_sp[l, rows].cpu().numpy(), ref.o_spec, what="o_spec")
+            churn.append(fetched_step)
+            assert c.ctx.resident_fetched() == (n_urg, n_pref)
+        # the first step fetches everything; later steps only the drift's delta
+        assert churn[0] >= L * G * k and max(churn[1:]) < churn[0]
+        # every occupied slot holds its block's bytes
+        for l in range(L):
+            bk, bv = c.ctx.buffer(2 + l)
+            bk, bv = synth.bits(bk.cpu()), synth.bits(bv.cpu())
+            for b in range(w.batch):
+                for g in range(w.n_kv_heads):
+                    i = b * w.n_kv_heads + g
+                    kr, vr = synth.bits(c.rows(l, b, g, "k")), synth.bits(c.rows(l, b, g, "v"))
+                    for sl, x in enumerate(state[l][i]):
+                        if x >= 0:
+                            assert np.array_equal(bk[i, sl], kr[x * B:(x + 1) * B])
+                            assert np.array_equal(bv[i, sl], vr[x * B:(x + 1) * B])
+    finally:
+        c.close()
+
+
+def test_resident_calls_need_resident_mode():
+    w = Workload("plain", 1, 4, 1, 64, 16, 4, 16, 1, (16 + 16 * 8, 16 + 16 * 8))
+    c = Case(w, 1, gen_device="cpu")
+    try:
+        with pytest.raises(Exception, match="resident"):
+            c.ctx.resident_slots(0)
+        with pytest.raises(Exception, match="resident"):
+            c.ctx.resident_fetched()
+    finally:
+        c.close()
