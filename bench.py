@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 from sparse_kv_cache_landmark_gb300 import synth  # noqa: E402
-from sparse_kv_cache_landmark_gb300.workloads import WORKLOADS  # noqa: E402
+from sparse_kv_cache_landmark_gb300.workloads import SPEC_SIGMA_88, WORKLOADS  # noqa: E402
 
 METRIC = "sparse decode steps/s and effective KV GB/s (1 GB300) as % of HBM/PCIe roofline"
 UNIT = "steps/s"
@@ -67,6 +67,11 @@ def parse():
     ap.add_argument("--attn-impl", type=int, default=-1,
                     help="attention kernel: 0 register-direct, 1 TMA-staged persistent (-1: default)")
     ap.add_argument("--attn-ctas", type=int, default=0, help="TMA-staged attention grid (0: fill the SMs)")
+    ap.add_argument("--resident", type=int, default=0,
+                    help="1: cross-step delta prefetch (per-layer resident block sets), queries drifting per step")
+    ap.add_argument("--drift", type=float, default=-1.0,
+                    help="per-step query drift with --resident (default: the speculative noise / sqrt(2))")
+    ap.add_argument("--query-steps", type=int, default=8, help="distinct step queries cycled with --resident")
     return ap.parse_args()
 
 
@@ -85,11 +90,13 @@ def peaks():
 NCU_TRAFFIC = {("llama3_8b_decode", "gather_flat_kernel"): 72.669952e6 + 43.264e3}
 
 
-def workload_bytes(w, lens, misses_per_step=0):
+def workload_bytes(w, lens, misses_per_step=0, fetched_per_step=None):
     """Algorithmic bytes of one step (all layers): HBM and host link.
 
     ``misses_per_step``: blocks fetched by the urgent stream per step (summed
     over layers and groups) on top of the k prefetched blocks per group.
+    ``fetched_per_step`` (resident block sets): all blocks fetched per step,
+    replacing the k per group and the misses.
     """
     G, d, k, B, W, L = w.batch * w.n_kv_heads, w.head_dim, w.top_k, w.block_size, w.window, w.n_layers
     tok = 4 * d                                             # K+V bf16 bytes per token per KV head
@@ -103,6 +110,11 @@ def workload_bytes(w, lens, misses_per_step=0):
     urgent = misses_per_step * B * tok
     hbm = (lm_bytes + gathered + attended + q_bytes + out_bytes + meta) * L + urgent
     host = gathered * L + urgent
+    if fetched_per_step is not None:
+        moved = fetched_per_step * B * tok
+        hbm = (lm_bytes + attended + q_bytes + out_bytes + meta) * L + moved
+        host = moved
+        gathered = moved / (2 * L)      # per prefetch launch, split evenly between the two streams
     kv_attended = attended * L
     return {"hbm": hbm, "host": host, "kv_attended": kv_attended, "gather_per_launch": gathered, "urgent": urgent,
             "landmark_per_layer": lm_bytes, "attended_per_layer": attended}
@@ -314,7 +326,8 @@ def build_workload(args, ws=1):
     B.setup_s = time.perf_counter() - t_gen
     B.ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
                     block_size=w.block_size, top_k=w.top_k, window=w.window, n_layers=w.n_layers, seq_lens=lens,
-                    k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win, max_append=app)
+                    k_host=k_host, v_host=v_host, k_win=k_win, v_win=v_win, max_append=app,
+                    resident=bool(args.resident))
     B.app = app
     B.app_used = 0
     if app:
@@ -341,10 +354,31 @@ def build_workload(args, ws=1):
     B.qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
     B.q_dev = B.q_pin.to("cuda")
     B.qs_dev = None if B.qs_pin is None else B.qs_pin.to("cuda")
+    B.q_steps = None
+    if args.resident:
+        # decode steps whose queries drift: step s of layer l from gen_queries_step
+        B.drift = args.drift if args.drift >= 0 else SPEC_SIGMA_88 / math.sqrt(2.0)
+        qsteps = [[synth.gen_queries_step(w, args.seed, l, s, B.drift) for l in range(w.n_layers)]
+                  for s in range(args.query_steps)]
+        B.q_steps_pin = torch.stack([torch.stack([x[0] for x in st]) for st in qsteps]).pin_memory()
+        B.qs_steps_pin = (None if qsteps[0][0][1] is None else
+                          torch.stack([torch.stack([x[1] for x in st]) for st in qsteps]).pin_memory())
+        B.q_steps = B.q_steps_pin.to("cuda")
+        B.qs_steps = None if B.qs_steps_pin is None else B.qs_steps_pin.to("cuda")
+    B.step_i = 0
     rows = w.batch * w.n_q_heads
     B.o = torch.empty(w.n_layers, rows, w.head_dim, dtype=torch.float32, device="cuda")
     B.lse = torch.empty(w.n_layers, rows, dtype=torch.float32, device="cuda")
     return B
+
+
+def step_queries(B):
+    """With --resident, point the step at the next of the drifting query sets."""
+    if B.q_steps is not None:
+        i = B.step_i % B.q_steps.shape[0]
+        B.q_dev = B.q_steps[i]
+        B.qs_dev = None if B.qs_steps is None else B.qs_steps[i]
+        B.step_i += 1
 
 
 def time_steps(B, steps, ws=1, profile=True):
@@ -361,6 +395,7 @@ def time_steps(B, steps, ws=1, profile=True):
         if B.app:
             ctx.append(B.fut_k[B.app_used], B.fut_v[B.app_used])
             B.app_used += 1
+        step_queries(B)
         ctx.decode_step(B.q_dev, B.qs_dev, B.o, B.lse)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -400,8 +435,11 @@ def run_ours(args):
     del probe_h, probe_d
 
     for _ in range(max(3, args.warmup)):
-        ctx.decode_step(q_dev, qs_dev, o, lse)
+        step_queries(Bw)
+        ctx.decode_step(Bw.q_dev, Bw.qs_dev, o, lse)
     torch.cuda.synchronize()
+    if args.resident:
+        ctx.resident_fetched(reset=True)
 
     clocks = Clocks(local)
     time.sleep(0.3)
@@ -411,6 +449,7 @@ def run_ours(args):
     # pass of the same steps launched stream by stream.
     t_ms, prof = time_steps(Bw, args.steps, ws, profile=not graphs)
     clk = clocks.stop()
+    fetched = ctx.resident_fetched(reset=True) if args.resident else None
     if graphs:
         ctx.set_graphs(False)
         for _ in range(2):
@@ -427,10 +466,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        q_dev.copy_(q_pin, non_blocking=True)
-        if qs_pin is not None:
-            qs_dev.copy_(qs_pin, non_blocking=True)
+    for i in range(args.steps):
+        src, srcs = q_pin, qs_pin
+        if args.resident:
+            j = Bw.step_i % args.query_steps
+            Bw.step_i += 1
+            src = Bw.q_steps_pin[j]
+            srcs = None if Bw.qs_steps_pin is None else Bw.qs_steps_pin[j]
+        q_dev.copy_(src, non_blocking=True)
+        if srcs is not None:
+            qs_dev.copy_(srcs, non_blocking=True)
         ctx.decode_step(q_dev, qs_dev, o, lse)
         o_pin.copy_(o, non_blocking=True)
         lse_pin.copy_(lse, non_blocking=True)
@@ -445,7 +490,7 @@ def run_ours(args):
 
     # steady-state misses per step: each layer's true index against the prediction of the previous step
     misses = 0
-    for l in range(w.n_layers):
+    for l in range(w.n_layers if not args.resident else 0):
         T, P = ctx.select_topk(l, q_dev[l], None if qs_dev is None else qs_dev[l])
         _, cnt, _ = ctx.index_diff(T, P if P is not None else T)
         misses += int(cnt.sum().item())
@@ -477,7 +522,10 @@ def run_ours(args):
                "cobatched_over_two": round(co / two, 3),
                "note": "one layer's attention, isolated (no gather running), 20 back-to-back calls"}
     hbm_peak, peak_kind = peaks()
-    by = workload_bytes(w, lens, misses)
+    fetched_step = None if fetched is None else sum(fetched) / args.steps
+    by = workload_bytes(w, lens, misses, fetched_per_step=fetched_step)
+    if fetched is not None:       # prefetch launches move only the prediction's delta
+        by["gather_per_launch"] = fetched[1] / args.steps / w.n_layers * w.block_size * 4 * w.head_dim
     t_hbm = by["hbm"] / (hbm_peak * 1e9)
     t_link = by["host"] / (link * 1e9)
     t_star = max(t_hbm, t_link)
@@ -553,6 +601,12 @@ def run_ours(args):
                              "drivers": args.gather_drivers or "default"},
             "attention_kernel": {"impl": "default" if args.attn_impl < 0 else args.attn_impl,
                                  "ctas": args.attn_ctas or "default"},
+            "resident": None if not args.resident else {
+                "drift": Bw.drift, "query_steps": args.query_steps,
+                "fetched_blocks_per_step": fetched_step,
+                "fetched_of_selected": fetched_step / (w.n_layers * w.batch * w.n_kv_heads * w.top_k),
+                "urgent_blocks_per_step": fetched[0] / args.steps, "prefetch_blocks_per_step": fetched[1] / args.steps,
+                "note": "cross-step delta prefetch: per-layer resident sets of 2k blocks; host bytes = fetched blocks"},
         }
         print(json.dumps(line), flush=True)
     ctx.close()
