@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--drift", type=float, default=-1.0,
                     help="per-step query drift with --resident (default: the speculative noise / sqrt(2))")
     ap.add_argument("--query-steps", type=int, default=8, help="distinct step queries cycled with --resident")
+    ap.add_argument("--prefetch-budget", type=int, default=-1,
+                    help="with --resident: prefetch fetches admitted per group, layer and step (-1: all)")
     return ap.parse_args()
 
 
@@ -349,6 +351,8 @@ def build_workload(args, ws=1):
         B.ctx.set_graphs(bool(args.graphs))
     if args.attn_impl >= 0:
         B.ctx.set_attn_impl(args.attn_impl, args.attn_ctas)
+    if args.resident and args.prefetch_budget >= 0:
+        B.ctx.set_prefetch_budget(args.prefetch_budget)
     B.keep = (k_host, v_host, k_win, v_win)
     B.q_pin = torch.stack(qs_l).pin_memory()
     B.qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
@@ -602,7 +606,7 @@ def run_ours(args):
             "attention_kernel": {"impl": "default" if args.attn_impl < 0 else args.attn_impl,
                                  "ctas": args.attn_ctas or "default"},
             "resident": None if not args.resident else {
-                "drift": Bw.drift, "query_steps": args.query_steps,
+                "drift": Bw.drift, "query_steps": args.query_steps, "prefetch_budget": args.prefetch_budget,
                 "fetched_blocks_per_step": fetched_step,
                 "fetched_of_selected": fetched_step / (w.n_layers * w.batch * w.n_kv_heads * w.top_k),
                 "urgent_blocks_per_step": fetched[0] / args.steps, "prefetch_blocks_per_step": fetched[1] / args.steps,

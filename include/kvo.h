@@ -306,6 +306,17 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
  *   Errors: KVO_ERR_STATE when the context was built with resident = 0;
  *   KVO_ERR_INVALID for a bad layer or a null pointer.
  */
+/*
+ * kvo_set_prefetch_budget -- admission cap on the host bytes of speculation
+ * (resident = 1; PulseInfer §2 names I/O-adaptive offloading admission
+ * without a rule): each prefetch phase fetches at most `blocks` missing blocks
+ * per (request, KV head) and layer, those with the lowest ids; -1 (default)
+ * admits all.  The urgent phase is never capped, so results do not change:
+ * a block the cap left out that the true index needs is fetched urgently.
+ * Synchronizes the context's streams.  Errors: KVO_ERR_STATE with
+ * resident = 0; KVO_ERR_INVALID for blocks < -1.
+ */
+kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks);
 kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out);
 kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset);
 kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);

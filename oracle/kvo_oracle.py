@@ -180,7 +180,7 @@ def gather_slots(rows_bits, block_size: int, runs, n_slots: int):
 #   Prefetching", title: fetch only what the previous step did not bring;
 #   DualDecoder §5.2 / Fig. 18: misses of the true index are fetched urgently)
 # ----------------------------------------------------------------------------
-def resident_assign(slots, need, keep=None):
+def resident_assign(slots, need, keep=None, budget=None):
     """Make every block of ``need`` resident in one (layer, group)'s slot table.
 
     ``slots``: sequence of length cap, the block id held by each slot (-1:
@@ -193,15 +193,22 @@ def resident_assign(slots, need, keep=None):
     being reusable when it is empty or holds a block in neither ``need`` nor
     ``keep``.
 
+    ``budget`` (None: no limit) admits at most that many fetches: the missing
+    blocks with the lowest ids are fetched, the rest stay out (an admission cap
+    on host bytes; "PulseInfer and the I/O Problem Behind Long-Context
+    Decoding", §2 names I/O-adaptive offloading admission without a rule).
+
     Returns (new slot table as a list, fetched [(block id, slot)] in ascending
-    id order, slot of each entry of ``need``).  Raises ValueError when the
-    reusable slots are too few.
+    id order, slot of each entry of ``need``, -1 for entries left out by the
+    budget).  Raises ValueError when the reusable slots are too few.
     """
     new = [int(x) for x in slots]
     where = {b: s for s, b in enumerate(new) if b >= 0}
     need = [int(x) for x in need]
     protect = set(need) | (set(int(x) for x in keep) if keep is not None else set())
     missing = [x for x in need if x not in where]
+    if budget is not None:
+        missing = missing[:max(0, int(budget))]
     reusable = [s for s, b in enumerate(new) if b < 0 or b not in protect]
     if len(missing) > len(reusable):
         raise ValueError("not enough reusable slots")
@@ -210,10 +217,10 @@ def resident_assign(slots, need, keep=None):
         new[s] = x
         fetched.append((x, s))
     where = {b: s for s, b in enumerate(new) if b >= 0}
-    return new, fetched, [where[x] for x in need]
+    return new, fetched, [where.get(x, -1) for x in need]
 
 
-def resident_step(slots, T, P_cur, P_next):
+def resident_step(slots, T, P_cur, P_next, budget=None):
     """One decode step of one (layer, group) with a resident block set.
 
     Urgent phase: the true index T becomes resident, sparing the blocks of the
@@ -222,13 +229,16 @@ def resident_step(slots, T, P_cur, P_next):
     resident, sparing the blocks of T.  With a slot table of 2k entries neither
     phase runs out of slots (k blocks needed, at most k more protected).
 
+    ``budget`` caps the prefetch phase's fetches (the urgent phase is never
+    capped: the true index must be resident for attention).
+
     Returns (table after both phases, urgent fetches, slot of each T entry,
     prefetch fetches); with P_next None the prefetch phase is skipped.
     """
     slots, urgent, slot_of_true = resident_assign(slots, T, P_cur)
     pref = []
     if P_next is not None:
-        slots, pref, _ = resident_assign(slots, P_next, T)
+        slots, pref, _ = resident_assign(slots, P_next, T, budget)
     return slots, urgent, slot_of_true, pref
 
 

@@ -65,6 +65,7 @@ struct Ctx {
     int32_t* res_pf_dslot = nullptr;// [L][G][k]
     unsigned long long* res_fetched = nullptr;   // [2] blocks fetched: urgent, prefetch
     std::vector<char> res_pending;  // [L] a prefetch into the layer's set was issued and not yet waited for
+    int res_budget = -1;            // prefetch fetches admitted per group, layer and step (-1: all)
     // K / V buffer by id: 0, 1 ping-pong halves; 2 + l resident set of layer l
     uint16_t* buf_k(int buf) const { return buf < 2 ? pp_k[buf] : res_k[buf - 2]; }
     uint16_t* buf_v(int buf) const { return buf < 2 ? pp_v[buf] : res_v[buf - 2]; }
@@ -201,7 +202,7 @@ cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* 
                                cudaStream_t s, const int32_t* dslot = nullptr);
 cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
                                    int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
-                                   int phase, cudaStream_t s);
+                                   int phase, cudaStream_t s, int max_fetch = -1);
 cudaError_t prepare_resident(const Ctx& c);
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,

@@ -749,7 +749,7 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             KVO_CUDA(&c, cudaStreamWaitEvent(c.s_prefetch, E.attn[l], 0));
             KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_prefetch, [&] {
                 return kvo::launch_resident_assign(c, l, pred_next + l * gk, T, pids, pcnt, pdsl, nullptr, 1,
-                                                   c.s_prefetch);
+                                                   c.s_prefetch, c.res_budget);
             }));
             KVO_CUDA(&c, cudaEventRecord(E.rassign[l], c.s_prefetch));
             KVO_CUDA(&c, timed(kvo::PK_GATHER_PREFETCH, c.s_prefetch,
@@ -926,6 +926,16 @@ kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out) {
     for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     const size_t n = (size_t)c.G * 2 * c.k;
     KVO_CUDA(&c, cudaMemcpy(slots_out, c.res_slots + (size_t)layer * n, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
+    return KVO_OK;
+}
+
+kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
+    if (blocks < -1) return fail(&c, KVO_ERR_INVALID, "blocks must be >= -1");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    c.res_budget = blocks;
     return KVO_OK;
 }
 

@@ -24,7 +24,8 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
-           "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched"]
+           "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched",
+           "kvo_set_prefetch_budget"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
 
 
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_attn_impl.argtypes = [P, I, I]
         L.kvo_resident_slots.argtypes = [P, I, ctypes.POINTER(ctypes.c_int32)]
         L.kvo_resident_fetched.argtypes = [P, ctypes.POINTER(ctypes.c_int64), I]
+        L.kvo_set_prefetch_budget.argtypes = [P, I]
         L.kvo_append.argtypes = [P, VP, VP, VP]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
@@ -302,6 +304,10 @@ class Context:
         self._c(lib().kvo_resident_slots(self.ctx, layer,
                                          ctypes.cast(out.data_ptr(), ctypes.POINTER(ctypes.c_int32))))
         return out
+
+    def set_prefetch_budget(self, blocks: int):
+        """Cap prefetch fetches per group, layer and step (-1: no cap) (C: kvo_set_prefetch_budget)."""
+        self._c(lib().kvo_set_prefetch_budget(self.ctx, blocks))
 
     def resident_fetched(self, reset: bool = False):
         """(urgent, prefetch) blocks fetched since init or the last reset (C: kvo_resident_fetched)."""

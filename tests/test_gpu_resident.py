@@ -45,15 +45,18 @@ def _attempts(c, steps, drift):
     return out
 
 
-@pytest.mark.parametrize("spec,L,B,k,dual", [(True, 2, 16, 16, True), (False, 1, 16, 16, False),
-                                             (True, 1, 1, 64, False), (True, 3, 32, 8, False)])
-def test_resident_steps_match_the_oracle(spec, L, B, k, dual):
+@pytest.mark.parametrize("spec,L,B,k,dual,budget", [(True, 2, 16, 16, True, None), (False, 1, 16, 16, False, None),
+                                                    (True, 1, 1, 64, False, None), (True, 3, 32, 8, False, None),
+                                                    (True, 2, 16, 16, False, 3)])
+def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget):
     W, drift, steps, seed = 32, 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
     w = Workload(f"resident_B{B}", 2, 8, 2, 128, B, k, W, L, (n, n), spec_sigma=0.3 if spec else None)
     c = Case(w, seed, gen_device="cpu", resident=True)
     try:
         att = _attempts(c, steps, drift)
+        if budget is not None:
+            c.ctx.set_prefetch_budget(budget)     # admission cap on speculative fetches
         G, r = w.batch * w.n_kv_heads, w.group_size
         state = [[[-1] * (2 * k) for _ in range(G)] for _ in range(L)]
         p_cur = [[None] * G for _ in range(L)]
@@ -81,7 +84,7 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual):
                         ref = orc.decode_group(synth.bits(c.rows(l, b, g, "k")), synth.bits(c.rows(l, b, g, "v")),
                                                qg, qsg, block_size=B, top_k=k, window=W)
                         new, urg, _, pref = orc.resident_step(state[l][i], ref.T.tolist(), p_cur[l][i],
-                                                              ref.P.tolist() if spec else None)
+                                                              ref.P.tolist() if spec else None, budget)
                         state[l][i] = new
                         p_cur[l][i] = ref.P.tolist() if spec else ref.T.tolist()
                         n_urg += len(urg)
@@ -121,5 +124,7 @@ def test_resident_calls_need_resident_mode():
             c.ctx.resident_slots(0)
         with pytest.raises(Exception, match="resident"):
             c.ctx.resident_fetched()
+        with pytest.raises(Exception, match="resident"):
+            c.ctx.set_prefetch_budget(4)
     finally:
         c.close()

@@ -108,3 +108,24 @@ def test_disjoint_selections_fetch_everything():
 def test_too_few_slots_raise():
     with pytest.raises(ValueError):
         orc.resident_assign([1, 2], [3, 4], [1])
+
+
+def test_budget_admits_the_lowest_missing_ids_and_urgent_fills_the_rest():
+    # hand case: 3 missing (5, 6, 8); budget 2 admits 5 and 6 only
+    new, fetched, slot_of = orc.resident_assign([3, 9, -1, 4, -1, -1], [4, 5, 6, 8], [9], budget=2)
+    assert fetched == [(5, 0), (6, 2)] and slot_of == [3, 0, 2, -1]
+    assert new == [5, 9, 6, 4, -1, -1]
+    # a capped prefetch never changes what the urgent phase leaves resident for T
+    rng = np.random.default_rng(7)
+    k, n = 8, 40
+    s_free = s_cap = [-1] * (2 * k)
+    P = None
+    for step in range(30):
+        T = _sorted_sample(rng, n, k)
+        P_next = _sorted_sample(rng, n, k)
+        s_free, u1, sot1, p1 = orc.resident_step(s_free, T, P, P_next)
+        s_cap, u2, sot2, p2 = orc.resident_step(s_cap, T, P, P_next, budget=2)
+        assert len(p2) <= 2
+        assert all(s_free[s] == x for x, s in zip(T, sot1))
+        assert all(s_cap[s] == x for x, s in zip(T, sot2))
+        P = P_next
