@@ -44,6 +44,7 @@ import numpy as np
 __all__ = [
     "bf16_bits_to_f64", "group_tokens", "landmarks", "block_scores", "topk_blocks",
     "kth_relative_gap", "index_diff", "coalesce_runs", "gather_slots", "resident_assign", "resident_step",
+    "lowrank_keys", "f32_to_bf16_bits",
     "attention_part", "merge_lse", "GroupResult", "decode_group", "decode_layer",
 ]
 
@@ -240,6 +241,35 @@ def resident_step(slots, T, P_cur, P_next, budget=None):
     if P_next is not None:
         slots, pref, _ = resident_assign(slots, P_next, T, budget)
     return slots, urgent, slot_of_true, pref
+
+
+# ----------------------------------------------------------------------------
+# low-rank key reconstruction   (DualDecoder §5.3: keys of missed entries are
+# rebuilt on the GPU from a GPU-resident low-rank key cache instead of fetched)
+# ----------------------------------------------------------------------------
+def f32_to_bf16_bits(x) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest, ties to even (finite inputs)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def lowrank_keys(coef_bits, basis_bits) -> np.ndarray:
+    """Key rows of rank-R factors as the synthetic low-rank keys define them.
+
+    K[t][c] = bf16( sum over j = 0 .. R-1 ascending of a[t][j] * e[j][c] ), with
+    a ``[n][R]`` and e ``[R][d]`` bf16, every product and every partial sum
+    rounded to float32 (no fused multiply-add), the total rounded to bf16 to
+    nearest-even.  Returns uint16 bits ``[n][d]``.  The precision is the one the
+    keys are defined with, so this is their exact value, not an approximation.
+    """
+    a = bf16_bits_to_f64(coef_bits).astype(np.float32)
+    e = bf16_bits_to_f64(basis_bits).astype(np.float32)
+    acc = np.zeros((a.shape[0], e.shape[1]), dtype=np.float32)
+    for j in range(a.shape[1]):
+        prod = (a[:, j:j + 1] * e[j:j + 1, :]).astype(np.float32)
+        acc = (acc + prod).astype(np.float32)
+    return f32_to_bf16_bits(acc)
 
 
 # ----------------------------------------------------------------------------

@@ -16,7 +16,10 @@ Recipe per workload (see ``workloads.py``)
 * q, V ~ N(0,1); K ~ N(0,1), or N(0,1) * s_c with a per-(layer, KV head,
   channel) scale s_c ~ U(0.5, 2) ("channel_scaled"), or mu_m + sigma N(0,1) with
   one of 32 per-(request, KV head) centroids mu_m ~ N(0,1) drawn per block
-  ("clustered").
+  ("clustered"), or a rank-R product ("lowrank"): K[t][c] = bf16(sum_j
+  a[t][j] * e[j][c]) with bf16 coefficients a ~ N(0,1) and basis rows
+  e ~ N(0,1)/sqrt(R), the sum taken in ascending j with every multiply and add
+  rounded to fp32 (so a GPU that repeats those roundings rebuilds K exactly).
 * planting: the keys of chosen blocks / tokens get + beta * u_hat, u_hat the
   unit direction of the group's summed query, so they are high scorers.
   "token_runs" places 60% of the planted tokens as isolated tokens and 40% in
@@ -43,7 +46,7 @@ from .workloads import Workload
 MASK32 = 0xFFFFFFFF
 
 # stream ids
-_Q, _QS, _K, _V, _KS, _MU, _ASSIGN, _PLANT, _LEN, _SEG, _QD = range(1, 12)
+_Q, _QS, _K, _V, _KS, _MU, _ASSIGN, _PLANT, _LEN, _SEG, _QD, _LRC, _LRB = range(1, 14)
 
 
 # ---------------------------------------------------------------------------
@@ -274,6 +277,32 @@ def planted_blocks(w: Workload, seed: int, layer: int, b: int, g: int, n_cand: i
     raise ValueError(w.plant)
 
 
+def gen_lowrank_factors(w: Workload, seed: int, layer: int, b: int, n_tok: int, device="cpu"):
+    """Rank-R key factors of request b: coefficients bf16 ``[Hkv][n_tok][R]``, basis bf16 ``[Hkv][R][d]``."""
+    H, d, R = w.n_kv_heads, w.head_dim, w.lowrank_rank
+    cidx = torch.arange(n_tok * R, dtype=torch.int64, device=device).view(1, -1)
+    kc = torch.tensor([stream_key(seed, _LRC, layer, b, g) for g in range(H)], dtype=torch.int64,
+                      device=device).view(H, 1)
+    coef = _bf16(normal_from_hash(hash_stream(cidx, kc))).view(H, n_tok, R)
+    bidx = torch.arange(R * d, dtype=torch.int64, device=device).view(1, -1)
+    kb = torch.tensor([stream_key(seed, _LRB, layer, b, g) for g in range(H)], dtype=torch.int64,
+                      device=device).view(H, 1)
+    scale = torch.tensor(1.0 / math.sqrt(R), dtype=torch.float32)
+    basis = _bf16(normal_from_hash(hash_stream(bidx, kb)) * scale.to(device)).view(H, R, d)
+    return coef, basis
+
+
+def lowrank_product(coef: torch.Tensor, basis: torch.Tensor) -> torch.Tensor:
+    """bf16 ``[H][n][d]`` = sum over j ascending of fp32(coef[..., j]) * fp32(basis[j]),
+    each product and each partial sum rounded to fp32 (separate multiply and add)."""
+    H, n, R = coef.shape
+    acc = torch.zeros(H, n, basis.shape[2], dtype=torch.float32, device=coef.device)
+    for j in range(R):
+        prod = coef[:, :, j:j + 1].to(torch.float32) * basis[:, j:j + 1, :].to(torch.float32)
+        acc = acc + prod
+    return _bf16(acc)
+
+
 def gen_request_kv(w: Workload, seed: int, layer: int, b: int, n_tok: int, q_req: torch.Tensor,
                    device="cpu"):
     """K, V of request b as bf16 ``[Hkv][n_tok][d]`` on ``device``.
@@ -309,6 +338,8 @@ def gen_request_kv(w: Workload, seed: int, layer: int, b: int, n_tok: int, q_req
         tok_assign = assign.repeat_interleave(w.block_size, dim=1)[:, :n_tok]
         mu_tok = torch.gather(mu, 1, tok_assign.unsqueeze(-1).expand(H, n_tok, d))
         K = mu_tok + torch.tensor(w.centroid_sigma, dtype=torch.float32, device=device) * n
+    elif w.key_dist == "lowrank":
+        K = lowrank_product(*gen_lowrank_factors(w, seed, layer, b, n_tok, device=device))
     else:
         raise ValueError(w.key_dist)
     K = _bf16(K)
@@ -336,6 +367,19 @@ class LayerInputs:
 
 def layer_numel(w: Workload, lens: List[int]) -> int:
     return sum(lens) * w.n_kv_heads * w.head_dim
+
+
+def fill_lowrank(w: Workload, seed: int, layer: int, coef_out: torch.Tensor, basis_out: torch.Tensor,
+                 lens: List[int], device="cpu") -> None:
+    """One layer's low-rank key factors, packed like the host K: coefficients
+    ``[b][Hkv][len_b][R]`` into flat ``coef_out``, basis ``[b][Hkv][R][d]`` into ``basis_out``."""
+    off = 0
+    H, d, R = w.n_kv_heads, w.head_dim, w.lowrank_rank
+    for b, n_tok in enumerate(lens):
+        coef, basis = gen_lowrank_factors(w, seed, layer, b, n_tok, device=device)
+        coef_out[off:off + coef.numel()].copy_(coef.reshape(-1))
+        basis_out[b * H * R * d:(b + 1) * H * R * d].copy_(basis.reshape(-1))
+        off += coef.numel()
 
 
 def fill_layer(w: Workload, seed: int, layer: int, k_out: torch.Tensor, v_out: torch.Tensor,

@@ -33,6 +33,7 @@ class Workload:
     spec_sigma: Optional[float] = None  # speculative query noise (None: no speculation)
     n_centroids: int = 0
     centroid_sigma: float = 0.0
+    lowrank_rank: int = 0                # key_dist "lowrank": rank of the synthetic keys
 
     @property
     def group_size(self) -> int:
@@ -68,6 +69,11 @@ WORKLOADS = {
     "fragmentation": Workload("fragmentation", 32, 32, 8, 128, 1, 2048, 512, 1, (65536, 65536),
                               key_dist="normal", plant="token_runs", n_planted=2048,
                               plant_beta=12.0),
+    # Low-rank keys with prediction (DualDecoder §5.3: low-rank key reconstruction
+    # for missed entries): the long-context shape at half the batch with rank-32
+    # keys, so missed keys can be rebuilt on the GPU instead of fetched.
+    "lowrank_predict": Workload("lowrank_predict", 32, 32, 8, 128, 32, 128, 512, 1, (65536, 131072),
+                                key_dist="lowrank", lowrank_rank=32, spec_sigma=SPEC_SIGMA_88),
 }
 
-ORDER = ["tiny", "llama3_8b_decode", "long_ctx_predict", "wide_budget", "fragmentation"]
+ORDER = ["tiny", "llama3_8b_decode", "long_ctx_predict", "wide_budget", "fragmentation", "lowrank_predict"]
