@@ -317,6 +317,28 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
  * resident = 0; KVO_ERR_INVALID for blocks < -1.
  */
 kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks);
+
+/*
+ * kvo_set_lowrank_keys -- rebuild the keys of a layer's missed blocks on the
+ * GPU instead of fetching them (DualDecoder §5.3: low-rank key reconstruction
+ * from a GPU-resident low-rank key cache; only the values of missed blocks
+ * then cross the host link).
+ *   coef: device bf16, packed like the host K cache with rank entries per
+ *     token row instead of d: [b][Hkv][cap_b][rank].
+ *   basis: device bf16 [b][Hkv][rank][d].
+ *   Both caller-owned; they must stay valid while set.  Key row t of a group
+ *   is bf16( sum over j = 0 .. rank-1 ascending of coef[t][j] * basis[j][c] ),
+ *   each product and each partial sum rounded to fp32 (no fused multiply-add),
+ *   the total rounded to bf16 to nearest-even; keys that are exactly this
+ *   product (synthetic low-rank keys) are rebuilt bit for bit, other keys are
+ *   replaced by their rank-`rank` image.
+ *   Applies to the urgent phase of kvo_decode_step / kvo_decode_step_dual
+ *   (both buffer modes); prefetches still copy K and V.  rank 0 turns it off.
+ *   Synchronizes the context's streams and drops captured graphs.
+ *   Errors: KVO_ERR_INVALID for a bad layer, rank outside 0..64, or null
+ *   factors with rank > 0.
+ */
+kvo_status kvo_set_lowrank_keys(kvo_ctx* ctx, int layer, int rank, const void* coef, const void* basis);
 kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out);
 kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset);
 kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);
@@ -412,8 +434,9 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
  * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.
  * kvo_profile_read synchronizes, then writes per kernel kind the summed
  * launch durations (ms) and launch counts, and clears the record.  Kinds:
- * 0 select, 1 index diff, 2 run coalescing, 3 prefetch gather, 4 urgent
- * gather, 5 attention (n_kinds >= 6).
+ * 0 select, 1 index diff (and residency assignment), 2 run coalescing,
+ * 3 prefetch gather, 4 urgent gather, 5 attention, 6 low-rank key
+ * reconstruction (n_kinds >= 7).
  */
 kvo_status kvo_profile(kvo_ctx* ctx, int enable);
 kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out, int n_kinds);

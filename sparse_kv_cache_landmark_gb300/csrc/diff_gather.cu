@@ -181,7 +181,9 @@ gather_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh, 
 // warp's metadata loads hit one or two cache lines.  The launch may reserve
 // shared memory it never uses so that each gather CTA has its SM to itself:
 // the other kernels then never queue their HBM loads behind zero-copy loads
-// waiting on the host link in the same SM's load/store pipeline.
+// waiting on the host link in the same SM's load/store pipeline.  With a slot
+// list (dslot) entry j goes to slot dslot[bg][j] instead; kv_mask bit 0 copies
+// K, bit 1 copies V (V alone where the keys are rebuilt on the GPU).
 template <int U, bool POW2>
 __global__ void __launch_bounds__(1024)
 gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh,
@@ -189,7 +191,7 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
                    const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int slot_base,
                    const int32_t* __restrict__ dslot,
                    uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int G, int k, int B, int D, int words_log2,
-                   int32_t* __restrict__ status) {
+                   int kv_mask, int32_t* __restrict__ status) {
     constexpr uint32_t CHUNK = 32 * U;                       // words per warp iteration
     const uint32_t words = (uint32_t)B * D / 8;             // 16-byte words per block
     const uint32_t per_group = ((uint32_t)k * words + CHUNK - 1) / CHUNK;   // chunks per group
@@ -224,8 +226,8 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
                 const int32_t sl = sg ? __ldg(sg + j) : slot_base + (int32_t)j;
                 if (blk >= 0 && blk < C && sl >= 0 && sl < 2 * k) {
                     const int64_t off = (int64_t)blk * B * D + 8 * (int64_t)w;
-                    a[u] = *reinterpret_cast<const uint4*>(kh + src0 + off);
-                    b[u] = *reinterpret_cast<const uint4*>(vh + src0 + off);
+                    if (kv_mask & 1) a[u] = *reinterpret_cast<const uint4*>(kh + src0 + off);
+                    if (kv_mask & 2) b[u] = *reinterpret_cast<const uint4*>(vh + src0 + off);
                     to[u] = ((int64_t)bg * 2 * k + sl) * B * D + 8 * (int64_t)w;
                     ok[u] = true;
                 } else {
@@ -236,15 +238,15 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (ok[u]) {
-                *reinterpret_cast<uint4*>(dk + to[u]) = a[u];
-                *reinterpret_cast<uint4*>(dv + to[u]) = b[u];
+                if (kv_mask & 1) *reinterpret_cast<uint4*>(dk + to[u]) = a[u];
+                if (kv_mask & 2) *reinterpret_cast<uint4*>(dv + to[u]) = b[u];
             }
     }
     if (bad) atomicOr(status, bad);
 }
 
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
-                               cudaStream_t s, const int32_t* dslot) {
+                               cudaStream_t s, const int32_t* dslot, int kv_mask) {
     const uint32_t words = (uint32_t)c.B * c.d / 8;
     int lg = -1;
     if ((words & (words - 1)) == 0) { lg = 0; while ((1u << lg) < words) ++lg; }
@@ -254,8 +256,7 @@ cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* 
 #define KVO_FLAT(U_, P_)                                                                                          \
     gather_flat_kernel<U_, P_><<<ctas, th, smem, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, idx, cnt, \
                                                       slot_base, dslot, c.buf_k(buf), c.buf_v(buf), c.G, c.k,     \
-                                                      c.B, c.d, lg,                                               \
-                                                      c.status)
+                                                      c.B, c.d, lg, kv_mask, c.status)
     if (lg >= 0) { if (c.gather_unroll >= 2) KVO_FLAT(2, true); else KVO_FLAT(1, true); }
     else { if (c.gather_unroll >= 2) KVO_FLAT(2, false); else KVO_FLAT(1, false); }
 #undef KVO_FLAT

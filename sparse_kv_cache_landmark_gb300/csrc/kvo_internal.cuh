@@ -66,6 +66,9 @@ struct Ctx {
     unsigned long long* res_fetched = nullptr;   // [2] blocks fetched: urgent, prefetch
     std::vector<char> res_pending;  // [L] a prefetch into the layer's set was issued and not yet waited for
     int res_budget = -1;            // prefetch fetches admitted per group, layer and step (-1: all)
+    // Low-rank keys per layer (caller-owned device factors; rank 0: not set)
+    std::vector<const uint16_t*> lr_coef, lr_basis;
+    std::vector<int> lr_rank;
     // K / V buffer by id: 0, 1 ping-pong halves; 2 + l resident set of layer l
     uint16_t* buf_k(int buf) const { return buf < 2 ? pp_k[buf] : res_k[buf - 2]; }
     uint16_t* buf_v(int buf) const { return buf < 2 ? pp_v[buf] : res_v[buf - 2]; }
@@ -145,7 +148,7 @@ struct Ctx {
 
 // kernel kinds reported by kvo_profile_read
 enum ProfKind { PK_SELECT = 0, PK_DIFF = 1, PK_COALESCE = 2, PK_GATHER_PREFETCH = 3, PK_GATHER_URGENT = 4,
-                PK_ATTENTION = 5, PK_COUNT = 6 };
+                PK_ATTENTION = 5, PK_RECON = 6, PK_COUNT = 7 };
 
 // --------------------------------------------------------- device helpers
 __device__ __forceinline__ uint32_t float_to_ordered(float f) {
@@ -199,7 +202,10 @@ cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs,
 cudaError_t launch_gather_tma(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                               cudaStream_t s);
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
-                               cudaStream_t s, const int32_t* dslot = nullptr);
+                               cudaStream_t s, const int32_t* dslot = nullptr, int kv_mask = 3);
+cudaError_t launch_lowrank_k(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
+                             const int32_t* dslot, cudaStream_t s);
+cudaError_t prepare_lowrank();
 cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
                                    int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
                                    int phase, cudaStream_t s, int max_fetch = -1);

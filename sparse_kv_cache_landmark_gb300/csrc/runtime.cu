@@ -389,6 +389,10 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * c.G, &sb));
     KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
     KVO_CUDA(&c, kvo::prepare_attention(c));
+    KVO_CUDA(&c, kvo::prepare_lowrank());
+    c.lr_coef.assign(c.L, nullptr);
+    c.lr_basis.assign(c.L, nullptr);
+    c.lr_rank.assign(c.L, 0);
     KVO_CUDA(&c, dalloc(&c.status, sizeof(int32_t), &sb));
     KVO_CUDA(&c, cudaMemsetAsync(c.status, 0, sizeof(int32_t), c.s_compute));
     // decode-step state
@@ -614,7 +618,15 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
         // 3. urgent gather of the misses into slots [k, 2k)
         cur_layer = l;
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.sel[l], 0));
-        if (c.gather_engine == 3) {
+        if (c.lr_rank[l] > 0) {
+            // low-rank layer: only V crosses the link; the missed keys are rebuilt on the GPU
+            KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent, [&] {
+                return kvo::launch_gather_flat(c, l, buf, miss, mcnt, c.k, c.s_urgent, nullptr, 2);
+            }));
+            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_urgent, [&] {
+                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, c.k, nullptr, c.s_urgent);
+            }));
+        } else if (c.gather_engine == 3) {
             KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
                                [&] { return kvo::launch_gather_flat(c, l, buf, miss, mcnt, c.k, c.s_urgent); }));
         } else {
@@ -728,8 +740,14 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.sel[l], 0));
         // without a prediction nothing is spared: in-flight prefetch copies must land first
         if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.rpref[l], 0));
-        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
-                           [&] { return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl); }));
+        const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
+        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent, [&] {
+            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl, urg_mask);
+        }));
+        if (c.lr_rank[l] > 0)
+            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_urgent, [&] {
+                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, c.s_urgent);
+            }));
         KVO_CUDA(&c, cudaEventRecord(E.urg[l], c.s_urgent));
         // 4. attention over the resident set once the urgent and prefetched blocks have landed
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
@@ -929,6 +947,20 @@ kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out) {
     return KVO_OK;
 }
 
+kvo_status kvo_set_lowrank_keys(kvo_ctx* ctx, int layer, int rank, const void* coef, const void* basis) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "bad layer");
+    if (rank < 0 || rank > 64) return fail(&c, KVO_ERR_INVALID, "rank must be in 0..64");
+    if (rank > 0 && (!coef || !basis)) return fail(&c, KVO_ERR_INVALID, "rank > 0 needs coef and basis");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    drop_graphs(c);
+    c.lr_rank[layer] = rank;
+    c.lr_coef[layer] = rank > 0 ? (const uint16_t*)coef : nullptr;
+    c.lr_basis[layer] = rank > 0 ? (const uint16_t*)basis : nullptr;
+    return KVO_OK;
+}
+
 kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
@@ -1021,7 +1053,7 @@ kvo_status kvo_profile(kvo_ctx* ctx, int enable) {
 kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out, int n_kinds) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
-    if (!ms_out || !launches_out || n_kinds < kvo::PK_COUNT) return fail(&c, KVO_ERR_INVALID, "need 6 output slots");
+    if (!ms_out || !launches_out || n_kinds < kvo::PK_COUNT) return fail(&c, KVO_ERR_INVALID, "need 7 output slots");
     for (int i = 0; i < n_kinds; ++i) { ms_out[i] = 0.0; launches_out[i] = 0; }
     for (size_t i = 0; i + 1 < c.prof_recs.size(); i += 2) {
         cudaEvent_t a = c.prof_pool[c.prof_recs[i].ev], b = c.prof_pool[c.prof_recs[i + 1].ev];

@@ -25,8 +25,8 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
            "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched",
-           "kvo_set_prefetch_budget"]
-PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention"]
+           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys"]
+PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention", "recon"]
 
 
 class KvoError(RuntimeError):
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_resident_slots.argtypes = [P, I, ctypes.POINTER(ctypes.c_int32)]
         L.kvo_resident_fetched.argtypes = [P, ctypes.POINTER(ctypes.c_int64), I]
         L.kvo_set_prefetch_budget.argtypes = [P, I]
+        L.kvo_set_lowrank_keys.argtypes = [P, I, I, VP, VP]
         L.kvo_append.argtypes = [P, VP, VP, VP]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
@@ -304,6 +305,16 @@ class Context:
         self._c(lib().kvo_resident_slots(self.ctx, layer,
                                          ctypes.cast(out.data_ptr(), ctypes.POINTER(ctypes.c_int32))))
         return out
+
+    def set_lowrank_keys(self, layer: int, rank: int, coef: Optional[torch.Tensor], basis: Optional[torch.Tensor]):
+        """Rebuild layer ``layer``'s missed keys from rank-``rank`` factors (C: kvo_set_lowrank_keys).
+
+        coef: CUDA bf16 packed like the host K with ``rank`` values per token; basis: CUDA bf16
+        ``[b][Hkv][rank][d]``.  The tensors must outlive their use; the context keeps references.
+        """
+        self._lr = getattr(self, "_lr", {})
+        self._lr[layer] = (coef, basis)
+        self._c(lib().kvo_set_lowrank_keys(self.ctx, layer, rank, _ptr(coef), _ptr(basis)))
 
     def set_prefetch_budget(self, blocks: int):
         """Cap prefetch fetches per group, layer and step (-1: no cap) (C: kvo_set_prefetch_budget)."""
