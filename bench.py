@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--drift", type=float, default=-1.0,
                     help="per-step query drift with --resident (default: the speculative noise / sqrt(2))")
     ap.add_argument("--query-steps", type=int, default=8, help="distinct step queries cycled with --resident")
+    ap.add_argument("--reconstruct", type=int, default=-1,
+                    help="rebuild missed keys from low-rank factors (1/0; -1: on for low-rank workloads)")
     ap.add_argument("--prefetch-budget", type=int, default=-1,
                     help="with --resident: prefetch fetches admitted per group, layer and step (-1: all)")
     return ap.parse_args()
@@ -92,13 +94,15 @@ def peaks():
 NCU_TRAFFIC = {("llama3_8b_decode", "gather_flat_kernel"): 72.669952e6 + 43.264e3}
 
 
-def workload_bytes(w, lens, misses_per_step=0, fetched_per_step=None):
+def workload_bytes(w, lens, misses_per_step=0, fetched_per_step=None, recon_rank=0):
     """Algorithmic bytes of one step (all layers): HBM and host link.
 
     ``misses_per_step``: blocks fetched by the urgent stream per step (summed
     over layers and groups) on top of the k prefetched blocks per group.
     ``fetched_per_step`` (resident block sets): all blocks fetched per step,
     replacing the k per group and the misses.
+    ``recon_rank`` > 0: missed keys are rebuilt on the GPU from rank-R factors,
+    so misses move V only over the link and read R coefficients per token.
     """
     G, d, k, B, W, L = w.batch * w.n_kv_heads, w.head_dim, w.top_k, w.block_size, w.window, w.n_layers
     tok = 4 * d                                             # K+V bf16 bytes per token per KV head
@@ -110,8 +114,11 @@ def workload_bytes(w, lens, misses_per_step=0, fetched_per_step=None):
     out_bytes = w.batch * w.n_q_heads * (d + 1) * 4
     meta = G * k * 4 * 8
     urgent = misses_per_step * B * tok
+    urgent_host = urgent if not recon_rank else misses_per_step * B * tok // 2
+    if recon_rank:
+        urgent += misses_per_step * B * recon_rank * 2          # coefficients read by the rebuild
     hbm = (lm_bytes + gathered + attended + q_bytes + out_bytes + meta) * L + urgent
-    host = gathered * L + urgent
+    host = gathered * L + urgent_host
     if fetched_per_step is not None:
         moved = fetched_per_step * B * tok
         hbm = (lm_bytes + attended + q_bytes + out_bytes + meta) * L + moved
@@ -353,6 +360,19 @@ def build_workload(args, ws=1):
         B.ctx.set_attn_impl(args.attn_impl, args.attn_ctas)
     if args.resident and args.prefetch_budget >= 0:
         B.ctx.set_prefetch_budget(args.prefetch_budget)
+    B.recon_rank = 0
+    if w.key_dist == "lowrank" and args.reconstruct != 0:
+        # GPU-resident low-rank key factors, packed like the host K (layers past n_host reuse l % n_host)
+        R = w.lowrank_rank
+        B.lr = []
+        for l in range(n_host):
+            coef = torch.empty(sum(gen_lens) * w.n_kv_heads * R, dtype=torch.bfloat16, device="cuda")
+            basis = torch.empty(w.batch * w.n_kv_heads * R * w.head_dim, dtype=torch.bfloat16, device="cuda")
+            synth.fill_lowrank(w, args.seed, l, coef, basis, gen_lens, device="cuda")
+            B.lr.append((coef, basis))
+        for l in range(w.n_layers):
+            B.ctx.set_lowrank_keys(l, R, *B.lr[l % n_host])
+        B.recon_rank = R
     B.keep = (k_host, v_host, k_win, v_win)
     B.q_pin = torch.stack(qs_l).pin_memory()
     B.qs_pin = None if qspec_l[0] is None else torch.stack(qspec_l).pin_memory()
@@ -527,7 +547,7 @@ def run_ours(args):
                "note": "one layer's attention, isolated (no gather running), 20 back-to-back calls"}
     hbm_peak, peak_kind = peaks()
     fetched_step = None if fetched is None else sum(fetched) / args.steps
-    by = workload_bytes(w, lens, misses, fetched_per_step=fetched_step)
+    by = workload_bytes(w, lens, misses, fetched_per_step=fetched_step, recon_rank=Bw.recon_rank)
     if fetched is not None:       # prefetch launches move only the prediction's delta
         by["gather_per_launch"] = fetched[1] / args.steps / w.n_layers * w.block_size * 4 * w.head_dim
     t_hbm = by["hbm"] / (hbm_peak * 1e9)
@@ -605,6 +625,10 @@ def run_ours(args):
                              "drivers": args.gather_drivers or "default"},
             "attention_kernel": {"impl": "default" if args.attn_impl < 0 else args.attn_impl,
                                  "ctas": args.attn_ctas or "default"},
+            "lowrank_keys": None if not Bw.recon_rank else {
+                "rank": Bw.recon_rank, "rebuilt_blocks_per_step": misses,
+                "host_bytes_saved_per_step": misses * w.block_size * 2 * w.head_dim,
+                "note": "missed keys rebuilt on the GPU from rank-R factors; misses move V only"},
             "resident": None if not args.resident else {
                 "drift": Bw.drift, "query_steps": args.query_steps, "prefetch_budget": args.prefetch_budget,
                 "fetched_blocks_per_step": fetched_step,
