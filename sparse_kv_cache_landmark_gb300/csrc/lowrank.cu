@@ -16,10 +16,13 @@
 namespace kvo {
 
 constexpr int LR_THREADS = 256;
+constexpr int LR_ROWS = 64;        // token rows per CTA
 
-// One CTA per group: every row of every listed block (entry j -> slot
-// slot_base + j, or dslot[j]) is rebuilt into the K buffer.  A warp owns one
-// row at a time; lane l holds channels CPL*l .. CPL*l + CPL-1.
+// Grid (group, row chunk): CTA y rebuilds the chunks y, y + gridDim.y, ... of
+// LR_ROWS rows of the group's listed blocks (entry j -> slot slot_base + j, or
+// dslot[j]; row j*B + i is token i of block j) into the K buffer; CTAs whose
+// first chunk lies past the list's rows exit at once.  A warp owns one row at a time; lane l holds channels
+// CPL*l .. CPL*l + CPL-1.
 template <int D>
 __global__ void __launch_bounds__(LR_THREADS)
 lowrank_k_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int slot_base,
@@ -30,18 +33,24 @@ lowrank_k_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cn
     constexpr int CPL = D / 32;                    // channels per lane
     extern __shared__ float e_s[];                 // [R][D] fp32 basis
     const int bg = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int n = cnt ? cnt[bg] : k;
+    int bad = 0;
+    if (n < 0 || n > k) { bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
+    const int nrows = n * B;
+    if ((int64_t)blockIdx.y * LR_ROWS >= nrows) {
+        if (bad && tid == 0 && blockIdx.y == 0) atomicOr(status, bad);
+        return;
+    }
     const uint16_t* eb = basis + (int64_t)bg * R * D;
     for (int i = tid; i < R * D; i += blockDim.x)
         e_s[i] = __uint_as_float((uint32_t)eb[i] << 16);
     __syncthreads();
-    int n = cnt ? cnt[bg] : k;
-    int bad = 0;
-    if (n < 0 || n > k) { bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
     const int C = g_C[bg];
     const int64_t row0 = g_off[bg] / D;            // the group's first token row
-    const int rows = n * B;
-    for (int rr = warp; rr < rows; rr += LR_THREADS / 32) {
-        const int j = rr / B, i = rr - j * B;
+    for (int64_t rr = (int64_t)blockIdx.y * LR_ROWS + warp; rr < nrows;
+         rr += ((rr % LR_ROWS) + LR_THREADS / 32 >= LR_ROWS) ? (int64_t)(gridDim.y - 1) * LR_ROWS + LR_THREADS / 32
+                                                             : LR_THREADS / 32) {
+        const int j = (int)(rr / B), i = (int)(rr - (int64_t)j * B);
         const int32_t x = __ldg(idx + (int64_t)bg * k + j);
         const int32_t s = dslot ? __ldg(dslot + (int64_t)bg * k + j) : slot_base + j;
         if (x < 0 || x >= C || s < 0 || s >= 2 * k) {
@@ -68,7 +77,7 @@ lowrank_k_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cn
             *reinterpret_cast<__nv_bfloat162*>(out + c) = v;
         }
     }
-    if (bad) atomicOr(status, bad);
+    if (bad && lane == 0) atomicOr(status, bad);
 }
 
 cudaError_t prepare_lowrank() {
@@ -83,12 +92,14 @@ cudaError_t launch_lowrank_k(const Ctx& c, int layer, int buf, const int32_t* id
                              const int32_t* dslot, cudaStream_t s) {
     const int R = c.lr_rank[layer];
     const size_t smem = sizeof(float) * R * c.d;
+    const int64_t chunks = ((int64_t)c.k * c.B + LR_ROWS - 1) / LR_ROWS;
+    const dim3 grid(c.G, (unsigned)std::min<int64_t>(chunks, 65535));
     if (c.d == 128)
-        lowrank_k_kernel<128><<<c.G, LR_THREADS, smem, s>>>(idx, cnt, slot_base, dslot, c.lr_coef[layer],
+        lowrank_k_kernel<128><<<grid, LR_THREADS, smem, s>>>(idx, cnt, slot_base, dslot, c.lr_coef[layer],
                                                             c.lr_basis[layer], c.g_off, c.g_C, c.buf_k(buf), c.k,
                                                             c.B, R, c.status);
     else
-        lowrank_k_kernel<64><<<c.G, LR_THREADS, smem, s>>>(idx, cnt, slot_base, dslot, c.lr_coef[layer],
+        lowrank_k_kernel<64><<<grid, LR_THREADS, smem, s>>>(idx, cnt, slot_base, dslot, c.lr_coef[layer],
                                                            c.lr_basis[layer], c.g_off, c.g_C, c.buf_k(buf), c.k,
                                                            c.B, R, c.status);
     return cudaGetLastError();

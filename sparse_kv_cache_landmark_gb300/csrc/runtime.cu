@@ -619,12 +619,13 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
         cur_layer = l;
         KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.sel[l], 0));
         if (c.lr_rank[l] > 0) {
-            // low-rank layer: only V crosses the link; the missed keys are rebuilt on the GPU
+            // low-rank layer: only V crosses the link (urgent stream) while the missed
+            // keys are rebuilt on the GPU (compute stream, before the attention that reads them)
             KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent, [&] {
                 return kvo::launch_gather_flat(c, l, buf, miss, mcnt, c.k, c.s_urgent, nullptr, 2);
             }));
-            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_urgent, [&] {
-                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, c.k, nullptr, c.s_urgent);
+            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_compute, [&] {
+                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, c.k, nullptr, c.s_compute);
             }));
         } else if (c.gather_engine == 3) {
             KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent,
@@ -744,9 +745,9 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent, [&] {
             return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl, urg_mask);
         }));
-        if (c.lr_rank[l] > 0)
-            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_urgent, [&] {
-                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, c.s_urgent);
+        if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
+            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_compute, [&] {
+                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, c.s_compute);
             }));
         KVO_CUDA(&c, cudaEventRecord(E.urg[l], c.s_urgent));
         // 4. attention over the resident set once the urgent and prefetched blocks have landed
