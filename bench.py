@@ -91,7 +91,7 @@ def peaks():
 # DRAM bytes per launch of the default gather kernel from one ncu capture of a
 # 134.2 MB launch (profiles/gather_flat_kernel_llama3_8b_decode.md); reported
 # only for the launch shape and workload it was taken on.
-NCU_TRAFFIC = {("llama3_8b_decode", "gather_flat_kernel"): 72.669952e6 + 43.264e3}
+NCU_TRAFFIC = {("llama3_8b_decode", "gather_flat_kernel"): 72.368384e6 + 45.312e3}
 
 
 def workload_bytes(w, lens, misses_per_step=0, fetched_per_step=None, recon_rank=0):
