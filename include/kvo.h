@@ -334,6 +334,9 @@ kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks);
  *   replaced by their rank-`rank` image.
  *   Applies to the urgent phase of kvo_decode_step / kvo_decode_step_dual
  *   (both buffer modes); prefetches still copy K and V.  rank 0 turns it off.
+ *   With kvo_append, the coefficient rows of appended tokens (rows len_b ..
+ *   len_b + max_append - 1) are the caller's to fill before their blocks can
+ *   be selected.
  *   Synchronizes the context's streams and drops captured graphs.
  *   Errors: KVO_ERR_INVALID for a bad layer, rank outside 0..64, or null
  *   factors with rank > 0.

@@ -16,9 +16,10 @@ from tests.margins import MARGIN
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,spec,L,att", [(16, True, 2, (1, 0)), (1, False, 1, (1, 0)), (32, False, 3, (1, 0)),
-                                          (16, False, 1, (0, 0)), (16, False, 1, (1, 2))])
-def test_append_grows_the_cache(B, spec, L, att):
+@pytest.mark.parametrize("B,spec,L,att,resident", [(16, True, 2, (1, 0), False), (1, False, 1, (1, 0), False),
+                                                   (32, False, 3, (1, 0), False), (16, False, 1, (0, 0), False),
+                                                   (16, False, 1, (1, 2), False), (16, True, 2, (1, 0), True)])
+def test_append_grows_the_cache(B, spec, L, att, resident):
     W, n_app, d = 32, 40 if B > 1 else 12, 128
     len0 = W + B * 20 if B > 1 else W + 400
     cap = len0 + n_app
@@ -40,7 +41,7 @@ def test_append_grows_the_cache(B, spec, L, att):
         v_win.append(vhv[:, :, len0 - W:len0].contiguous().cuda())
     ctx = Context(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=d, block_size=B,
                   top_k=w.top_k, window=W, n_layers=L, seq_lens=[len0] * w.batch, k_host=k_host, v_host=v_host,
-                  k_win=k_win, v_win=v_win, max_append=n_app)
+                  k_win=k_win, v_win=v_win, max_append=n_app, resident=resident)
     try:
         ctx.set_attn_impl(*att)        # the window ring wraps inside and across attention tiles
         q = torch.stack([full[l].q for l in range(L)]).cuda()
