@@ -290,37 +290,72 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
     bar_named(1, nthr);
     if (!*s_last) return;
 
+    // Merge of the group's partials, per part, by log-sum-exp.  When the group's
+    // items fit the table (MI; always, for the work plans built here): the (m, l)
+    // of every (item, row) go to shared memory (the warps' state area, free since
+    // the partial write), one thread per (part, row) turns them into weights, and
+    // every element's partial loads are then independent of one another.  More
+    // items: an online merge per element.
+    constexpr int MI = D == 128 ? 96 : 48;              // items the table holds
+    float* s_w = const_cast<float*>(sm_o);              // [MI][16] m, then weight, of (item, row)
+    float* s_l = s_w + MI * 16;                         // [MI][16] l of (item, row)
+    int* s_p = reinterpret_cast<int*>(s_l + MI * 16);   // [MI] part of each item
+    float* s_M = reinterpret_cast<float*>(s_p + MI);    // [2][16] maximum of (part, row)
+    float* s_L = s_M + 32;                              // [2][16] sum of (part, row)
     const int first = att_first[bg], cnt = att_count[bg];
     const int64_t rows_total = (int64_t)batch * Hq;
+    const bool table = cnt <= MI;
+    if (table) {
+        for (int t = tid; t < cnt * nrows; t += nthr) {
+            const int i = t / nrows, row = t - i * nrows;
+            const int64_t base = ((int64_t)(first + i) * nrows + row) * 2;
+            s_w[i * 16 + row] = __ldcg(part_ml + base);
+            s_l[i * 16 + row] = __ldcg(part_ml + base + 1);
+            if (row == 0) s_p[i] = __ldg(&items[first + i].y);
+        }
+        bar_named(1, nthr);
+        if (tid < 2 * nrows) {
+            const int pp = tid / nrows, row = tid - pp * nrows;
+            float Mn = -INFINITY;
+            for (int i = 0; i < cnt; ++i)
+                if (s_p[i] == pp) Mn = fmaxf(Mn, s_w[i * 16 + row]);
+            float L = 0.f;
+            for (int i = 0; i < cnt; ++i) {
+                if (s_p[i] != pp) continue;
+                const float m = s_w[i * 16 + row];
+                const float w = m == -INFINITY ? 0.f : ex2f(m - Mn);
+                s_w[i * 16 + row] = w;
+                L += w * s_l[i * 16 + row];
+            }
+            s_M[pp * 16 + row] = Mn;
+            s_L[pp * 16 + row] = L;
+        }
+        bar_named(1, nthr);
+    }
     for (int e = tid; e < nrows * D; e += nthr) {
         const int row = e / D, c = e - row * D;
-        // online log-sum-exp merge of the group's partials, per part; the loads
-        // of four partials are issued together
-        float Mp[2] = {-INFINITY, -INFINITY}, Lp[2] = {0.f, 0.f}, Ap[2] = {0.f, 0.f};
-        for (int i0 = first; i0 < first + cnt; i0 += 4) {
-            float mi[4], li[4], ai[4];
-            int pi[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool ok = i0 + j < first + cnt;
-                const int64_t base = (int64_t)(ok ? i0 + j : first) * nrows + row;
-                mi[j] = ok ? __ldcg(part_ml + base * 2) : -INFINITY;
-                li[j] = ok ? __ldcg(part_ml + base * 2 + 1) : 0.f;
-                ai[j] = ok ? __ldcg(part_o + base * D + c) : 0.f;
-                pi[j] = ok ? __ldg(&items[i0 + j].y) : 0;
+        float Mp[2], Lp[2], Ap[2] = {0.f, 0.f};
+        if (table) {
+            Mp[0] = s_M[row]; Mp[1] = s_M[16 + row];
+            Lp[0] = s_L[row]; Lp[1] = s_L[16 + row];
+#pragma unroll 4
+            for (int i = 0; i < cnt; ++i) {
+                const float v = __ldcg(part_o + ((int64_t)(first + i) * nrows + row) * D + c) * s_w[i * 16 + row];
+                if (s_p[i]) Ap[1] += v; else Ap[0] += v;
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (mi[j] == -INFINITY) continue;
-                const int pp = pi[j];
-                const float Mo = pp ? Mp[1] : Mp[0];
-                const float Mn = fmaxf(Mo, mi[j]);
-                const float so = ex2f(Mo - Mn), sn = ex2f(mi[j] - Mn);
-                if (pp) {
-                    Lp[1] = Lp[1] * so + li[j] * sn; Ap[1] = Ap[1] * so + ai[j] * sn; Mp[1] = Mn;
-                } else {
-                    Lp[0] = Lp[0] * so + li[j] * sn; Ap[0] = Ap[0] * so + ai[j] * sn; Mp[0] = Mn;
-                }
+        } else {
+            Mp[0] = Mp[1] = -INFINITY;
+            Lp[0] = Lp[1] = 0.f;
+            for (int i = first; i < first + cnt; ++i) {
+                const int64_t base = (int64_t)i * nrows + row;
+                const float mi = __ldcg(part_ml + base * 2);
+                if (mi == -INFINITY) continue;
+                const int pp = __ldg(&items[i].y);
+                const float Mn = fmaxf(Mp[pp], mi);
+                const float so = ex2f(Mp[pp] - Mn), sn = ex2f(mi - Mn);
+                Lp[pp] = Lp[pp] * so + __ldcg(part_ml + base * 2 + 1) * sn;
+                Ap[pp] = Ap[pp] * so + __ldcg(part_o + base * D + c) * sn;
+                Mp[pp] = Mn;
             }
         }
         const bool spec_row = row >= r;

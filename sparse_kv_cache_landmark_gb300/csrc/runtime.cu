@@ -68,9 +68,11 @@ cudaError_t part_alloc(kvo::Ctx& c, int items) {
 
 // Work items of the TMA-staged attention kernel: the tiles of every group
 // (sparse part, then window part; window tiles up to the largest window the
-// context can hold), group after group, split into `grid` equal contiguous
-// ranges (their bounds rounded to a multiple of the CTA's warps, so the warps
-// of an item get equal tile counts), each range cut at part boundaries.
+// context can hold), group after group, split into `grid` contiguous ranges of
+// equal cost -- a tile costs 1, and each part costs kItemCost more, the price
+// of the work-item epilogue a range pays where it enters a part -- with their
+// bounds rounded to a multiple of the CTA's warps (so the warps of an item get
+// equal tile counts), each range cut at part boundaries.
 kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
     const int64_t sp_tiles = (c.k * c.B + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
     const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;
@@ -79,9 +81,27 @@ kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
     grid = std::max<int64_t>(1, std::min<int64_t>(grid, T));
     std::vector<int4> items;
     std::vector<int32_t> cta(grid + 1), first(c.G, 0), count(c.G, 0);
+    // parts in tile order with their first tile and first cost unit
+    constexpr int64_t kItemCost = 3;     // epilogue of a work item, in tiles (measured ~7K vs ~2.4K cycles)
+    std::vector<int64_t> p_t0, p_c0, p_len;
+    int64_t cost = 0;
+    for (int g = 0; g < c.G; ++g)
+        for (int part = 0; part < 2; ++part) {
+            const int64_t len = part == 0 ? sp_tiles : w_tiles;
+            if (len == 0) continue;
+            p_t0.push_back(g * per_g + (part == 0 ? 0 : sp_tiles));
+            p_c0.push_back(cost);
+            p_len.push_back(len);
+            cost += kItemCost + len;
+        }
+    auto tile_at = [&](int64_t x) -> int64_t {      // tile where cost point x falls (part starts absorb their extra)
+        const size_t i = (size_t)(std::upper_bound(p_c0.begin(), p_c0.end(), x) - p_c0.begin()) - 1;
+        return p_t0[i] + std::min(p_len[i], std::max<int64_t>(0, x - p_c0[i] - kItemCost));
+    };
     auto bound = [&](int64_t j) {
-        const int64_t b = T * j / grid;
-        return j == grid ? T : std::min(T, b - b % kvo::ATT_WARPS);
+        if (j == grid) return T;
+        const int64_t b = tile_at(cost * j / grid);
+        return std::min(T, b - b % kvo::ATT_WARPS);
     };
     for (int64_t j = 0; j < grid; ++j) {
         cta[j] = (int32_t)items.size();
