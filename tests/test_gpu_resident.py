@@ -45,13 +45,18 @@ def _attempts(c, steps, drift):
     return out
 
 
-@pytest.mark.parametrize("spec,L,B,k,dual,budget", [(True, 2, 16, 16, True, None), (False, 1, 16, 16, False, None),
-                                                    (True, 1, 1, 64, False, None), (True, 3, 32, 8, False, None),
-                                                    (True, 2, 16, 16, False, 3)])
-def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget):
-    W, drift, steps, seed = 32, 0.15, 6, 321
+@pytest.mark.parametrize("spec,L,B,k,dual,budget,W,ragged", [
+    (True, 2, 16, 16, True, None, 32, False), (False, 1, 16, 16, False, None, 32, False),
+    (True, 1, 1, 64, False, None, 32, False), (True, 3, 32, 8, False, None, 32, False),
+    (True, 2, 16, 16, False, 3, 32, False),
+    (True, 1, 16, 16, False, None, 0, False),          # no window: attention over the resident blocks alone
+    (True, 2, 32, 12, False, None, 64, True)])         # ragged lengths, k not a multiple of the warp count
+def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged):
+    drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
-    w = Workload(f"resident_B{B}", 2, 8, 2, 128, B, k, W, L, (n, n), spec_sigma=0.3 if spec else None)
+    ctx = (n, n + 40 * B) if ragged else (n, n)
+    w = Workload(f"resident_B{B}", 3 if ragged else 2, 8, 2, 128, B, k, W, L, ctx,
+                 spec_sigma=0.3 if spec else None)
     c = Case(w, seed, gen_device="cpu", resident=True)
     try:
         att = _attempts(c, steps, drift)
