@@ -25,6 +25,9 @@ CASES = {
     "clustered": Workload("clustered", 1, 16, 2, 128, 64, 8, 64, 1, (6464, 6464), key_dist="clustered",
                           n_centroids=32, centroid_sigma=0.3),
     "multi_chunk": Workload("multi_chunk", 2, 8, 2, 128, 2, 64, 16, 1, (6016, 6016), spec_sigma=0.2),
+    # 800 register-direct tiles per group = 50 work items: more than the merge's
+    # shared-memory table holds at d = 64, so the online merge runs
+    "many_items": Workload("many_items", 1, 8, 2, 64, 32, 400, 32, 1, (32 + 32 * 420, 32 + 32 * 420)),
 }
 
 
