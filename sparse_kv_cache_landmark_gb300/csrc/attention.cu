@@ -278,13 +278,13 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
         }
     }
     // the barrier makes the CTA's partial stores visible to thread 0, whose
-    // device-scope fence (cumulative) orders them before its ticket; the last
-    // CTA's fence after the ticket orders the merge's loads after it
+    // device-scope release fence (cumulative) orders them before its ticket;
+    // the last CTA's acquire fence after the ticket orders the merge's loads
     bar_named(1, nthr);
     if (tid == 0) {
-        __threadfence();
+        fence_acq_rel_gpu();
         const bool last = atomicAdd(&done[bg], 1u) + 1 == (uint32_t)att_count[bg];
-        if (last) __threadfence();
+        if (last) fence_acq_rel_gpu();
         *s_last = last;
     }
     bar_named(1, nthr);

@@ -162,6 +162,12 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_fl
 // Block-wide exclusive scan of one uint32 per thread (blockDim.x multiple of 32, <= 1024).
 // `warp_sums` needs blockDim.x / 32 entries of shared memory.  Returns the
 // exclusive prefix; *total receives the block total.  Contains __syncthreads().
+// Release/acquire fence at device scope: orders the memory operations the
+// calling thread has performed or observed (through a CTA barrier) before the
+// ones after it, as the last-CTA ticket protocols need; lighter than the
+// sequentially consistent fence of __threadfence().
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     uint32_t x = v;

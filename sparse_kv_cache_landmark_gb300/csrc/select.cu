@@ -236,15 +236,18 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         const uint32_t v = (&h_s[0][0])[i];
         if (v) atomicAdd(&hist[((int64_t)(i / 256) * G + bg) * 256 + (i % 256)], v);
     }
-    __threadfence();
+    // the CTA's key and histogram writes reach thread 0 through the barrier; its
+    // release fence orders them before the ticket, the last CTA's acquire fence
+    // orders the selection's loads after it
     __syncthreads();
     if (tid == 0) {
+        fence_acq_rel_gpu();
         const uint32_t prev = atomicAdd(&done[bg], 1u);
         s_last = (prev + 1 == (uint32_t)nchunks[bg]);
+        if (s_last) fence_acq_rel_gpu();
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
 
     // ---- last CTA of the group: exact top-k for each query
     for (int qi = 0; qi < NQ; ++qi) {
