@@ -109,7 +109,9 @@ typedef struct {
  *   synchronously from k_host; the two ping-pong halves of K and V
  *   ([2][G][2k][B][d] bf16: slots [0,k) take prefetched blocks, [k,2k) misses);
  *   scratch; and three streams: compute, prefetch (lowest priority) and
- *   urgent (highest priority; DualDecoder Fig. 10).
+ *   urgent (highest priority; DualDecoder Fig. 10).  With resident = 1 it also
+ *   owns one resident set per layer ([G][2k][B][d] K and V each), its slot
+ *   table and block map (see kvo_resident_slots).
  *   Errors: KVO_ERR_INVALID (config or pointers), KVO_ERR_OOM, KVO_ERR_CUDA.
  */
 kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* const* v_host,
@@ -214,7 +216,10 @@ kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const 
  *   ordered after `stream`, and `stream` waits for the outputs; the prefetches
  *   this step issues for the next step may still be in flight on return (the
  *   next step orders itself after them; kvo_device_status, kvo_reset_prediction
- *   and kv_offload_destroy synchronize them).
+ *   and kv_offload_destroy synchronize them).  With resident = 1 the step
+ *   keeps per-layer resident sets and fetches only their delta instead (see
+ *   kvo_resident_slots); layers given low-rank factors rebuild their missed
+ *   keys on the GPU (kvo_set_lowrank_keys).
  */
 kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o,
                            float* lse, kvo_stream_t stream);
@@ -234,7 +239,8 @@ kvo_status kvo_decode_step_dual(kvo_ctx* ctx, const void* q, const void* q_spec,
  * captured once per step parity into a CUDA graph and replayed, which removes
  * the host launch work and shortens the gaps between dependent kernels; a
  * graph is re-captured when the q/o/lse pointers of the call change or a
- * gather tuning call is made.  Profiling (kvo_profile) bypasses the graphs.
+ * gather tuning call is made.  Profiling (kvo_profile) bypasses the graphs,
+ * and so does resident = 1.
  * 0 (default): every step is launched stream by stream.
  */
 kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable);
