@@ -121,6 +121,24 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged)
         c.close()
 
 
+def test_resident_setters_check_their_arguments():
+    w = Workload("res_args", 1, 4, 1, 64, 16, 4, 16, 1, (16 + 16 * 8, 16 + 16 * 8))
+    c = Case(w, 1, gen_device="cpu", resident=True)
+    try:
+        with pytest.raises(Exception, match="blocks"):
+            c.ctx.set_prefetch_budget(-2)
+        c.ctx.set_prefetch_budget(-1)
+        with pytest.raises(Exception, match="layer"):
+            c.ctx.resident_slots(1)
+        with pytest.raises(Exception, match="implementation"):
+            c.ctx.set_attn_impl(2)
+        with pytest.raises(Exception, match="implementation"):
+            c.ctx.set_attn_impl(1, -1)
+        c.ctx.set_attn_impl(1, 0)
+    finally:
+        c.close()
+
+
 def test_resident_calls_need_resident_mode():
     w = Workload("plain", 1, 4, 1, 64, 16, 4, 16, 1, (16 + 16 * 8, 16 + 16 * 8))
     c = Case(w, 1, gen_device="cpu")
