@@ -263,9 +263,15 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         for (int shift = 16; shift >= 0; shift -= 8) {
             h_s[0][tid] = 0u;
             __syncthreads();
-            for (int j = tid; j < C; j += SEL_THREADS) {
-                const uint32_t key = __ldcg(kq + j);
-                if ((key & mask) == prefix) atomicAdd(&h_s[0][(key >> shift) & 0xFFu], 1u);
+            // four keys per thread per step (16-byte loads; the key rows are padded to
+            // a multiple of 4), two steps unrolled so their loads are in flight together
+#pragma unroll 2
+            for (int j0 = 4 * tid; j0 < C; j0 += 4 * SEL_THREADS) {
+                const uint4 kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
+                const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (j0 + e < C && (kv[e] & mask) == prefix) atomicAdd(&h_s[0][(kv[e] >> shift) & 0xFFu], 1u);
             }
             __syncthreads();
             const uint32_t cnt = h_s[0][255 - tid];
