@@ -303,7 +303,9 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
  * speculative query) the prediction for the next step becomes resident the
  * same way, sparing the blocks of T, on the low-priority stream.  Without a
  * speculative query only the urgent phase runs (the previous step's T is
- * spared).  CUDA-graph replay is not used in this mode.
+ * spared).  CUDA-graph replay is not used in this mode, and its copies
+ * always use the flat gather engine (engine 3, with per-entry destination
+ * slots) whatever kvo_set_gather_engine chose.
  *   kvo_resident_slots: synchronize, copy layer `layer`'s slot table
  *   [G][2k] int32 to host memory `slots_out`.
  *   kvo_resident_fetched: synchronize, write the blocks fetched since init (or
