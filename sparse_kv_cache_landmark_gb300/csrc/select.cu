@@ -117,8 +117,13 @@ __device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, in
     __syncthreads();
 }
 
+// resident CTAs per SM requested: enough to keep the landmark loads in flight
+// without the last-CTA selection code pushing the register count up
+template <bool BF16LM, int SEL_RPT>
+constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 6 : (BF16LM ? 1 : 5); }
+
 template <int D, bool BF16LM, bool DUAL, int SEL_RPT>
-__global__ void __launch_bounds__(SEL_THREADS)
+__global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
 select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
               const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
               uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
@@ -249,7 +254,12 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     __syncthreads();
     if (!s_last) return;
 
-    // ---- last CTA of the group: exact top-k for each query
+    // ---- last CTA of the group: exact top-k for each query.  Thread t owns the
+    // contiguous keys [c0, c1) of the group (a multiple of 4 of them, so 16-byte
+    // loads stay inside the padded key row), read 16 at a time with independent
+    // loads; the compaction then needs two block scans in all.
+    const int per = ((C + SEL_THREADS - 1) / SEL_THREADS + 3) & ~3;
+    const int c0 = min(C, tid * per), c1 = min(C, c0 + per);
     for (int qi = 0; qi < NQ; ++qi) {
         const uint32_t* kq = keys + ((int64_t)qi * G + bg) * Cmax4;
         int32_t* out = (qi == 0 ? idx_true : idx_pred) + (int64_t)bg * k;
@@ -260,18 +270,40 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         pick_digit(cnt0, warp_sums, &s_digit, &s_krem, k_rem);
         uint32_t prefix = (uint32_t)s_digit << 24, mask = 0xFF000000u;
         k_rem = s_krem;
+        // visit this thread's keys in ascending order: f(j, key)
+        auto scan_chunk = [&](auto&& f) {
+            for (int j = c0; j < c1; j += 16) {
+                uint4 kv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    kv[u] = j + 4 * u < c1 ? __ldcg(reinterpret_cast<const uint4*>(kq + j + 4 * u))
+                                           : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (j + 4 * u + e < c1) f(j + 4 * u + e, kk[e]);
+                }
+            }
+        };
+        const bool small = C <= 4 * SEL_THREADS;             // at most 4 keys per thread
         for (int shift = 16; shift >= 0; shift -= 8) {
             h_s[0][tid] = 0u;
             __syncthreads();
-            // four keys per thread per step (16-byte loads; the key rows are padded to
-            // a multiple of 4), two steps unrolled so their loads are in flight together
-#pragma unroll 2
-            for (int j0 = 4 * tid; j0 < C; j0 += 4 * SEL_THREADS) {
-                const uint4 kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
-                const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
+            if (small) {
+                const int j0 = 4 * tid;
+                if (j0 < C) {
+                    const uint4 kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
+                    const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (j0 + e < C && (kv[e] & mask) == prefix) atomicAdd(&h_s[0][(kv[e] >> shift) & 0xFFu], 1u);
+                    for (int e = 0; e < 4; ++e)
+                        if (j0 + e < C && (kv[e] & mask) == prefix) atomicAdd(&h_s[0][(kv[e] >> shift) & 0xFFu], 1u);
+                }
+            } else {
+                scan_chunk([&](int, uint32_t key) {
+                    if ((key & mask) == prefix) atomicAdd(&h_s[0][(key >> shift) & 0xFFu], 1u);
+                });
             }
             __syncthreads();
             const uint32_t cnt = h_s[0][255 - tid];
@@ -285,38 +317,48 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         // k_rem keys equal to it, in ascending id order.
         const uint32_t thr = prefix;
         const uint32_t k_eq = k_rem;
-        const uint32_t k_out = (uint32_t)min(k, C);
-        uint32_t n_out = 0, eq_seen = 0;
-        for (int base = 0; base < C && n_out < k_out; base += 4 * SEL_THREADS) {
-            const int j0 = base + 4 * tid;
+        if (small) {
+            // one sweep: 4 keys per thread in id order, two block scans
+            const int j0 = 4 * tid;
             uint4 kv4 = make_uint4(0u, 0u, 0u, 0u);
             if (j0 < C) kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
             const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
             uint32_t n_eq = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) n_eq += (j0 + e < C && kv[e] == thr);
-            uint32_t eq_total;
-            const uint32_t eq_excl = block_exclusive_scan(n_eq, warp_sums, &eq_total);
-            uint32_t sel = 0, eq_run = eq_seen + eq_excl;
+            uint32_t tot;
+            uint32_t eq_run = block_exclusive_scan(n_eq, warp_sums, &tot);
+            uint32_t sel = 0;
             bool take[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const bool valid = j0 + e < C;
                 bool t = valid && kv[e] > thr;
-                if (valid && kv[e] == thr) {
-                    t = eq_run < k_eq;
-                    ++eq_run;
-                }
+                if (valid && kv[e] == thr) t = eq_run++ < k_eq;
                 take[e] = t;
                 sel += t;
             }
-            uint32_t sel_total;
-            uint32_t pos = n_out + block_exclusive_scan(sel, warp_sums, &sel_total);
+            uint32_t pos = block_exclusive_scan(sel, warp_sums, &tot);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (take[e]) out[pos++] = j0 + e;
-            n_out += sel_total;
-            eq_seen += eq_total;
+        } else {
+            // counts per chunk, two block scans for the offsets, then the writes
+            uint32_t n_gt = 0, n_eq = 0;
+            scan_chunk([&](int, uint32_t key) {
+                n_gt += key > thr;
+                n_eq += key == thr;
+            });
+            uint32_t tot;
+            const uint32_t eq_before = block_exclusive_scan(n_eq, warp_sums, &tot);
+            const uint32_t eq_take = eq_before >= k_eq ? 0u : min(n_eq, k_eq - eq_before);
+            uint32_t pos = block_exclusive_scan(n_gt + eq_take, warp_sums, &tot);
+            uint32_t eq_run = eq_before;
+            scan_chunk([&](int j, uint32_t key) {
+                bool take = key > thr;
+                if (key == thr) take = eq_run++ < k_eq;
+                if (take) out[pos++] = j;
+            });
         }
         __syncthreads();
     }
