@@ -117,10 +117,11 @@ __device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, in
     __syncthreads();
 }
 
-// resident CTAs per SM requested: enough to keep the landmark loads in flight
-// without the last-CTA selection code pushing the register count up
+// resident CTAs per SM requested (a register budget): measured on the four
+// large workloads, 4 for fp32 landmarks and none for bf16 ones, whose deeper
+// per-thread load batches beat occupancy
 template <bool BF16LM, int SEL_RPT>
-constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 6 : (BF16LM ? 1 : 5); }
+constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 4 : (BF16LM ? 1 : 4); }
 
 template <int D, bool BF16LM, bool DUAL, int SEL_RPT>
 __global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
