@@ -133,19 +133,17 @@ struct WarpAttn {
         }
     }
 
-    // online softmax of the 16 tokens of a tile, log2 domain; bit i of vmask
-    // says whether token i exists (at least one does).  Gives the bf16 P
-    // fragments and the rescale factors of the old state.
-    __device__ __forceinline__ void softmax(const float (&s)[2][4], uint32_t vmask, float scale_log2, int tq,
+    // online softmax of tokens tb .. tb+15 (valid below n_tok), log2 domain;
+    // gives the bf16 P fragments and the rescale factors of the old state
+    __device__ __forceinline__ void softmax(const float (&s)[2][4], int tb, int n_tok, float scale_log2, int tq,
                                             uint32_t (&pa)[4], float& al0, float& al1) {
         // lane holds tokens 2t, 2t+1 of each n8 tile
         float x[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int t0 = 8 * nt + 2 * tq;
+            const int t0 = tb + 8 * nt + 2 * tq;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                x[nt][e] = ((vmask >> (t0 + (e & 1))) & 1u) ? s[nt][e] * scale_log2 : -INFINITY;
+            for (int e = 0; e < 4; ++e) x[nt][e] = (t0 + (e & 1) < n_tok) ? s[nt][e] * scale_log2 : -INFINITY;
         }
         float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -213,8 +211,7 @@ struct WarpAttn {
         qk(kf, s);
         uint32_t pa[4];
         float al0, al1;
-        const int nv = n_tok - tb;                          // tokens of the tile that exist
-        softmax(s, nv >= 16 ? 0xFFFFu : (1u << nv) - 1u, scale_log2, tq, pa, al0, al1);
+        softmax(s, tb, n_tok, scale_log2, tq, pa, al0, al1);
         pv(vf, pa, al0, al1);
     }
 
@@ -519,8 +516,7 @@ struct AttnTmaCfg {
     static constexpr int RING = ATT_WARPS * STG * STAGE_BYTES;
     static constexpr int O_FLOATS = ATT_WARPS * 8 * NR * D;
     static constexpr size_t BYTES = (size_t)RING + sizeof(float) * (O_FLOATS + 2 * ATT_WARPS * 16) +
-                                    sizeof(uint64_t) * ATT_WARPS * STG + sizeof(int4) * ATT_ITEMS_SMEM +
-                                    sizeof(uint32_t) * ATT_WARPS * STG + 16;
+                                    sizeof(uint64_t) * ATT_WARPS * STG + sizeof(int4) * ATT_ITEMS_SMEM + 16;
 };
 
 constexpr long long kAttWaitNs = 2000000000LL;   // 2 s per mbarrier wait
@@ -561,13 +557,10 @@ __device__ __forceinline__ int4 item_hdr(const int4* s_items, const int4* __rest
 // prefetching caller does not wait for the window length here.
 __device__ __forceinline__ void cursor_fields(AttnCursor& c, int4 it, int k, int B, int W,
                                               const int32_t* __restrict__ w_start,
-                                              const int32_t* __restrict__ w_len,
-                                              const int32_t* __restrict__ sp_cnt) {
+                                              const int32_t* __restrict__ w_len) {
     c.bg = it.x; c.part = it.y; c.tile0 = it.z; c.ntiles = it.w;
     c.ws = (c.part == 1 && w_start) ? __ldg(w_start + c.bg) : 0;
-    // sparse part: k blocks, or the first sp_cnt[g] entries of the slot list when given
-    c.n_tok = c.part == 0 ? (sp_cnt ? min(k, max(0, __ldg(sp_cnt + c.bg))) : k) * B
-                          : (w_len ? __ldg(w_len + c.bg) : W);
+    c.n_tok = c.part == 0 ? k * B : (w_len ? __ldg(w_len + c.bg) : W);
 }
 // tiles of the item that hold tokens (a window may be shorter than its items cover)
 __device__ __forceinline__ void cursor_nt(AttnCursor& c) {
@@ -580,9 +573,8 @@ struct ItemSrc {
     int lo, k, B, W;
     const int32_t* w_start;
     const int32_t* w_len;
-    const int32_t* sp_cnt;
     __device__ __forceinline__ void load(AttnCursor& c) const {
-        cursor_fields(c, item_hdr(s_items, items, lo, c.item), k, B, W, w_start, w_len, sp_cnt);
+        cursor_fields(c, item_hdr(s_items, items, lo, c.item), k, B, W, w_start, w_len);
         cursor_nt(c);
     }
 };
@@ -618,48 +610,40 @@ __device__ __forceinline__ int cursor_slot(const AttnCursor& c, const int32_t* _
 }
 
 // Copy the cursor's tile into a stage: lane j copies row j & 15 of the K tile
-// (j < 16) or of the V tile (j >= 16); `sl` is the lane's cursor_slot.  A
-// row exists when it lies inside the part and, for the sparse part, its block
-// is not marked in `skip` ([G][k], nullable); only existing rows are copied.
-// Returns the tile's 16-bit mask of existing rows (same in every lane).
+// (j < 16) or of the V tile (j >= 16); `sl` is the lane's cursor_slot.
 template <int D>
-__device__ __forceinline__ uint32_t tile_copy(const AttnCursor& c, int sl, unsigned char* stage, uint32_t fb,
-                                              const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
-                                              const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv,
-                                              const uint8_t* __restrict__ skip, int k, int B, int Wcap, int& bad) {
+__device__ __forceinline__ void tile_copy(const AttnCursor& c, int sl, unsigned char* stage, uint32_t fb,
+                                          const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
+                                          const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, int k,
+                                          int B, int Wcap, int& bad) {
     const int lane = threadIdx.x & 31, kv = lane >> 4, row = lane & 15;
     const int tb = (c.tile0 + c.tl) * ATT_TILE;
     const int rows = min(ATT_TILE, c.n_tok - tb);
+    if (lane == 0) mbar_expect_tx(fb, (uint32_t)(rows * D * 2 * 2));
+    __syncwarp();
     const int tok = tb + row;
-    bool valid = row < rows;
+    const bool valid = row < rows;
     const uint16_t* src;
     bool start;
     if (c.part == 0) {
         const int blk = tok / B, off = tok - blk * B;
-        if (valid && skip && skip[(int64_t)c.bg * k + blk]) valid = false;
         if (valid && (sl < 0 || sl >= 2 * k)) { bad |= KVO_DEV_BAD_SLOT; sl = 0; }
         const int sl_prev = __shfl_up_sync(0xffffffffu, sl, 1);
-        const bool valid_prev = __shfl_up_sync(0xffffffffu, valid, 1);
         src = (kv ? bv : bk) + (((int64_t)c.bg * 2 * k + sl) * B + off) * D;
-        start = valid && (row == 0 || !valid_prev || (off == 0 && sl != sl_prev + 1));
+        start = valid && (row == 0 || (off == 0 && sl != sl_prev + 1));
     } else {
         int sw = c.ws + tok;
         if (sw >= Wcap) sw -= Wcap;
         src = (kv ? wv : wk) + ((int64_t)c.bg * Wcap + sw) * D;
         start = valid && (row == 0 || sw == 0);
     }
-    const uint32_t vmask = __ballot_sync(0xffffffffu, valid) & 0xffffu;   // K half == V half
-    if (lane == 0) mbar_expect_tx(fb, (uint32_t)(__popc(vmask) * D * 2 * 2));
-    __syncwarp();
-    // a copy runs from a start to the next start or the next row that does not exist
-    const unsigned stops = (__ballot_sync(0xffffffffu, start || !valid) >> (kv * 16)) & 0xffffu;
+    const unsigned starts = (__ballot_sync(0xffffffffu, start) >> (kv * 16)) & 0xffffu;
     if (start) {
-        const unsigned later = stops & ~((2u << row) - 1u);
+        const unsigned later = starts & ~((2u << row) - 1u);
         const int next = later ? __ffs(later) - 1 : rows;
         bulk_load(smem_u32(stage + kv * (ATT_TILE * D * 2) + row * D * 2), src, (uint32_t)((next - row) * D * 2),
                   fb);
     }
-    return vmask;
 }
 
 template <int D, int NR>
@@ -672,8 +656,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
                 uint32_t* __restrict__ done, float* __restrict__ out_o, float* __restrict__ out_lse,
                 float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec, int fuse, int batch, int r,
                 int Hkv, int k, int B, int W, int Wcap, const int32_t* __restrict__ w_start,
-                const int32_t* __restrict__ w_len, const uint8_t* __restrict__ skip,
-                const int32_t* __restrict__ sp_cnt, float scale_log2, int32_t* __restrict__ status) {
+                const int32_t* __restrict__ w_len, float scale_log2, int32_t* __restrict__ status) {
     using WA = WarpAttn<D, NR>;
     using CF = AttnTmaCfg<D, NR>;
     constexpr int CH = WA::CH, CPT = WA::CPT, STG = CF::STG;
@@ -684,8 +667,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     float (*sm_l)[16] = sm_m + ATT_WARPS;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm_l + ATT_WARPS);   // [ATT_WARPS][STG]
     int4* s_items = reinterpret_cast<int4*>(full + ATT_WARPS * STG);  // [ATT_ITEMS_SMEM]
-    uint32_t* s_vm = reinterpret_cast<uint32_t*>(s_items + ATT_ITEMS_SMEM);   // [ATT_WARPS][STG] tile row masks
-    int* s_last = reinterpret_cast<int*>(s_vm + ATT_WARPS * STG);
+    int* s_last = reinterpret_cast<int*>(s_items + ATT_ITEMS_SMEM);
     volatile int* s_abort = s_last + 1;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -699,7 +681,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
 
     const int Hq = Hkv * r;
     const int nrows = q_spec ? 2 * r : r;
-    const ItemSrc src{s_items, items, lo, k, B, W, w_start, w_len, sp_cnt};
+    const ItemSrc src{s_items, items, lo, k, B, W, w_start, w_len};
     unsigned char* ring = smem + warp * STG * CF::STAGE_BYTES;
     uint64_t* wfull = full + warp * STG;
     int bad = 0;
@@ -712,9 +694,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     auto issue = [&]() {
         if (ic.item >= ic.hi) return;
         const int st = (int)(nissue % STG);
-        const uint32_t vm = tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv,
-                                         skip, k, B, Wcap, bad);
-        if (lane == 0) s_vm[warp * STG + st] = vm;
+        tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad);
         ++nissue;
         cursor_next(ic, warp, src);
         isl = cursor_slot(ic, slot, k, B, row);
@@ -728,7 +708,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     uint4 nq0[CH], nq1[CH];
     auto fetch = [&](int item) {
         nc.item = item; nc.hi = hi; nc.tl = warp;
-        cursor_fields(nc, item_hdr(s_items, items, lo, item), k, B, W, w_start, w_len, sp_cnt);
+        cursor_fields(nc, item_hdr(s_items, items, lo, item), k, B, W, w_start, w_len);
         const int b = nc.bg / Hkv, gk = nc.bg % Hkv;
         auto qrow = [&](int rr) -> const uint16_t* {
             return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
@@ -747,34 +727,26 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
             const int st = (int)(ncons % STG);
             if (!*s_abort) att_wait(smem_u32(&wfull[st]), (uint32_t)((ncons / STG) & 1), s_abort, status);
             ++ncons;
-            const uint32_t vm = s_vm[warp * STG + st];       // rows of the tile that exist
-            if (vm != 0u) {
-                const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * CF::STAGE_BYTES);
-                const uint16_t* vs = ks + ATT_TILE * D;
-                // rows that do not exist hold stale data: read the tile's first existing row instead
-                const int r0 = __ffs(vm) - 1;
-                auto row_of = [&](int rr) { return ((vm >> rr) & 1u) ? rr : r0; };
-                uint4 kf[2][CH];
+            const int tb = (cc.tile0 + tl) * ATT_TILE;
+            const int rows = min(ATT_TILE, cc.n_tok - tb);
+            const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * CF::STAGE_BYTES);
+            const uint16_t* vs = ks + ATT_TILE * D;
+            // rows past the tile's end hold stale data: read the last valid row instead
+            uint4 kf[2][CH];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint16_t* kp = ks + row_of(8 * h + gq) * D + 8 * tq;
+            for (int h = 0; h < 2; ++h) {
+                const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
 #pragma unroll
-                    for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
-                }
-                uint4 vf[4][CPT / 8];
-#pragma unroll
-                for (int vi = 0; vi < 4; ++vi) {
-                    const uint16_t* vp = vs + row_of(2 * tq + (vi & 1) + 8 * (vi >> 1)) * D + CPT * gq;
-#pragma unroll
-                    for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
-                }
-                float sc[2][4];
-                stt.qk(kf, sc);
-                uint32_t pa[4];
-                float al0, al1;
-                stt.softmax(sc, vm, scale_log2, tq, pa, al0, al1);
-                stt.pv(vf, pa, al0, al1);
+                for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
             }
+            uint4 vf[4][CPT / 8];
+#pragma unroll
+            for (int vi = 0; vi < 4; ++vi) {
+                const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
+#pragma unroll
+                for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
+            }
+            stt.tile(kf, vf, tb, cc.n_tok, scale_log2, tq);
             // the stage's shared-memory reads are done (their values fed the mma):
             // order them before the async-proxy refill of the same stage
             __syncwarp();
@@ -817,22 +789,18 @@ cudaError_t prepare_attention(Ctx& c) {
 
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step, const uint8_t* skip,
-                             const int32_t* sp_cnt, bool win) {
+                             bool in_step) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
     const int nrows = q_spec ? 2 * c.r : c.r;
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
-    // block skipping, partial block lists and window-less passes exist in the TMA-staged kernel only
-    if ((skip || sp_cnt || !win) && c.att_impl != 1) return cudaErrorInvalidValue;
 #define KVO_ATT(D_, NR_)                                                                                         \
     if (c.att_impl == 1)                                                                                        \
         attn_tma_kernel<D_, NR_><<<pl.grid, ATT_WARPS * 32, AttnTmaCfg<D_, NR_>::BYTES, s>>>(                   \
             (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, pl.items,      \
             pl.cta, pl.first, pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec,     \
-            fuse, c.batch, c.r, c.Hkv, c.k, c.B, win ? c.W : 0, c.Wcap, c.g_wstart, win ? c.g_wlen : nullptr,  \
-            skip, sp_cnt, scale_log2, c.status);                                                                \
+            fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status);      \
     else                                                                                                        \
         attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                           \
             (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, c.att_items,   \

@@ -66,12 +66,6 @@ struct Ctx {
     unsigned long long* res_fetched = nullptr;   // [2] blocks fetched: urgent, prefetch
     std::vector<char> res_pending;  // [L] a prefetch into the layer's set was issued and not yet waited for
     int res_budget = -1;            // prefetch fetches admitted per group, layer and step (-1: all)
-    // split attention of the resident step: hits + window, then the fetched misses
-    uint8_t* res_miss = nullptr;    // [G][k] 1 where the true index entry was fetched this step
-    float* res_oA = nullptr;        // [rows][d] hits + window
-    float* res_lA = nullptr;        // [rows]
-    float* res_oB = nullptr;        // [2][rows][d] fetched misses (part 0), empty window part (part 1)
-    float* res_lB = nullptr;        // [2][rows]
     // Low-rank keys per layer (caller-owned device factors; rank 0: not set)
     std::vector<const uint16_t*> lr_coef, lr_basis;
     std::vector<int> lr_rank;
@@ -220,12 +214,11 @@ cudaError_t launch_lowrank_k(const Ctx& c, int layer, int buf, const int32_t* id
 cudaError_t prepare_lowrank();
 cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
                                    int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
-                                   int phase, cudaStream_t s, int max_fetch = -1, uint8_t* miss_flag = nullptr);
+                                   int phase, cudaStream_t s, int max_fetch = -1);
 cudaError_t prepare_resident(const Ctx& c);
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step = false, const uint8_t* skip = nullptr, const int32_t* sp_cnt = nullptr,
-                             bool win = true);
+                             bool in_step = false);
 cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
                              float* lse, int rows, int d, cudaStream_t s);
 cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s);

@@ -31,8 +31,7 @@ __device__ __forceinline__ bool sorted_contains(const int32_t* a, int n, int32_t
 
 // One CTA per group.  map [G][Ccap] and slots [G][cap] are this layer's tables.
 // Outputs: the fetched blocks (ascending ids) with their destination slots and
-// count, and (optional) the slot of every need entry after the update and
-// whether it was missing (fetched by this call) or already resident.
+// count, and (optional) the slot of every need entry after the update.
 // max_fetch >= 0 admits only the max_fetch missing blocks with the lowest ids
 // (a cap on host bytes, used for the prefetch phase only; "PulseInfer and the
 // I/O Problem Behind Long-Context Decoding", §2: I/O-adaptive offloading
@@ -41,9 +40,8 @@ __global__ void __launch_bounds__(RES_THREADS)
 resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restrict__ keep,
                        int32_t* __restrict__ map, int32_t* __restrict__ slots, const int32_t* __restrict__ g_C,
                        int32_t* __restrict__ out_ids, int32_t* __restrict__ out_cnt, int32_t* __restrict__ out_dslot,
-                       int32_t* __restrict__ slot_of, uint8_t* __restrict__ miss_flag,
-                       unsigned long long* __restrict__ fetched, int k, int cap, int Ccap, int max_fetch,
-                       int32_t* __restrict__ status) {
+                       int32_t* __restrict__ slot_of, unsigned long long* __restrict__ fetched, int k, int cap,
+                       int Ccap, int max_fetch, int32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t rs[];
     int32_t* s_need = rs;                  // [k]
     int32_t* s_keep = s_need + k;          // [k]
@@ -91,9 +89,7 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
     const uint32_t n_miss = s_tot;
     for (int i = i0; i < i1; ++i) {
         const int32_t x = s_need[i];
-        const bool miss = x >= 0 && x < C && mg[x] < 0;
-        if (miss) s_mid[base++] = x;
-        if (miss_flag) miss_flag[(int64_t)g * k + i] = miss ? 1 : 0;
+        if (x >= 0 && x < C && mg[x] < 0) s_mid[base++] = x;
     }
     __syncthreads();
     // admission: at most max_fetch fetches (lowest ids first) when max_fetch >= 0
@@ -140,12 +136,11 @@ cudaError_t prepare_resident(const Ctx& c) {
 // phase 0: urgent (counts into res_fetched[0]), 1: prefetch (res_fetched[1])
 cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
                                    int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
-                                   int phase, cudaStream_t s, int max_fetch, uint8_t* miss_flag) {
+                                   int phase, cudaStream_t s, int max_fetch) {
     const int cap = 2 * c.k;
     resident_assign_kernel<<<c.G, RES_THREADS, res_smem(c), s>>>(
         need, keep, c.res_map + (size_t)layer * c.G * c.Cmax, c.res_slots + (size_t)layer * c.G * cap, c.g_C,
-        out_ids, out_cnt, out_dslot, slot_of, miss_flag, c.res_fetched + phase, c.k, cap, c.Cmax, max_fetch,
-        c.status);
+        out_ids, out_cnt, out_dslot, slot_of, c.res_fetched + phase, c.k, cap, c.Cmax, max_fetch, c.status);
     return cudaGetLastError();
 }
 

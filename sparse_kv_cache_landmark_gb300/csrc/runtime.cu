@@ -164,7 +164,7 @@ void free_ctx(kvo::Ctx& c) {
     for (void* p : c.res_k) F(p);
     for (void* p : c.res_v) F(p);
     F(c.res_map); F(c.res_slots); F(c.res_dslot); F(c.res_pf_ids); F(c.res_pf_cnt); F(c.res_pf_dslot);
-    F(c.res_fetched); F(c.res_miss); F(c.res_oA); F(c.res_lA); F(c.res_oB); F(c.res_lB);
+    F(c.res_fetched);
     F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
     F(c.runs); F(c.nruns);
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
@@ -352,12 +352,6 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, dalloc(&c.res_pf_cnt, sizeof(int32_t) * lg, &sb));
         KVO_CUDA(&c, dalloc(&c.res_pf_dslot, sizeof(int32_t) * lg * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_fetched, sizeof(unsigned long long) * 2, &sb));
-        const size_t rows = (size_t)c.batch * c.Hq;
-        KVO_CUDA(&c, dalloc(&c.res_miss, (size_t)c.G * c.k, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * rows * c.d, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * rows, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_oB, sizeof(float) * 2 * rows * c.d, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_lB, sizeof(float) * 2 * rows, &sb));
         KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
         c.res_pending.assign(c.L, 0);
         KVO_CUDA(&c, kvo::prepare_resident(c));
@@ -758,11 +752,9 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, c.s_compute);
         }));
         // 2. urgent assign: T resident, sparing the prediction fetched for this step
-        // split attention: hits + window first (beside the urgent copies), then the misses
-        const bool split = c.att_impl == 1 && !o_spec;
         KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_compute, [&] {
             return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
-                                               c.s_compute, -1, split ? c.res_miss : nullptr);
+                                               c.s_compute);
         }));
         KVO_CUDA(&c, cudaEventRecord(E.sel[l], c.s_compute));
         // 3. urgent gather of the blocks that were missing
@@ -778,32 +770,15 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
                 return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, c.s_compute);
             }));
         KVO_CUDA(&c, cudaEventRecord(E.urg[l], c.s_urgent));
-        // 4. attention over the resident set
+        // 4. attention over the resident set once the urgent and prefetched blocks have landed
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.rpref[l], 0));
         c.res_pending[l] = 0;
-        if (split) {
-            // (a) blocks that were resident already, plus the window, beside the urgent copies
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
-                return kvo::launch_attention(c, l, buf, ql, nullptr, slot, c.res_oA, c.res_lA, nullptr, nullptr, 1,
-                                             c.s_compute, true, c.res_miss);
-            }));
-            // (b) the blocks this step fetched, once they have landed; (c) log-sum-exp merge
-            KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
-                return kvo::launch_attention(c, l, buf, ql, nullptr, dsl, c.res_oB, c.res_lB, nullptr, nullptr, 0,
-                                             c.s_compute, true, nullptr, mcnt, false);
-            }));
-            const int rows = c.batch * c.Hq;
-            KVO_CUDA(&c, kvo::launch_merge_lse(c.res_oA, c.res_lA, c.res_oB, c.res_lB, o + l * o_layer,
-                                               lse + l * lse_layer, rows, c.d, c.s_compute));
-        } else {
-            KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
-                return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
-                                             lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
-                                             lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute, true);
-            }));
-        }
+        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
+            return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
+                                         lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute, true);
+        }));
         KVO_CUDA(&c, cudaEventRecord(E.attn[l], c.s_compute));
         // 5. prefetch of the next step's prediction, sparing T
         if (q_spec) {

@@ -45,14 +45,13 @@ def _attempts(c, steps, drift):
     return out
 
 
-@pytest.mark.parametrize("spec,L,B,k,dual,budget,W,ragged,impl", [
-    (True, 2, 16, 16, True, None, 32, False, 1), (False, 1, 16, 16, False, None, 32, False, 1),
-    (True, 1, 1, 64, False, None, 32, False, 1), (True, 3, 32, 8, False, None, 32, False, 1),
-    (True, 2, 16, 16, False, 3, 32, False, 1),
-    (True, 1, 16, 16, False, None, 0, False, 1),       # no window: attention over the resident blocks alone
-    (True, 2, 32, 12, False, None, 64, True, 1),       # ragged lengths, k not a multiple of the warp count
-    (True, 2, 16, 16, False, None, 32, False, 0)])     # register-direct kernel: one attention pass per layer
-def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged, impl):
+@pytest.mark.parametrize("spec,L,B,k,dual,budget,W,ragged", [
+    (True, 2, 16, 16, True, None, 32, False), (False, 1, 16, 16, False, None, 32, False),
+    (True, 1, 1, 64, False, None, 32, False), (True, 3, 32, 8, False, None, 32, False),
+    (True, 2, 16, 16, False, 3, 32, False),
+    (True, 1, 16, 16, False, None, 0, False),          # no window: attention over the resident blocks alone
+    (True, 2, 32, 12, False, None, 64, True)])         # ragged lengths, k not a multiple of the warp count
+def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged):
     drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
     ctx = (n, n + 40 * B) if ragged else (n, n)
@@ -61,7 +60,6 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged,
     c = Case(w, seed, gen_device="cpu", resident=True)
     try:
         att = _attempts(c, steps, drift)
-        c.ctx.set_attn_impl(impl)     # impl 1 splits each layer's attention: resident hits, then fetched misses
         if budget is not None:
             c.ctx.set_prefetch_budget(budget)     # admission cap on speculative fetches
         G, r = w.batch * w.n_kv_heads, w.group_size
