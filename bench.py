@@ -68,7 +68,8 @@ def parse():
                     help="attention kernel: 0 register-direct, 1 TMA-staged persistent (-1: default)")
     ap.add_argument("--attn-ctas", type=int, default=0, help="TMA-staged attention grid (0: fill the SMs)")
     ap.add_argument("--resident", type=int, default=0,
-                    help="1: cross-step delta prefetch (per-layer resident block sets), queries drifting per step")
+                    help="1: cross-step delta prefetch (per-layer resident block sets), queries drifting per step; "
+                         "2: the resident sets without speculation (each step fetches only its misses)")
     ap.add_argument("--drift", type=float, default=-1.0,
                     help="per-step query drift with --resident (default: the speculative noise / sqrt(2))")
     ap.add_argument("--query-steps", type=int, default=8, help="distinct step queries cycled with --resident")
@@ -385,8 +386,10 @@ def build_workload(args, ws=1):
         qsteps = [[synth.gen_queries_step(w, args.seed, l, s, B.drift) for l in range(w.n_layers)]
                   for s in range(args.query_steps)]
         B.q_steps_pin = torch.stack([torch.stack([x[0] for x in st]) for st in qsteps]).pin_memory()
-        B.qs_steps_pin = (None if qsteps[0][0][1] is None else
+        B.qs_steps_pin = (None if qsteps[0][0][1] is None or args.resident == 2 else
                           torch.stack([torch.stack([x[1] for x in st]) for st in qsteps]).pin_memory())
+        if args.resident == 2:
+            B.qs_pin = B.qs_dev = None
         B.q_steps = B.q_steps_pin.to("cuda")
         B.qs_steps = None if B.qs_steps_pin is None else B.qs_steps_pin.to("cuda")
     B.step_i = 0
@@ -630,6 +633,7 @@ def run_ours(args):
                 "host_bytes_saved_per_step": misses * w.block_size * 2 * w.head_dim,
                 "note": "missed keys rebuilt on the GPU from rank-R factors; misses move V only"},
             "resident": None if not args.resident else {
+                "speculation": args.resident == 1,
                 "drift": Bw.drift, "query_steps": args.query_steps, "prefetch_budget": args.prefetch_budget,
                 "fetched_blocks_per_step": fetched_step,
                 "fetched_of_selected": fetched_step / (w.n_layers * w.batch * w.n_kv_heads * w.top_k),

@@ -414,7 +414,8 @@ kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers);
 
 /*
  * kvo_set_gather_reserve -- engine 3 only: shared memory each gather CTA
- * reserves without using it (0..227 KiB).  A reservation near the SM's
+ * reserves without using it (0..232,320 bytes: 227 KiB less the kernel's own
+ * 128-byte table).  A reservation near the SM's
  * capacity gives each gather CTA an SM of its own, so HBM-bound kernels never
  * share an SM (and its load/store pipeline) with loads waiting on the link.
  * Set the engine before kvo_set_gather_shape when asking for > 256 threads.

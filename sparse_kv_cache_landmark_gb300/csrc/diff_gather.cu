@@ -178,12 +178,18 @@ gather_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh, 
 // adjacent block ids is one contiguous source range and one contiguous
 // destination range.  Persistent warps walk chunks of 32*U 16-byte words of
 // one group's entry stream (K and V): no per-run dependency chain, and a
-// warp's metadata loads hit one or two cache lines.  The launch may reserve
-// shared memory it never uses so that each gather CTA has its SM to itself:
-// the other kernels then never queue their HBM loads behind zero-copy loads
-// waiting on the host link in the same SM's load/store pipeline.  With a slot
-// list (dslot) entry j goes to slot dslot[bg][j] instead; kv_mask bit 0 copies
-// K, bit 1 copies V (V alone where the keys are rebuilt on the GPU).
+// warp's metadata loads hit one or two cache lines.  With `compact` every CTA
+// first builds, in shared memory, the prefix over the groups of their chunk
+// counts (listed entries x words per block, rounded up to chunks), so the warps
+// stride over the listed chunks only -- a short miss list costs a short walk --
+// and find a chunk's group by binary search; without it (more groups than the
+// prefix may hold) the warps stride over k entries' chunks of every group.
+// The launch may reserve shared memory it never uses so that each gather CTA
+// has its SM to itself: the other kernels then never queue their HBM loads
+// behind zero-copy loads waiting on the host link in the same SM's load/store
+// pipeline.  With a slot list (dslot) entry j goes to slot dslot[bg][j]
+// instead; kv_mask bit 0 copies K, bit 1 copies V (V alone where the keys are
+// rebuilt on the GPU).
 template <int U, bool POW2>
 __global__ void __launch_bounds__(1024)
 gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh,
@@ -191,20 +197,73 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
                    const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int slot_base,
                    const int32_t* __restrict__ dslot,
                    uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int G, int k, int B, int D, int words_log2,
-                   int kv_mask, int32_t* __restrict__ status) {
+                   int kv_mask, bool compact, int32_t* __restrict__ status) {
     constexpr uint32_t CHUNK = 32 * U;                       // words per warp iteration
+    extern __shared__ uint32_t s_pre[];                      // [G + 1] chunk prefix (compact)
+    __shared__ uint32_t s_wsum[32];
     const uint32_t words = (uint32_t)B * D / 8;             // 16-byte words per block
     const uint32_t per_group = ((uint32_t)k * words + CHUNK - 1) / CHUNK;   // chunks per group
-    const int64_t total = (int64_t)G * per_group;
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     int bad = 0;
+    int64_t total = (int64_t)G * per_group;
+    if (compact) {
+        // block-wide exclusive scan: thread t owns groups [t*per, t*per + per)
+        const int nt = blockDim.x, t = threadIdx.x, per = (G + nt - 1) / nt;
+        const int g0 = min(t * per, G), g1 = min(g0 + per, G);
+        auto chunks_of = [&](int g, int& flag) -> uint32_t {
+            int n = cnt ? __ldg(cnt + g) : k;
+            if (n < 0 || n > k) { flag |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
+            return ((uint32_t)n * words + CHUNK - 1) / CHUNK;
+        };
+        int flag = 0;
+        uint32_t own = 0;
+        for (int g = g0; g < g1; ++g) own += chunks_of(g, flag);
+        uint32_t inc = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) s_wsum[t >> 5] = inc;
+        __syncthreads();
+        if (t < 32) {
+            uint32_t x = t < (nt >> 5) ? s_wsum[t] : 0u, xi = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, xi, o);
+                if (lane >= o) xi += y;
+            }
+            s_wsum[t] = xi - x;                              // exclusive prefix of the warp sums
+            if (t == 31) s_pre[G] = xi;                      // all chunks
+        }
+        __syncthreads();
+        uint32_t run = s_wsum[t >> 5] + inc - own;
+        int unused = 0;
+        for (int g = g0; g < g1; ++g) { s_pre[g] = run; run += chunks_of(g, unused); }
+        if (blockIdx.x == 0) bad |= flag;                   // counts are reported once
+        __syncthreads();
+        total = s_pre[G];
+    }
     for (int64_t ch = warp; ch < total; ch += n_warps) {
-        const int bg = (int)(ch / per_group);
-        const uint32_t c0 = (uint32_t)(ch - (int64_t)bg * per_group) * CHUNK;
+        int bg;
+        uint32_t c0;
+        if (compact) {
+            // the last group whose first chunk is <= ch (groups without chunks share their successor's start)
+            int lo = 0, hi = G - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_pre[mid] <= (uint32_t)ch) lo = mid; else hi = mid - 1;
+            }
+            bg = lo;
+            c0 = ((uint32_t)ch - s_pre[bg]) * CHUNK;
+        } else {
+            bg = (int)(ch / per_group);
+            c0 = (uint32_t)(ch - (int64_t)bg * per_group) * CHUNK;
+        }
         int n = cnt ? cnt[bg] : k;
-        if (n < 0 || n > k) { bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
+        if (n < 0 || n > k) { if (!compact) bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
         const uint32_t lim = (uint32_t)n * words;
         if (c0 >= lim) continue;
         const int C = g_C[bg];
@@ -245,26 +304,36 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
     if (bad) atomicOr(status, bad);
 }
 
+// Largest group count whose chunk prefix the flat gather keeps in shared memory.
+constexpr int FLAT_PREFIX_MAX_G = 16384;
+
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
-                               cudaStream_t s, const int32_t* dslot, int kv_mask) {
+                               cudaStream_t s, const int32_t* dslot, int kv_mask, bool alone) {
     const uint32_t words = (uint32_t)c.B * c.d / 8;
     int lg = -1;
     if ((words & (words - 1)) == 0) { lg = 0; while ((1u << lg) < words) ++lg; }
-    const int ctas = c.gather_ctas > 0 ? c.gather_ctas : 2 * 152;
-    const int th = c.gather_threads;
-    const size_t smem = (size_t)c.gather_reserve_smem;
+    // `alone`: nothing else runs beside this copy, so it takes every SM (one
+    // 1024-thread CTA each, no reservation) to cut the latency of small lists
+    const int ctas = alone ? c.n_sms : (c.gather_ctas > 0 ? c.gather_ctas : 2 * 152);
+    const int th = alone ? 1024 : c.gather_threads;
+    // the chunk prefix needs G + 1 words and must not overflow 32 bits
+    const int U = c.gather_unroll >= 2 ? 2 : 1;
+    const int64_t all_chunks = (int64_t)c.G * (((int64_t)c.k * words + 32 * U - 1) / (32 * U));
+    const bool compact = c.G <= FLAT_PREFIX_MAX_G && all_chunks < (int64_t)1 << 31;
+    const size_t pre = compact ? sizeof(uint32_t) * (c.G + 1) : 0;
+    const size_t smem = std::max(alone ? (size_t)0 : (size_t)c.gather_reserve_smem, pre);
 #define KVO_FLAT(U_, P_)                                                                                          \
     gather_flat_kernel<U_, P_><<<ctas, th, smem, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, idx, cnt, \
                                                       slot_base, dslot, c.buf_k(buf), c.buf_v(buf), c.G, c.k,     \
-                                                      c.B, c.d, lg, kv_mask, c.status)
-    if (lg >= 0) { if (c.gather_unroll >= 2) KVO_FLAT(2, true); else KVO_FLAT(1, true); }
-    else { if (c.gather_unroll >= 2) KVO_FLAT(2, false); else KVO_FLAT(1, false); }
+                                                      c.B, c.d, lg, kv_mask, compact, c.status)
+    if (lg >= 0) { if (U == 2) KVO_FLAT(2, true); else KVO_FLAT(1, true); }
+    else { if (U == 2) KVO_FLAT(2, false); else KVO_FLAT(1, false); }
 #undef KVO_FLAT
     return cudaGetLastError();
 }
 
 cudaError_t prepare_gather_flat() {
-    const int mx = 227 * 1024;
+    const int mx = 227 * 1024 - 32 * (int)sizeof(uint32_t);     // less the warp-sum table
     cudaError_t e = cudaFuncSetAttribute(gather_flat_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gather_flat_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);

@@ -208,7 +208,7 @@ cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs,
 cudaError_t launch_gather_tma(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                               cudaStream_t s);
 cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
-                               cudaStream_t s, const int32_t* dslot = nullptr, int kv_mask = 3);
+                               cudaStream_t s, const int32_t* dslot = nullptr, int kv_mask = 3, bool alone = false);
 cudaError_t launch_lowrank_k(const Ctx& c, int layer, int buf, const int32_t* idx, const int32_t* cnt, int slot_base,
                              const int32_t* dslot, cudaStream_t s);
 cudaError_t prepare_lowrank();

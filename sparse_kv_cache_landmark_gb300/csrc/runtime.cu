@@ -716,6 +716,11 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     int32_t* pred_cur = c.st_pred + (size_t)par * c.L * gk;
     int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
     const bool have = c.have_pred;
+    // Without speculation, and with no prefetch of an earlier step still in
+    // flight, nothing runs beside the urgent copies: they may take every SM, and
+    // attention the whole-device plan.
+    bool alone_step = !q_spec;
+    for (int l = 0; l < c.L; ++l) alone_step = alone_step && !c.res_pending[l];
 
     KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
     for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
@@ -762,8 +767,10 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // without a prediction nothing is spared: in-flight prefetch copies must land first
         if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
+        // a low-rank layer's V copy runs beside the key rebuild
+        const bool alone = alone_step && c.lr_rank[l] == 0;
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent, [&] {
-            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl, urg_mask);
+            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl, urg_mask, alone);
         }));
         if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
             KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_compute, [&] {
@@ -777,7 +784,8 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
             return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
                                          lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
-                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute, true);
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute,
+                                         !alone_step);
         }));
         KVO_CUDA(&c, cudaEventRecord(E.attn[l], c.s_compute));
         // 5. prefetch of the next step's prediction, sparing T
@@ -1025,7 +1033,8 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
-    if (smem_bytes < 0 || smem_bytes > 227 * 1024) return fail(&ctx->c, KVO_ERR_INVALID, "0 <= smem_bytes <= 227 KiB");
+    if (smem_bytes < 0 || smem_bytes > 227 * 1024 - 128)
+        return fail(&ctx->c, KVO_ERR_INVALID, "0 <= smem_bytes <= 232320 (227 KiB less 128 bytes)");
     ctx->c.gather_reserve_smem = smem_bytes;
     return build_tma_plans(ctx->c);   // the step's attention plan depends on the gather's SMs
 }

@@ -7,6 +7,7 @@ import torch
 
 import oracle as orc
 from sparse_kv_cache_landmark_gb300 import synth
+from sparse_kv_cache_landmark_gb300.kvo import KvoError
 from sparse_kv_cache_landmark_gb300.workloads import WORKLOADS, Workload
 from tests.harness import Case, assert_attn_close
 from tests.margins import MARGIN, find_attempts
@@ -147,6 +148,38 @@ def test_gather_engines_bit_exact(case, engine, drivers):
     finally:
         c.ctx.set_gather_engine(3, 0)          # back to the default engine
     bufK, bufV = c.ctx.buffer(0)
+    bufK, bufV = synth.bits(bufK.cpu()), synth.bits(bufV.cpu())
+    for (b, g), ref in refs.items():
+        i = b * w.n_kv_heads + g
+        for kv, buf in (("k", bufK), ("v", bufV)):
+            exp, written = orc.gather_slots(synth.bits(c.rows(0, b, g, kv)), w.block_size,
+                                            ref.runs_prefetch + ref.runs_urgent, 2 * k)
+            assert np.array_equal(buf[i][written], exp[written]), (b, g, kv)
+
+
+def test_flat_gather_reserve_limits(case):
+    """The flat gather's reservation tops out at 227 KiB less its own 128-byte
+    table; the largest one still writes the oracle's bytes."""
+    c, refs = case
+    w = c.w
+    k = w.top_k
+    with pytest.raises(KvoError):
+        c.ctx.set_gather_reserve(227 * 1024 - 127)
+    with pytest.raises(KvoError):
+        c.ctx.set_gather_reserve(-1)
+    T, P = c.ctx.select_topk(0, c.q_dev(0), c.q_dev(0, spec=True))
+    if P is None:
+        P = T.clone()
+    miss, cnt, slot = c.ctx.index_diff(T, P)
+    c.ctx.set_gather_reserve(227 * 1024 - 128)
+    try:
+        c.ctx.gather_coalesced(0, 1, P, None, slot_base=0)
+        c.ctx.gather_coalesced(0, 1, miss, cnt, slot_base=k, urgent=True)
+        torch.cuda.synchronize()
+        assert c.ctx.device_status() == 0
+    finally:
+        c.ctx.set_gather_reserve(200 * 1024)
+    bufK, bufV = c.ctx.buffer(1)
     bufK, bufV = synth.bits(bufK.cpu()), synth.bits(bufV.cpu())
     for (b, g), ref in refs.items():
         i = b * w.n_kv_heads + g

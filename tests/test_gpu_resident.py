@@ -50,7 +50,9 @@ def _attempts(c, steps, drift):
     (True, 1, 1, 64, False, None, 32, False), (True, 3, 32, 8, False, None, 32, False),
     (True, 2, 16, 16, False, 3, 32, False),
     (True, 1, 16, 16, False, None, 0, False),          # no window: attention over the resident blocks alone
-    (True, 2, 32, 12, False, None, 64, True)])         # ragged lengths, k not a multiple of the warp count
+    (True, 2, 32, 12, False, None, 64, True),          # ragged lengths, k not a multiple of the warp count
+    (False, 2, 32, 12, False, None, 64, True),         # no speculation: every SM copies the misses
+    ("alt", 2, 16, 16, False, None, 32, False)])       # speculative and plain steps alternate
 def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged):
     drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
@@ -68,9 +70,10 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged)
         n_urg = n_pref = 0
         churn = []
         for s in range(steps):
+            spec_s = spec is True or (spec == "alt" and s % 2 == 0)
             qq = [synth.gen_queries_step(w, seed, l, s, drift, att[l]) for l in range(L)]
             q = torch.stack([x[0] for x in qq]).cuda().contiguous()
-            qs = torch.stack([x[1] for x in qq]).cuda().contiguous() if spec else None
+            qs = torch.stack([x[1] for x in qq]).cuda().contiguous() if spec_s else None
             if dual:
                 o, lse, o_sp, lse_sp = c.ctx.decode_step_dual(q, qs)
             else:
@@ -85,13 +88,13 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged)
                     for g in range(w.n_kv_heads):
                         i = b * w.n_kv_heads + g
                         qg = synth.bits(qq[l][0][b, g * r:(g + 1) * r])
-                        qsg = synth.bits(qq[l][1][b, g * r:(g + 1) * r]) if spec else None
+                        qsg = synth.bits(qq[l][1][b, g * r:(g + 1) * r]) if spec_s else None
                         ref = orc.decode_group(synth.bits(c.rows(l, b, g, "k")), synth.bits(c.rows(l, b, g, "v")),
                                                qg, qsg, block_size=B, top_k=k, window=W)
                         new, urg, _, pref = orc.resident_step(state[l][i], ref.T.tolist(), p_cur[l][i],
-                                                              ref.P.tolist() if spec else None, budget)
+                                                              ref.P.tolist() if spec_s else None, budget)
                         state[l][i] = new
-                        p_cur[l][i] = ref.P.tolist() if spec else ref.T.tolist()
+                        p_cur[l][i] = ref.P.tolist() if spec_s else ref.T.tolist()
                         n_urg += len(urg)
                         n_pref += len(pref)
                         fetched_step += len(urg) + len(pref)
