@@ -239,8 +239,11 @@ kvo_status kvo_decode_step_dual(kvo_ctx* ctx, const void* q, const void* q_spec,
  * captured once per step parity into a CUDA graph and replayed, which removes
  * the host launch work and shortens the gaps between dependent kernels; a
  * graph is re-captured when the q/o/lse pointers of the call change or a
- * gather tuning call is made.  Profiling (kvo_profile) bypasses the graphs,
- * and so does resident = 1.
+ * gather tuning call is made.  Profiling (kvo_profile) bypasses the graphs.
+ * With resident = 1 only chain steps are replayed: no q_spec, no prefetch of
+ * an earlier step still in flight and no layer with low-rank keys (their
+ * kernels run one after another on the compute stream); other resident steps
+ * are launched stream by stream.
  * 0 (default): every step is launched stream by stream.
  */
 kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable);
@@ -303,9 +306,12 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
  * speculative query) the prediction for the next step becomes resident the
  * same way, sparing the blocks of T, on the low-priority stream.  Without a
  * speculative query only the urgent phase runs (the previous step's T is
- * spared).  CUDA-graph replay is not used in this mode, and its copies
- * always use the flat gather engine (engine 3, with per-entry destination
- * slots) whatever kvo_set_gather_engine chose.
+ * spared); when moreover no prefetch is in flight and no layer has low-rank
+ * keys, the step is one chain on the compute stream: its urgent copies take
+ * every SM and its attention the whole device, and kvo_set_graphs(1) replays
+ * it from a CUDA graph.  The copies of this mode always use the flat gather
+ * engine (engine 3, with per-entry destination slots) whatever
+ * kvo_set_gather_engine chose.
  *   kvo_resident_slots: synchronize, copy layer `layer`'s slot table
  *   [G][2k] int32 to host memory `slots_out`.
  *   kvo_resident_fetched: synchronize, write the blocks fetched since init (or

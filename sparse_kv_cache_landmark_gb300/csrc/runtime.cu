@@ -12,6 +12,8 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
+#include <initializer_list>
 #include <string>
 #include <vector>
 
@@ -705,6 +707,15 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
 // assign of l (it reads T and the slot table), and its attention for the
 // prefetch gather; urgent copies never touch slots of the prediction being
 // prefetched, because the urgent assign spares them.
+// A resident step whose kernels form one chain: no speculative query, no
+// prefetch of an earlier step in flight, no layer with low-rank keys.
+static bool resident_alone(const kvo::Ctx& c, const void* q_spec) {
+    if (q_spec) return false;
+    for (int l = 0; l < c.L; ++l)
+        if (c.res_pending[l] || c.lr_rank[l] > 0) return false;
+    return true;
+}
+
 static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
                                        float* o_spec, float* lse_spec, cudaStream_t s_user) {
     kvo::Ctx& c = ctx->c;
@@ -716,14 +727,20 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     int32_t* pred_cur = c.st_pred + (size_t)par * c.L * gk;
     int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
     const bool have = c.have_pred;
-    // Without speculation, and with no prefetch of an earlier step still in
-    // flight, nothing runs beside the urgent copies: they may take every SM, and
-    // attention the whole-device plan.
-    bool alone_step = !q_spec;
-    for (int l = 0; l < c.L; ++l) alone_step = alone_step && !c.res_pending[l];
+    // Without speculation, with no prefetch of an earlier step still in flight
+    // and no layer rebuilding keys beside its copies, every kernel of the step
+    // depends on the one before: the whole step runs in order on the compute
+    // stream, the urgent copies take every SM and attention the whole-device plan.
+    const bool alone_step = resident_alone(c, q_spec);
+    const cudaStream_t sc = c.s_compute;                          // select, assign, attention
+    const cudaStream_t su = alone_step ? c.s_compute : c.s_urgent;   // urgent copies
 
     KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
+    if (alone_step)
+        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.start, 0));
+    else
+        for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent})
+            KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
     int cur_layer = -1;
     auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
         int e0, e1;
@@ -751,43 +768,44 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         int32_t* dsl = c.res_dslot + l * gk;
         const bool pending = c.res_pending[l] != 0;
         // the previous step's prefetch of this layer has read T and written the slot table
-        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.rassign[l], 0));
+        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rassign[l], 0));
         // 1. retrieval index (true; speculative -> next step's prediction)
-        KVO_CUDA(&c, timed(kvo::PK_SELECT, c.s_compute, [&] {
-            return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, c.s_compute);
+        KVO_CUDA(&c, timed(kvo::PK_SELECT, sc, [&] {
+            return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, sc);
         }));
         // 2. urgent assign: T resident, sparing the prediction fetched for this step
-        KVO_CUDA(&c, timed(kvo::PK_DIFF, c.s_compute, [&] {
+        KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
             return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
-                                               c.s_compute);
+                                               sc);
         }));
-        KVO_CUDA(&c, cudaEventRecord(E.sel[l], c.s_compute));
         // 3. urgent gather of the blocks that were missing
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.sel[l], 0));
+        if (!alone_step) {
+            KVO_CUDA(&c, cudaEventRecord(E.sel[l], sc));
+            KVO_CUDA(&c, cudaStreamWaitEvent(su, E.sel[l], 0));
+        }
         // without a prediction nothing is spared: in-flight prefetch copies must land first
-        if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_urgent, E.rpref[l], 0));
+        if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
-        // a low-rank layer's V copy runs beside the key rebuild
-        const bool alone = alone_step && c.lr_rank[l] == 0;
-        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, c.s_urgent, [&] {
-            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, c.s_urgent, dsl, urg_mask, alone);
+        KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, su, [&] {
+            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask, alone_step);
         }));
         if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
-            KVO_CUDA(&c, timed(kvo::PK_RECON, c.s_compute, [&] {
-                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, c.s_compute);
+            KVO_CUDA(&c, timed(kvo::PK_RECON, sc, [&] {
+                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, sc);
             }));
-        KVO_CUDA(&c, cudaEventRecord(E.urg[l], c.s_urgent));
         // 4. attention over the resident set once the urgent and prefetched blocks have landed
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.urg[l], 0));
-        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.rpref[l], 0));
+        if (!alone_step) {
+            KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
+            KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.urg[l], 0));
+        }
+        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rpref[l], 0));
         c.res_pending[l] = 0;
-        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, c.s_compute, [&] {
+        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
             return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
                                          lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
-                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, c.s_compute,
-                                         !alone_step);
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, sc, !alone_step);
         }));
-        KVO_CUDA(&c, cudaEventRecord(E.attn[l], c.s_compute));
+        if (!alone_step) KVO_CUDA(&c, cudaEventRecord(E.attn[l], sc));
         // 5. prefetch of the next step's prediction, sparing T
         if (q_spec) {
             int32_t* pids = c.res_pf_ids + l * gk;
@@ -807,6 +825,7 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     }
     // the caller's stream waits for the outputs; prefetches stay in flight
     for (cudaStream_t s : {c.s_compute, c.s_urgent}) {
+        if (alone_step && s != c.s_compute) continue;
         KVO_CUDA(&c, cudaEventRecord(E.start, s));
         KVO_CUDA(&c, cudaStreamWaitEvent(s_user, E.start, 0));
     }
@@ -818,39 +837,61 @@ static void drop_graphs(kvo::Ctx& c) {
         if (g) { cudaGraphExecDestroy(g); g = nullptr; }
 }
 
+// Replay the step graph of this step's parity, capturing it first when it is
+// missing or was captured for other buffers.  The replay waits for the
+// caller's stream and for `after` (work of earlier stream-launched steps it
+// must follow); the compute stream and the caller's stream wait for it.
+static kvo_status graph_step(kvo::Ctx& c, std::initializer_list<const void*> key_list, cudaStream_t s_user,
+                             cudaStream_t after, const std::function<kvo_status()>& body) {
+    const int par = c.step_parity;
+    const void* key[6];
+    int n = 0;
+    for (const void* p : key_list) key[n++] = p;
+    bool same = c.gexec[par] != nullptr;
+    for (int i = 0; i < 6 && same; ++i) same = c.gkey[par][i] == key[i];
+    if (!same) {
+        if (c.gexec[par]) { cudaGraphExecDestroy(c.gexec[par]); c.gexec[par] = nullptr; }
+        KVO_CUDA(&c, cudaStreamBeginCapture(c.s_graph, cudaStreamCaptureModeThreadLocal));
+        kvo_status st = body();
+        cudaGraph_t g = nullptr;
+        cudaError_t e = cudaStreamEndCapture(c.s_graph, &g);
+        if (st != KVO_OK) { if (g) cudaGraphDestroy(g); return st; }
+        if (e != cudaSuccess) return cuda_fail(&c, e, "cudaStreamEndCapture(decode step)");
+        e = cudaGraphInstantiate(&c.gexec[par], g, 0);
+        cudaGraphDestroy(g);
+        if (e != cudaSuccess) { c.gexec[par] = nullptr; return cuda_fail(&c, e, "cudaGraphInstantiate(decode step)"); }
+        for (int i = 0; i < 6; ++i) c.gkey[par][i] = key[i];
+    }
+    KVO_CUDA(&c, cudaEventRecord(c.ev_gin, s_user));
+    KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
+    KVO_CUDA(&c, cudaEventRecord(c.ev_gin, after));
+    KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
+    KVO_CUDA(&c, cudaGraphLaunch(c.gexec[par], c.s_graph));
+    KVO_CUDA(&c, cudaEventRecord(c.ev_gout, c.s_graph));
+    KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_gout, 0));
+    KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, c.ev_gout, 0));
+    return KVO_OK;
+}
+
 static kvo_status decode_step_impl(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
                                    float* o_spec, float* lse_spec, kvo_stream_t stream) {
     kvo::Ctx& c = ctx->c;
     cudaStream_t s_user = pick(c, stream);
-    if (c.resident) {
+    if (c.resident && c.use_graphs && c.have_pred && !c.prof_on && resident_alone(c, q_spec)) {
+        // a chain step: replayed from the graph of its parity
+        kvo_status st = graph_step(c, {q, q_spec, o, lse, o_spec, lse_spec}, s_user, c.s_compute, [&] {
+            return decode_step_resident(ctx, q, q_spec, o, lse, o_spec, lse_spec, c.s_graph);
+        });
+        if (st != KVO_OK) return st;
+    } else if (c.resident) {
         kvo_status st = decode_step_resident(ctx, q, q_spec, o, lse, o_spec, lse_spec, s_user);
         if (st != KVO_OK) return st;
     } else if (c.use_graphs && c.have_pred && !c.prof_on) {
-        const int par = c.step_parity;
-        const void* key[6] = {q, q_spec, o, lse, o_spec, lse_spec};
-        bool same = c.gexec[par] != nullptr;
-        for (int i = 0; i < 6 && same; ++i) same = c.gkey[par][i] == key[i];
-        if (!same) {
-            if (c.gexec[par]) { cudaGraphExecDestroy(c.gexec[par]); c.gexec[par] = nullptr; }
-            KVO_CUDA(&c, cudaStreamBeginCapture(c.s_graph, cudaStreamCaptureModeThreadLocal));
-            kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, c.s_graph, true);
-            cudaGraph_t g = nullptr;
-            cudaError_t e = cudaStreamEndCapture(c.s_graph, &g);
-            if (st != KVO_OK) { if (g) cudaGraphDestroy(g); return st; }
-            if (e != cudaSuccess) return cuda_fail(&c, e, "cudaStreamEndCapture(decode step)");
-            e = cudaGraphInstantiate(&c.gexec[par], g, 0);
-            cudaGraphDestroy(g);
-            if (e != cudaSuccess) { c.gexec[par] = nullptr; return cuda_fail(&c, e, "cudaGraphInstantiate(decode step)"); }
-            for (int i = 0; i < 6; ++i) c.gkey[par][i] = key[i];
-        }
-        KVO_CUDA(&c, cudaEventRecord(c.ev_gin, s_user));
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
         // prefetches an earlier stream-launched step left in flight finish first
-        KVO_CUDA(&c, cudaEventRecord(c.ev_gin, c.s_prefetch));
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_graph, c.ev_gin, 0));
-        KVO_CUDA(&c, cudaGraphLaunch(c.gexec[par], c.s_graph));
-        KVO_CUDA(&c, cudaEventRecord(c.ev_gout, c.s_graph));
-        KVO_CUDA(&c, cudaStreamWaitEvent(s_user, c.ev_gout, 0));
+        kvo_status st = graph_step(c, {q, q_spec, o, lse, o_spec, lse_spec}, s_user, c.s_prefetch, [&] {
+            return decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, c.s_graph, true);
+        });
+        if (st != KVO_OK) return st;
     } else {
         kvo_status st = decode_step_body(ctx, q, q_spec, o, lse, o_spec, lse_spec, s_user, false);
         if (st != KVO_OK) return st;

@@ -45,15 +45,17 @@ def _attempts(c, steps, drift):
     return out
 
 
-@pytest.mark.parametrize("spec,L,B,k,dual,budget,W,ragged", [
-    (True, 2, 16, 16, True, None, 32, False), (False, 1, 16, 16, False, None, 32, False),
-    (True, 1, 1, 64, False, None, 32, False), (True, 3, 32, 8, False, None, 32, False),
-    (True, 2, 16, 16, False, 3, 32, False),
-    (True, 1, 16, 16, False, None, 0, False),          # no window: attention over the resident blocks alone
-    (True, 2, 32, 12, False, None, 64, True),          # ragged lengths, k not a multiple of the warp count
-    (False, 2, 32, 12, False, None, 64, True),         # no speculation: every SM copies the misses
-    ("alt", 2, 16, 16, False, None, 32, False)])       # speculative and plain steps alternate
-def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged):
+@pytest.mark.parametrize("spec,L,B,k,dual,budget,W,ragged,graphs", [
+    (True, 2, 16, 16, True, None, 32, False, False), (False, 1, 16, 16, False, None, 32, False, False),
+    (True, 1, 1, 64, False, None, 32, False, False), (True, 3, 32, 8, False, None, 32, False, False),
+    (True, 2, 16, 16, False, 3, 32, False, False),
+    (True, 1, 16, 16, False, None, 0, False, False),   # no window: attention over the resident blocks alone
+    (True, 2, 32, 12, False, None, 64, True, False),   # ragged lengths, k not a multiple of the warp count
+    (False, 2, 32, 12, False, None, 64, True, False),  # no speculation: one chain, every SM copies the misses
+    (False, 2, 32, 12, False, None, 64, True, True),   # ... replayed from CUDA graphs
+    ("alt", 2, 16, 16, False, None, 32, False, False),  # speculative and plain steps alternate
+    ("s3", 2, 16, 16, False, None, 32, False, True)])  # graph replays, one speculative step, replays again
+def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged, graphs):
     drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
     ctx = (n, n + 40 * B) if ragged else (n, n)
@@ -64,17 +66,28 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged)
         att = _attempts(c, steps, drift)
         if budget is not None:
             c.ctx.set_prefetch_budget(budget)     # admission cap on speculative fetches
+        if graphs:
+            c.ctx.set_graphs(True)
         G, r = w.batch * w.n_kv_heads, w.group_size
         state = [[[-1] * (2 * k) for _ in range(G)] for _ in range(L)]
         p_cur = [[None] * G for _ in range(L)]
         n_urg = n_pref = 0
         churn = []
         for s in range(steps):
-            spec_s = spec is True or (spec == "alt" and s % 2 == 0)
+            spec_s = spec is True or (spec == "alt" and s % 2 == 0) or (spec == "s3" and s == 3)
             qq = [synth.gen_queries_step(w, seed, l, s, drift, att[l]) for l in range(L)]
             q = torch.stack([x[0] for x in qq]).cuda().contiguous()
             qs = torch.stack([x[1] for x in qq]).cuda().contiguous() if spec_s else None
-            if dual:
+            if graphs:
+                # the same q, o and lse buffers every step, so warm chain steps replay one graph per parity
+                if s == 0:
+                    q_buf = torch.empty_like(q)
+                    o_buf = torch.empty(L, w.batch * w.n_q_heads, w.head_dim, dtype=torch.float32, device="cuda")
+                    lse_buf = torch.empty(L, w.batch * w.n_q_heads, dtype=torch.float32, device="cuda")
+                q_buf.copy_(q)
+                o_buf.fill_(float("nan"))
+                o, lse = c.ctx.decode_step(q_buf, qs, o_buf, lse_buf)
+            elif dual:
                 o, lse, o_sp, lse_sp = c.ctx.decode_step_dual(q, qs)
             else:
                 o, lse = c.ctx.decode_step(q, qs)
