@@ -557,10 +557,13 @@ __device__ __forceinline__ int4 item_hdr(const int4* s_items, const int4* __rest
 // prefetching caller does not wait for the window length here.
 __device__ __forceinline__ void cursor_fields(AttnCursor& c, int4 it, int k, int B, int W,
                                               const int32_t* __restrict__ w_start,
-                                              const int32_t* __restrict__ w_len) {
+                                              const int32_t* __restrict__ w_len,
+                                              const int32_t* __restrict__ sp_cnt) {
     c.bg = it.x; c.part = it.y; c.tile0 = it.z; c.ntiles = it.w;
     c.ws = (c.part == 1 && w_start) ? __ldg(w_start + c.bg) : 0;
-    c.n_tok = c.part == 0 ? k * B : (w_len ? __ldg(w_len + c.bg) : W);
+    // sparse part: k blocks, or the first sp_cnt[g] entries of the slot list when given
+    c.n_tok = c.part == 0 ? (sp_cnt ? min(k, max(0, __ldg(sp_cnt + c.bg))) : k) * B
+                          : (w_len ? __ldg(w_len + c.bg) : W);
 }
 // tiles of the item that hold tokens (a window may be shorter than its items cover)
 __device__ __forceinline__ void cursor_nt(AttnCursor& c) {
@@ -573,8 +576,9 @@ struct ItemSrc {
     int lo, k, B, W;
     const int32_t* w_start;
     const int32_t* w_len;
+    const int32_t* sp_cnt;
     __device__ __forceinline__ void load(AttnCursor& c) const {
-        cursor_fields(c, item_hdr(s_items, items, lo, c.item), k, B, W, w_start, w_len);
+        cursor_fields(c, item_hdr(s_items, items, lo, c.item), k, B, W, w_start, w_len, sp_cnt);
         cursor_nt(c);
     }
 };
@@ -656,7 +660,8 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
                 uint32_t* __restrict__ done, float* __restrict__ out_o, float* __restrict__ out_lse,
                 float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec, int fuse, int batch, int r,
                 int Hkv, int k, int B, int W, int Wcap, const int32_t* __restrict__ w_start,
-                const int32_t* __restrict__ w_len, float scale_log2, int32_t* __restrict__ status) {
+                const int32_t* __restrict__ w_len, const int32_t* __restrict__ sp_cnt, int dep_wait,
+                float scale_log2, int32_t* __restrict__ status) {
     using WA = WarpAttn<D, NR>;
     using CF = AttnTmaCfg<D, NR>;
     constexpr int CH = WA::CH, CPT = WA::CPT, STG = CF::STG;
@@ -681,7 +686,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
 
     const int Hq = Hkv * r;
     const int nrows = q_spec ? 2 * r : r;
-    const ItemSrc src{s_items, items, lo, k, B, W, w_start, w_len};
+    const ItemSrc src{s_items, items, lo, k, B, W, w_start, w_len, sp_cnt};
     unsigned char* ring = smem + warp * STG * CF::STAGE_BYTES;
     uint64_t* wfull = full + warp * STG;
     int bad = 0;
@@ -708,7 +713,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     uint4 nq0[CH], nq1[CH];
     auto fetch = [&](int item) {
         nc.item = item; nc.hi = hi; nc.tl = warp;
-        cursor_fields(nc, item_hdr(s_items, items, lo, item), k, B, W, w_start, w_len);
+        cursor_fields(nc, item_hdr(s_items, items, lo, item), k, B, W, w_start, w_len, sp_cnt);
         const int b = nc.bg / Hkv, gk = nc.bg % Hkv;
         auto qrow = [&](int rr) -> const uint16_t* {
             return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
@@ -759,6 +764,9 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
                              out_lse, out_o_spec, out_lse_spec, fuse, batch, r, Hkv, cc.bg, nrows, item, NTHR);
     }
     if (bad) atomicOr(status, bad);
+    // launched as a programmatic dependent: this grid completes only after the
+    // grid it depends on, so the launches behind it see that grid's writes
+    if (dep_wait && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, int NR>
@@ -787,31 +795,230 @@ cudaError_t prepare_attention(Ctx& c) {
     return cudaSuccess;
 }
 
+template <int D, int NR>
+static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, const void* q, const void* q_spec,
+                              const uint16_t* wk, const uint16_t* wv, const int32_t* slot, float* o, float* lse,
+                              float* o_spec, float* lse_spec, int fuse, cudaStream_t s, const int32_t* sp_cnt,
+                              bool win, bool pdl, float scale_log2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(ATT_WARPS * 32);
+    cfg.dynamicSmemBytes = AttnTmaCfg<D, NR>::BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_tma_kernel<D, NR>, (const uint16_t*)q, (const uint16_t*)q_spec,
+                              (const uint16_t*)c.buf_k(buf), (const uint16_t*)c.buf_v(buf), wk, wv, slot,
+                              (const int4*)pl.items, (const int32_t*)pl.cta, (const int32_t*)pl.first,
+                              (const int32_t*)pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec,
+                              lse_spec, fuse, c.batch, c.r, c.Hkv, c.k, c.B, win ? c.W : 0, c.Wcap,
+                              (const int32_t*)c.g_wstart, win ? (const int32_t*)c.g_wlen : (const int32_t*)nullptr,
+                              sp_cnt, pdl ? 1 : 0, scale_log2, c.status);
+}
+
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step) {
+                             bool in_step, const int32_t* sp_cnt, bool win, bool pdl) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
     const int nrows = q_spec ? 2 * c.r : c.r;
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
+    if (c.att_impl == 1) {
+#define KVO_TMA(D_, NR_) \
+        launch_tma<D_, NR_>(c, pl, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, fuse, s, sp_cnt, win, pdl, \
+                            scale_log2)
+        if (c.d == 128) return nrows <= 8 ? KVO_TMA(128, 1) : KVO_TMA(128, 2);
+        return nrows <= 8 ? KVO_TMA(64, 1) : KVO_TMA(64, 2);
+#undef KVO_TMA
+    }
+    // partial slot lists, window-less passes and dependent launches exist in the TMA-staged kernel only
+    if (sp_cnt || !win || pdl) return cudaErrorInvalidValue;
 #define KVO_ATT(D_, NR_)                                                                                         \
-    if (c.att_impl == 1)                                                                                        \
-        attn_tma_kernel<D_, NR_><<<pl.grid, ATT_WARPS * 32, AttnTmaCfg<D_, NR_>::BYTES, s>>>(                   \
-            (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, pl.items,      \
-            pl.cta, pl.first, pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec,     \
-            fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status);      \
-    else                                                                                                        \
-        attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                           \
-            (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, c.att_items,   \
-            c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,  \
-            c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
+    attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
+        (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, c.att_items,       \
+        c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,      \
+        c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
     if (c.d == 128) {
         if (nrows <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);
     } else {
         if (nrows <= 8) KVO_ATT(64, 1); else KVO_ATT(64, 2);
     }
 #undef KVO_ATT
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------- attention over a few more blocks
+// Attention of each group's r query rows over the first cnt[g] entries of a
+// slot list, merged by log-sum-exp with a prior part (prior_o, prior_lse: the
+// attention over the group's other keys) into out_o / out_lse.  A decode step
+// whose blocks were resident but for a few fetched ones attends to the
+// resident ones beside the fetch and to the fetched ones here, after it.
+// Grid (G, S): the S CTAs of a group take its tiles round-robin (CTA s, warp
+// w: tiles 4s + w, 4s + w + 4S, ...; register-direct, each warp's next tile
+// pulled into L2 while it computes the current one), so a group with many
+// fetched blocks still spreads over 4S warps.  With S > 1 each CTA leaves an
+// unnormalised partial and the last one to finish (atomic ticket) merges them.
+template <int D, int NR>
+__global__ void __launch_bounds__(ATT_WARPS * 32)
+attn_merge_part_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ bk,
+                       const uint16_t* __restrict__ bv, const int32_t* __restrict__ slot,
+                       const int32_t* __restrict__ cnt, const float* __restrict__ prior_o,
+                       const float* __restrict__ prior_lse, float* __restrict__ out_o, float* __restrict__ out_lse,
+                       float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* __restrict__ done, int r,
+                       int Hkv, int k, int B, float scale_log2, int32_t* __restrict__ status) {
+    using WA = WarpAttn<D, NR>;
+    constexpr int CH = WA::CH, CPT = WA::CPT;
+    __shared__ float sm_m[ATT_WARPS][16];
+    __shared__ float sm_l[ATT_WARPS][16];
+    __shared__ __align__(16) float sm_o[ATT_WARPS * 8 * NR * D];
+    __shared__ int s_last;
+    const int bg = blockIdx.x, S = gridDim.y, sl_i = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int b = bg / Hkv, gk = bg % Hkv, Hq = Hkv * r;
+    int bad = 0;
+    int n = cnt[bg];
+    if (n < 0 || n > k) { bad |= KVO_DEV_BAD_COUNT; n = n < 0 ? 0 : k; }
+    const int n_tok = n * B;
+    const int64_t row0 = (int64_t)b * Hq + gk * r;      // the group's first output row
+    WA st;
+    {
+        const bool v0 = gq < r, v1 = NR == 2 && gq + 8 < r;
+        st.init(q + (row0 + (v0 ? gq : 0)) * D, q + (row0 + (v1 ? gq + 8 : 0)) * D, v0, v1, tq);
+    }
+    auto row_ptr = [&](const uint16_t* base, int tok) -> const uint16_t* {
+        const int blk = tok / B;
+        int sl = slot[(int64_t)bg * k + blk];
+        if (sl < 0 || sl >= 2 * k) { bad |= KVO_DEV_BAD_SLOT; sl = 0; }
+        return base + (((int64_t)bg * 2 * k + sl) * B + (tok - blk * B)) * D;
+    };
+    const int stride = S * ATT_WARPS * ATT_TILE;
+    for (int tb = (sl_i * ATT_WARPS + warp) * ATT_TILE; tb < n_tok; tb += stride) {
+        if (tb + stride < n_tok) {
+            // lane l: token l & 15 of the warp's next tile, K rows for l < 16, V rows otherwise
+            const int ntok = min(tb + stride + (lane & 15), n_tok - 1);
+            const char* p = (const char*)row_ptr(lane < 16 ? bk : bv, ntok);
+#pragma unroll
+            for (int off = 0; off < D * 2; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+        }
+        uint4 kf[2][CH];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint16_t* kp = row_ptr(bk, min(tb + 8 * nt + gq, n_tok - 1)) + 8 * tq;
+#pragma unroll
+            for (int s2 = 0; s2 < CH; ++s2) kf[nt][s2] = ldg16(kp + 32 * s2);
+        }
+        uint4 vf[4][CPT / 8];
+#pragma unroll
+        for (int vi = 0; vi < 4; ++vi) {
+            const uint16_t* vp = row_ptr(bv, min(tb + 2 * tq + (vi & 1) + 8 * (vi >> 1), n_tok - 1)) + CPT * gq;
+#pragma unroll
+            for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = ldg16(vp + 8 * c);
+        }
+        st.tile(kf, vf, tb, n_tok, scale_log2, tq);
+    }
+    if (bad && lane == 0) atomicOr(status, bad);
+    st.to_smem(sm_m, sm_l, sm_o + warp * 8 * NR * D, warp, gq, tq);
+    __syncthreads();
+    // this CTA's part: unnormalised sum a and mass l relative to its maximum M (log2 domain)
+    auto cta_part = [&](int row, int c, float& M, float& a, float& l) {
+        M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w) M = fmaxf(M, sm_m[w][row]);
+        a = 0.f; l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < ATT_WARPS; ++w) {
+                const float sc = ex2f(sm_m[w][row] - M);
+                a += sc * sm_o[(w * 8 * NR + row) * D + c];
+                l += sc * sm_l[w][row];
+            }
+        }
+    };
+    if (S > 1) {
+        const int64_t pbase = ((int64_t)bg * S + sl_i) * r;
+        for (int e = tid; e < r * D; e += ATT_WARPS * 32) {
+            const int row = e / D, c = e - row * D;
+            float M, a, l;
+            cta_part(row, c, M, a, l);
+            part_o[(pbase + row) * D + c] = a;
+            if (c == 0) { part_ml[(pbase + row) * 2] = M; part_ml[(pbase + row) * 2 + 1] = l; }
+        }
+        // the same release / acquire ticket as the attention epilogue
+        __syncthreads();
+        if (tid == 0) {
+            fence_acq_rel_gpu();
+            const bool last = atomicAdd(&done[bg], 1u) + 1 == (uint32_t)S;
+            if (last) fence_acq_rel_gpu();
+            s_last = last;
+        }
+        __syncthreads();
+        if (!s_last) return;
+    }
+    constexpr float kLog2e = 1.4426950408889634f;
+    for (int e = tid; e < r * D; e += ATT_WARPS * 32) {
+        const int row = e / D, c = e - row * D;
+        float M, a, l;
+        if (S == 1) {
+            cta_part(row, c, M, a, l);
+        } else {
+            M = -INFINITY; a = 0.f; l = 0.f;
+            for (int j = 0; j < S; ++j) {
+                const int64_t pr = ((int64_t)bg * S + j) * r + row;
+                const float mj = __ldcg(part_ml + pr * 2);
+                if (mj == -INFINITY) continue;
+                const float Mn = fmaxf(M, mj);
+                const float so = ex2f(M - Mn), sn = ex2f(mj - Mn);
+                l = l * so + __ldcg(part_ml + pr * 2 + 1) * sn;
+                a = a * so + __ldcg(part_o + pr * D + c) * sn;
+                M = Mn;
+            }
+        }
+        // the prior part: normalised output and lse (natural log) -> mass 2^(lse*log2e - Mx)
+        const int64_t orow = row0 + row;
+        const float pl = prior_lse[orow] * kLog2e;
+        const float Mx = fmaxf(pl, M);
+        float o = 0.f, lse = -INFINITY;
+        if (Mx != -INFINITY) {
+            const float wp = pl == -INFINITY ? 0.f : ex2f(pl - Mx);
+            const float wn = M == -INFINITY ? 0.f : ex2f(M - Mx);
+            const float L = wp + wn * l;
+            o = (wp * prior_o[orow * D + c] + wn * a) / L;
+            lse = (Mx + lg2f(L)) * kLn2;
+        }
+        out_o[orow * D + c] = o;
+        if (c == 0) out_lse[orow] = lse;
+    }
+    if (S > 1 && tid == 0) done[bg] = 0u;
+}
+
+// CTAs per group of attn_merge_part_kernel: enough for about four per SM, 1..MP_SPLIT_MAX
+int merge_part_split(const Ctx& c) {
+    return std::max(1, std::min(MP_SPLIT_MAX, (4 * std::max(1, c.n_sms)) / std::max(1, c.G)));
+}
+
+cudaError_t launch_attn_merge_part(const Ctx& c, int buf, const void* q, const int32_t* slot, const int32_t* cnt,
+                                   const float* prior_o, const float* prior_lse, float* o, float* lse,
+                                   cudaStream_t s) {
+    const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
+    const int S = merge_part_split(c);
+    if (S > 1 && (!c.mp_part_o || !c.mp_part_ml || !c.mp_done)) return cudaErrorInvalidValue;
+    const dim3 grid(c.G, S);
+#define KVO_MP(D_, NR_)                                                                                          \
+    attn_merge_part_kernel<D_, NR_><<<grid, ATT_WARPS * 32, 0, s>>>((const uint16_t*)q, c.buf_k(buf), c.buf_v(buf), \
+                                                                   slot, cnt, prior_o, prior_lse, o, lse,       \
+                                                                   c.mp_part_o, c.mp_part_ml, c.mp_done, c.r,   \
+                                                                   c.Hkv, c.k, c.B, scale_log2, c.status)
+    if (c.d == 128) {
+        if (c.r <= 8) KVO_MP(128, 1); else KVO_MP(128, 2);
+    } else {
+        if (c.r <= 8) KVO_MP(64, 1); else KVO_MP(64, 2);
+    }
+#undef KVO_MP
     return cudaGetLastError();
 }
 

@@ -198,6 +198,10 @@ gather_flat_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__
                    const int32_t* __restrict__ dslot,
                    uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int G, int k, int B, int D, int words_log2,
                    int kv_mask, bool compact, int32_t* __restrict__ status) {
+    // a kernel launched as this one's programmatic dependent may start as soon
+    // as every CTA of this grid is resident (it waits for this grid's
+    // completion before it reads what this grid writes)
+    asm volatile("griddepcontrol.launch_dependents;");
     constexpr uint32_t CHUNK = 32 * U;                       // words per warp iteration
     extern __shared__ uint32_t s_pre[];                      // [G + 1] chunk prefix (compact)
     __shared__ uint32_t s_wsum[32];

@@ -66,6 +66,16 @@ struct Ctx {
     unsigned long long* res_fetched = nullptr;   // [2] blocks fetched: urgent, prefetch
     std::vector<char> res_pending;  // [L] a prefetch into the layer's set was issued and not yet waited for
     int res_budget = -1;            // prefetch fetches admitted per group, layer and step (-1: all)
+    // chain steps: attention over the blocks resident already (and the window)
+    // beside the urgent copies, then over the fetched ones, merged by lse
+    int32_t* res_hit_slot = nullptr;  // [G][k] slots of the hits, in index order
+    int32_t* res_hit_cnt = nullptr;   // [G]
+    float* res_oA = nullptr;          // [rows][d], [rows]: hits + window
+    float* res_lA = nullptr;
+    // partials of the fetched-block attention when a group spans several CTAs
+    float* mp_part_o = nullptr;       // [G][S][r][d]
+    float* mp_part_ml = nullptr;      // [G][S][r][2]
+    uint32_t* mp_done = nullptr;      // [G] tickets (zero between launches)
     // Low-rank keys per layer (caller-owned device factors; rank 0: not set)
     std::vector<const uint16_t*> lr_coef, lr_basis;
     std::vector<int> lr_rank;
@@ -214,11 +224,25 @@ cudaError_t launch_lowrank_k(const Ctx& c, int layer, int buf, const int32_t* id
 cudaError_t prepare_lowrank();
 cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
                                    int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
-                                   int phase, cudaStream_t s, int max_fetch = -1);
+                                   int phase, cudaStream_t s, int max_fetch = -1, int32_t* hit_slot = nullptr,
+                                   int32_t* hit_cnt = nullptr);
 cudaError_t prepare_resident(const Ctx& c);
+// Optional for the TMA-staged kernel only: sp_cnt[g] limits the sparse part to
+// the first sp_cnt[g] entries of the slot list; win = false drops the window
+// part; pdl launches it as a programmatic dependent of the kernel before it on
+// the stream (it starts once that kernel's CTAs are all resident, and ends only
+// after that kernel has completed).
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step = false);
+                             bool in_step = false, const int32_t* sp_cnt = nullptr, bool win = true,
+                             bool pdl = false);
+// Attention over the first cnt[g] entries of a slot list, merged by lse with a
+// prior part into (o, lse); merge_part_split(c) CTAs per group.
+constexpr int MP_SPLIT_MAX = 8;
+int merge_part_split(const Ctx& c);
+cudaError_t launch_attn_merge_part(const Ctx& c, int buf, const void* q, const int32_t* slot, const int32_t* cnt,
+                                   const float* prior_o, const float* prior_lse, float* o, float* lse,
+                                   cudaStream_t s);
 cudaError_t launch_merge_lse(const float* o1, const float* lse1, const float* o2, const float* lse2, float* o,
                              float* lse, int rows, int d, cudaStream_t s);
 cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStream_t s);

@@ -31,7 +31,9 @@ __device__ __forceinline__ bool sorted_contains(const int32_t* a, int n, int32_t
 
 // One CTA per group.  map [G][Ccap] and slots [G][cap] are this layer's tables.
 // Outputs: the fetched blocks (ascending ids) with their destination slots and
-// count, and (optional) the slot of every need entry after the update.
+// count, (optional) the slot of every need entry after the update, and
+// (optional) the slots of the need entries that were resident already, in need
+// order, with their count (the blocks attention may read before the fetch).
 // max_fetch >= 0 admits only the max_fetch missing blocks with the lowest ids
 // (a cap on host bytes, used for the prefetch phase only; "PulseInfer and the
 // I/O Problem Behind Long-Context Decoding", §2: I/O-adaptive offloading
@@ -40,8 +42,9 @@ __global__ void __launch_bounds__(RES_THREADS)
 resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restrict__ keep,
                        int32_t* __restrict__ map, int32_t* __restrict__ slots, const int32_t* __restrict__ g_C,
                        int32_t* __restrict__ out_ids, int32_t* __restrict__ out_cnt, int32_t* __restrict__ out_dslot,
-                       int32_t* __restrict__ slot_of, unsigned long long* __restrict__ fetched, int k, int cap,
-                       int Ccap, int max_fetch, int32_t* __restrict__ status) {
+                       int32_t* __restrict__ slot_of, int32_t* __restrict__ hit_slot, int32_t* __restrict__ hit_cnt,
+                       unsigned long long* __restrict__ fetched, int k, int cap, int Ccap, int max_fetch,
+                       int32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t rs[];
     int32_t* s_need = rs;                  // [k]
     int32_t* s_keep = s_need + k;          // [k]
@@ -91,6 +94,19 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
         const int32_t x = s_need[i];
         if (x >= 0 && x < C && mg[x] < 0) s_mid[base++] = x;
     }
+    if (hit_slot) {   // entries resident before the update keep their slots through it
+        uint32_t nh = 0;
+        for (int i = i0; i < i1; ++i) {
+            const int32_t x = s_need[i];
+            nh += (x >= 0 && x < C && mg[x] >= 0) ? 1u : 0u;
+        }
+        uint32_t hb = block_exclusive_scan(nh, warp_sums, &s_tot);
+        for (int i = i0; i < i1; ++i) {
+            const int32_t x = s_need[i];
+            if (x >= 0 && x < C && mg[x] >= 0) hit_slot[(int64_t)g * k + hb++] = mg[x];
+        }
+        if (tid == 0) hit_cnt[g] = (int32_t)s_tot;
+    }
     __syncthreads();
     // admission: at most max_fetch fetches (lowest ids first) when max_fetch >= 0
     const uint32_t wanted = max_fetch >= 0 ? min(n_miss, (uint32_t)max_fetch) : n_miss;
@@ -136,11 +152,12 @@ cudaError_t prepare_resident(const Ctx& c) {
 // phase 0: urgent (counts into res_fetched[0]), 1: prefetch (res_fetched[1])
 cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
                                    int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
-                                   int phase, cudaStream_t s, int max_fetch) {
+                                   int phase, cudaStream_t s, int max_fetch, int32_t* hit_slot, int32_t* hit_cnt) {
     const int cap = 2 * c.k;
     resident_assign_kernel<<<c.G, RES_THREADS, res_smem(c), s>>>(
         need, keep, c.res_map + (size_t)layer * c.G * c.Cmax, c.res_slots + (size_t)layer * c.G * cap, c.g_C,
-        out_ids, out_cnt, out_dslot, slot_of, c.res_fetched + phase, c.k, cap, c.Cmax, max_fetch, c.status);
+        out_ids, out_cnt, out_dslot, slot_of, hit_slot, hit_cnt, c.res_fetched + phase, c.k, cap, c.Cmax, max_fetch,
+        c.status);
     return cudaGetLastError();
 }
 

@@ -166,7 +166,7 @@ void free_ctx(kvo::Ctx& c) {
     for (void* p : c.res_k) F(p);
     for (void* p : c.res_v) F(p);
     F(c.res_map); F(c.res_slots); F(c.res_dslot); F(c.res_pf_ids); F(c.res_pf_cnt); F(c.res_pf_dslot);
-    F(c.res_fetched);
+    F(c.res_fetched); F(c.res_hit_slot); F(c.res_hit_cnt); F(c.res_oA); F(c.res_lA); F(c.mp_part_o); F(c.mp_part_ml); F(c.mp_done);
     F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
     F(c.runs); F(c.nruns);
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
@@ -354,6 +354,11 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, dalloc(&c.res_pf_cnt, sizeof(int32_t) * lg, &sb));
         KVO_CUDA(&c, dalloc(&c.res_pf_dslot, sizeof(int32_t) * lg * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_fetched, sizeof(unsigned long long) * 2, &sb));
+        const size_t rows = (size_t)c.batch * c.Hq;
+        KVO_CUDA(&c, dalloc(&c.res_hit_slot, sizeof(int32_t) * c.G * c.k, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_hit_cnt, sizeof(int32_t) * c.G, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * rows * c.d, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * rows, &sb));
         KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
         c.res_pending.assign(c.L, 0);
         KVO_CUDA(&c, kvo::prepare_resident(c));
@@ -411,6 +416,13 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * c.G, &sb));
     KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
     KVO_CUDA(&c, kvo::prepare_attention(c));
+    if (c.resident) {   // partials of the fetched-block attention of chain steps
+        const size_t parts = (size_t)c.G * kvo::merge_part_split(c) * c.r;
+        KVO_CUDA(&c, dalloc(&c.mp_part_o, sizeof(float) * parts * c.d, &sb));
+        KVO_CUDA(&c, dalloc(&c.mp_part_ml, sizeof(float) * parts * 2, &sb));
+        KVO_CUDA(&c, dalloc(&c.mp_done, sizeof(uint32_t) * c.G, &sb));
+        KVO_CUDA(&c, cudaMemsetAsync(c.mp_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
+    }
     KVO_CUDA(&c, kvo::prepare_lowrank());
     c.lr_coef.assign(c.L, nullptr);
     c.lr_basis.assign(c.L, nullptr);
@@ -773,10 +785,16 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         KVO_CUDA(&c, timed(kvo::PK_SELECT, sc, [&] {
             return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, sc);
         }));
+        // A chain step splits attention: the blocks resident already and the window
+        // are attended beside the urgent copies (a programmatic dependent launch,
+        // dispatched once the copy's SM-exclusive CTAs are all resident), the
+        // fetched blocks after them, and the two results merge by log-sum-exp.
+        const bool split = alone_step && c.att_impl == 1 && !o_spec;
         // 2. urgent assign: T resident, sparing the prediction fetched for this step
         KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
             return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
-                                               sc);
+                                               sc, -1, split ? c.res_hit_slot : nullptr,
+                                               split ? c.res_hit_cnt : nullptr);
         }));
         // 3. urgent gather of the blocks that were missing
         if (!alone_step) {
@@ -787,8 +805,19 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, su, [&] {
-            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask, alone_step);
+            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask, alone_step && !split);
         }));
+        if (split) {
+            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
+                return kvo::launch_attention(c, l, buf, ql, nullptr, c.res_hit_slot, c.res_oA, c.res_lA, nullptr,
+                                             nullptr, 1, sc, true, c.res_hit_cnt, true, true);
+            }));
+            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
+                return kvo::launch_attn_merge_part(c, buf, ql, dsl, mcnt, c.res_oA, c.res_lA, o + l * o_layer,
+                                                   lse + l * lse_layer, sc);
+            }));
+            continue;
+        }
         if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
             KVO_CUDA(&c, timed(kvo::PK_RECON, sc, [&] {
                 return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, sc);

@@ -54,13 +54,18 @@ def _attempts(c, steps, drift):
     (False, 2, 32, 12, False, None, 64, True, False),  # no speculation: one chain, every SM copies the misses
     (False, 2, 32, 12, False, None, 64, True, True),   # ... replayed from CUDA graphs
     ("alt", 2, 16, 16, False, None, 32, False, False),  # speculative and plain steps alternate
-    ("s3", 2, 16, 16, False, None, 32, False, True)])  # graph replays, one speculative step, replays again
+    ("s3", 2, 16, 16, False, None, 32, False, True),   # graph replays, one speculative step, replays again
+    (False, 1, 16, 8, False, None, 32, "many", False)])  # 320 groups: one CTA per group for the fetched blocks
 def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged, graphs):
     drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
-    ctx = (n, n + 40 * B) if ragged else (n, n)
-    w = Workload(f"resident_B{B}", 3 if ragged else 2, 8, 2, 128, B, k, W, L, ctx,
-                 spec_sigma=0.3 if spec else None)
+    if ragged == "many":
+        w = Workload(f"resident_B{B}_many", 40, 16, 8, 128, B, k, W, L, (n, n), spec_sigma=None)
+        ragged, graphs, steps = False, False, 3
+    else:
+        ctx = (n, n + 40 * B) if ragged else (n, n)
+        w = Workload(f"resident_B{B}", 3 if ragged else 2, 8, 2, 128, B, k, W, L, ctx,
+                     spec_sigma=0.3 if spec else None)
     c = Case(w, seed, gen_device="cpu", resident=True)
     try:
         att = _attempts(c, steps, drift)
