@@ -307,11 +307,16 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
  * same way, sparing the blocks of T, on the low-priority stream.  Without a
  * speculative query only the urgent phase runs (the previous step's T is
  * spared); when moreover no prefetch is in flight and no layer has low-rank
- * keys, the step is one chain on the compute stream: its urgent copies take
- * every SM and its attention the whole device, and kvo_set_graphs(1) replays
- * it from a CUDA graph.  The copies of this mode always use the flat gather
- * engine (engine 3, with per-entry destination slots) whatever
- * kvo_set_gather_engine chose.
+ * keys, the step is one chain on the compute stream, and kvo_set_graphs(1)
+ * replays it from a CUDA graph.  In a chain step attention is split: the
+ * blocks of T that were resident already, and the window, are attended while
+ * the urgent copy runs (the TMA-staged kernel, launched as a programmatic
+ * dependent of the copy so that it takes the SMs the copy leaves free), then
+ * the fetched blocks, merged into the first result by log-sum-exp (with the
+ * register-direct attention kernel, kvo_set_attn_impl 0, the step attends to
+ * the whole set after the copy instead).  The copies of this mode always use
+ * the flat gather engine (engine 3, with per-entry destination slots)
+ * whatever kvo_set_gather_engine chose.
  *   kvo_resident_slots: synchronize, copy layer `layer`'s slot table
  *   [G][2k] int32 to host memory `slots_out`.
  *   kvo_resident_fetched: synchronize, write the blocks fetched since init (or

@@ -55,7 +55,8 @@ def _attempts(c, steps, drift):
     (False, 2, 32, 12, False, None, 64, True, True),   # ... replayed from CUDA graphs
     ("alt", 2, 16, 16, False, None, 32, False, False),  # speculative and plain steps alternate
     ("s3", 2, 16, 16, False, None, 32, False, True),   # graph replays, one speculative step, replays again
-    (False, 1, 16, 8, False, None, 32, "many", False)])  # 320 groups: one CTA per group for the fetched blocks
+    (False, 1, 16, 8, False, None, 32, "many", False),  # 320 groups: one CTA per group for the fetched blocks
+    (False, 2, 32, 12, False, None, 64, True, "impl0")])  # chain steps with the register-direct attention
 def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged, graphs):
     drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
@@ -71,6 +72,9 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged,
         att = _attempts(c, steps, drift)
         if budget is not None:
             c.ctx.set_prefetch_budget(budget)     # admission cap on speculative fetches
+        if graphs == "impl0":
+            c.ctx.set_attn_impl(0)                # one attention pass after the copy, whole set
+            graphs = False
         if graphs:
             c.ctx.set_graphs(True)
         G, r = w.batch * w.n_kv_heads, w.group_size
