@@ -410,6 +410,17 @@ def step_queries(B):
         B.step_i += 1
 
 
+def join_ctx_streams(ctx, stream):
+    """Make ``stream`` wait for all work on the context's own streams: a step
+    returns with the prefetches it issued for the next step still in flight,
+    and a timed region that ends without them would leave out link work the
+    steps it counts depend on."""
+    for which in (0, 1, 2):
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.ExternalStream(ctx.get_stream(which)))
+        stream.wait_event(ev)
+
+
 def time_steps(B, steps, ws=1, profile=True):
     """(ms per step, per-kind profile) over ``steps`` decode steps on the current stream."""
     stream = torch.cuda.current_stream()
@@ -426,6 +437,7 @@ def time_steps(B, steps, ws=1, profile=True):
             B.app_used += 1
         step_queries(B)
         ctx.decode_step(B.q_dev, B.qs_dev, B.o, B.lse)
+    join_ctx_streams(ctx, stream)
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -525,6 +537,7 @@ def run_ours(args):
         ctx.decode_step(q_dev, qs_dev, o, lse)
         o_pin.copy_(o, non_blocking=True)
         lse_pin.copy_(lse, non_blocking=True)
+    join_ctx_streams(ctx, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)

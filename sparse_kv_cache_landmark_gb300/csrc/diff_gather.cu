@@ -182,8 +182,9 @@ gather_kernel(const uint16_t* __restrict__ kh, const uint16_t* __restrict__ vh, 
 // first builds, in shared memory, the prefix over the groups of their chunk
 // counts (listed entries x words per block, rounded up to chunks), so the warps
 // stride over the listed chunks only -- a short miss list costs a short walk --
-// and find a chunk's group by binary search; without it (more groups than the
-// prefix may hold) the warps stride over k entries' chunks of every group.
+// and find a chunk's group by binary search; without it (full lists, or more
+// groups than the prefix may hold) the warps stride over k entries' chunks of
+// every group.
 // The launch may reserve shared memory it never uses so that each gather CTA
 // has its SM to itself: the other kernels then never queue their HBM loads
 // behind zero-copy loads waiting on the host link in the same SM's load/store
@@ -320,10 +321,12 @@ cudaError_t launch_gather_flat(const Ctx& c, int layer, int buf, const int32_t* 
     // 1024-thread CTA each, no reservation) to cut the latency of small lists
     const int ctas = alone ? c.n_sms : (c.gather_ctas > 0 ? c.gather_ctas : 2 * 152);
     const int th = alone ? 1024 : c.gather_threads;
-    // the chunk prefix needs G + 1 words and must not overflow 32 bits
+    // Lists with counts walk the listed chunks through the prefix (G + 1 words,
+    // no 32-bit overflow); full lists (no counts) have no empty chunk to skip
+    // and stride over k entries per group without the per-chunk group search.
     const int U = c.gather_unroll >= 2 ? 2 : 1;
     const int64_t all_chunks = (int64_t)c.G * (((int64_t)c.k * words + 32 * U - 1) / (32 * U));
-    const bool compact = c.G <= FLAT_PREFIX_MAX_G && all_chunks < (int64_t)1 << 31;
+    const bool compact = cnt && c.G <= FLAT_PREFIX_MAX_G && all_chunks < (int64_t)1 << 31;
     const size_t pre = compact ? sizeof(uint32_t) * (c.G + 1) : 0;
     const size_t smem = std::max(alone ? (size_t)0 : (size_t)c.gather_reserve_smem, pre);
 #define KVO_FLAT(U_, P_)                                                                                          \
