@@ -709,6 +709,15 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
     return KVO_OK;
 }
 
+// A resident step whose kernels form one chain: no speculative query, no
+// prefetch of an earlier step in flight, no layer with low-rank keys.
+static bool resident_alone(const kvo::Ctx& c, const void* q_spec) {
+    if (q_spec) return false;
+    for (int l = 0; l < c.L; ++l)
+        if (c.res_pending[l] || c.lr_rank[l] > 0) return false;
+    return true;
+}
+
 // Decode step with per-layer resident block sets (cross-step delta prefetch).
 // Per layer l: select (true index, and with q_spec the prediction for the next
 // step); urgent assign (T resident, sparing the prediction fetched for this
@@ -719,15 +728,9 @@ static kvo_status decode_step_body(kvo_ctx* ctx, const void* q, const void* q_sp
 // assign of l (it reads T and the slot table), and its attention for the
 // prefetch gather; urgent copies never touch slots of the prediction being
 // prefetched, because the urgent assign spares them.
-// A resident step whose kernels form one chain: no speculative query, no
-// prefetch of an earlier step in flight, no layer with low-rank keys.
-static bool resident_alone(const kvo::Ctx& c, const void* q_spec) {
-    if (q_spec) return false;
-    for (int l = 0; l < c.L; ++l)
-        if (c.res_pending[l] || c.lr_rank[l] > 0) return false;
-    return true;
-}
-
+// Without a speculative query (nothing in flight, no low-rank layer) the step
+// is one chain on the compute stream; its attention is split around the
+// urgent copy (see below).
 static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
                                        float* o_spec, float* lse_spec, cudaStream_t s_user) {
     kvo::Ctx& c = ctx->c;
