@@ -452,6 +452,29 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes);
 kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
 
 /*
+ * kvo_plan_attention -- the work split of the TMA-staged attention kernel
+ * (kvo_set_attn_impl 1) for a shape, computed on the host: no context, no GPU.
+ * The tiles (16 tokens) of every group -- its sparse part of sparse_tokens
+ * (k * block_size), then its window part of window_tokens (W, or W + B - 1
+ * when the cache grows) -- are laid out group after group and split into
+ * `grid` contiguous ranges of equal cost (a tile costs 1, entering a part 3
+ * more: the work-item epilogue), range bounds rounded down to a multiple of
+ * the CTA's 4 warps; each range is cut at part boundaries into work items.
+ *   n_groups: b * Hkv.  grid: CTAs asked for; the plan uses min(grid, tiles).
+ *   items_out: host [items_cap][4] int32, nullable: {group, part (0 sparse,
+ *     1 window), first tile within the part, tiles}, in range order.
+ *   cta_out: host [grid + 1] int32, nullable: first item of each range, then
+ *     the item count.
+ *   n_items_out, grid_out: host, the item count and the grid used.
+ * Call once with items_out = NULL to size the buffers.  Errors:
+ * KVO_ERR_INVALID (message via kvo_last_error(NULL)) for n_groups or grid <= 0,
+ * negative token counts, both zero, null count pointers, or items_cap below the
+ * item count when items_out is given.
+ */
+kvo_status kvo_plan_attention(int n_groups, int sparse_tokens, int window_tokens, int grid, int32_t* items_out,
+                              int items_cap, int32_t* cta_out, int32_t* n_items_out, int32_t* grid_out);
+
+/*
  * Per-launch timing of kvo_decode_step, for benchmarks.  kvo_profile(ctx, 1)
  * clears and starts recording a timing event before and after every kernel
  * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.

@@ -74,20 +74,21 @@ cudaError_t part_alloc(kvo::Ctx& c, int items) {
 // equal cost -- a tile costs 1, and each part costs kItemCost more, the price
 // of the work-item epilogue a range pays where it enters a part -- with their
 // bounds rounded to a multiple of the CTA's warps (so the warps of an item get
-// equal tile counts), each range cut at part boundaries.
-kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
-    const int64_t sp_tiles = (c.k * c.B + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
-    const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;
-    const int64_t w_tiles = (w_max + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
-    const int64_t per_g = sp_tiles + w_tiles, T = per_g * c.G;
+// equal tile counts), each range cut at part boundaries.  Pure host logic;
+// returns the grid used (at least 1, at most the tile count).
+int64_t plan_tma_items(int G, int sp_tokens, int w_tokens, int64_t grid, std::vector<int4>& items,
+                       std::vector<int32_t>& cta) {
+    const int64_t sp_tiles = (sp_tokens + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    const int64_t w_tiles = (w_tokens + kvo::ATT_TILE - 1) / kvo::ATT_TILE;
+    const int64_t per_g = sp_tiles + w_tiles, T = per_g * G;
     grid = std::max<int64_t>(1, std::min<int64_t>(grid, T));
-    std::vector<int4> items;
-    std::vector<int32_t> cta(grid + 1), first(c.G, 0), count(c.G, 0);
+    items.clear();
+    cta.assign(grid + 1, 0);
     // parts in tile order with their first tile and first cost unit
     constexpr int64_t kItemCost = 3;     // epilogue of a work item, in tiles (measured ~7K vs ~2.4K cycles)
     std::vector<int64_t> p_t0, p_c0, p_len;
     int64_t cost = 0;
-    for (int g = 0; g < c.G; ++g)
+    for (int g = 0; g < G; ++g)
         for (int part = 0; part < 2; ++part) {
             const int64_t len = part == 0 ? sp_tiles : w_tiles;
             if (len == 0) continue;
@@ -119,6 +120,14 @@ kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
         }
     }
     cta[grid] = (int32_t)items.size();
+    return grid;
+}
+
+kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
+    const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;
+    std::vector<int4> items;
+    std::vector<int32_t> cta, first(c.G, 0), count(c.G, 0);
+    grid = plan_tma_items(c.G, c.k * c.B, w_max, grid, items, cta);
     for (size_t i = 0; i < items.size(); ++i) {
         const int g = items[i].x;
         if (count[g] == 0) first[g] = (int32_t)i;
@@ -1084,6 +1093,33 @@ kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset) {
     out2[0] = (int64_t)h[0];
     out2[1] = (int64_t)h[1];
     if (reset) KVO_CUDA(&c, cudaMemset(c.res_fetched, 0, sizeof(h)));
+    return KVO_OK;
+}
+
+kvo_status kvo_plan_attention(int n_groups, int sparse_tokens, int window_tokens, int grid, int32_t* items_out,
+                              int items_cap, int32_t* cta_out, int32_t* n_items_out, int32_t* grid_out) {
+    if (n_groups <= 0 || sparse_tokens < 0 || window_tokens < 0 || sparse_tokens + window_tokens <= 0 || grid <= 0 ||
+        items_cap < 0 || !n_items_out || !grid_out) {
+        kvo::set_last_error("kvo_plan_attention: need n_groups, grid > 0, token counts >= 0 (not both 0), non-null counts");
+        return KVO_ERR_INVALID;
+    }
+    std::vector<int4> items;
+    std::vector<int32_t> cta;
+    const int64_t used = plan_tma_items(n_groups, sparse_tokens, window_tokens, grid, items, cta);
+    *n_items_out = (int32_t)items.size();
+    *grid_out = (int32_t)used;
+    if (items_out) {
+        if ((size_t)items_cap < items.size()) {
+            kvo::set_last_error("kvo_plan_attention: items_cap below the item count (see n_items_out)");
+            return KVO_ERR_INVALID;
+        }
+        for (size_t i = 0; i < items.size(); ++i) {
+            items_out[4 * i + 0] = items[i].x; items_out[4 * i + 1] = items[i].y;
+            items_out[4 * i + 2] = items[i].z; items_out[4 * i + 3] = items[i].w;
+        }
+    }
+    if (cta_out)
+        for (size_t j = 0; j < cta.size(); ++j) cta_out[j] = cta[j];
     return KVO_OK;
 }
 

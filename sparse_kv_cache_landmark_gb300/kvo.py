@@ -25,7 +25,7 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
            "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched",
-           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys"]
+           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention", "recon"]
 
 
@@ -126,6 +126,25 @@ def merge_lse(o1, lse1, o2, lse2, o=None, lse=None, stream=None):
     lse = torch.empty_like(lse1) if lse is None else lse
     _check(lib().merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(o), _ptr(lse), rows, d, _stream(stream)))
     return o, lse
+
+
+def plan_attention(n_groups: int, sparse_tokens: int, window_tokens: int, grid: int):
+    """Work split of the TMA-staged attention (C: kvo_plan_attention; host only).
+
+    Returns (items int32 [n][4] = {group, part, first tile, tiles}, cta int32
+    [grid_used + 1] = first item of each CTA's range, then the item count).
+    """
+    n = ctypes.c_int32(0)
+    g = ctypes.c_int32(0)
+    L = lib()
+    _check(L.kvo_plan_attention(n_groups, sparse_tokens, window_tokens, grid, None, 0, None, ctypes.byref(n),
+                                ctypes.byref(g)))
+    items = torch.empty(max(1, n.value), 4, dtype=torch.int32)
+    cta = torch.empty(g.value + 1, dtype=torch.int32)
+    _check(L.kvo_plan_attention(n_groups, sparse_tokens, window_tokens, grid,
+                                ctypes.c_void_p(items.data_ptr()), items.shape[0],
+                                ctypes.c_void_p(cta.data_ptr()), ctypes.byref(n), ctypes.byref(g)))
+    return items[:n.value], cta
 
 
 def sparse_decode_attn_static(q, k_buf, v_buf, slot_of_true, k_win, v_win, *, batch, n_q_heads, n_kv_heads,
