@@ -147,6 +147,8 @@ class Clocks:
 
     def stop(self):
         if self.p is None:
+            self.f.close()
+            os.unlink(self.f.name)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.p.terminate()
         self.p.wait()
@@ -165,6 +167,7 @@ class Clocks:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        self.f.close()
         os.unlink(self.f.name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
