@@ -799,7 +799,7 @@ template <int D, int NR>
 static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, const void* q, const void* q_spec,
                               const uint16_t* wk, const uint16_t* wv, const int32_t* slot, float* o, float* lse,
                               float* o_spec, float* lse_spec, int fuse, cudaStream_t s, const int32_t* sp_cnt,
-                              bool win, bool pdl, float scale_log2) {
+                              bool pdl, float scale_log2) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(ATT_WARPS * 32);
@@ -814,14 +814,13 @@ static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, con
                               (const uint16_t*)c.buf_k(buf), (const uint16_t*)c.buf_v(buf), wk, wv, slot,
                               (const int4*)pl.items, (const int32_t*)pl.cta, (const int32_t*)pl.first,
                               (const int32_t*)pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec,
-                              lse_spec, fuse, c.batch, c.r, c.Hkv, c.k, c.B, win ? c.W : 0, c.Wcap,
-                              (const int32_t*)c.g_wstart, win ? (const int32_t*)c.g_wlen : (const int32_t*)nullptr,
-                              sp_cnt, pdl ? 1 : 0, scale_log2, c.status);
+                              lse_spec, fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, (const int32_t*)c.g_wstart,
+                              (const int32_t*)c.g_wlen, sp_cnt, pdl ? 1 : 0, scale_log2, c.status);
 }
 
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step, const int32_t* sp_cnt, bool win, bool pdl) {
+                             bool in_step, const int32_t* sp_cnt, bool pdl) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
@@ -829,14 +828,14 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
     if (c.att_impl == 1) {
 #define KVO_TMA(D_, NR_) \
-        launch_tma<D_, NR_>(c, pl, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, fuse, s, sp_cnt, win, pdl, \
+        launch_tma<D_, NR_>(c, pl, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, fuse, s, sp_cnt, pdl, \
                             scale_log2)
         if (c.d == 128) return nrows <= 8 ? KVO_TMA(128, 1) : KVO_TMA(128, 2);
         return nrows <= 8 ? KVO_TMA(64, 1) : KVO_TMA(64, 2);
 #undef KVO_TMA
     }
-    // partial slot lists, window-less passes and dependent launches exist in the TMA-staged kernel only
-    if (sp_cnt || !win || pdl) return cudaErrorInvalidValue;
+    // partial slot lists and dependent launches exist in the TMA-staged kernel only
+    if (sp_cnt || pdl) return cudaErrorInvalidValue;
 #define KVO_ATT(D_, NR_)                                                                                         \
     attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
         (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, c.att_items,       \

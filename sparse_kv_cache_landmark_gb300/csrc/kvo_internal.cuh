@@ -228,14 +228,13 @@ cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need,
                                    int32_t* hit_cnt = nullptr);
 cudaError_t prepare_resident(const Ctx& c);
 // Optional for the TMA-staged kernel only: sp_cnt[g] limits the sparse part to
-// the first sp_cnt[g] entries of the slot list; win = false drops the window
-// part; pdl launches it as a programmatic dependent of the kernel before it on
-// the stream (it starts once that kernel's CTAs are all resident, and ends only
-// after that kernel has completed).
+// the first sp_cnt[g] entries of the slot list; pdl launches it as a
+// programmatic dependent of the kernel before it on the stream (it starts once
+// that kernel's CTAs are all resident, and ends only after that kernel has
+// completed).
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step = false, const int32_t* sp_cnt = nullptr, bool win = true,
-                             bool pdl = false);
+                             bool in_step = false, const int32_t* sp_cnt = nullptr, bool pdl = false);
 // Attention over the first cnt[g] entries of a slot list, merged by lse with a
 // prior part into (o, lse); merge_part_split(c) CTAs per group.
 constexpr int MP_SPLIT_MAX = 8;

@@ -822,7 +822,7 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         if (split) {
             KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
                 return kvo::launch_attention(c, l, buf, ql, nullptr, c.res_hit_slot, c.res_oA, c.res_lA, nullptr,
-                                             nullptr, 1, sc, true, c.res_hit_cnt, true, true);
+                                             nullptr, 1, sc, true, c.res_hit_cnt, true);
             }));
             KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
                 return kvo::launch_attn_merge_part(c, buf, ql, dsl, mcnt, c.res_oA, c.res_lA, o + l * o_layer,
