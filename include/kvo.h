@@ -41,6 +41,30 @@
  *    KV head g serves query heads g*r .. g*r + r - 1.
  *  - No CPU fallback exists: without a CUDA device the calls fail with
  *    KVO_ERR_CUDA.
+ *  - Concurrency on one context.  The context owns scratch that some calls
+ *    use while their kernels run; two calls using the same scratch must not
+ *    overlap on the GPU (issue them on one stream, or order them with events),
+ *    or their results are undefined.  The scratch classes:
+ *      [sel]  selection keys, histograms and tickets: select_topk;
+ *      [att]  attention work items, partial results and tickets:
+ *             sparse_decode_attn, sparse_decode_attn_cobatch;
+ *      [runs] the run list of gather_coalesced when runs_out is NULL (one per
+ *             value of `urgent`);
+ *      [buf]  the ping-pong halves / resident sets: gather_coalesced writes the
+ *             slots it is given, the attention calls read the slots named by
+ *             slot_of_true -- a slot must not be written while it is read;
+ *      [all]  kvo_decode_step, kvo_decode_step_dual and kvo_append use every
+ *             class (and the step state, window and landmarks): nothing else
+ *             may overlap them on the same context.
+ *    Calls of different classes may overlap freely (e.g. select_topk of layer
+ *    l + 1 on one stream beside sparse_decode_attn of layer l on another).
+ *    index_diff uses no context scratch (only its own outputs); merge_lse and
+ *    kvo_plan_attention need no context.  The device status word is updated
+ *    atomically and may be written by overlapping calls.  Host-side calls that
+ *    change settings (kvo_set_*, kvo_reset_prediction, kvo_profile*) first
+ *    synchronize the context's own streams but not the caller's: make sure no
+ *    call of this context is in flight on other streams.  Distinct contexts
+ *    share nothing.
  */
 #ifndef KVO_H
 #define KVO_H
@@ -128,6 +152,7 @@ kvo_status kv_offload_destroy(kvo_ctx* ctx);
  *   blocks in ascending id order, ties to the lower id.  When q_spec is given,
  *   idx_pred[G][k] receives the same for q_spec from the same landmark pass
  *   (the speculative look-ahead query of the dual-token scheme, §5.2).
+ *   Concurrency: [sel] -- one select_topk at a time per context.
  */
 kvo_status select_topk(kvo_ctx* ctx, int layer, const void* q, const void* q_spec,
                        int32_t* idx_true, int32_t* idx_pred, kvo_stream_t stream);
@@ -140,6 +165,7 @@ kvo_status select_topk(kvo_ctx* ctx, int layer, const void* q, const void* q_spe
  *   (first miss_cnt[g] entries valid), miss_cnt[G], slot_of_true[G][k]:
  *   the ping-pong slot holding idx_true[g][i] -- its position in idx_pred if
  *   predicted, else k + its rank among the misses.
+ *   Concurrency: uses no context scratch; may overlap any call.
  */
 kvo_status index_diff(kvo_ctx* ctx, const int32_t* idx_true, const int32_t* idx_pred,
                       int32_t* miss_idx, int32_t* miss_cnt, int32_t* slot_of_true,
@@ -157,6 +183,9 @@ kvo_status index_diff(kvo_ctx* ctx, const int32_t* idx_true, const int32_t* idx_
  *   (device int32 [G]) are optional.  `urgent` is informational for stream
  *   choice when stream is NULL: 1 = the urgent stream, 0 = the prefetch
  *   stream; the caller orders other work after it with events.
+ *   Concurrency: [buf] (the slots written) and, with runs_out NULL, [runs] of
+ *   its `urgent` value; gathers into disjoint slots with caller-owned run
+ *   lists (or different `urgent` values) may overlap.
  */
 kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx,
                             const int32_t* cnt, int slot_base, int urgent, int32_t* runs_out,
@@ -172,6 +201,8 @@ kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx
  *   window and sparse parts fused by log-sum-exp.  fuse_window_merge = 0:
  *   o[2][b][Hq][d], lse[2][b][Hq]: part 0 sparse, part 1 window (an empty
  *   part has lse = -inf, o = 0).
+ *   Concurrency: [att], and it reads [buf] -- one attention call at a time
+ *   per context, with no write to the slots it reads in flight.
  */
 kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q,
                               const int32_t* slot_of_true, float* o, float* lse,
@@ -186,6 +217,7 @@ kvo_status sparse_decode_attn(kvo_ctx* ctx, int layer, int buf, const void* q,
  * r..2r-1 of the tensor-core tiles, so 2r <= 16 is required.
  *   q, q_spec: device [b][Hq][d] bf16.  o, lse as in sparse_decode_attn;
  *   o_spec, lse_spec: the same layouts for the speculative query.
+ *   Concurrency: as sparse_decode_attn ([att], reads [buf]).
  */
 kvo_status sparse_decode_attn_cobatch(kvo_ctx* ctx, int layer, int buf, const void* q, const void* q_spec,
                                       const int32_t* slot_of_true, float* o, float* lse, float* o_spec,
@@ -220,6 +252,8 @@ kvo_status merge_lse(const float* o1, const float* lse1, const float* o2, const 
  *   keeps per-layer resident sets and fetches only their delta instead (see
  *   kvo_resident_slots); layers given low-rank factors rebuild their missed
  *   keys on the GPU (kvo_set_lowrank_keys).
+ *   Concurrency: [all] -- no other call on this context may overlap a step
+ *   (the in-flight prefetches it leaves are ordered by the library itself).
  */
 kvo_status kvo_decode_step(kvo_ctx* ctx, const void* q, const void* q_spec, float* o,
                            float* lse, kvo_stream_t stream);
@@ -261,6 +295,7 @@ kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable);
  *   window (W to W + B - 1 tokens).  Ordered on `stream` like the other calls.
  *   Errors: KVO_ERR_STATE when the context was built with max_append == 0 or
  *   the reserved capacity is used up.
+ *   Concurrency: [all].
  */
 kvo_status kvo_append(kvo_ctx* ctx, const void* k_new, const void* v_new, kvo_stream_t stream);
 
@@ -377,7 +412,10 @@ kvo_status kvo_info(kvo_ctx* ctx, int64_t* out4);
  *   [b][Hkv][W][d] bf16 (may be NULL when W == 0).  Outputs as in
  *   sparse_decode_attn (fuse_window_merge picks one fused part or two parts);
  *   status (device int32, optional) receives KVO_DEV_BAD_SLOT for a slot
- *   outside [0, 2k), which is then not read.
+ *   outside [0, 2k), which is then not read (slot 0 is read in its place);
+ *   with status == NULL such errors are dropped -- nothing reports them.
+ *   The call cannot check buffer sizes (it has no context): each buffer must
+ *   hold at least the elements its shape above implies.
  *   Scratch: one static device array of 24 MiB, reserved on every GPU that
  *   loads the library until the process exits.  A call needs
  *   items * r * (d + 2) * 4 bytes plus small tables, items = G * (ceil(k*B/256)

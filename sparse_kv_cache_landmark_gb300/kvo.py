@@ -159,14 +159,46 @@ def sparse_decode_attn_static(q, k_buf, v_buf, slot_of_true, k_win, v_win, *, ba
     array shared by every call, so calls must not overlap on the GPU.
     ``k_buf``/``v_buf`` are bf16 CUDA tensors laid out like a ping-pong half,
     [G][2k][B][d].  Pass ``o``/``lse`` (and ``status``) to keep this wrapper from
-    allocating its outputs with torch.
+    allocating its outputs with torch (it allocates them on ``q``'s device).
+    Every buffer's dtype, contiguity, size and device is checked against the
+    shape arguments before the call; a mismatch raises ``KvoError``.  A slot
+    outside [0, 2k) is reported in ``status`` (int32, optional); without a
+    status word such errors are dropped.
     """
     rows = batch * n_q_heads
     parts = 1 if fuse_window_merge else 2
+    G = batch * n_kv_heads
+    # this call has no context to size the buffers by: a short buffer would be
+    # an out-of-bounds device access, so every buffer is checked here first
+    need = [("q", q, torch.bfloat16, rows * head_dim),
+            ("k_buf", k_buf, torch.bfloat16, G * 2 * top_k * block_size * head_dim),
+            ("v_buf", v_buf, torch.bfloat16, G * 2 * top_k * block_size * head_dim),
+            ("slot_of_true", slot_of_true, torch.int32, G * top_k)]
+    if window > 0:
+        need += [("k_win", k_win, torch.bfloat16, G * window * head_dim),
+                 ("v_win", v_win, torch.bfloat16, G * window * head_dim)]
+    if o is not None:
+        need.append(("o", o, torch.float32, parts * rows * head_dim))
+    if lse is not None:
+        need.append(("lse", lse, torch.float32, parts * rows))
+    if status is not None:
+        need.append(("status", status, torch.int32, 1))
+    for name, t, dt, n in need:
+        if t is None:
+            raise KvoError(KVO_ERR_INVALID, f"{name} is required")
+        if t.dtype != dt:
+            raise KvoError(KVO_ERR_INVALID, f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise KvoError(KVO_ERR_INVALID, f"{name} must be contiguous")
+        if t.numel() < n:
+            raise KvoError(KVO_ERR_INVALID, f"{name} holds {t.numel()} elements, the shape needs {n}")
+    devs = {t.device for _, t, _, _ in need}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise KvoError(KVO_ERR_INVALID, f"all buffers must be on one CUDA device, got {sorted(map(str, devs))}")
     if o is None:
-        o = torch.empty(parts, rows, head_dim, dtype=torch.float32, device="cuda")
+        o = torch.empty(parts, rows, head_dim, dtype=torch.float32, device=q.device)
     if lse is None:
-        lse = torch.empty(parts, rows, dtype=torch.float32, device="cuda")
+        lse = torch.empty(parts, rows, dtype=torch.float32, device=q.device)
     _check(lib().sparse_decode_attn_static(_ptr(q), _ptr(k_buf), _ptr(v_buf), _ptr(slot_of_true), _ptr(k_win),
                                            _ptr(v_win), _ptr(o), _ptr(lse), _ptr(status), batch, n_q_heads,
                                            n_kv_heads, head_dim, block_size, top_k, window,

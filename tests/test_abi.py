@@ -86,3 +86,41 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kvo, "_LIB", None)
     with pytest.raises(RuntimeError, match="not built"):
         kvo.lib()
+
+
+def test_static_attention_wrapper_checks_every_buffer():
+    """sparse_decode_attn_static has no context to size its buffers by: the
+    binding checks dtype, contiguity, size and device of each one before the
+    call, so a short buffer never reaches the GPU (no library call is made)."""
+    import torch
+    from sparse_kv_cache_landmark_gb300 import kvo
+    shape = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=64, block_size=16, top_k=4, window=16)
+    G, rows = 4, 16
+    bf = lambda n: torch.zeros(n, dtype=torch.bfloat16)
+    q, kb, vb = bf(rows * 64), bf(G * 8 * 16 * 64), bf(G * 8 * 16 * 64)
+    slot = torch.zeros(G * 4, dtype=torch.int32)
+    kw, vw = bf(G * 16 * 64), bf(G * 16 * 64)
+    call = lambda **over: kvo.sparse_decode_attn_static(
+        *[over.get(n, t) for n, t in (("q", q), ("k_buf", kb), ("v_buf", vb), ("slot", slot), ("k_win", kw),
+                                      ("v_win", vw))], **{**shape, **over.get("shape", {})},
+        **{k: v for k, v in over.items() if k in ("o", "lse", "status")})
+    with pytest.raises(kvo.KvoError, match="k_buf holds"):
+        call(k_buf=bf(G * 8 * 16 * 64 - 1))
+    with pytest.raises(kvo.KvoError, match="slot_of_true must be torch.int32"):
+        call(slot=slot.long())
+    with pytest.raises(kvo.KvoError, match="v_win holds"):
+        call(v_win=bf(10))
+    with pytest.raises(kvo.KvoError, match="k_win is required"):
+        call(k_win=None)
+    with pytest.raises(kvo.KvoError, match="contiguous"):
+        call(q=bf(2 * rows * 64)[::2])
+    with pytest.raises(kvo.KvoError, match="o holds"):
+        call(o=torch.zeros(5, dtype=torch.float32))
+    with pytest.raises(kvo.KvoError, match="status must be torch.int32"):
+        call(status=torch.zeros(1, dtype=torch.float32))
+    # right sizes on the CPU: rejected for the device, still before any library call
+    with pytest.raises(kvo.KvoError, match="one CUDA device"):
+        call()
+    # no window: the window buffers may be None
+    with pytest.raises(kvo.KvoError, match="one CUDA device"):
+        call(k_win=None, v_win=None, shape=dict(window=0))

@@ -52,3 +52,61 @@ def test_missing_tool(tmp_path, monkeypatch):
     monkeypatch.setenv("PATH", str(tmp_path))  # an empty directory: no nvidia-smi
     out = bench.Clocks(0).stop()
     assert out["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_sampler_names_the_gpu_it_was_given(tmp_path, monkeypatch):
+    """The sampler passes nvidia-smi the id it was given (a UUID), not a CUDA
+    ordinal, which nvidia-smi would read in its own (PCI) numbering."""
+    log = tmp_path / "args.txt"
+    exe = tmp_path / "nvidia-smi"
+    exe.write_text(f"#!/bin/sh\necho \"$@\" > {log}\necho '{ROWS[0]}'\nexec sleep 30\n")
+    exe.chmod(exe.stat().st_mode | stat.S_IXUSR)
+    monkeypatch.setenv("PATH", str(tmp_path) + os.pathsep + os.environ["PATH"])
+    c = bench.Clocks("GPU-7aebdb66-0000-4d0a-8503-96f012cef09c")
+    time.sleep(0.5)
+    c.stop()
+    args = log.read_text().split()
+    assert args[args.index("-i") + 1] == "GPU-7aebdb66-0000-4d0a-8503-96f012cef09c"
+
+
+class _Props:
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def test_gpu_id_prefers_uuid_then_pci_bus(monkeypatch):
+    import torch
+    monkeypatch.setattr(torch.cuda, "get_device_properties",
+                        lambda i: _Props(uuid="7aebdb66-67b0-4d0a-8503-96f012cef09c"))
+    assert bench.smi_gpu_id(3) == "GPU-7aebdb66-67b0-4d0a-8503-96f012cef09c"
+    monkeypatch.setattr(torch.cuda, "get_device_properties",
+                        lambda i: _Props(uuid="GPU-abc", pci_bus_id=7))
+    assert bench.smi_gpu_id(0) == "GPU-abc"
+    monkeypatch.setattr(torch.cuda, "get_device_properties",
+                        lambda i: _Props(pci_domain_id=0, pci_bus_id=0x1b, pci_device_id=0))
+    assert bench.smi_gpu_id(0) == "00000000:1b:00.0"
+
+    def boom(i):
+        raise RuntimeError("no device")
+    monkeypatch.setattr(torch.cuda, "get_device_properties", boom)
+    assert bench.smi_gpu_id(5) == "5"
+
+
+def test_host_description_and_numa_helpers():
+    h = bench.host_info()
+    assert h["nproc"] == os.cpu_count() and h["cpu_model"] and h["numa_nodes"] >= 1
+    nodes = bench.cpu_numa_nodes()
+    assert nodes and all(isinstance(n, int) for n in nodes)
+    with bench.numa_bind(None) as bound:        # the default policy: nothing to bind
+        assert bound is False
+    import torch
+    t = torch.empty(1 << 16, dtype=torch.uint8)
+    t.fill_(1)
+    assert bench.page_node(t.data_ptr()) in [-1] + nodes
+
+
+def test_default_run_covers_the_four_roofline_workloads():
+    a = bench.parse([])
+    names = [a.workload] + [x for x in a.workloads.split(",") if x]
+    assert names == ["llama3_8b_decode", "long_ctx_predict", "wide_budget", "fragmentation"]
+    assert a.warmup >= 3
