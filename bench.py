@@ -946,10 +946,9 @@ def run_ours(args):
     smi_id = smi_gpu_id(local)
     host = host_info()
 
-    # host->device link bandwidth: pinned copies on 1, 2 and 4 streams, per NUMA placement
-    probe = probe_link(local, stream)
-    near = probe["gpu_nearest_node"]
-    numa_node = near if (near is not None and len(probe["numa_nodes"]) > 1) else None
+    # pinned host caches on the GPU's nearest NUMA node when the host has several
+    near = gpu_host_numa_node(local)
+    numa_node = near if (near is not None and len(cpu_numa_nodes()) > 1) else None
 
     head = measure(args, ws, rank, smi_id, True, args.steps, numa_node)
     extra = []
@@ -959,6 +958,9 @@ def run_ours(args):
             a2.workload, a2.layers, a2.batch, a2.host_layers, a2.trace = name, 0, 0, 0, args.trace
             a2.append = 0
             extra.append(measure(a2, ws, rank, smi_id, False, args.extra_steps, numa_node))
+    # host->device link bandwidth: pinned copies on 1, 2 and 4 streams, per NUMA
+    # placement (after the workloads, whose own pinned caches are allocated first)
+    probe = probe_link(local, stream)
     link_zc = max([head["link_zc"]] + [m["link_zc"] for m in extra])
     link = max(probe["best_pinned_memcpy"], link_zc)
     hbm_peak, peak_kind = peaks()

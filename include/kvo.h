@@ -531,6 +531,20 @@ kvo_status kvo_profile_read(kvo_ctx* ctx, double* ms_out, int64_t* launches_out,
 kvo_status kvo_profile_trace(kvo_ctx* ctx, double* start_ms, double* end_ms, int32_t* kind, int32_t* layer,
                              int cap, int* n_out);
 
+/*
+ * kvo_set_wait_test -- for testing the bounded waits of the TMA-staged
+ * attention kernel (kvo_set_attn_impl 1).  limit_ns (1 ms .. 10 s; default
+ * 2 s) bounds every mbarrier wait of that kernel.  skip_tile >= 0 makes the
+ * first warp of CTA 0 in every later launch announce its tile number skip_tile
+ * (counted from 0 in that warp's own order) without copying it, so the wait
+ * for that tile runs out: the kernel then sets KVO_DEV_TIMEOUT in the device
+ * status word, stops waiting and issuing, lets every copy it did issue land,
+ * and returns; its outputs are invalid.  skip_tile = -1 (default) copies everything.  Synchronizes the
+ * context's streams and drops captured graphs.  Errors: KVO_ERR_INVALID for
+ * limit_ns outside 1 ms .. 10 s or skip_tile < -1.  Not for production use.
+ */
+kvo_status kvo_set_wait_test(kvo_ctx* ctx, int64_t limit_ns, int skip_tile);
+
 /* Human-readable description of the last error of ctx (or of the last
  * context-free call when ctx is NULL).  Never NULL. */
 const char* kvo_last_error(const kvo_ctx* ctx);

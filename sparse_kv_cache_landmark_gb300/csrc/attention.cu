@@ -297,6 +297,7 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
     // every element's partial loads are then independent of one another.  More
     // items: an online merge per element.
     constexpr int MI = D == 128 ? 96 : 48;              // items the table holds
+    static_assert(MI * 33 + 64 <= ATT_WARPS * 8 * NR * D, "merge table does not fit the warps' state area");
     float* s_w = const_cast<float*>(sm_o);              // [MI][16] m, then weight, of (item, row)
     float* s_l = s_w + MI * 16;                         // [MI][16] l of (item, row)
     int* s_p = reinterpret_cast<int*>(s_l + MI * 16);   // [MI] part of each item
@@ -388,6 +389,9 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
         }
     }
     if (tid == 0) done[bg] = 0u;
+    // the merge table lives in the warps' state area: no warp may write its
+    // next state there before every thread is done reading the table
+    bar_named(1, nthr);
 }
 
 // ---------------------------------------------------------------------------
@@ -503,8 +507,9 @@ attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
 // warps and the loads stay STG tiles ahead of the math.  The fragments are
 // read from shared memory with the lane mapping of the register-direct kernel.
 // Every mbarrier wait is bounded by the global timer: on expiry the CTA
-// records KVO_DEV_TIMEOUT and stops waiting (its results are then invalid;
-// the host sees the status bit).
+// records KVO_DEV_TIMEOUT, stops waiting and issues no more copies (its
+// results are then invalid; the host sees the status bit), and each warp lets
+// the copies it already issued land before it exits.
 constexpr int ATT_ITEMS_SMEM = 8;    // work-item headers a CTA keeps in shared memory
 
 template <int D, int NR>
@@ -519,23 +524,31 @@ struct AttnTmaCfg {
                                     sizeof(uint64_t) * ATT_WARPS * STG + sizeof(int4) * ATT_ITEMS_SMEM + 16;
 };
 
-constexpr long long kAttWaitNs = 2000000000LL;   // 2 s per mbarrier wait
-
 // Bounded wait; false (and the CTA's abort flag set) when the limit passed.
 __device__ __forceinline__ bool att_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag,
-                                         int32_t* status) {
+                                         int32_t* status, long long limit_ns) {
     if (mbar_try_wait(mbar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (int it = 0;; ++it) {
         if (mbar_try_wait(mbar, parity)) return true;
         if ((it & 63) == 63) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > (uint64_t)kAttWaitNs) {
+            if (global_ns() - t0 > (uint64_t)limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, KVO_DEV_TIMEOUT);
                 return false;
             }
         }
+    }
+}
+
+// Bounded wait that ignores the abort flag (a warp's drain before it exits).
+__device__ __forceinline__ void att_drain_wait(uint32_t mbar, uint32_t parity, long long limit_ns) {
+    if (mbar_try_wait(mbar, parity)) return;
+    const uint64_t t0 = global_ns();
+    for (int it = 0;; ++it) {
+        if (mbar_try_wait(mbar, parity)) return;
+        if ((it & 63) == 63 && global_ns() - t0 > (uint64_t)limit_ns) return;
     }
 }
 
@@ -614,12 +627,14 @@ __device__ __forceinline__ int cursor_slot(const AttnCursor& c, const int32_t* _
 }
 
 // Copy the cursor's tile into a stage: lane j copies row j & 15 of the K tile
-// (j < 16) or of the V tile (j >= 16); `sl` is the lane's cursor_slot.
+// (j < 16) or of the V tile (j >= 16); `sl` is the lane's cursor_slot.  With
+// `skip` the stage is announced but nothing is copied, so its barrier never
+// completes (the bounded-wait test).
 template <int D>
 __device__ __forceinline__ void tile_copy(const AttnCursor& c, int sl, unsigned char* stage, uint32_t fb,
                                           const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
                                           const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv, int k,
-                                          int B, int Wcap, int& bad) {
+                                          int B, int Wcap, int& bad, bool skip) {
     const int lane = threadIdx.x & 31, kv = lane >> 4, row = lane & 15;
     const int tb = (c.tile0 + c.tl) * ATT_TILE;
     const int rows = min(ATT_TILE, c.n_tok - tb);
@@ -642,7 +657,7 @@ __device__ __forceinline__ void tile_copy(const AttnCursor& c, int sl, unsigned 
         start = valid && (row == 0 || sw == 0);
     }
     const unsigned starts = (__ballot_sync(0xffffffffu, start) >> (kv * 16)) & 0xffffu;
-    if (start) {
+    if (start && !skip) {
         const unsigned later = starts & ~((2u << row) - 1u);
         const int next = later ? __ffs(later) - 1 : rows;
         bulk_load(smem_u32(stage + kv * (ATT_TILE * D * 2) + row * D * 2), src, (uint32_t)((next - row) * D * 2),
@@ -661,7 +676,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
                 float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec, int fuse, int batch, int r,
                 int Hkv, int k, int B, int W, int Wcap, const int32_t* __restrict__ w_start,
                 const int32_t* __restrict__ w_len, const int32_t* __restrict__ sp_cnt, int dep_wait,
-                float scale_log2, int32_t* __restrict__ status) {
+                float scale_log2, int32_t* __restrict__ status, long long wait_ns, int skip_tile) {
     using WA = WarpAttn<D, NR>;
     using CF = AttnTmaCfg<D, NR>;
     constexpr int CH = WA::CH, CPT = WA::CPT, STG = CF::STG;
@@ -697,9 +712,10 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     int isl = cursor_slot(ic, slot, k, B, row);
     int64_t nissue = 0, ncons = 0;
     auto issue = [&]() {
-        if (ic.item >= ic.hi) return;
+        if (ic.item >= ic.hi || *s_abort) return;       // nothing more is issued once the CTA gave up
         const int st = (int)(nissue % STG);
-        tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad);
+        tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad,
+                     blockIdx.x == 0 && warp == 0 && nissue == skip_tile);
         ++nissue;
         cursor_next(ic, warp, src);
         isl = cursor_slot(ic, slot, k, B, row);
@@ -730,7 +746,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
         if (item + 1 < hi) fetch(item + 1);
         for (int tl = warp; tl < cc.nt; tl += ATT_WARPS) {
             const int st = (int)(ncons % STG);
-            if (!*s_abort) att_wait(smem_u32(&wfull[st]), (uint32_t)((ncons / STG) & 1), s_abort, status);
+            if (!*s_abort) att_wait(smem_u32(&wfull[st]), (uint32_t)((ncons / STG) & 1), s_abort, status, wait_ns);
             ++ncons;
             const int tb = (cc.tile0 + tl) * ATT_TILE;
             const int rows = min(ATT_TILE, cc.n_tok - tb);
@@ -764,6 +780,15 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
                              out_lse, out_o_spec, out_lse_spec, fuse, batch, r, Hkv, cc.bg, nrows, item, NTHR);
     }
     if (bad) atomicOr(status, bad);
+    // Before the warp exits, every copy it issued has landed: without an abort
+    // it waited for each; after one it may have stopped waiting, so it checks
+    // -- with bounded waits -- its last STG copies, the only ones that can
+    // still be in flight, and no bulk copy is left writing into the shared
+    // memory of a CTA that has finished.
+    if (lane == 0)
+        for (int64_t s2 = nissue > STG ? nissue - STG : 0; s2 < nissue; ++s2)
+            att_drain_wait(smem_u32(&wfull[s2 % STG]), (uint32_t)((s2 / STG) & 1), wait_ns);
+    __syncwarp();
     // launched as a programmatic dependent: this grid completes only after the
     // grid it depends on, so the launches behind it see that grid's writes
     if (dep_wait && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -815,7 +840,8 @@ static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, con
                               (const int4*)pl.items, (const int32_t*)pl.cta, (const int32_t*)pl.first,
                               (const int32_t*)pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec,
                               lse_spec, fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, (const int32_t*)c.g_wstart,
-                              (const int32_t*)c.g_wlen, sp_cnt, pdl ? 1 : 0, scale_log2, c.status);
+                              (const int32_t*)c.g_wlen, sp_cnt, pdl ? 1 : 0, scale_log2, c.status,
+                              (long long)c.att_wait_ns, c.att_skip_tile);
 }
 
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,

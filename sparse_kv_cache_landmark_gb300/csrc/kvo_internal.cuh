@@ -113,6 +113,8 @@ struct Ctx {
         int32_t* first = nullptr;   // [G] first item of each group
         int32_t* count = nullptr;   // [G] items of each group
     } tma[2];
+    long long att_wait_ns = 2000000000LL;   // limit of each mbarrier wait of the TMA-staged kernel
+    int att_skip_tile = -1;         // >= 0: CTA 0 announces this tile without copying it (wait test)
     float* att_part_o = nullptr;    // [items][r][d]
     float* att_part_ml = nullptr;   // [items][r][2]
     uint32_t* att_done = nullptr;   // [G]

@@ -1180,6 +1180,18 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas) {
     return build_tma_plans(ctx->c);
 }
 
+kvo_status kvo_set_wait_test(kvo_ctx* ctx, int64_t limit_ns, int skip_tile) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (limit_ns < 1000000 || limit_ns > 10000000000LL || skip_tile < -1)
+        return fail(&c, KVO_ERR_INVALID, "need 1 ms <= limit_ns <= 10 s and skip_tile >= -1");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    drop_graphs(c);
+    c.att_wait_ns = limit_ns;
+    c.att_skip_tile = skip_tile;
+    return KVO_OK;
+}
+
 kvo_status kvo_profile(kvo_ctx* ctx, int enable) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;

@@ -25,7 +25,7 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
            "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched",
-           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention"]
+           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention", "kvo_set_wait_test"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention", "recon"]
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_prefetch_budget.argtypes = [P, I]
         L.kvo_set_lowrank_keys.argtypes = [P, I, I, VP, VP]
         L.kvo_append.argtypes = [P, VP, VP, VP]
+        L.kvo_set_wait_test.argtypes = [P, ctypes.c_int64, I]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
         L.kvo_last_error.argtypes = [P]
@@ -381,6 +382,10 @@ class Context:
         """Attention kernel: 0 register-direct loads, 1 TMA-staged persistent with
         ``ctas`` CTAs (0: as many as fit) (C: kvo_set_attn_impl)."""
         self._c(lib().kvo_set_attn_impl(self.ctx, impl, ctas))
+
+    def set_wait_test(self, limit_ns: int = 2_000_000_000, skip_tile: int = -1):
+        """Bounded-wait test switch of the TMA-staged attention (C: kvo_set_wait_test)."""
+        self._c(lib().kvo_set_wait_test(self.ctx, int(limit_ns), int(skip_tile)))
 
     def set_gather_reserve(self, smem_bytes: int):
         self._c(lib().kvo_set_gather_reserve(self.ctx, smem_bytes))

@@ -81,7 +81,9 @@ class Case:
 def assert_attn_close(got, ref, atol=1e-2, rtol=1e-2, what="o"):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    err = np.abs(got - ref)
+    same = got == ref                      # equal values, including equal infinities (an empty part's lse)
+    with np.errstate(invalid="ignore"):
+        err = np.where(same, 0.0, np.abs(got - ref))
     bound = atol + rtol * np.abs(ref)
-    bad = err > bound
+    bad = ~(err <= bound)                  # NaN in either never passes
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside {atol}+{rtol}|ref|; max err {err.max():.3e}"
