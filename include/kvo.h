@@ -495,7 +495,7 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
  * The tiles (16 tokens) of every group -- its sparse part of sparse_tokens
  * (k * block_size), then its window part of window_tokens (W, or W + B - 1
  * when the cache grows) -- are laid out group after group and split into
- * `grid` contiguous ranges of equal cost (a tile costs 1, entering a part 3
+ * `grid` contiguous ranges of equal cost (a tile costs 1, entering a part 12
  * more: the work-item epilogue), range bounds rounded down to a multiple of
  * the CTA's 4 warps; each range is cut at part boundaries into work items.
  *   n_groups: b * Hkv.  grid: CTAs asked for; the plan uses min(grid, tiles).

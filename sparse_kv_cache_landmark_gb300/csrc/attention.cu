@@ -720,8 +720,31 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
         cursor_next(ic, warp, src);
         isl = cursor_slot(ic, slot, k, B, row);
     };
+    // prologue: the cursors of the warp's first STG tiles, then their slot
+    // loads side by side, then the copies -- rather than STG issues that each
+    // wait for the slot load the previous one started (the launch ramp)
+    {
+        AttnCursor pc[STG];
+        int ps[STG];
+        pc[0] = ic;
 #pragma unroll
-    for (int i = 0; i < STG; ++i) issue();
+        for (int i = 1; i < STG; ++i) {
+            pc[i] = pc[i - 1];
+            cursor_next(pc[i], warp, src);
+        }
+#pragma unroll
+        for (int i = 0; i < STG; ++i) ps[i] = cursor_slot(pc[i], slot, k, B, row);
+#pragma unroll
+        for (int i = 0; i < STG; ++i) {
+            if (pc[i].item >= pc[i].hi || *s_abort) break;
+            tile_copy<D>(pc[i], ps[i], ring + i * CF::STAGE_BYTES, smem_u32(&wfull[i]), bk, bv, wk, wv, k, B, Wcap,
+                         bad, blockIdx.x == 0 && warp == 0 && nissue == skip_tile);
+            ++nissue;
+        }
+        ic = pc[STG - 1];
+        cursor_next(ic, warp, src);
+        isl = cursor_slot(ic, slot, k, B, row);
+    }
 
     // the next item's fields and Q words, fetched one item ahead
     const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;

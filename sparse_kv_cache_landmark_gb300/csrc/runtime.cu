@@ -85,7 +85,10 @@ int64_t plan_tma_items(int G, int sp_tokens, int w_tokens, int64_t grid, std::ve
     items.clear();
     cta.assign(grid + 1, 0);
     // parts in tile order with their first tile and first cost unit
-    constexpr int64_t kItemCost = 3;     // epilogue of a work item, in tiles (measured ~7K vs ~2.4K cycles)
+    // epilogue of a work item, in tiles: per-CTA timing on the Llama-shaped
+    // layer put it at ~4.4 us, the time of ~12 tiles (partial write, ticket
+    // round trip, group merge)
+    constexpr int64_t kItemCost = 12;
     std::vector<int64_t> p_t0, p_c0, p_len;
     int64_t cost = 0;
     for (int g = 0; g < G; ++g)

@@ -4,7 +4,7 @@ Properties every plan must have, whatever the shape: the work items cover
 each group's sparse tiles and then its window tiles exactly once, in order;
 no item crosses a part boundary; the CTA ranges are contiguous, in order and
 start on a multiple of the CTA's 4 warps; and no range costs much more than
-an equal share (a tile costs 1, a work-item epilogue 3).
+an equal share (a tile costs 1, a work-item epilogue 12).
 """
 import random
 
@@ -13,7 +13,7 @@ import pytest
 from sparse_kv_cache_landmark_gb300 import kvo
 from sparse_kv_cache_landmark_gb300.kvo import KvoError
 
-TILE, WARPS, ITEM_COST = 16, 4, 3
+TILE, WARPS, ITEM_COST = 16, 4, 12
 
 
 def _check_plan(G, sp_tok, w_tok, grid):
@@ -49,7 +49,7 @@ def _check_plan(G, sp_tok, w_tok, grid):
         assert start % WARPS == 0
         cost = sum(n + ITEM_COST for *_, n in rng)
         # rounding a bound down to the warp multiple moves it by < 4 tiles, each of
-        # which may start a part (1 + 3 each); plus one item that continues a part
+        # which may start a part (1 + ITEM_COST each); plus one item that continues a part
         # (its epilogue is not among the split's cost points) and integer division
         slack = (WARPS - 1) * (1 + ITEM_COST) + ITEM_COST + 1
         assert cost <= share + slack, (G, sp_tok, w_tok, grid, j, cost, share)
