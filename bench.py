@@ -95,7 +95,8 @@ def parse(argv=None):
     ap.add_argument("--prefetch-budget", type=int, default=-1,
                     help="with --resident: prefetch fetches admitted per group, layer and step (-1: all)")
     ap.add_argument("--spec-policy", type=int, default=-1,
-                    help="with --resident 1: 1 prefetches a layer's prediction only while it pays (-1: default)")
+                    help="with --resident 1: 1 prefetches a layer's prediction only while it pays (the default "
+                         "here), 0 always")
     ap.add_argument("--trace", default="",
                     help="write the launch trace (kind, layer, start, end) of one profiled step to this JSON file")
     return ap.parse_args(argv)
@@ -572,8 +573,8 @@ def build_workload(args, ws=1, numa_node=None):
         B.ctx.set_attn_impl(args.attn_impl, args.attn_ctas)
     if args.resident and args.prefetch_budget >= 0:
         B.ctx.set_prefetch_budget(args.prefetch_budget)
-    if args.resident and args.spec_policy >= 0:
-        B.ctx.set_spec_policy(args.spec_policy)
+    if args.resident == 1:      # speculation only while it pays, unless asked otherwise
+        B.ctx.set_spec_policy(1 if args.spec_policy < 0 else args.spec_policy)
     B.recon_rank = 0
     if w.key_dist == "lowrank" and args.reconstruct != 0:
         # GPU-resident low-rank key factors, packed like the host K (layers past n_host reuse l % n_host)
@@ -791,6 +792,13 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
     t_ms, prof = time_steps(Bw, steps, ws, profile=not graphs)
     m["clocks"] = clocks.stop()
     m["fetched"] = ctx.resident_fetched(reset=True) if args.resident else None
+    m["spec"] = None
+    if args.resident == 1:
+        st = ctx.spec_stats()
+        m["spec"] = {"prefetched_blocks": sum(x[0] for x in st), "used_blocks": sum(x[1] for x in st),
+                     "layers_prefetching": sum(x[2] for x in st), "layers": len(st),
+                     "note": "since init, warm-up included: speculative blocks fetched and those a later true "
+                             "index used"}
     if graphs:
         ctx.set_graphs(False)
         for _ in range(2):
@@ -1047,10 +1055,11 @@ def run_ours(args):
                 "speculation": args.resident == 1,
                 "drift": SPEC_SIGMA_88 / math.sqrt(2.0) if args.drift < 0 else args.drift,
                 "query_steps": args.query_steps, "prefetch_budget": args.prefetch_budget,
-                "spec_policy": args.spec_policy,
+                "spec_policy": ("adaptive" if args.spec_policy != 0 else "always") if args.resident == 1 else None,
                 "fetched_blocks_per_step": fetched_step,
                 "fetched_of_selected": fetched_step / (w.n_layers * w.batch * w.n_kv_heads * w.top_k),
                 "urgent_blocks_per_step": fetched[0] / args.steps, "prefetch_blocks_per_step": fetched[1] / args.steps,
+                "speculation_counters": head["spec"],
                 "note": "cross-step delta prefetch: per-layer resident sets of 2k blocks; host bytes = fetched blocks"},
         }
         print(json.dumps(line), flush=True)

@@ -373,6 +373,31 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
 kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks);
 
 /*
+ * kvo_set_spec_policy -- when the speculative prefetch runs (resident = 1,
+ * steps with a speculative query).  mode 0 (default): every layer prefetches
+ * its prediction for the next step.  mode 1: per layer, only while it pays.
+ * The resident assign kernel counts, per layer, the blocks its prefetch phase
+ * fetched and those of them a later true index used; a used prefetch saves an
+ * urgent fetch, an unused one costs a fetch, so prefetching lowers the host
+ * bytes only while more than half of the prefetched blocks are used.  The
+ * decision is taken on the GPU, in stream order, by the last CTA of each
+ * layer's urgent assign: a layer whose prefetches were used less over a window
+ * of 4 steps fetches nothing in its prefetch phase for the next 32 steps, then
+ * tries again (the rest doubles after every try that fails, up to 1024 steps,
+ * and returns to 32 after a window that pays).  Outputs never depend on the policy (a block the true index
+ * needs is fetched urgently when missing).
+ * Synchronizes the context's streams.  Errors: KVO_ERR_STATE with
+ * resident = 0; KVO_ERR_INVALID for a mode outside 0..1.
+ *
+ * kvo_spec_stats -- synchronize, then write per layer l to host out3[3 l ..]:
+ * blocks prefetched since init, prefetched blocks a true index used, and 1 if
+ * the layer's prefetch phase is on (always 1 with mode 0).
+ * Errors: KVO_ERR_STATE with resident = 0; KVO_ERR_INVALID for a null output.
+ */
+kvo_status kvo_set_spec_policy(kvo_ctx* ctx, int mode);
+kvo_status kvo_spec_stats(kvo_ctx* ctx, int64_t* out3);
+
+/*
  * kvo_set_lowrank_keys -- rebuild the keys of a layer's missed blocks on the
  * GPU instead of fetching them (DualDecoder §5.3: low-rank key reconstruction
  * from a GPU-resident low-rank key cache; only the values of missed blocks

@@ -66,6 +66,13 @@ struct Ctx {
     unsigned long long* res_fetched = nullptr;   // [2] blocks fetched: urgent, prefetch
     std::vector<char> res_pending;  // [L] a prefetch into the layer's set was issued and not yet waited for
     int res_budget = -1;            // prefetch fetches admitted per group, layer and step (-1: all)
+    // speculation policy: 0 prefetch every layer's prediction; 1 per layer, only
+    // while its prefetches pay (kvo_set_spec_policy)
+    int spec_policy = 0;
+    uint8_t* res_pfbit = nullptr;             // [L][G][2k] slot filled by a prefetch, not used yet
+    unsigned long long* res_stat = nullptr;   // [L][2] blocks prefetched, prefetched blocks used (since init)
+    unsigned long long* res_pol = nullptr;    // [L][8] policy state: on, steps, window fetched, window used, rest
+    uint32_t* res_pol_ticket = nullptr;       // [L] last-CTA tickets of the policy update (zero between launches)
     // chain steps: attention over the blocks resident already (and the window)
     // beside the urgent copies, then over the fetched ones, merged by lse
     int32_t* res_hit_slot = nullptr;  // [G][k] slots of the hits, in index order

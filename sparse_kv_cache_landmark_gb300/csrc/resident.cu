@@ -38,12 +38,33 @@ __device__ __forceinline__ bool sorted_contains(const int32_t* a, int n, int32_t
 // (a cap on host bytes, used for the prefetch phase only; "PulseInfer and the
 // I/O Problem Behind Long-Context Decoding", §2: I/O-adaptive offloading
 // admission, given there without a rule).
+//
+// Speculation accounting (pfbit, stat; nullable): a slot filled by the
+// prefetch phase is marked until a true index uses it; stat[0] counts the
+// blocks the prefetch phase fetched, stat[1] the marked blocks an urgent phase
+// found in its true index -- a speculative fetch that saved an urgent one.
+//
+// Speculation policy (pol, ticket; nullable): pol = {on, steps, fetched,
+// used, rest} of the layer's current window.  A used prefetch saves an urgent
+// fetch, an unused one costs a fetch, so prefetching pays while more than half
+// of the prefetched blocks are used.  The last CTA of an urgent phase (atomic
+// ticket) closes a window of KVO_SPEC_WINDOW steps: a layer whose window failed
+// that test stops prefetching for `rest` steps and then tries again; rest
+// starts at KVO_SPEC_REST, doubles with every failed try (up to KVO_SPEC_REST_MAX)
+// and returns to KVO_SPEC_REST after a window that paid.  A prefetch phase of a layer
+// that is off fetches nothing.  Both phases of a layer run in stream order, so
+// the state needs no other synchronisation.
+#define KVO_SPEC_WINDOW 4ull
+#define KVO_SPEC_REST 32ull
+#define KVO_SPEC_REST_MAX 1024ull
 __global__ void __launch_bounds__(RES_THREADS)
 resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restrict__ keep,
                        int32_t* __restrict__ map, int32_t* __restrict__ slots, const int32_t* __restrict__ g_C,
                        int32_t* __restrict__ out_ids, int32_t* __restrict__ out_cnt, int32_t* __restrict__ out_dslot,
                        int32_t* __restrict__ slot_of, int32_t* __restrict__ hit_slot, int32_t* __restrict__ hit_cnt,
                        unsigned long long* __restrict__ fetched, int k, int cap, int Ccap, int max_fetch,
+                       uint8_t* __restrict__ pfbit, unsigned long long* __restrict__ stat, int phase,
+                       unsigned long long* __restrict__ pol, uint32_t* __restrict__ ticket,
                        int32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t rs[];
     int32_t* s_need = rs;                  // [k]
@@ -56,6 +77,7 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
     const int C = min(g_C[g], Ccap);
     int32_t* mg = map + (int64_t)g * Ccap;
     int32_t* sg = slots + (int64_t)g * cap;
+    uint8_t* pg = pfbit ? pfbit + (int64_t)g * cap : nullptr;
     int bad = 0;
     for (int i = tid; i < k; i += nt) {
         s_need[i] = need[(int64_t)g * k + i];
@@ -82,12 +104,21 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
     // 2. missing need entries (contiguous chunks keep the ascending order)
     const int pk = (k + nt - 1) / nt;
     const int i0 = min(k, tid * pk), i1 = min(k, i0 + pk);
-    uint32_t nm = 0;
+    uint32_t nm = 0, used = 0;
     for (int i = i0; i < i1; ++i) {
         const int32_t x = s_need[i];
         if (x < 0 || x >= C) { bad |= KVO_DEV_BAD_BLOCK_ID; continue; }
-        nm += mg[x] < 0 ? 1u : 0u;
+        const int32_t sx = mg[x];
+        nm += sx < 0 ? 1u : 0u;
+        // a true index meeting a block the prefetch phase fetched (need entries
+        // are distinct, so no two threads touch one slot)
+        if (phase == 0 && pg && sx >= 0 && pg[sx]) {
+            ++used;
+            pg[sx] = 0;
+        }
     }
+    if (stat && used) atomicAdd(stat + 1, (unsigned long long)used);
+    if (pol && used) atomicAdd(pol + 3, (unsigned long long)used);
     base = block_exclusive_scan(nm, warp_sums, &s_tot);
     const uint32_t n_miss = s_tot;
     for (int i = i0; i < i1; ++i) {
@@ -108,7 +139,9 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
         if (tid == 0) hit_cnt[g] = (int32_t)s_tot;
     }
     __syncthreads();
-    // admission: at most max_fetch fetches (lowest ids first) when max_fetch >= 0
+    // admission: at most max_fetch fetches (lowest ids first) when max_fetch >= 0;
+    // none when the speculation policy has switched the layer's prefetch off
+    if (phase == 1 && pol && *(volatile unsigned long long*)pol == 0ull) max_fetch = 0;
     const uint32_t wanted = max_fetch >= 0 ? min(n_miss, (uint32_t)max_fetch) : n_miss;
     const int n_fetch = (int)min(wanted, n_ev);
     if (wanted > n_ev && tid == 0) bad |= KVO_DEV_BAD_COUNT;
@@ -123,6 +156,7 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
         const int32_t x = s_mid[j], s = s_ev[j];
         mg[x] = s;
         sg[s] = x;
+        if (pg) pg[s] = phase == 1 ? 1 : 0;
         out_ids[(int64_t)g * k + j] = x;
         out_dslot[(int64_t)g * k + j] = s;
     }
@@ -138,6 +172,40 @@ resident_assign_kernel(const int32_t* __restrict__ need, const int32_t* __restri
     if (tid == 0) {
         out_cnt[g] = n_fetch;
         if (fetched && n_fetch) atomicAdd(fetched, (unsigned long long)n_fetch);
+        if (phase == 1 && stat && n_fetch) atomicAdd(stat, (unsigned long long)n_fetch);
+        if (phase == 1 && pol && n_fetch) atomicAdd(pol + 2, (unsigned long long)n_fetch);
+    }
+    if (phase == 0 && pol) {
+        // the CTA's counts reach thread 0 through the barrier; its release fence
+        // orders them before the ticket, the last CTA's acquire fence after it
+        __syncthreads();
+        if (tid == 0) {
+            fence_acq_rel_gpu();
+            if (atomicAdd(ticket, 1u) + 1 == gridDim.x) {
+                fence_acq_rel_gpu();
+                volatile unsigned long long* v = pol;
+                const unsigned long long steps = v[1] + 1;
+                const unsigned long long rest = v[4] ? v[4] : KVO_SPEC_REST;
+                if (v[0]) {
+                    if (steps >= KVO_SPEC_WINDOW) {
+                        if (v[2] > 0 && 2 * v[3] < v[2]) {
+                            v[0] = 0;                                   // off for `rest` steps
+                        } else {
+                            v[4] = KVO_SPEC_REST;                       // a window that paid
+                        }
+                        v[1] = 0; v[2] = 0; v[3] = 0;
+                    } else {
+                        v[1] = steps;
+                    }
+                } else if (steps >= rest) {
+                    v[0] = 1; v[1] = 0; v[2] = 0; v[3] = 0;             // try again; rest doubles if it fails
+                    v[4] = rest * 2 < KVO_SPEC_REST_MAX ? rest * 2 : KVO_SPEC_REST_MAX;
+                } else {
+                    v[1] = steps;
+                }
+                *ticket = 0u;
+            }
+        }
     }
     if (bad) atomicOr(status, bad);
 }
@@ -157,7 +225,10 @@ cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need,
     resident_assign_kernel<<<c.G, RES_THREADS, res_smem(c), s>>>(
         need, keep, c.res_map + (size_t)layer * c.G * c.Cmax, c.res_slots + (size_t)layer * c.G * cap, c.g_C,
         out_ids, out_cnt, out_dslot, slot_of, hit_slot, hit_cnt, c.res_fetched + phase, c.k, cap, c.Cmax, max_fetch,
-        c.status);
+        c.res_pfbit ? c.res_pfbit + (size_t)layer * c.G * cap : nullptr,
+        c.res_stat ? c.res_stat + 2 * (size_t)layer : nullptr, phase,
+        (c.spec_policy == 1 && c.res_pol) ? c.res_pol + 8 * (size_t)layer : nullptr,
+        c.res_pol_ticket ? c.res_pol_ticket + layer : nullptr, c.status);
     return cudaGetLastError();
 }
 

@@ -178,7 +178,7 @@ void free_ctx(kvo::Ctx& c) {
     for (void* p : c.res_k) F(p);
     for (void* p : c.res_v) F(p);
     F(c.res_map); F(c.res_slots); F(c.res_dslot); F(c.res_pf_ids); F(c.res_pf_cnt); F(c.res_pf_dslot);
-    F(c.res_fetched); F(c.res_hit_slot); F(c.res_hit_cnt); F(c.res_oA); F(c.res_lA); F(c.mp_part_o); F(c.mp_part_ml); F(c.mp_done);
+    F(c.res_fetched); F(c.res_pfbit); F(c.res_stat); F(c.res_pol); F(c.res_pol_ticket); F(c.res_hit_slot); F(c.res_hit_cnt); F(c.res_oA); F(c.res_lA); F(c.mp_part_o); F(c.mp_part_ml); F(c.mp_done);
     F(c.sel_keys); F(c.sel_hist); F(c.sel_done); F(c.sel_items); F(c.sel_nchunks);
     F(c.runs); F(c.nruns);
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
@@ -372,6 +372,13 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * rows * c.d, &sb));
         KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * rows, &sb));
         KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
+        KVO_CUDA(&c, dalloc(&c.res_pfbit, (size_t)c.L * c.G * 2 * c.k, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_stat, sizeof(unsigned long long) * 2 * c.L, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_pol, sizeof(unsigned long long) * 8 * c.L, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_pol_ticket, sizeof(uint32_t) * c.L, &sb));
+        KVO_CUDA(&c, cudaMemsetAsync(c.res_pfbit, 0, (size_t)c.L * c.G * 2 * c.k, c.s_compute));
+        KVO_CUDA(&c, cudaMemsetAsync(c.res_stat, 0, sizeof(unsigned long long) * 2 * c.L, c.s_compute));
+        KVO_CUDA(&c, cudaMemsetAsync(c.res_pol_ticket, 0, sizeof(uint32_t) * c.L, c.s_compute));
         c.res_pending.assign(c.L, 0);
         KVO_CUDA(&c, kvo::prepare_resident(c));
     }
@@ -850,7 +857,8 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
                                          lse_spec ? lse_spec + l * lse_layer : nullptr, 1, sc, !alone_step);
         }));
         if (!alone_step) KVO_CUDA(&c, cudaEventRecord(E.attn[l], sc));
-        // 5. prefetch of the next step's prediction, sparing T
+        // 5. prefetch of the next step's prediction, sparing T (with the adaptive
+        // policy the assign fetches nothing while the layer's prefetches do not pay)
         if (q_spec) {
             int32_t* pids = c.res_pf_ids + l * gk;
             int32_t* pcnt = c.res_pf_cnt + (size_t)l * c.G;
@@ -1082,6 +1090,39 @@ kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks) {
     if (blocks < -1) return fail(&c, KVO_ERR_INVALID, "blocks must be >= -1");
     for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     c.res_budget = blocks;
+    return KVO_OK;
+}
+
+kvo_status kvo_set_spec_policy(kvo_ctx* ctx, int mode) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
+    if (mode < 0 || mode > 1) return fail(&c, KVO_ERR_INVALID, "mode must be 0 or 1");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph})
+        KVO_CUDA(&c, cudaStreamSynchronize(s));
+    drop_graphs(c);
+    // every layer starts a fresh window with its prefetch on
+    std::vector<unsigned long long> init(8 * (size_t)c.L, 0ull);
+    for (int l = 0; l < c.L; ++l) init[8 * l] = 1;
+    KVO_CUDA(&c, cudaMemcpy(c.res_pol, init.data(), sizeof(unsigned long long) * 8 * c.L, cudaMemcpyHostToDevice));
+    c.spec_policy = mode;
+    return KVO_OK;
+}
+
+kvo_status kvo_spec_stats(kvo_ctx* ctx, int64_t* out3) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
+    if (!out3) return fail(&c, KVO_ERR_INVALID, "null output");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    std::vector<unsigned long long> h(2 * (size_t)c.L), p(8 * (size_t)c.L);
+    KVO_CUDA(&c, cudaMemcpy(h.data(), c.res_stat, sizeof(unsigned long long) * 2 * c.L, cudaMemcpyDeviceToHost));
+    KVO_CUDA(&c, cudaMemcpy(p.data(), c.res_pol, sizeof(unsigned long long) * 8 * c.L, cudaMemcpyDeviceToHost));
+    for (int l = 0; l < c.L; ++l) {
+        out3[3 * l + 0] = (int64_t)h[2 * l];
+        out3[3 * l + 1] = (int64_t)h[2 * l + 1];
+        out3[3 * l + 2] = c.spec_policy == 1 ? (p[8 * l] ? 1 : 0) : 1;
+    }
     return KVO_OK;
 }
 

@@ -25,7 +25,8 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
            "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched",
-           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention", "kvo_set_wait_test"]
+           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention", "kvo_set_wait_test",
+           "kvo_set_spec_policy", "kvo_spec_stats"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention", "recon"]
 
 
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_lowrank_keys.argtypes = [P, I, I, VP, VP]
         L.kvo_append.argtypes = [P, VP, VP, VP]
         L.kvo_set_wait_test.argtypes = [P, ctypes.c_int64, I]
+        L.kvo_set_spec_policy.argtypes = [P, I]
+        L.kvo_spec_stats.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
         DP, IP = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32)
         L.kvo_profile_trace.argtypes = [P, DP, DP, IP, IP, I, ctypes.POINTER(ctypes.c_int)]
         L.kvo_last_error.argtypes = [P]
@@ -371,6 +374,16 @@ class Context:
     def set_prefetch_budget(self, blocks: int):
         """Cap prefetch fetches per group, layer and step (-1: no cap) (C: kvo_set_prefetch_budget)."""
         self._c(lib().kvo_set_prefetch_budget(self.ctx, blocks))
+
+    def set_spec_policy(self, mode: int):
+        """0: prefetch every layer's prediction; 1: per layer, only while it pays (C: kvo_set_spec_policy)."""
+        self._c(lib().kvo_set_spec_policy(self.ctx, int(mode)))
+
+    def spec_stats(self):
+        """Per layer (blocks prefetched, prefetched blocks used, prefetch on) (C: kvo_spec_stats)."""
+        out = (ctypes.c_int64 * (3 * self.n_layers))()
+        self._c(lib().kvo_spec_stats(self.ctx, out))
+        return [(int(out[3 * l]), int(out[3 * l + 1]), int(out[3 * l + 2])) for l in range(self.n_layers)]
 
     def resident_fetched(self, reset: bool = False):
         """(urgent, prefetch) blocks fetched since init or the last reset (C: kvo_resident_fetched)."""

@@ -176,3 +176,69 @@ def test_resident_calls_need_resident_mode():
             c.ctx.set_prefetch_budget(4)
     finally:
         c.close()
+
+
+def test_adaptive_speculation_stops_when_prefetches_do_not_pay():
+    """With a speculative query that predicts badly (noise 1.0), prefetching
+    every step's prediction moves more host bytes than fetching only the
+    misses.  The adaptive policy counts, per layer, how many prefetched blocks
+    a later true index used and stops prefetching a layer whose prefetches are
+    used less than half the time, so it must recover most of that waste --
+    while every output still matches the oracle (the true index is always
+    completed by urgent fetches)."""
+    steps, drift, seed = 24, 0.15, 77
+    n = 32 + 16 * 64
+    w = Workload("spec_policy", 2, 8, 2, 128, 16, 16, 32, 2, (n, n), spec_sigma=1.0)
+    r, G = w.group_size, w.batch * w.n_kv_heads
+    totals, final = {}, {}
+    for mode in ("always", "adaptive", "none"):
+        c = Case(w, seed, gen_device="cpu", resident=True)
+        try:
+            if mode == "adaptive":
+                c.ctx.set_spec_policy(1)
+            # the last step's true query gets its selection margin (its outputs are compared)
+            att = []
+            for l in range(w.n_layers):
+                a = np.zeros((w.batch, w.n_kv_heads), dtype=np.int64)
+                for b in range(w.batch):
+                    for g in range(w.n_kv_heads):
+                        C = (c.lens[b] - w.window) // w.block_size
+                        lm = orc.landmarks(synth.bits(c.rows(l, b, g)), w.block_size, C)
+                        for t in range(300):
+                            qg, _ = synth.gen_group_query_step(w, seed, l, b, g, steps - 1, drift, t)
+                            if orc.kth_relative_gap(orc.block_scores(synth.bits(qg), lm), w.top_k) >= MARGIN:
+                                a[b, g] = t
+                                break
+                        else:
+                            raise AssertionError("no attempt with a margin")
+                att.append(a)
+            for s in range(steps):
+                qq = [synth.gen_queries_step(w, seed, l, s, drift, att[l]) for l in range(w.n_layers)]
+                q = torch.stack([x[0] for x in qq]).cuda().contiguous()
+                qs = None if mode == "none" else torch.stack([x[1] for x in qq]).cuda().contiguous()
+                o, lse = c.ctx.decode_step(q, qs)
+                torch.cuda.synchronize()
+                assert c.ctx.device_status() == 0
+            totals[mode] = sum(c.ctx.resident_fetched())
+            if mode != "none":
+                final[mode] = c.ctx.spec_stats()
+            o, lse = o.cpu().numpy(), lse.cpu().numpy()
+            for l in range(w.n_layers):
+                for b in range(w.batch):
+                    for g in range(w.n_kv_heads):
+                        qg = synth.bits(qq[l][0][b, g * r:(g + 1) * r])
+                        ref = orc.decode_group(synth.bits(c.rows(l, b, g, "k")), synth.bits(c.rows(l, b, g, "v")),
+                                               qg, None, block_size=w.block_size, top_k=w.top_k, window=w.window)
+                        rows = slice(b * w.n_q_heads + g * r, b * w.n_q_heads + (g + 1) * r)
+                        assert_attn_close(o[l, rows], ref.o, what=f"o {mode} layer {l}")
+                        assert_attn_close(lse[l, rows], ref.lse, what=f"lse {mode} layer {l}")
+        finally:
+            c.close()
+    # bad predictions: always prefetching costs host bytes; the counters say so
+    assert totals["always"] > totals["none"]
+    for pf, used, _ in final["always"]:
+        assert pf > 0 and 2 * used < pf
+    # the adaptive policy recovers most of the waste
+    waste = totals["always"] - totals["none"]
+    assert totals["adaptive"] <= totals["none"] + 0.6 * waste, totals
+    assert any(on == 0 for *_, on in final["adaptive"]) or totals["adaptive"] < totals["always"]
