@@ -482,7 +482,14 @@ kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll)
  * the decode step then skips building run lists.  Engine 3 is the default:
  * 38 CTAs x 1024 threads, 2 loads of K and of V in flight per lane, 200 KiB of
  * shared memory reserved per CTA so each gather CTA has an SM to itself.
+ * engine 4: the copy engine -- the run list is read back to pinned host
+ * memory (the call synchronizes its stream for it) and every run becomes one
+ * cudaMemcpyAsync of K and one of V on the stream, issued by the host: no SM
+ * moves a byte, but the host issues two calls per run and waits for the run
+ * list inside each gather (so decode steps with engine 4 are never captured
+ * into graphs; kvo_set_graphs(1) then fails with KVO_ERR_STATE).
  * Selecting an engine resets the launch shape to that engine's default.
+ * Resident sets (resident = 1) always copy with engine 3.
  */
 kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers);
 

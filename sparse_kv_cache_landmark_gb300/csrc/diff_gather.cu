@@ -355,9 +355,51 @@ int gather_default_ctas(const Ctx& c) {
     return c.gather_ctas > 0 ? c.gather_ctas : 2 * 152;
 }
 
+__global__ void status_or_kernel(int32_t* status, int bits) { atomicOr(status, bits); }
+
+// Copy engine: the run list is read back to the host (the stream is
+// synchronised for it), then every run becomes one cudaMemcpyAsync of K and
+// one of V from the pinned host cache into the buffer's slots, on the stream.
+// No SM takes part in moving the bytes; the host issues one call per copy.
+// A run outside the group's blocks or the buffer's slots is skipped and
+// reported in the device status word.
+static cudaError_t gather_copy_engine(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
+                                      cudaStream_t s) {
+    if (!c.h_runs || !c.h_nruns || c.h_off.size() != (size_t)c.G) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemcpyAsync(c.h_nruns, nruns, sizeof(int32_t) * c.G, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(c.h_runs, runs, sizeof(int32_t) * 4 * (size_t)c.G * c.k, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    const int64_t blk = (int64_t)c.B * c.d;
+    bool bad = false;
+    for (int g = 0; g < c.G; ++g) {
+        const int n = std::min(std::max(c.h_nruns[g], 0), c.k);
+        for (int j = 0; j < n; ++j) {
+            const int32_t* r = c.h_runs + 4 * ((int64_t)g * c.k + j);
+            const int32_t x = r[0], nb = r[1], sl = r[2];
+            if (x < 0 || nb < 1 || (int64_t)x + nb > c.h_Ccap[g] || sl < 0 || sl + nb > 2 * c.k) {
+                bad = true;
+                continue;
+            }
+            const int64_t src = c.h_off[g] + x * blk, dst = ((int64_t)g * 2 * c.k + sl) * blk;
+            const size_t bytes = (size_t)nb * blk * sizeof(uint16_t);
+            e = cudaMemcpyAsync(c.buf_k(buf) + dst, c.k_host[layer] + src, bytes, cudaMemcpyDefault, s);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(c.buf_v(buf) + dst, c.v_host[layer] + src, bytes, cudaMemcpyDefault, s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    if (bad) {
+        status_or_kernel<<<1, 1, 0, s>>>(c.status, KVO_DEV_BAD_SLOT);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_gather(const Ctx& c, int layer, int buf, const int32_t* runs, const int32_t* nruns,
                           cudaStream_t s) {
     if (c.gather_engine == 1) return launch_gather_tma(c, layer, buf, runs, nruns, s);
+    if (c.gather_engine == 4) return gather_copy_engine(c, layer, buf, runs, nruns, s);
     const int ctas = gather_default_ctas(c), th = c.gather_threads;
 #define KVO_GATHER(U_)                                                                                          \
     gather_kernel<U_><<<ctas, th, 0, s>>>(c.k_host[layer], c.v_host[layer], c.g_off, c.g_C, (const int4*)runs, \

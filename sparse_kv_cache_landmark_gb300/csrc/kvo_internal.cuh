@@ -129,7 +129,12 @@ struct Ctx {
     // Gather launch shape and engine.  Default: the flat lane-load engine on 38
     // SM-exclusive CTAs of 1024 threads, 2 loads of K and of V in flight per lane.
     int gather_ctas = 38, gather_threads = 1024, gather_unroll = 2;
-    int gather_engine = 3;          // 0: lane loads over runs, 1: TMA bulk copies, 3: flat lane loads over entries
+    int gather_engine = 3;          // 0: lane loads over runs, 1: TMA bulk copies, 3: flat lane loads over
+                                    // entries, 4: copy engine (one cudaMemcpyAsync per run, issued by the host)
+    std::vector<int64_t> h_off;     // host copies of the group offsets and candidate capacities (engine 4)
+    std::vector<int32_t> h_Ccap;
+    int32_t* h_runs = nullptr;      // pinned [G][k][4] run list read back for engine 4
+    int32_t* h_nruns = nullptr;     // pinned [G]
     int gather_drivers = 0;         // TMA engine: driver warps (0: default)
     int gather_stages = 4;          // TMA engine: batches per driver (4 or 8)
     int gather_reserve_smem = 200 * 1024;   // flat engine: shared memory reserved per CTA (SM exclusivity)

@@ -184,6 +184,8 @@ void free_ctx(kvo::Ctx& c) {
     F(c.att_items); F(c.att_first); F(c.att_count); F(c.att_part_o); F(c.att_part_ml); F(c.att_done);
     for (auto& pl : c.tma) { F(pl.items); F(pl.cta); F(pl.first); F(pl.count); }
     F(c.status);
+    if (c.h_runs) cudaFreeHost(c.h_runs);
+    if (c.h_nruns) cudaFreeHost(c.h_nruns);
     F(c.st_true); F(c.st_pred); F(c.st_miss); F(c.st_miss_cnt); F(c.st_slot);
     for (auto* E : {&c.ev_eager, &c.ev_graph}) {
         for (auto* v : {&E->sel, &E->attn, &E->pref, &E->urg, &E->rassign, &E->rpref})
@@ -258,6 +260,8 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         c.Cmax = std::max<int>(c.Cmax, (int)Cc);
         tok += cap;
     }
+    c.h_off = off;
+    c.h_Ccap = Ccap;
     // host caches: page-locked and device-addressable
     for (int l = 0; l < c.L; ++l) {
         for (int kv = 0; kv < 2; ++kv) {
@@ -955,6 +959,8 @@ static kvo_status decode_step_impl(kvo_ctx* ctx, const void* q, const void* q_sp
 
 kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    if (enable && ctx->c.gather_engine == 4)
+        return fail(&ctx->c, KVO_ERR_STATE, "graph replay needs a device-side gather engine (not engine 4)");
     for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph})
         cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
@@ -1197,9 +1203,18 @@ kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
     for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     // engine 1: 4 batches per driver; engine 2: 8 batches per driver (one driver per CTA)
-    if (engine < 0 || engine > 3 || drivers < 0 || drivers > 4096)
-        return fail(&ctx->c, KVO_ERR_INVALID, "engine must be 0..3 and 0 <= drivers <= 4096");
-    ctx->c.gather_engine = engine == 0 ? 0 : engine == 3 ? 3 : 1;
+    if (engine < 0 || engine > 4 || drivers < 0 || drivers > 4096)
+        return fail(&ctx->c, KVO_ERR_INVALID, "engine must be 0..4 and 0 <= drivers <= 4096");
+    kvo::Ctx& c = ctx->c;
+    if (engine == 4) {
+        // the copy engine reads the run list back: pinned staging, and no graph
+        // capture (the host waits for the list inside the step)
+        if (!c.h_runs) KVO_CUDA(&c, cudaHostAlloc((void**)&c.h_runs, sizeof(int32_t) * 4 * (size_t)c.G * c.k,
+                                                  cudaHostAllocDefault));
+        if (!c.h_nruns) KVO_CUDA(&c, cudaHostAlloc((void**)&c.h_nruns, sizeof(int32_t) * c.G, cudaHostAllocDefault));
+        c.use_graphs = false;
+    }
+    ctx->c.gather_engine = engine == 0 ? 0 : engine == 3 ? 3 : engine == 4 ? 4 : 1;
     // each engine starts from its own default launch shape
     if (engine == 3) {
         ctx->c.gather_ctas = 38; ctx->c.gather_threads = 1024; ctx->c.gather_unroll = 2;

@@ -128,9 +128,10 @@ def test_diff_gather_attention_chain(case):
             assert np.all(lse2[1, rows] == -np.inf) and not o2[1, rows].any()
 
 
-@pytest.mark.parametrize("engine,drivers", [(1, 1), (1, 3), (1, 32), (2, 5), (3, 0)])
+@pytest.mark.parametrize("engine,drivers", [(1, 1), (1, 3), (1, 32), (2, 5), (3, 0), (4, 0)])
 def test_gather_engines_bit_exact(case, engine, drivers):
-    """TMA bulk copies (engines 1, 2) and the flat lane-load gather (engine 3)
+    """TMA bulk copies (engines 1, 2), the flat lane-load gather (engine 3) and
+    the copy engine (engine 4: one cudaMemcpyAsync per run, issued by the host)
     write the same bytes as the oracle's gather."""
     c, refs = case
     w = c.w
