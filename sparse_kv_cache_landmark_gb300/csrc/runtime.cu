@@ -371,8 +371,8 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, dalloc(&c.res_pf_dslot, sizeof(int32_t) * lg * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_fetched, sizeof(unsigned long long) * 2, &sb));
         const size_t rows = (size_t)c.batch * c.Hq;
-        KVO_CUDA(&c, dalloc(&c.res_hit_slot, sizeof(int32_t) * c.G * c.k, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_hit_cnt, sizeof(int32_t) * c.G, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_hit_slot, sizeof(int32_t) * lg * c.k, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_hit_cnt, sizeof(int32_t) * lg, &sb));
         KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * rows * c.d, &sb));
         KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * rows, &sb));
         KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
@@ -766,19 +766,21 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
     const bool have = c.have_pred;
     // Without speculation, with no prefetch of an earlier step still in flight
-    // and no layer rebuilding keys beside its copies, every kernel of the step
-    // depends on the one before: the whole step runs in order on the compute
-    // stream, the urgent copies take every SM and attention the whole-device plan.
+    // and no layer rebuilding keys beside its copies, the step is two chains:
+    // the compute stream selects and assigns layer after layer, and the urgent
+    // stream copies each layer's missing blocks and attends to the layer once
+    // its assign is done -- so layer l + 1's selection runs beside layer l's
+    // copy and attention.
     const bool alone_step = resident_alone(c, q_spec);
-    const cudaStream_t sc = c.s_compute;                          // select, assign, attention
-    const cudaStream_t su = alone_step ? c.s_compute : c.s_urgent;   // urgent copies
+    const cudaStream_t sc = c.s_compute;                          // select, assign (and attention when speculating)
+    const cudaStream_t su = c.s_urgent;                           // urgent copies (and attention in a chain step)
+    const cudaStream_t sa = alone_step ? su : sc;                 // attention
 
     KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
-    if (alone_step)
-        KVO_CUDA(&c, cudaStreamWaitEvent(c.s_compute, E.start, 0));
-    else
-        for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent})
-            KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) {
+        if (alone_step && s == c.s_prefetch) continue;
+        KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
+    }
     int cur_layer = -1;
     auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
         int e0, e1;
@@ -804,6 +806,8 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         int32_t* miss = c.st_miss + l * gk;
         int32_t* mcnt = c.st_miss_cnt + (size_t)l * c.G;
         int32_t* dsl = c.res_dslot + l * gk;
+        int32_t* hit_slot = c.res_hit_slot + l * gk;       // per layer: layer l + 1's assign runs beside
+        int32_t* hit_cnt = c.res_hit_cnt + (size_t)l * c.G;  // layer l's attention in a chain step
         const bool pending = c.res_pending[l] != 0;
         // the previous step's prefetch of this layer has read T and written the slot table
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rassign[l], 0));
@@ -819,28 +823,25 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // 2. urgent assign: T resident, sparing the prediction fetched for this step
         KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
             return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
-                                               sc, -1, split ? c.res_hit_slot : nullptr,
-                                               split ? c.res_hit_cnt : nullptr);
+                                               sc, -1, split ? hit_slot : nullptr, split ? hit_cnt : nullptr);
         }));
         // 3. urgent gather of the blocks that were missing
-        if (!alone_step) {
-            KVO_CUDA(&c, cudaEventRecord(E.sel[l], sc));
-            KVO_CUDA(&c, cudaStreamWaitEvent(su, E.sel[l], 0));
-        }
+        KVO_CUDA(&c, cudaEventRecord(E.sel[l], sc));
+        KVO_CUDA(&c, cudaStreamWaitEvent(su, E.sel[l], 0));
         // without a prediction nothing is spared: in-flight prefetch copies must land first
         if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, su, [&] {
-            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask, alone_step && !split);
+            return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask);
         }));
         if (split) {
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
-                return kvo::launch_attention(c, l, buf, ql, nullptr, c.res_hit_slot, c.res_oA, c.res_lA, nullptr,
-                                             nullptr, 1, sc, true, c.res_hit_cnt, true);
+            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
+                return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, c.res_oA, c.res_lA, nullptr,
+                                             nullptr, 1, sa, true, hit_cnt, true);
             }));
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
+            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
                 return kvo::launch_attn_merge_part(c, buf, ql, dsl, mcnt, c.res_oA, c.res_lA, o + l * o_layer,
-                                                   lse + l * lse_layer, sc);
+                                                   lse + l * lse_layer, sa);
             }));
             continue;
         }
@@ -855,10 +856,10 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         }
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rpref[l], 0));
         c.res_pending[l] = 0;
-        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sc, [&] {
+        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
             return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
                                          lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
-                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, sc, !alone_step);
+                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, sa, true);
         }));
         if (!alone_step) KVO_CUDA(&c, cudaEventRecord(E.attn[l], sc));
         // 5. prefetch of the next step's prediction, sparing T (with the adaptive
@@ -881,7 +882,6 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     }
     // the caller's stream waits for the outputs; prefetches stay in flight
     for (cudaStream_t s : {c.s_compute, c.s_urgent}) {
-        if (alone_step && s != c.s_compute) continue;
         KVO_CUDA(&c, cudaEventRecord(E.start, s));
         KVO_CUDA(&c, cudaStreamWaitEvent(s_user, E.start, 0));
     }
