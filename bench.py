@@ -97,6 +97,9 @@ def parse(argv=None):
     ap.add_argument("--spec-policy", type=int, default=-1,
                     help="with --resident 1: 1 prefetches a layer's prediction only while it pays (the default "
                          "here), 0 always")
+    ap.add_argument("--gather-engines", default="",
+                    help="also time an isolated gather of layer 0's true index with each listed engine "
+                         "(e.g. 3,4) and report it under gather_engines")
     ap.add_argument("--trace", default="",
                     help="write the launch trace (kind, layer, start, end) of one profiled step to this JSON file")
     return ap.parse_args(argv)
@@ -877,6 +880,20 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
     sel = _t(lambda: ctx.select_topk(0, q0, idx_true=T))
     m["isolated"] = {"attention_us": round(one, 2), "select_us": round(sel, 2),
                      "note": "layer 0, 20 back-to-back calls, nothing else running"}
+    m["gather_engines"] = None
+    if headline and args.gather_engines and not args.resident:
+        # one layer's prefetch-sized gather (k blocks per group, the true index) per engine
+        by = G * w.top_k * w.block_size * w.head_dim * 4
+        _, nr = ctx.gather_coalesced(0, 0, T, None, slot_base=0)
+        n_runs = int(nr.sum().item())
+        ge = {"runs": n_runs, "bytes": by, "note": "layer 0's true index into ping-pong half 0, mean of 5 calls"}
+        for eng in [int(x) for x in args.gather_engines.split(",") if x]:
+            ctx.set_gather_engine(eng, 0)
+            ms = _t(lambda: ctx.gather_coalesced(0, 0, T, None, slot_base=0, want_runs=False,
+                                                 stream=stream.cuda_stream), n=5) / 1e3
+            ge[f"engine{eng}"] = {"ms": round(ms, 3), "gbs": round(by / (ms * 1e-3) / 1e9, 1)}
+        ctx.set_gather_engine(args.gather_engine if args.gather_engine >= 0 else 3, args.gather_drivers)
+        m["gather_engines"] = ge
     if headline and 2 * w.group_size <= 16:
         two = _t(lambda: (ctx.sparse_decode_attn(0, 0, q0, slot), ctx.sparse_decode_attn(0, 0, qs0, slot)))
         co = _t(lambda: ctx.sparse_decode_attn_cobatch(0, 0, q0, qs0, slot))
@@ -1009,6 +1026,7 @@ def run_ours(args):
             "effective_kv_gbs": by["kv_attended"] / (t_ms * 1e-3) / 1e9 * ws,
             "urgent_misses_per_step": head["misses"],
             "cobatched_attention": head["cob"],
+            "gather_engines": head["gather_engines"],
             "step_roofline": {"t_star_ms": hf["t_star"] * 1e3, "frac": hf["t_star"] * 1e3 / t_ms,
                               "bound": "link" if hf["t_link"] >= hf["t_hbm"] else "hbm",
                               "host_bytes": by["host"], "hbm_bytes": by["hbm"], "link_gbs": link,
