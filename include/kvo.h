@@ -505,19 +505,29 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes);
 
 /*
  * kvo_set_attn_impl -- which kernel computes the attention of
- * sparse_decode_attn, sparse_decode_attn_cobatch and the decode step.  Both
- * do the same arithmetic but split a group's tiles into work items
- * differently, so their results agree up to float rounding, not bit for bit.
+ * sparse_decode_attn, sparse_decode_attn_cobatch and the decode step.  All
+ * do the same arithmetic but split a group's tiles differently, so their
+ * results agree up to float rounding, not bit for bit.
  * impl 0: register-direct, one CTA per 256-token work item, each warp loading
- * its tiles' K/V fragments from HBM with 16-byte loads.  impl 1 (default):
- * TMA-staged persistent kernel; each of a CTA's four warps keeps its next 2-4
- * tiles in flight in shared-memory stages filled by bulk copies, and the tiles
- * of all groups are split into one equal contiguous range per CTA, over as
- * many CTAs as are resident on the device at once (in the decode step: on the
- * SMs the flat gather leaves free), or over `ctas` CTAs when ctas > 0.  Waits inside impl 1 are bounded (2 s); on expiry the
- * kernel sets KVO_DEV_TIMEOUT.  Synchronises the context's streams and drops
- * captured graphs.  Errors: KVO_ERR_INVALID for a null context, impl outside
- * 0..1 or ctas < 0; KVO_ERR_CUDA if the work lists cannot be allocated.
+ * its tiles' K/V fragments from HBM with 16-byte loads.
+ * impl 1: TMA-staged persistent kernel; each of a CTA's four warps keeps its
+ * next 2-4 tiles in flight in shared-memory stages filled by bulk copies, and
+ * the tiles of all groups are split into one equal contiguous range per CTA,
+ * over as many CTAs as are resident on the device at once (in the decode step:
+ * on the SMs the flat gather leaves free), or over `ctas` CTAs when ctas > 0.
+ * impl 2 (default): group-split clusters for the fused output (the window
+ * merged in; "Scaling Attention Beyond GPUs for LLM Inference", abstract): a
+ * cluster of S CTAs per (request, KV head) group splits the group's tiles,
+ * attends with one softmax over both parts and merges the CTAs' states through
+ * distributed shared memory, with no partial results in global memory.
+ * ctas = S (1..8), or 0: S = the resident CTA slots / groups (at most 8), and
+ * clusters only where the groups' CTAs then fill at least 3/4 of the slots --
+ * otherwise, and for separate parts (fuse_window_merge = 0), impl 1 runs.
+ * Waits inside impls 1 and 2 are bounded (2 s); on expiry the kernel sets
+ * KVO_DEV_TIMEOUT.  Synchronises the context's streams and drops captured
+ * graphs.  Errors: KVO_ERR_INVALID for a null context, impl outside 0..2,
+ * ctas < 0, or ctas > 8 with impl 2; KVO_ERR_CUDA if the work lists cannot be
+ * allocated.
  */
 kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
 

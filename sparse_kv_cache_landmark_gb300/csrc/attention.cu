@@ -215,9 +215,28 @@ struct WarpAttn {
         pv(vf, pa, al0, al1);
     }
 
+    // Shared-memory layout of a warp's state: 8*NR rows of D floats.  Lane
+    // (g, t) holds channels [2*CPT*t, 2*CPT*(t+1)) of rows g and 8+g (column
+    // 2t of n-tile j is channel CPT*2t + j, column 2t+1 is CPT*(2t+1) + j), so
+    // it stores them as NC = CPT/2 float4 chunks; its chunk i goes to position
+    // NC*t + a rotation of i that differs across the 8 lanes of a 16-byte store
+    // phase (t = 0..3, g even and odd), so the phase hits 8 different bank
+    // groups rather than one.
+    static constexpr int NC = CPT / 2;
+    static __device__ __forceinline__ int chunk_pos(int row, int t, int i) {
+        if constexpr (D == 128) return 8 * t + ((i + t + 4 * (row & 1)) & 7);
+        else return 4 * t + ((i + 2 * (t >> 1) + (row & 1)) & 3);
+    }
+    // float index of element (row, channel c) in a warp's state area
+    static __device__ __forceinline__ int state_idx(int row, int c) {
+        const int t = c / (2 * CPT), i = (c % (2 * CPT)) >> 2;
+        return row * D + 4 * chunk_pos(row, t, i) + (c & 3);
+    }
+
     // warp state -> shared memory (row sums reduced over the lane quad)
     __device__ __forceinline__ void to_smem(float (*sm_m)[16], float (*sm_l)[16], float* sm_o_w, int warp, int gq,
                                             int tq) {
+        static_assert(D == 128 || D == 64, "state layout for d = 64 and 128");
         float a0 = l0, a1 = l1;
         a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
         a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
@@ -228,13 +247,14 @@ struct WarpAttn {
             sm_m[warp][gq + 8] = NR == 2 ? m1 : -INFINITY; sm_l[warp][gq + 8] = NR == 2 ? a1 : 0.f;
         }
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            // column 2t of n-tile j is channel CPT*2t + j; column 2t+1 is CPT*(2t+1) + j
-            sm_o_w[gq * D + CPT * (2 * tq) + j] = acc[j][0];
-            sm_o_w[gq * D + CPT * (2 * tq + 1) + j] = acc[j][1];
+        for (int i = 0; i < NC; ++i) {
+            // chunk i: channels 2*CPT*t + 4i .. +3, from accumulator column 2t (4i < CPT) or 2t+1
+            const int j0 = (4 * i) % CPT, e = 4 * i < CPT ? 0 : 1;
+            const float4 v = make_float4(acc[j0][e], acc[j0 + 1][e], acc[j0 + 2][e], acc[j0 + 3][e]);
+            *reinterpret_cast<float4*>(sm_o_w + gq * D + 4 * chunk_pos(gq, tq, i)) = v;
             if constexpr (NR == 2) {
-                sm_o_w[(gq + 8) * D + CPT * (2 * tq) + j] = acc[j][2];
-                sm_o_w[(gq + 8) * D + CPT * (2 * tq + 1) + j] = acc[j][3];
+                const float4 w = make_float4(acc[j0][e + 2], acc[j0 + 1][e + 2], acc[j0 + 2][e + 2], acc[j0 + 3][e + 2]);
+                *reinterpret_cast<float4*>(sm_o_w + (gq + 8) * D + 4 * chunk_pos(gq + 8, tq, i)) = w;
             }
         }
     }
@@ -267,7 +287,7 @@ __device__ __forceinline__ void attn_epilogue(float (*sm_m)[16], float (*sm_l)[1
 #pragma unroll
             for (int w = 0; w < ATT_WARPS; ++w) {
                 const float sc = ex2f(sm_m[w][row] - M);
-                a += sc * sm_o[(w * 8 * NR + row) * D + c];
+                a += sc * sm_o[w * 8 * NR * D + WarpAttn<D, NR>::state_idx(row, c)];
                 l += sc * sm_l[w][row];
             }
         }
@@ -712,7 +732,8 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     int isl = cursor_slot(ic, slot, k, B, row);
     int64_t nissue = 0, ncons = 0;
     auto issue = [&]() {
-        if (ic.item >= ic.hi || *s_abort) return;       // nothing more is issued once the CTA gave up
+        // nothing more is issued once the CTA gave up (lane 0's view, so the whole warp agrees)
+        if (ic.item >= ic.hi || __shfl_sync(0xffffffffu, *s_abort, 0)) return;
         const int st = (int)(nissue % STG);
         tile_copy<D>(ic, isl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad,
                      blockIdx.x == 0 && warp == 0 && nissue == skip_tile);
@@ -736,7 +757,7 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
         for (int i = 0; i < STG; ++i) ps[i] = cursor_slot(pc[i], slot, k, B, row);
 #pragma unroll
         for (int i = 0; i < STG; ++i) {
-            if (pc[i].item >= pc[i].hi || *s_abort) break;
+            if (pc[i].item >= pc[i].hi || __shfl_sync(0xffffffffu, *s_abort, 0)) break;
             tile_copy<D>(pc[i], ps[i], ring + i * CF::STAGE_BYTES, smem_u32(&wfull[i]), bk, bv, wk, wv, k, B, Wcap,
                          bad, blockIdx.x == 0 && warp == 0 && nissue == skip_tile);
             ++nissue;
@@ -817,10 +838,288 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
     if (dep_wait && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Group-split cluster kernel (fused output only).  Each (request, KV head)
+// group gets a cluster of S CTAs that split the group's tiles (sparse part,
+// then window part): warp j of the cluster (j = rank * 4 + warp) takes the
+// blocks of STG consecutive tiles j, j + 4S, j + 8S, ... .  A warp copies its
+// tiles into its ring of STG shared-memory stages with bulk copies (as in the
+// persistent kernel) and refills a stage right after computing it.  The
+// fused output is the softmax over the union of the two parts (log-sum-exp
+// merge of the parts is that softmax, regrouped), so a warp keeps one
+// online-softmax state whatever part its tiles come from, and no CTA has a
+// per-item epilogue: after its last tile the warps' states are merged in the
+// CTA's own shared memory, the cluster synchronises once, and each CTA merges
+// a 1/S slice of the group's output elements by reading the S CTA states
+// through distributed shared memory -- no partials in global memory, no
+// ticket, no device-scope fence.  A second cluster barrier keeps every CTA's
+// shared memory alive until the last remote read.  The group's slot list is
+// staged in shared memory by asynchronous copies that overlap the first tile
+// copies (whose slots are read from global memory).  Two stages per warp and
+// two CTAs per SM measured faster than deeper rings or three CTAs per SM, and
+// a tile counter drawn through a shared-memory atomic (to balance a cluster's
+// CTAs dynamically) cost more than the imbalance it removed.  Waits are
+// bounded as in the persistent kernel; a CTA that gave up still reaches both
+// cluster barriers.
 template <int D, int NR>
-static cudaError_t tma_attr(int* per_sm) {
+struct AttnCluCfg {
+    static constexpr int STG = D == 128 ? 2 : 4;                          // stages per warp
+    static constexpr int STAGE_BYTES = 2 * ATT_TILE * D * 2;              // K and V tile
+    static constexpr int RING = ATT_WARPS * STG * STAGE_BYTES;
+    static constexpr int O_FLOATS = ATT_WARPS * 8 * NR * D;               // warp states, in the idle ring
+    static constexpr int SLOT_CAP = 4096;                                 // slot entries staged in shared memory
+    static_assert(sizeof(float) * (O_FLOATS + 32 + 16 * D + 16 * 8) <= (size_t)RING,
+                  "end-phase state does not fit the ring");
+    // ring | m, l [ATT_WARPS][16] each | full [ATT_WARPS][STG] | tile of each stage [ATT_WARPS][STG] |
+    // abort flag (16 B) | slot table [SLOT_CAP]: 82 KB, two CTAs per SM
+    static constexpr size_t BYTES = (size_t)RING + sizeof(float) * 2 * ATT_WARPS * 16 +
+                                    sizeof(uint64_t) * ATT_WARPS * STG + sizeof(int) * ATT_WARPS * STG + 16 +
+                                    sizeof(int) * SLOT_CAP;
+};
+constexpr int ATT_CLU_MAX = 8;       // CTAs per group (portable cluster size)
+
+template <int D, int NR>
+__global__ void __launch_bounds__(ATT_WARPS * 32, 2)
+attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_spec,
+                    const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv,
+                    const uint16_t* __restrict__ wk, const uint16_t* __restrict__ wv,
+                    const int32_t* __restrict__ slot, float* __restrict__ out_o, float* __restrict__ out_lse,
+                    float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec, int r, int Hkv, int k, int B,
+                    int W, int Wcap, const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len,
+                    const int32_t* __restrict__ sp_cnt, int dep_wait, float scale_log2,
+                    int32_t* __restrict__ status, long long wait_ns, int skip_tile) {
+    using WA = WarpAttn<D, NR>;
+    using CF = AttnCluCfg<D, NR>;
+    constexpr int CH = WA::CH, CPT = WA::CPT, STG = CF::STG;
+    constexpr int NTHR = ATT_WARPS * 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float (*sm_m)[16] = reinterpret_cast<float (*)[16]>(smem + CF::RING);
+    float (*sm_l)[16] = sm_m + ATT_WARPS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm_l + ATT_WARPS);     // [ATT_WARPS][STG]
+    int* s_tile = reinterpret_cast<int*>(full + ATT_WARPS * STG);       // [ATT_WARPS][STG] tile in each stage
+    volatile int* s_abort = s_tile + ATT_WARPS * STG;
+    int* s_slot = s_tile + ATT_WARPS * STG + 4;                         // [SLOT_CAP]
+    float* sm_o = reinterpret_cast<float*>(smem);                      // end phase only (ring idle)
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, tq = lane & 3, row = lane & 15;
+    const uint32_t S = max(1u, cluster_size()), rank = S > 1 ? cluster_rank() : 0u;
+    const int bg = (int)(blockIdx.x / S);
+    const bool tab = k <= CF::SLOT_CAP;
+    // the group's slot list into shared memory, asynchronously (read after the first copies are out)
+    if (tab) {
+        const int32_t* src = slot + (int64_t)bg * k;
+        for (int i = tid; i < k; i += NTHR)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s_slot + i)), "l"(src + i) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    // the group's tiles: sparse part (tiles [0, t_sp)), then window part
+    const int n_sp = (sp_cnt ? min(k, max(0, __ldg(sp_cnt + bg))) : k) * B;
+    const int n_w = max(0, w_len ? __ldg(w_len + bg) : W);
+    const int ws = w_start ? __ldg(w_start + bg) : 0;
+    const int t_sp = (n_sp + ATT_TILE - 1) / ATT_TILE;
+    const int T = t_sp + (n_w + ATT_TILE - 1) / ATT_TILE;
+    if (tid < ATT_WARPS * STG) mbar_init(smem_u32(&full[tid]), 1);
+    if (tid == 0) *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+
+    const int Hq = Hkv * r;
+    const int nrows = q_spec ? 2 * r : r;
+    unsigned char* ring = smem + warp * STG * CF::STAGE_BYTES;
+    uint64_t* wfull = full + warp * STG;
+    int* wtile = s_tile + warp * STG;
+    int bad = 0;
+    const bool skip_cta = blockIdx.x == 0 && warp == 0;
+
+    // tile t as the cursor the copy routine takes
+    auto cur = [&](int t) {
+        AttnCursor c;
+        c.item = 0; c.hi = 1; c.tl = 0; c.bg = bg; c.ntiles = 1; c.nt = 1;
+        c.part = t < t_sp ? 0 : 1;
+        c.tile0 = c.part ? t - t_sp : t;
+        c.n_tok = c.part ? n_w : n_sp;
+        c.ws = c.part ? ws : 0;
+        return c;
+    };
+    // slot of this lane's row of tile t (0 outside the sparse part)
+    auto slot_of = [&](int t, bool from_tab) -> int {
+        if (t >= t_sp) return 0;
+        const int tok = t * ATT_TILE + row;
+        if (tok >= n_sp) return 0;
+        return from_tab ? s_slot[tok / B] : __ldg(slot + (int64_t)bg * k + tok / B);
+    };
+    int64_t nissue = 0, ncons = 0;
+    auto copy = [&](int t, int sl) {
+        const int st = (int)(nissue % STG);
+        if (lane == 0) wtile[st] = t;
+        tile_copy<D>(cur(t), sl, ring + st * CF::STAGE_BYTES, smem_u32(&wfull[st]), bk, bv, wk, wv, k, B, Wcap, bad,
+                     skip_cta && nissue == skip_tile);
+        ++nissue;
+    };
+    // this warp's tiles: blocks of STG consecutive tiles (one gathered block
+    // when B = 32), block j of the cluster's warp j, j + 4S, j + 8S, ...
+    const int stride = (int)S * ATT_WARPS * STG;
+    int next = ((int)rank * ATT_WARPS + warp) * STG;
+    // the first block: slots straight from global memory, copies out
+    {
+        int ps[STG];
+#pragma unroll
+        for (int i = 0; i < STG; ++i) ps[i] = next + i < T ? slot_of(next + i, false) : 0;
+#pragma unroll
+        for (int i = 0; i < STG; ++i)
+            if (next + i < T) copy(next + i, ps[i]);
+        next += stride;
+    }
+    if (tab) asm volatile("cp.async.wait_all;" ::: "memory");
+    bar_named(1, NTHR);                      // slot table visible to every warp
+    int nidx = 0;
+    auto refill = [&]() {
+        if (__shfl_sync(0xffffffffu, *s_abort, 0)) return;      // lane 0's view: the warp agrees
+        const int t = next + nidx;
+        if (t >= T) return;
+        if (++nidx == STG) { nidx = 0; next += stride; }
+        copy(t, slot_of(t, tab));
+    };
+
+    // one state over all the group's rows, whatever part each tile comes from
+    WA stt;
+    {
+        const int b = bg / Hkv, gk = bg % Hkv;
+        auto qrow = [&](int rr) -> const uint16_t* {
+            return rr < r ? q + ((int64_t)b * Hq + gk * r + rr) * D : q_spec + ((int64_t)b * Hq + gk * r + rr - r) * D;
+        };
+        const bool v0 = gq < nrows, v1 = NR == 2 && gq + 8 < nrows;
+        stt.init(v0 ? qrow(gq) : q, v1 ? qrow(gq + 8) : q, v0, v1, tq);
+    }
+    while (ncons < nissue) {
+        const int st = (int)(ncons % STG);
+        if (!*s_abort) att_wait(smem_u32(&wfull[st]), (uint32_t)((ncons / STG) & 1), s_abort, status, wait_ns);
+        ++ncons;
+        const int t = wtile[st];
+        const bool sp = t < t_sp;
+        const int tb = (sp ? t : t - t_sp) * ATT_TILE, n_tok = sp ? n_sp : n_w;
+        const int rows = min(ATT_TILE, n_tok - tb);
+        const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * CF::STAGE_BYTES);
+        const uint16_t* vs = ks + ATT_TILE * D;
+        uint4 kf[2][CH];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
+#pragma unroll
+            for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
+        }
+        uint4 vf[4][CPT / 8];
+#pragma unroll
+        for (int vi = 0; vi < 4; ++vi) {
+            const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
+#pragma unroll
+            for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
+        }
+        stt.tile(kf, vf, tb, n_tok, scale_log2, tq);
+        // the stage's reads are done: order them before the async-proxy refill
+        __syncwarp();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        refill();
+    }
+    if (bad) atomicOr(status, bad);
+    // every copy has landed before the ring is reused (bounded, as in the persistent kernel)
+    if (lane == 0)
+        for (int64_t s2 = nissue > STG ? nissue - STG : 0; s2 < nissue; ++s2)
+            att_drain_wait(smem_u32(&wfull[s2 % STG]), (uint32_t)((s2 / STG) & 1), wait_ns);
+    __syncthreads();
+    stt.to_smem(sm_m, sm_l, sm_o + warp * 8 * NR * D, warp, gq, tq);
+    __syncthreads();
+
+    // this CTA's state, its warps merged: max and mass per row (log2 domain)
+    // and the unnormalised sum per element, in the ring after the warp states
+    float* c_m = sm_o + CF::O_FLOATS;
+    float* c_l = c_m + 16;
+    float* c_a = c_l + 16;
+    for (int e = tid; e < nrows * D; e += NTHR) {
+        const int rr = e / D, c = e - rr * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w) M = fmaxf(M, sm_m[w][rr]);
+        float a = 0.f, l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < ATT_WARPS; ++w) {
+                const float sc = ex2f(sm_m[w][rr] - M);
+                a += sc * sm_o[w * 8 * NR * D + WA::state_idx(rr, c)];
+                l += sc * sm_l[w][rr];
+            }
+        }
+        c_a[rr * D + c] = a;
+        if (c == 0) { c_m[rr] = M; c_l[rr] = l; }
+    }
+    if (S > 1) cluster_barrier(); else __syncthreads();
+
+    // per row: the weight of each CTA state (its share of the row's softmax
+    // mass, normalised) and the row's log-sum-exp, written by the first CTA
+    const int b = bg / Hkv, gk = bg % Hkv;
+    float* s_wt = c_a + 16 * D;              // [16][ATT_CLU_MAX]
+    if (tid < nrows) {
+        float ms[ATT_CLU_MAX], ls[ATT_CLU_MAX];
+#pragma unroll
+        for (int s2 = 0; s2 < ATT_CLU_MAX; ++s2)
+            if (s2 < (int)S) {
+                ms[s2] = S > 1 ? ld_cluster_f32(c_m + tid, s2) : c_m[tid];
+                ls[s2] = S > 1 ? ld_cluster_f32(c_l + tid, s2) : c_l[tid];
+            }
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < ATT_CLU_MAX; ++s2)
+            if (s2 < (int)S) M = fmaxf(M, ms[s2]);
+        float L = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < ATT_CLU_MAX; ++s2)
+            if (s2 < (int)S) {
+                ms[s2] = (M == -INFINITY || ms[s2] == -INFINITY) ? 0.f : ex2f(ms[s2] - M);
+                L += ms[s2] * ls[s2];
+            }
+        const float inv = M == -INFINITY ? 0.f : __frcp_rn(L);
+#pragma unroll
+        for (int s2 = 0; s2 < ATT_CLU_MAX; ++s2)
+            if (s2 < (int)S) s_wt[tid * ATT_CLU_MAX + s2] = ms[s2] * inv;
+        if (rank == 0) {
+            const bool spec_row = tid >= r;
+            const int64_t orow = (int64_t)b * Hq + gk * r + (spec_row ? tid - r : tid);
+            (spec_row ? out_lse_spec : out_lse)[orow] = M == -INFINITY ? -INFINITY : (M + lg2f(L)) * kLn2;
+        }
+    }
+    __syncthreads();
+    // the group's output: CTA `rank` merges elements rank*NTHR + tid, + S*NTHR, ...
+    // (each element's S remote loads issued together)
+    for (int e = (int)rank * NTHR + tid; e < nrows * D; e += (int)S * NTHR) {
+        const int rr = e / D, c = e - rr * D;
+        float as[ATT_CLU_MAX];
+#pragma unroll
+        for (int s2 = 0; s2 < ATT_CLU_MAX; ++s2)
+            if (s2 < (int)S) as[s2] = S > 1 ? ld_cluster_f32(c_a + rr * D + c, s2) : c_a[rr * D + c];
+        float o = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < ATT_CLU_MAX; ++s2)
+            if (s2 < (int)S) o += s_wt[rr * ATT_CLU_MAX + s2] * as[s2];
+        const bool spec_row = rr >= r;
+        const int64_t orow = (int64_t)b * Hq + gk * r + (spec_row ? rr - r : rr);
+        (spec_row ? out_o_spec : out_o)[orow * D + c] = o;
+    }
+    // no CTA leaves (and frees its shared memory) while another may still read it
+    if (S > 1) cluster_barrier();
+    if (dep_wait && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <int D, int NR>
+static cudaError_t tma_attr(int* per_sm, int* clu_per_sm) {
     cudaError_t e = cudaFuncSetAttribute(attn_tma_kernel<D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)AttnTmaCfg<D, NR>::BYTES);
+    if (e != cudaSuccess) return e;
+    using CC = AttnCluCfg<D, NR>;
+    e = cudaFuncSetAttribute(attn_cluster_kernel<D, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CC::BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(clu_per_sm, attn_cluster_kernel<D, NR>, ATT_WARPS * 32,
+                                                      CC::BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, attn_tma_kernel<D, NR>, ATT_WARPS * 32,
                                                          AttnTmaCfg<D, NR>::BYTES);
@@ -829,16 +1128,19 @@ static cudaError_t tma_attr(int* per_sm) {
 // Shared-memory attribute of the TMA-staged kernel; SMs of the device and
 // CTAs of the kernel per SM (the smaller count of its two query-row variants).
 cudaError_t prepare_attention(Ctx& c) {
-    int dev = 0, sms = 0, p1 = 0, p2 = 0;
+    int dev = 0, sms = 0, p1 = 0, p2 = 0, q1 = 0, q2 = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (c.d == 128) {
-        if ((e = tma_attr<128, 1>(&p1)) != cudaSuccess || (e = tma_attr<128, 2>(&p2)) != cudaSuccess) return e;
+        if ((e = tma_attr<128, 1>(&p1, &q1)) != cudaSuccess || (e = tma_attr<128, 2>(&p2, &q2)) != cudaSuccess)
+            return e;
     } else {
-        if ((e = tma_attr<64, 1>(&p1)) != cudaSuccess || (e = tma_attr<64, 2>(&p2)) != cudaSuccess) return e;
+        if ((e = tma_attr<64, 1>(&p1, &q1)) != cudaSuccess || (e = tma_attr<64, 2>(&p2, &q2)) != cudaSuccess)
+            return e;
     }
     c.tma_per_sm = std::max(1, std::min(p1, p2));
+    c.clu_per_sm = std::max(1, std::min(q1, q2));
     c.n_sms = std::max(1, sms);
     return cudaSuccess;
 }
@@ -867,6 +1169,39 @@ static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, con
                               (long long)c.att_wait_ns, c.att_skip_tile);
 }
 
+template <int D, int NR>
+static cudaError_t launch_cluster(const Ctx& c, int S, int buf, const void* q, const void* q_spec,
+                                  const uint16_t* wk, const uint16_t* wv, const int32_t* slot, float* o, float* lse,
+                                  float* o_spec, float* lse_spec, cudaStream_t s, const int32_t* sp_cnt, bool pdl,
+                                  float scale_log2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(c.G * S));
+    cfg.blockDim = dim3(ATT_WARPS * 32);
+    cfg.dynamicSmemBytes = AttnCluCfg<D, NR>::BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (S > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)S;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<D, NR>, (const uint16_t*)q, (const uint16_t*)q_spec,
+                              (const uint16_t*)c.buf_k(buf), (const uint16_t*)c.buf_v(buf), wk, wv, slot, o, lse,
+                              o_spec, lse_spec, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, (const int32_t*)c.g_wstart,
+                              (const int32_t*)c.g_wlen, sp_cnt, pdl ? 1 : 0, scale_log2, c.status,
+                              (long long)c.att_wait_ns, c.att_skip_tile);
+}
+
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
                              bool in_step, const int32_t* sp_cnt, bool pdl) {
@@ -875,7 +1210,18 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
     const int nrows = q_spec ? 2 * c.r : c.r;
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
-    if (c.att_impl == 1) {
+    if (c.att_impl == 2 && fuse && c.clu_use[in_step ? 1 : 0]) {
+        const int S = c.clu_S[in_step ? 1 : 0];
+#define KVO_CLU(D_, NR_) \
+        launch_cluster<D_, NR_>(c, S, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, s, sp_cnt, pdl, \
+                                scale_log2)
+        if (c.d == 128) return nrows <= 8 ? KVO_CLU(128, 1) : KVO_CLU(128, 2);
+        return nrows <= 8 ? KVO_CLU(64, 1) : KVO_CLU(64, 2);
+#undef KVO_CLU
+    }
+    // impl 2 with separate parts (fuse 0), or with too few groups to fill the
+    // device, uses the persistent kernel
+    if (c.att_impl >= 1) {
 #define KVO_TMA(D_, NR_) \
         launch_tma<D_, NR_>(c, pl, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, fuse, s, sp_cnt, pdl, \
                             scale_log2)
@@ -982,7 +1328,7 @@ attn_merge_part_kernel(const uint16_t* __restrict__ q, const uint16_t* __restric
 #pragma unroll
             for (int w = 0; w < ATT_WARPS; ++w) {
                 const float sc = ex2f(sm_m[w][row] - M);
-                a += sc * sm_o[(w * 8 * NR + row) * D + c];
+                a += sc * sm_o[w * 8 * NR * D + WA::state_idx(row, c)];
                 l += sc * sm_l[w][row];
             }
         }

@@ -105,12 +105,17 @@ struct Ctx {
     int32_t* att_first = nullptr;   // [G] first item of the group
     int32_t* att_count = nullptr;   // [G] items of the group
     int n_att_items = 0;
-    int att_impl = 1;               // attention kernel: 0 register-direct loads, 1 TMA-staged persistent
+    int att_impl = 2;               // attention kernel: 0 register-direct loads, 1 TMA-staged persistent,
+                                    // 2 group-split clusters (fused output; separate parts use 1)
+    int att_cluster = 0;            // impl 2: CTAs per group asked for (0: automatic)
+    int clu_S[2] = {1, 1};          // impl 2: CTAs per group, whole device and decode step
+    bool clu_use[2] = {false, false};   // impl 2: clusters used (else the persistent kernel)
     int att_part_cap = 0;           // work items the partial-result buffers hold
     // TMA-staged kernel: balanced per-CTA tile ranges cut into work items, one
     // plan for the whole device (standalone calls) and one for the decode step,
     // whose attention shares the device with a gather holding SMs of its own
     int tma_per_sm = 1;             // CTAs of the kernel resident per SM
+    int clu_per_sm = 1;             // CTAs of the group-split cluster kernel resident per SM
     int n_sms = 1;
     int tma_ctas = 0;               // requested grid (0: fill the available SMs)
     struct TmaPlan {

@@ -163,6 +163,22 @@ kvo_status build_tma_plans(kvo::Ctx& c) {
     if (c.gather_engine == 3 && c.gather_reserve_smem >= 64 * 1024)
         held = std::min(c.gather_ctas > 0 ? c.gather_ctas : 2 * c.n_sms, c.n_sms - 1);
     const int64_t step = (int64_t)c.tma_per_sm * (c.n_sms - held);
+    // group-split clusters: as many CTAs per group as the resident CTAs allow,
+    // 1 .. 8 (the portable cluster size); chosen automatically only when the
+    // groups' CTAs then fill at least 3/4 of the resident CTA slots -- fewer
+    // groups leave SMs idle, and the persistent kernel's balanced tile ranges
+    // measured faster there
+    auto plan_clu = [&](int i, int64_t slots) {
+        if (c.att_cluster > 0) {
+            c.clu_S[i] = c.att_cluster;
+            c.clu_use[i] = true;
+            return;
+        }
+        c.clu_S[i] = (int)std::max<int64_t>(1, std::min<int64_t>(8, slots / std::max(1, c.G)));
+        c.clu_use[i] = 4 * (int64_t)c.G * c.clu_S[i] >= 3 * slots;
+    };
+    plan_clu(0, (int64_t)c.clu_per_sm * c.n_sms);
+    plan_clu(1, (int64_t)c.clu_per_sm * (c.n_sms - held));
     if (kvo_status st = build_tma_plan(c, c.tma[0], c.tma_ctas > 0 ? c.tma_ctas : dev)) return st;
     return build_tma_plan(c, c.tma[1], c.tma_ctas > 0 ? c.tma_ctas : step);
 }
@@ -819,7 +835,7 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // are attended beside the urgent copies (a programmatic dependent launch,
         // dispatched once the copy's SM-exclusive CTAs are all resident), the
         // fetched blocks after them, and the two results merge by log-sum-exp.
-        const bool split = alone_step && c.att_impl == 1 && !o_spec;
+        const bool split = alone_step && c.att_impl >= 1 && !o_spec;
         // 2. urgent assign: T resident, sparing the prediction fetched for this step
         KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
             return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
@@ -1230,12 +1246,14 @@ kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
 
 kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    if (impl < 0 || impl > 1 || ctas < 0)
-        return fail(&ctx->c, KVO_ERR_INVALID, "attention implementation must be 0 or 1 and ctas >= 0");
+    if (impl < 0 || impl > 2 || ctas < 0 || (impl == 2 && ctas > 8))
+        return fail(&ctx->c, KVO_ERR_INVALID,
+                    "attention implementation must be 0, 1 or 2, ctas >= 0, and ctas <= 8 for implementation 2");
     for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     ctx->c.att_impl = impl;
-    ctx->c.tma_ctas = ctas;
+    ctx->c.tma_ctas = impl == 2 ? 0 : ctas;
+    ctx->c.att_cluster = impl == 2 ? ctas : 0;
     return build_tma_plans(ctx->c);
 }
 

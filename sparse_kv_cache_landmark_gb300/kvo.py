@@ -393,7 +393,8 @@ class Context:
 
     def set_attn_impl(self, impl: int, ctas: int = 0):
         """Attention kernel: 0 register-direct loads, 1 TMA-staged persistent with
-        ``ctas`` CTAs (0: as many as fit) (C: kvo_set_attn_impl)."""
+        ``ctas`` CTAs (0: as many as fit), 2 (default) group-split clusters of
+        ``ctas`` CTAs per group (0: automatic) (C: kvo_set_attn_impl)."""
         self._c(lib().kvo_set_attn_impl(self.ctx, impl, ctas))
 
     def set_wait_test(self, limit_ns: int = 2_000_000_000, skip_tile: int = -1):

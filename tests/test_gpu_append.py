@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("B,spec,L,att,resident", [(16, True, 2, (1, 0), False), (1, False, 1, (1, 0), False),
                                                    (32, False, 3, (1, 0), False), (16, False, 1, (0, 0), False),
-                                                   (16, False, 1, (1, 2), False), (16, True, 2, (1, 0), True)])
+                                                   (16, False, 1, (1, 2), False), (16, True, 2, (1, 0), True),
+                                                   (16, True, 2, (2, 3), False), (16, False, 2, (2, 0), True)])
 def test_append_grows_the_cache(B, spec, L, att, resident):
     W, n_app, d = 32, 40 if B > 1 else 12, 128
     len0 = W + B * 20 if B > 1 else W + 400

@@ -216,7 +216,7 @@ def test_attention_kernels_agree(case, ctas):
             assert c.ctx.device_status() == 0
             out[impl] = res
     finally:
-        c.ctx.set_attn_impl(1, 0)
+        c.ctx.set_attn_impl(2, 0)
     for a, b in zip(out[0], out[1]):
         assert a.shape == b.shape
         np.testing.assert_allclose(b.numpy(), a.numpy(), rtol=1e-2, atol=2e-3)
@@ -231,6 +231,54 @@ def test_attention_kernels_agree(case, ctas):
             if w.window:
                 assert_attn_close(o2[1, rows], ref.o_window, what="o_window")
                 assert_attn_close(lse2[1, rows], ref.lse_window, what="lse_window")
+
+
+@pytest.mark.parametrize("per_group", [0, 1, 3, 8])
+def test_cluster_attention_matches_oracle(case, per_group):
+    """The group-split cluster kernel (impl 2): per_group CTAs per group (0: as
+    many as fill the device; 3 leaves uneven shares that cut a part inside a
+    CTA; 8 on the small cases gives CTAs with no tiles at all) attend with one
+    softmax over both parts and merge through distributed shared memory.  The
+    fused output, the co-batched output and -- through the persistent kernel it
+    falls back to -- the separate parts all match the oracle."""
+    c, refs = case
+    w = c.w
+    r = w.group_size
+    q = c.q_dev(0)
+    qs = c.q_dev(0, spec=True)
+    if qs is None:
+        qs = (q.float() * 0.5).to(torch.bfloat16)     # any second query works
+    T, _ = c.ctx.select_topk(0, q)
+    miss, cnt, slot = c.ctx.index_diff(T, None)
+    c.ctx.gather_coalesced(0, 0, miss, cnt, slot_base=w.top_k, urgent=True)
+    try:
+        c.ctx.set_attn_impl(2, per_group)
+        o, lse = (t.cpu().numpy() for t in c.ctx.sparse_decode_attn(0, 0, q, slot, fuse_window_merge=True))
+        o2, lse2 = (t.cpu().numpy() for t in c.ctx.sparse_decode_attn(0, 0, q, slot, fuse_window_merge=False))
+        cob = None
+        if 2 * r <= 16:
+            cob = [t.cpu().numpy() for t in c.ctx.sparse_decode_attn_cobatch(0, 0, q, qs, slot)]
+        torch.cuda.synchronize()
+        assert c.ctx.device_status() == 0
+    finally:
+        c.ctx.set_attn_impl(2, 0)
+    qs_bits = synth.bits(qs.cpu()) if cob is not None else None
+    for (b, g), ref in refs.items():
+        rows = slice(b * w.n_q_heads + g * r, b * w.n_q_heads + (g + 1) * r)
+        assert_attn_close(o[0, rows], ref.o)
+        assert_attn_close(lse[0, rows], ref.lse, what="lse")
+        assert_attn_close(o2[0, rows], ref.o_sparse, what="o_sparse")
+        assert_attn_close(lse2[0, rows], ref.lse_sparse, what="lse_sparse")
+        if w.window:
+            assert_attn_close(o2[1, rows], ref.o_window, what="o_window")
+            assert_attn_close(lse2[1, rows], ref.lse_window, what="lse_window")
+        if cob is not None:
+            assert_attn_close(cob[0][0, rows], ref.o, what="cobatched o")
+            rs = orc.decode_group(synth.bits(c.rows(0, b, g, "k")), synth.bits(c.rows(0, b, g, "v")),
+                                  synth.bits(c.q[0][b, g * r:(g + 1) * r]), qs_bits[b, g * r:(g + 1) * r],
+                                  block_size=w.block_size, top_k=w.top_k, window=w.window)
+            assert_attn_close(cob[2][0, rows], rs.o_spec, what="cobatched o_spec")
+            assert_attn_close(cob[3][0, rows], rs.lse_spec, what="cobatched lse_spec")
 
 
 def test_cobatched_attention(case):

@@ -56,7 +56,9 @@ def _attempts(c, steps, drift):
     ("alt", 2, 16, 16, False, None, 32, False, False),  # speculative and plain steps alternate
     ("s3", 2, 16, 16, False, None, 32, False, True),   # graph replays, one speculative step, replays again
     (False, 1, 16, 8, False, None, 32, "many", False),  # 320 groups: one CTA per group for the fetched blocks
-    (False, 2, 32, 12, False, None, 64, True, "impl0")])  # chain steps with the register-direct attention
+    (False, 2, 32, 12, False, None, 64, True, "impl0"),  # chain steps with the register-direct attention
+    (False, 2, 32, 12, False, None, 64, True, "impl2g"),  # chain steps, group-split cluster attention, graphs
+    (True, 2, 16, 16, True, None, 32, False, "impl2")])  # speculative resident steps, cluster attention
 def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged, graphs):
     drift, steps, seed = 0.15, 6, 321
     n = W + B * 64 if B > 1 else W + 600
@@ -75,6 +77,9 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged,
         if graphs == "impl0":
             c.ctx.set_attn_impl(0)                # one attention pass after the copy, whole set
             graphs = False
+        elif graphs in ("impl2", "impl2g"):
+            c.ctx.set_attn_impl(2, 2)             # two CTAs per group: the clusters merge in shared memory
+            graphs = graphs == "impl2g"
         if graphs:
             c.ctx.set_graphs(True)
         G, r = w.batch * w.n_kv_heads, w.group_size
@@ -156,10 +161,12 @@ def test_resident_setters_check_their_arguments():
         with pytest.raises(Exception, match="layer"):
             c.ctx.resident_slots(1)
         with pytest.raises(Exception, match="implementation"):
-            c.ctx.set_attn_impl(2)
+            c.ctx.set_attn_impl(3)
+        with pytest.raises(Exception, match="implementation"):
+            c.ctx.set_attn_impl(2, 9)
         with pytest.raises(Exception, match="implementation"):
             c.ctx.set_attn_impl(1, -1)
-        c.ctx.set_attn_impl(1, 0)
+        c.ctx.set_attn_impl(2, 0)
     finally:
         c.close()
 

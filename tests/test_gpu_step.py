@@ -65,13 +65,14 @@ def test_decode_step_cold_and_warm(L, spec, engine):
 
 
 def test_decode_step_attention_kernels_agree():
-    """The decode step matches the oracle with either attention kernel and any
-    TMA grid (the kernels split tiles differently: equal up to rounding)."""
+    """The decode step matches the oracle with any attention kernel, TMA grid
+    or cluster split (the kernels split tiles differently: equal up to
+    rounding)."""
     c = _case(4, True)
     try:
         q, qs = c.q_stack(), c.q_stack(spec=True)
         res = []
-        for impl, ctas in ((1, 0), (0, 0), (1, 2)):
+        for impl, ctas in ((1, 0), (0, 0), (1, 2), (2, 0), (2, 3)):
             c.ctx.set_attn_impl(impl, ctas)
             for _ in range(2):
                 o, lse = c.ctx.decode_step(q, qs)

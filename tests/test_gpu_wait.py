@@ -20,8 +20,8 @@ from tests.margins import find_attempts
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("skip_tile", [0, 3])
-def test_attention_wait_runs_out_and_context_survives(skip_tile):
+@pytest.mark.parametrize("impl,skip_tile", [(1, 0), (1, 3), (2, 0), (2, 3)])
+def test_attention_wait_runs_out_and_context_survives(impl, skip_tile):
     w = Workload("wait_test", 2, 8, 2, 128, 16, 24, 80, 1, (1104, 1104))
     seed = 5
     lens = synth.seq_lens(w, seed)
@@ -35,8 +35,10 @@ def test_attention_wait_runs_out_and_context_survives(skip_tile):
         T, _ = ctx.select_topk(0, q)
         miss, cnt, slot = ctx.index_diff(T, None)
         ctx.gather_coalesced(0, 0, miss, cnt, slot_base=w.top_k, urgent=True)
-        # two CTAs, so the first warp of CTA 0 has several tiles and both skip positions exist
-        ctx.set_attn_impl(1, 2)
+        # two CTAs (impl 1), or two per group (impl 2: CTA 0's cluster partner
+        # waits for it at the cluster barriers), so the first warp of CTA 0 has
+        # several tiles and both skip positions exist
+        ctx.set_attn_impl(impl, 2)
         assert ctx.device_status() == 0
         ctx.set_wait_test(50_000_000, skip_tile)
         t0 = time.perf_counter()
@@ -58,7 +60,7 @@ def test_attention_wait_runs_out_and_context_survives(skip_tile):
             assert_attn_close(o[0, rows].cpu().numpy(), ref.o)
             assert_attn_close(lse[0, rows].cpu().numpy(), ref.lse, what="lse")
     finally:
-        c.ctx.set_attn_impl(1, 0)
+        c.ctx.set_attn_impl(2, 0)
         c.close()
 
 
