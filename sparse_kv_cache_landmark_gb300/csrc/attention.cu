@@ -886,7 +886,7 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
                     const int32_t* __restrict__ slot, float* __restrict__ out_o, float* __restrict__ out_lse,
                     float* __restrict__ out_o_spec, float* __restrict__ out_lse_spec, int r, int Hkv, int k, int B,
                     int W, int Wcap, const int32_t* __restrict__ w_start, const int32_t* __restrict__ w_len,
-                    const int32_t* __restrict__ sp_cnt, int dep_wait, float scale_log2,
+                    const int32_t* __restrict__ sp_cnt, int dep_mode, float scale_log2,
                     int32_t* __restrict__ status, long long wait_ns, int skip_tile) {
     using WA = WarpAttn<D, NR>;
     using CF = AttnCluCfg<D, NR>;
@@ -906,6 +906,11 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
     const uint32_t S = max(1u, cluster_size()), rank = S > 1 ? cluster_rank() : 0u;
     const int bg = (int)(blockIdx.x / S);
     const bool tab = k <= CF::SLOT_CAP;
+    if (tid < ATT_WARPS * STG) mbar_init(smem_u32(&full[tid]), 1);
+    if (tid == 0) *s_abort = 0;
+    // dep_mode 2: launched as a programmatic dependent of the kernel before it
+    // on the stream, which may have written any input -- nothing is read before it is done
+    if (dep_mode == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     // the group's slot list into shared memory, asynchronously (read after the first copies are out)
     if (tab) {
         const int32_t* src = slot + (int64_t)bg * k;
@@ -919,8 +924,6 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
     const int ws = w_start ? __ldg(w_start + bg) : 0;
     const int t_sp = (n_sp + ATT_TILE - 1) / ATT_TILE;
     const int T = t_sp + (n_w + ATT_TILE - 1) / ATT_TILE;
-    if (tid < ATT_WARPS * STG) mbar_init(smem_u32(&full[tid]), 1);
-    if (tid == 0) *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
 
@@ -1022,6 +1025,9 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         refill();
     }
+    // the kernel behind this one on the stream may be scheduled now (it waits
+    // for this grid to finish before it reads anything)
+    if (dep_mode == 2) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (bad) atomicOr(status, bad);
     // every copy has landed before the ring is reused (bounded, as in the persistent kernel)
     if (lane == 0)
@@ -1107,7 +1113,10 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
     }
     // no CTA leaves (and frees its shared memory) while another may still read it
     if (S > 1) cluster_barrier();
-    if (dep_wait && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // dep_mode 1: launched as a programmatic dependent of a kernel whose output
+    // it does not read; it completes only after that kernel, so the launches
+    // behind it see that kernel's writes
+    if (dep_mode == 1 && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, int NR>
@@ -1172,8 +1181,9 @@ static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, con
 template <int D, int NR>
 static cudaError_t launch_cluster(const Ctx& c, int S, int buf, const void* q, const void* q_spec,
                                   const uint16_t* wk, const uint16_t* wv, const int32_t* slot, float* o, float* lse,
-                                  float* o_spec, float* lse_spec, cudaStream_t s, const int32_t* sp_cnt, bool pdl,
-                                  float scale_log2) {
+                                  float* o_spec, float* lse_spec, cudaStream_t s, const int32_t* sp_cnt,
+                                  int dep_mode, float scale_log2) {
+    const bool pdl = dep_mode != 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(c.G * S));
     cfg.blockDim = dim3(ATT_WARPS * 32);
@@ -1198,7 +1208,7 @@ static cudaError_t launch_cluster(const Ctx& c, int S, int buf, const void* q, c
     return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<D, NR>, (const uint16_t*)q, (const uint16_t*)q_spec,
                               (const uint16_t*)c.buf_k(buf), (const uint16_t*)c.buf_v(buf), wk, wv, slot, o, lse,
                               o_spec, lse_spec, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, (const int32_t*)c.g_wstart,
-                              (const int32_t*)c.g_wlen, sp_cnt, pdl ? 1 : 0, scale_log2, c.status,
+                              (const int32_t*)c.g_wlen, sp_cnt, dep_mode, scale_log2, c.status,
                               (long long)c.att_wait_ns, c.att_skip_tile);
 }
 
@@ -1212,8 +1222,11 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
     if (c.att_impl == 2 && fuse && c.clu_use[in_step ? 1 : 0]) {
         const int S = c.clu_S[in_step ? 1 : 0];
+        // a dependent of an independent kernel (pdl), else a dependent of whatever
+        // ran before it on the stream when the context allows it
+        const int dep_mode = pdl ? 1 : (c.att_pdl ? 2 : 0);
 #define KVO_CLU(D_, NR_) \
-        launch_cluster<D_, NR_>(c, S, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, s, sp_cnt, pdl, \
+        launch_cluster<D_, NR_>(c, S, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, s, sp_cnt, dep_mode, \
                                 scale_log2)
         if (c.d == 128) return nrows <= 8 ? KVO_CLU(128, 1) : KVO_CLU(128, 2);
         return nrows <= 8 ? KVO_CLU(64, 1) : KVO_CLU(64, 2);

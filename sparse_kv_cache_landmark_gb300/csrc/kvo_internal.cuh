@@ -110,6 +110,7 @@ struct Ctx {
     int att_cluster = 0;            // impl 2: CTAs per group asked for (0: automatic)
     int clu_S[2] = {1, 1};          // impl 2: CTAs per group, whole device and decode step
     bool clu_use[2] = {false, false};   // impl 2: clusters used (else the persistent kernel)
+    bool att_pdl = true;            // impl 2: launched as a programmatic dependent of the kernel before it
     int att_part_cap = 0;           // work items the partial-result buffers hold
     // TMA-staged kernel: balanced per-CTA tile ranges cut into work items, one
     // plan for the whole device (standalone calls) and one for the decode step,
