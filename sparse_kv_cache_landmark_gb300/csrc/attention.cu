@@ -215,6 +215,39 @@ struct WarpAttn {
         pv(vf, pa, al0, al1);
     }
 
+    // K and V fragments of one tile from a shared-memory stage of K rows then
+    // V rows (D channels each); rows past `rows` read the last valid row.  At a
+    // row pitch of 2D bytes all rows start in the same bank, so a 16-byte load
+    // phase (lanes g even and odd, t = 0..3) would hit few bank groups: lanes of
+    // odd g fetch the two 64-byte halves of their K run in swapped order (the
+    // phase's two K rows then use both halves of the banks), and lanes of odd t
+    // the two 16-byte chunks of their V run; the registers are put back in
+    // order after the loads.
+    static __device__ __forceinline__ void stage_frags(const uint16_t* ks, const uint16_t* vs, int rows, int gq, int tq,
+                                                       uint4 (&kf)[2][CH], uint4 (&vf)[4][CPT / 8]) {
+        const bool kx = CH >= 2 && (gq & 1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
+            uint4 t[CH];
+#pragma unroll
+            for (int s2 = 0; s2 < CH; ++s2) t[s2] = *reinterpret_cast<const uint4*>(kp + 32 * (CH >= 2 ? s2 ^ (int)kx : s2));
+#pragma unroll
+            for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = (CH >= 2 && kx) ? t[CH >= 2 ? s2 ^ 1 : s2] : t[s2];
+        }
+        constexpr int VC = CPT / 8;
+        const bool vx = VC >= 2 && (tq & 1);
+#pragma unroll
+        for (int vi = 0; vi < 4; ++vi) {
+            const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
+            uint4 t[VC];
+#pragma unroll
+            for (int c = 0; c < VC; ++c) t[c] = *reinterpret_cast<const uint4*>(vp + 8 * (VC >= 2 ? c ^ (int)vx : c));
+#pragma unroll
+            for (int c = 0; c < VC; ++c) vf[vi][c] = (VC >= 2 && vx) ? t[VC >= 2 ? c ^ 1 : c] : t[c];
+        }
+    }
+
     // Shared-memory layout of a warp's state: 8*NR rows of D floats.  Lane
     // (g, t) holds channels [2*CPT*t, 2*CPT*(t+1)) of rows g and 8+g (column
     // 2t of n-tile j is channel CPT*2t + j, column 2t+1 is CPT*(2t+1) + j), so
@@ -795,22 +828,10 @@ attn_tma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ q_s
             const int tb = (cc.tile0 + tl) * ATT_TILE;
             const int rows = min(ATT_TILE, cc.n_tok - tb);
             const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * CF::STAGE_BYTES);
-            const uint16_t* vs = ks + ATT_TILE * D;
-            // rows past the tile's end hold stale data: read the last valid row instead
+            // rows past the tile's end hold stale data: the last valid row is read instead
             uint4 kf[2][CH];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
-#pragma unroll
-                for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
-            }
             uint4 vf[4][CPT / 8];
-#pragma unroll
-            for (int vi = 0; vi < 4; ++vi) {
-                const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
-#pragma unroll
-                for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
-            }
+            WA::stage_frags(ks, ks + ATT_TILE * D, rows, gq, tq, kf, vf);
             stt.tile(kf, vf, tb, cc.n_tok, scale_log2, tq);
             // the stage's shared-memory reads are done (their values fed the mma):
             // order them before the async-proxy refill of the same stage
@@ -1004,21 +1025,9 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
         const int tb = (sp ? t : t - t_sp) * ATT_TILE, n_tok = sp ? n_sp : n_w;
         const int rows = min(ATT_TILE, n_tok - tb);
         const uint16_t* ks = reinterpret_cast<const uint16_t*>(ring + st * CF::STAGE_BYTES);
-        const uint16_t* vs = ks + ATT_TILE * D;
         uint4 kf[2][CH];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint16_t* kp = ks + min(8 * h + gq, rows - 1) * D + 8 * tq;
-#pragma unroll
-            for (int s2 = 0; s2 < CH; ++s2) kf[h][s2] = *reinterpret_cast<const uint4*>(kp + 32 * s2);
-        }
         uint4 vf[4][CPT / 8];
-#pragma unroll
-        for (int vi = 0; vi < 4; ++vi) {
-            const uint16_t* vp = vs + min(2 * tq + (vi & 1) + 8 * (vi >> 1), rows - 1) * D + CPT * gq;
-#pragma unroll
-            for (int c = 0; c < CPT / 8; ++c) vf[vi][c] = *reinterpret_cast<const uint4*>(vp + 8 * c);
-        }
+        WA::stage_frags(ks, ks + ATT_TILE * D, rows, gq, tq, kf, vf);
         stt.tile(kf, vf, tb, n_tok, scale_log2, tq);
         // the stage's reads are done: order them before the async-proxy refill
         __syncwarp();
