@@ -1229,11 +1229,15 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
     const int nrows = q_spec ? 2 * c.r : c.r;
     const Ctx::TmaPlan& pl = c.tma[in_step ? 1 : 0];
-    if (c.att_impl == 2 && fuse && c.clu_use[in_step ? 1 : 0]) {
+    // A dependent launch that waits for its predecessor at its end (pdl) keeps
+    // its CTAs resident until then, so it must fit in one wave: the persistent
+    // kernel's plan is exactly the resident slots, a cluster grid may not be.
+    if (c.att_impl == 2 && fuse && c.clu_use[in_step ? 1 : 0] && !pdl) {
         const int S = c.clu_S[in_step ? 1 : 0];
-        // a dependent of an independent kernel (pdl), else a dependent of whatever
-        // ran before it on the stream when the context allows it
-        const int dep_mode = pdl ? 1 : (c.att_pdl ? 2 : 0);
+        // a standalone call: a dependent of whatever ran before it on the stream
+        // (inside a decode step an early launch could hold SMs the step's gathers
+        // are about to take)
+        const int dep_mode = c.att_pdl && !in_step ? 2 : 0;
 #define KVO_CLU(D_, NR_) \
         launch_cluster<D_, NR_>(c, S, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, s, sp_cnt, dep_mode, \
                                 scale_log2)
@@ -1241,8 +1245,8 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
         return nrows <= 8 ? KVO_CLU(64, 1) : KVO_CLU(64, 2);
 #undef KVO_CLU
     }
-    // impl 2 with separate parts (fuse 0), or with too few groups to fill the
-    // device, uses the persistent kernel
+    // impl 2 with separate parts (fuse 0), with too few groups to fill the
+    // device, or launched to wait at its end, uses the persistent kernel
     if (c.att_impl >= 1) {
 #define KVO_TMA(D_, NR_) \
         launch_tma<D_, NR_>(c, pl, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, fuse, s, sp_cnt, pdl, \

@@ -146,6 +146,7 @@ struct Ctx {
     int gather_reserve_smem = 200 * 1024;   // flat engine: shared memory reserved per CTA (SM exclusivity)
     size_t scratch_bytes = 0;
     cudaStream_t s_compute = nullptr, s_prefetch = nullptr, s_urgent = nullptr;
+    cudaStream_t s_urgent2 = nullptr;   // a chain step's odd layers' copies
     // decode-step state
     int32_t* st_true = nullptr;     // [L][G][k]
     int32_t* st_pred = nullptr;     // [2][L][G][k]  predictions by step parity

@@ -164,18 +164,23 @@ kvo_status build_tma_plans(kvo::Ctx& c) {
         held = std::min(c.gather_ctas > 0 ? c.gather_ctas : 2 * c.n_sms, c.n_sms - 1);
     const int64_t step = (int64_t)c.tma_per_sm * (c.n_sms - held);
     // group-split clusters: as many CTAs per group as the resident CTAs allow,
-    // 1 .. 8 (the portable cluster size); chosen automatically only when the
-    // groups' CTAs then fill at least 3/4 of the resident CTA slots -- fewer
-    // groups leave SMs idle, and the persistent kernel's balanced tile ranges
-    // measured faster there
+    // 1 .. 8 (the portable cluster size), one more when that fills less than
+    // 3/4 of the slots and one more stays within 5/4 of them (the Llama layer
+    // beside the decode step's gather: 256 CTAs on 228 slots beat 128); chosen
+    // automatically only when the groups' CTAs then fill at least 3/4 of the
+    // slots -- fewer groups leave SMs idle, and the persistent kernel's
+    // balanced tile ranges measured faster there
     auto plan_clu = [&](int i, int64_t slots) {
         if (c.att_cluster > 0) {
             c.clu_S[i] = c.att_cluster;
             c.clu_use[i] = true;
             return;
         }
-        c.clu_S[i] = (int)std::max<int64_t>(1, std::min<int64_t>(8, slots / std::max(1, c.G)));
-        c.clu_use[i] = 4 * (int64_t)c.G * c.clu_S[i] >= 3 * slots;
+        const int64_t G = std::max(1, c.G);
+        int64_t S = std::max<int64_t>(1, std::min<int64_t>(8, slots / G));
+        if (4 * G * S < 3 * slots && S < 8 && 4 * G * (S + 1) <= 5 * slots) ++S;
+        c.clu_S[i] = (int)S;
+        c.clu_use[i] = 4 * G * S >= 3 * slots;
     };
     plan_clu(0, (int64_t)c.clu_per_sm * c.n_sms);
     plan_clu(1, (int64_t)c.clu_per_sm * (c.n_sms - held));
@@ -212,7 +217,7 @@ void free_ctx(kvo::Ctx& c) {
     if (c.ev_gout) cudaEventDestroy(c.ev_gout);
     for (cudaGraphExec_t g : c.gexec) if (g) cudaGraphExecDestroy(g);
     for (cudaEvent_t e : c.prof_pool) if (e) cudaEventDestroy(e);
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph}) if (s) cudaStreamDestroy(s);
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph}) if (s) cudaStreamDestroy(s);
 }
 
 // Records a timing event on `s` when profiling is on; returns its pool index or -1.
@@ -314,6 +319,7 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_compute, cudaStreamNonBlocking, (least + greatest) / 2));
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_prefetch, cudaStreamNonBlocking, least));
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_urgent, cudaStreamNonBlocking, greatest));
+    KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_urgent2, cudaStreamNonBlocking, greatest));
     size_t sb = 0;
     KVO_CUDA(&c, dalloc(&c.g_off, sizeof(int64_t) * c.G, &sb));
     KVO_CUDA(&c, dalloc(&c.g_C, sizeof(int32_t) * c.G, &sb));
@@ -389,8 +395,9 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         const size_t rows = (size_t)c.batch * c.Hq;
         KVO_CUDA(&c, dalloc(&c.res_hit_slot, sizeof(int32_t) * lg * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_hit_cnt, sizeof(int32_t) * lg, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * rows * c.d, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * rows, &sb));
+        // two layers' worth: a chain step attends to layer l's hits while layer l - 1's merge runs
+        KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * 2 * rows * c.d, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * 2 * rows, &sb));
         KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
         KVO_CUDA(&c, dalloc(&c.res_pfbit, (size_t)c.L * c.G * 2 * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_stat, sizeof(unsigned long long) * 2 * c.L, &sb));
@@ -528,7 +535,7 @@ kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* con
 
 kvo_status kv_offload_destroy(kvo_ctx* ctx) {
     if (!ctx) return KVO_OK;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph})
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph})
         if (s) cudaStreamSynchronize(s);
     free_ctx(ctx->c);
     delete ctx;
@@ -782,21 +789,22 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     int32_t* pred_next = c.st_pred + (size_t)(1 - par) * c.L * gk;
     const bool have = c.have_pred;
     // Without speculation, with no prefetch of an earlier step still in flight
-    // and no layer rebuilding keys beside its copies, the step is two chains:
-    // the compute stream selects and assigns layer after layer, and the urgent
-    // stream copies each layer's missing blocks and attends to the layer once
-    // its assign is done -- so layer l + 1's selection runs beside layer l's
-    // copy and attention.
+    // and no layer rebuilding keys beside its copies, the step is four chains:
+    // the compute stream selects and assigns layer after layer; two urgent
+    // streams take the layers in turn, each copying a layer's missing blocks
+    // once its assign is done and attending to the layer's resident blocks
+    // beside the copy (a dependent launch that follows the copy's SMs, so the
+    // copy keeps them); the attention stream (the prefetch stream, idle without
+    // speculation) attends to the fetched blocks once they have landed and
+    // merges.  So layer l + 1's copy starts while layer l's hit pass runs, and
+    // the host link, HBM and the selection of later layers stay busy together.
     const bool alone_step = resident_alone(c, q_spec);
     const cudaStream_t sc = c.s_compute;                          // select, assign (and attention when speculating)
-    const cudaStream_t su = c.s_urgent;                           // urgent copies (and attention in a chain step)
-    const cudaStream_t sa = alone_step ? su : sc;                 // attention
+    const cudaStream_t sa = alone_step ? c.s_prefetch : sc;       // attention
 
     KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) {
-        if (alone_step && s == c.s_prefetch) continue;
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2})
         KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
-    }
     int cur_layer = -1;
     auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
         int e0, e1;
@@ -824,6 +832,7 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         int32_t* dsl = c.res_dslot + l * gk;
         int32_t* hit_slot = c.res_hit_slot + l * gk;       // per layer: layer l + 1's assign runs beside
         int32_t* hit_cnt = c.res_hit_cnt + (size_t)l * c.G;  // layer l's attention in a chain step
+        const cudaStream_t su = alone_step && (l & 1) ? c.s_urgent2 : c.s_urgent;   // urgent copies
         const bool pending = c.res_pending[l] != 0;
         // the previous step's prefetch of this layer has read T and written the slot table
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rassign[l], 0));
@@ -832,9 +841,8 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, sc);
         }));
         // A chain step splits attention: the blocks resident already and the window
-        // are attended beside the urgent copies (a programmatic dependent launch,
-        // dispatched once the copy's SM-exclusive CTAs are all resident), the
-        // fetched blocks after them, and the two results merge by log-sum-exp.
+        // are attended beside the urgent copies, the fetched blocks after them,
+        // and the two results merge by log-sum-exp.
         const bool split = alone_step && c.att_impl >= 1 && !o_spec;
         // 2. urgent assign: T resident, sparing the prediction fetched for this step
         KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
@@ -844,6 +852,9 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // 3. urgent gather of the blocks that were missing
         KVO_CUDA(&c, cudaEventRecord(E.sel[l], sc));
         KVO_CUDA(&c, cudaStreamWaitEvent(su, E.sel[l], 0));
+        // layer l's hit pass reuses layer l - 2's half of the hit-pass scratch:
+        // that layer's merge has read it
+        if (split && l >= 2) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.attn[l - 2], 0));
         // without a prediction nothing is spared: in-flight prefetch copies must land first
         if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
@@ -851,14 +862,24 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask);
         }));
         if (split) {
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
-                return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, c.res_oA, c.res_lA, nullptr,
-                                             nullptr, 1, sa, true, hit_cnt, true);
+            // hits + window beside the copy: a programmatic dependent of the copy,
+            // dispatched once the copy's SM-exclusive CTAs are all resident (so it
+            // cannot take their SMs), completing after it; layer l - 1's merge may
+            // still run -- it reads the other half of the hit-pass scratch
+            float* oA = c.res_oA + (size_t)(l & 1) * o_layer;
+            float* lA = c.res_lA + (size_t)(l & 1) * lse_layer;
+            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, su, [&] {
+                return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, su, true,
+                                             hit_cnt, true);
             }));
+            // the fetched blocks once they have landed, merged with the hits
+            KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
+            KVO_CUDA(&c, cudaStreamWaitEvent(sa, E.urg[l], 0));
             KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
-                return kvo::launch_attn_merge_part(c, buf, ql, dsl, mcnt, c.res_oA, c.res_lA, o + l * o_layer,
+                return kvo::launch_attn_merge_part(c, buf, ql, dsl, mcnt, oA, lA, o + l * o_layer,
                                                    lse + l * lse_layer, sa);
             }));
+            KVO_CUDA(&c, cudaEventRecord(E.attn[l], sa));
             continue;
         }
         if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
@@ -866,10 +887,8 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
                 return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, sc);
             }));
         // 4. attention over the resident set once the urgent and prefetched blocks have landed
-        if (!alone_step) {
-            KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
-            KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.urg[l], 0));
-        }
+        KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
+        KVO_CUDA(&c, cudaStreamWaitEvent(sa, E.urg[l], 0));
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rpref[l], 0));
         c.res_pending[l] = 0;
         KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
@@ -896,8 +915,10 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             c.res_pending[l] = 1;
         }
     }
-    // the caller's stream waits for the outputs; prefetches stay in flight
-    for (cudaStream_t s : {c.s_compute, c.s_urgent}) {
+    // the caller's stream waits for the outputs; prefetches stay in flight (a
+    // chain step's attention stream is joined)
+    for (cudaStream_t s : {c.s_compute, c.s_urgent, c.s_prefetch, c.s_urgent2}) {
+        if (s == c.s_prefetch && !alone_step) break;
         KVO_CUDA(&c, cudaEventRecord(E.start, s));
         KVO_CUDA(&c, cudaStreamWaitEvent(s_user, E.start, 0));
     }
@@ -977,7 +998,7 @@ kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     if (enable && ctx->c.gather_engine == 4)
         return fail(&ctx->c, KVO_ERR_STATE, "graph replay needs a device-side gather engine (not engine 4)");
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph})
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph})
         cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     ctx->c.use_graphs = enable != 0;
@@ -1028,7 +1049,7 @@ kvo_status kvo_append(kvo_ctx* ctx, const void* k_new, const void* v_new, kvo_st
 
 kvo_status kvo_reset_prediction(kvo_ctx* ctx) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
     ctx->c.have_pred = false;
     ctx->c.step_parity = 0;
     return KVO_OK;
@@ -1045,7 +1066,7 @@ kvo_status kvo_device_status(kvo_ctx* ctx, int32_t* code_out, kvo_stream_t strea
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
     if (stream) KVO_CUDA(&c, cudaStreamSynchronize((cudaStream_t)stream));
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     int32_t v = 0;
     KVO_CUDA(&c, cudaMemcpy(&v, c.status, sizeof(v), cudaMemcpyDeviceToHost));
     KVO_CUDA(&c, cudaMemset(c.status, 0, sizeof(int32_t)));
@@ -1085,7 +1106,7 @@ kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (layer < 0 || layer >= c.L || !slots_out) return fail(&c, KVO_ERR_INVALID, "bad layer or null output");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     const size_t n = (size_t)c.G * 2 * c.k;
     KVO_CUDA(&c, cudaMemcpy(slots_out, c.res_slots + (size_t)layer * n, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
     return KVO_OK;
@@ -1097,7 +1118,7 @@ kvo_status kvo_set_lowrank_keys(kvo_ctx* ctx, int layer, int rank, const void* c
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "bad layer");
     if (rank < 0 || rank > 64) return fail(&c, KVO_ERR_INVALID, "rank must be in 0..64");
     if (rank > 0 && (!coef || !basis)) return fail(&c, KVO_ERR_INVALID, "rank > 0 needs coef and basis");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     drop_graphs(c);
     c.lr_rank[layer] = rank;
     c.lr_coef[layer] = rank > 0 ? (const uint16_t*)coef : nullptr;
@@ -1110,7 +1131,7 @@ kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (blocks < -1) return fail(&c, KVO_ERR_INVALID, "blocks must be >= -1");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     c.res_budget = blocks;
     return KVO_OK;
 }
@@ -1120,7 +1141,7 @@ kvo_status kvo_set_spec_policy(kvo_ctx* ctx, int mode) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (mode < 0 || mode > 1) return fail(&c, KVO_ERR_INVALID, "mode must be 0 or 1");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph})
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph})
         KVO_CUDA(&c, cudaStreamSynchronize(s));
     drop_graphs(c);
     // every layer starts a fresh window with its prefetch on
@@ -1136,7 +1157,7 @@ kvo_status kvo_spec_stats(kvo_ctx* ctx, int64_t* out3) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (!out3) return fail(&c, KVO_ERR_INVALID, "null output");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     std::vector<unsigned long long> h(2 * (size_t)c.L), p(8 * (size_t)c.L);
     KVO_CUDA(&c, cudaMemcpy(h.data(), c.res_stat, sizeof(unsigned long long) * 2 * c.L, cudaMemcpyDeviceToHost));
     KVO_CUDA(&c, cudaMemcpy(p.data(), c.res_pol, sizeof(unsigned long long) * 8 * c.L, cudaMemcpyDeviceToHost));
@@ -1153,7 +1174,7 @@ kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (!out2) return fail(&c, KVO_ERR_INVALID, "null output");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     unsigned long long h[2];
     KVO_CUDA(&c, cudaMemcpy(h, c.res_fetched, sizeof(h), cudaMemcpyDeviceToHost));
     out2[0] = (int64_t)h[0];
@@ -1191,7 +1212,7 @@ kvo_status kvo_plan_attention(int n_groups, int sparse_tokens, int window_tokens
 
 kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     const int max_threads = ctx->c.gather_engine == 3 ? 1024 : kvo::GATHER_THREADS;
     if (ctas < 0 || ctas > 65535 || threads < 32 || threads > max_threads || threads % 32 ||
@@ -1206,7 +1227,7 @@ kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll)
 
 kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     if (smem_bytes < 0 || smem_bytes > 227 * 1024 - 128)
         return fail(&ctx->c, KVO_ERR_INVALID, "0 <= smem_bytes <= 232320 (227 KiB less 128 bytes)");
@@ -1216,7 +1237,7 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
 
 kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     // engine 1: 4 batches per driver; engine 2: 8 batches per driver (one driver per CTA)
     if (engine < 0 || engine > 4 || drivers < 0 || drivers > 4096)
@@ -1249,7 +1270,7 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas) {
     if (impl < 0 || impl > 2 || ctas < 0 || (impl == 2 && ctas > 8))
         return fail(&ctx->c, KVO_ERR_INVALID,
                     "attention implementation must be 0, 1 or 2, ctas >= 0, and ctas <= 8 for implementation 2");
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     ctx->c.att_impl = impl;
     ctx->c.tma_ctas = impl == 2 ? 0 : ctas;
@@ -1262,7 +1283,7 @@ kvo_status kvo_set_wait_test(kvo_ctx* ctx, int64_t limit_ns, int skip_tile) {
     kvo::Ctx& c = ctx->c;
     if (limit_ns < 1000000 || limit_ns > 10000000000LL || skip_tile < -1)
         return fail(&c, KVO_ERR_INVALID, "need 1 ms <= limit_ns <= 10 s and skip_tile >= -1");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     drop_graphs(c);
     c.att_wait_ns = limit_ns;
     c.att_skip_tile = skip_tile;
