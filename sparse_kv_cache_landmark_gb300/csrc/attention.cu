@@ -1167,7 +1167,7 @@ template <int D, int NR>
 static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, const void* q, const void* q_spec,
                               const uint16_t* wk, const uint16_t* wv, const int32_t* slot, float* o, float* lse,
                               float* o_spec, float* lse_spec, int fuse, cudaStream_t s, const int32_t* sp_cnt,
-                              bool pdl, float scale_log2) {
+                              bool pdl, float scale_log2, float* part_o, float* part_ml, uint32_t* done) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(ATT_WARPS * 32);
@@ -1181,7 +1181,7 @@ static cudaError_t launch_tma(const Ctx& c, const Ctx::TmaPlan& pl, int buf, con
     return cudaLaunchKernelEx(&cfg, attn_tma_kernel<D, NR>, (const uint16_t*)q, (const uint16_t*)q_spec,
                               (const uint16_t*)c.buf_k(buf), (const uint16_t*)c.buf_v(buf), wk, wv, slot,
                               (const int4*)pl.items, (const int32_t*)pl.cta, (const int32_t*)pl.first,
-                              (const int32_t*)pl.count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec,
+                              (const int32_t*)pl.count, part_o, part_ml, done, o, lse, o_spec,
                               lse_spec, fuse, c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, (const int32_t*)c.g_wstart,
                               (const int32_t*)c.g_wlen, sp_cnt, pdl ? 1 : 0, scale_log2, c.status,
                               (long long)c.att_wait_ns, c.att_skip_tile);
@@ -1223,7 +1223,12 @@ static cudaError_t launch_cluster(const Ctx& c, int S, int buf, const void* q, c
 
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step, const int32_t* sp_cnt, bool pdl) {
+                             bool in_step, const int32_t* sp_cnt, bool pdl, int scratch) {
+    // the scratch set of the work-item kernels: partial results and tickets
+    const size_t prow = 2 * c.r <= 16 ? 2 * c.r : c.r;
+    float* part_o = c.att_part_o + (scratch ? (size_t)c.att_part_cap * prow * c.d : 0);
+    float* part_ml = c.att_part_ml + (scratch ? (size_t)c.att_part_cap * prow * 2 : 0);
+    uint32_t* done = c.att_done + (scratch ? c.G : 0);
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     const uint16_t* wk = c.W > 0 ? c.k_win[layer] : nullptr;
     const uint16_t* wv = c.W > 0 ? c.v_win[layer] : nullptr;
@@ -1250,7 +1255,7 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
     if (c.att_impl >= 1) {
 #define KVO_TMA(D_, NR_) \
         launch_tma<D_, NR_>(c, pl, buf, q, q_spec, wk, wv, slot, o, lse, o_spec, lse_spec, fuse, s, sp_cnt, pdl, \
-                            scale_log2)
+                            scale_log2, part_o, part_ml, done)
         if (c.d == 128) return nrows <= 8 ? KVO_TMA(128, 1) : KVO_TMA(128, 2);
         return nrows <= 8 ? KVO_TMA(64, 1) : KVO_TMA(64, 2);
 #undef KVO_TMA
@@ -1260,7 +1265,7 @@ cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, co
 #define KVO_ATT(D_, NR_)                                                                                         \
     attn_kernel<D_, NR_><<<c.n_att_items, ATT_WARPS * 32, 0, s>>>(                                               \
         (const uint16_t*)q, (const uint16_t*)q_spec, c.buf_k(buf), c.buf_v(buf), wk, wv, slot, c.att_items,       \
-        c.att_first, c.att_count, c.att_part_o, c.att_part_ml, c.att_done, o, lse, o_spec, lse_spec, fuse,      \
+        c.att_first, c.att_count, part_o, part_ml, done, o, lse, o_spec, lse_spec, fuse,                          \
         c.batch, c.r, c.Hkv, c.k, c.B, c.W, c.Wcap, c.g_wstart, c.g_wlen, scale_log2, c.status)
     if (c.d == 128) {
         if (nrows <= 8) KVO_ATT(128, 1); else KVO_ATT(128, 2);

@@ -128,9 +128,9 @@ struct Ctx {
     } tma[2];
     long long att_wait_ns = 2000000000LL;   // limit of each mbarrier wait of the TMA-staged kernel
     int att_skip_tile = -1;         // >= 0: CTA 0 announces this tile without copying it (wait test)
-    float* att_part_o = nullptr;    // [items][r][d]
-    float* att_part_ml = nullptr;   // [items][r][2]
-    uint32_t* att_done = nullptr;   // [G]
+    float* att_part_o = nullptr;    // [2][items][r][d]: two sets (launches side by side)
+    float* att_part_ml = nullptr;   // [2][items][r][2]
+    uint32_t* att_done = nullptr;   // [2][G]
     int32_t* status = nullptr;      // device status word
     // Gather launch shape and engine.  Default: the flat lane-load engine on 38
     // SM-exclusive CTAs of 1024 threads, 2 loads of K and of V in flight per lane.
@@ -228,8 +228,12 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
 // ---------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() after the launch.
 cudaError_t launch_landmarks(const Ctx& c, int layer, cudaStream_t s);
+struct ResAssignArgs;   // resident_assign.cuh
+// With `assign` (single-query steps only), the last CTA of each group also
+// assigns the group's resident slots for the true index it selected.
 cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
-                          int32_t* idx_pred, cudaStream_t s);
+                          int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign = nullptr);
+cudaError_t prepare_select_assign(const Ctx& c);
 cudaError_t launch_index_diff(const Ctx& c, const int32_t* idx_true, const int32_t* idx_pred, int32_t* miss,
                               int32_t* miss_cnt, int32_t* slot, cudaStream_t s);
 cudaError_t launch_coalesce(const Ctx& c, const int32_t* idx, const int32_t* cnt, int slot_base, int32_t* runs,
@@ -248,14 +252,21 @@ cudaError_t launch_resident_assign(const Ctx& c, int layer, const int32_t* need,
                                    int phase, cudaStream_t s, int max_fetch = -1, int32_t* hit_slot = nullptr,
                                    int32_t* hit_cnt = nullptr);
 cudaError_t prepare_resident(const Ctx& c);
+// The arguments launch_resident_assign passes (need, phase 0 or 1, ...), for
+// the selection kernel's fused assignment.
+ResAssignArgs resident_assign_args(const Ctx& c, int layer, const int32_t* need, const int32_t* keep,
+                                   int32_t* out_ids, int32_t* out_cnt, int32_t* out_dslot, int32_t* slot_of,
+                                   int phase, int max_fetch, int32_t* hit_slot, int32_t* hit_cnt);
 // Optional for the TMA-staged kernel only: sp_cnt[g] limits the sparse part to
 // the first sp_cnt[g] entries of the slot list; pdl launches it as a
 // programmatic dependent of the kernel before it on the stream (it starts once
 // that kernel's CTAs are all resident, and ends only after that kernel has
-// completed).
+// completed).  scratch (0 or 1) picks one of the two sets of partial results
+// and tickets the work-item kernels use, so two launches may run side by side.
 cudaError_t launch_attention(const Ctx& c, int layer, int buf, const void* q, const void* q_spec, const int32_t* slot,
                              float* o, float* lse, float* o_spec, float* lse_spec, int fuse, cudaStream_t s,
-                             bool in_step = false, const int32_t* sp_cnt = nullptr, bool pdl = false);
+                             bool in_step = false, const int32_t* sp_cnt = nullptr, bool pdl = false,
+                             int scratch = 0);
 // Attention over the first cnt[g] entries of a slot list, merged by lse with a
 // prior part into (o, lse); merge_part_split(c) CTAs per group.
 constexpr int MP_SPLIT_MAX = 8;

@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "kvo_internal.cuh"
+#include "resident_assign.cuh"
 
 struct kvo_ctx {
     kvo::Ctx c;
@@ -62,8 +63,9 @@ cudaError_t part_alloc(kvo::Ctx& c, int items) {
     c.att_part_ml = nullptr;
     c.att_part_cap = 0;
     const size_t rows = 2 * c.r <= 16 ? 2 * c.r : c.r;   // room for co-batched speculative rows
-    cudaError_t e = dalloc(&c.att_part_o, sizeof(float) * items * rows * c.d, nullptr);
-    if (e == cudaSuccess) e = dalloc(&c.att_part_ml, sizeof(float) * items * rows * 2, nullptr);
+    // two sets: a chain step runs two layers' hit passes side by side
+    cudaError_t e = dalloc(&c.att_part_o, sizeof(float) * 2 * items * rows * c.d, nullptr);
+    if (e == cudaSuccess) e = dalloc(&c.att_part_ml, sizeof(float) * 2 * items * rows * 2, nullptr);
     if (e == cudaSuccess) c.att_part_cap = items;
     return e;
 }
@@ -408,6 +410,7 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, cudaMemsetAsync(c.res_pol_ticket, 0, sizeof(uint32_t) * c.L, c.s_compute));
         c.res_pending.assign(c.L, 0);
         KVO_CUDA(&c, kvo::prepare_resident(c));
+        KVO_CUDA(&c, kvo::prepare_select_assign(c));
     }
     // selection scratch and work items
     const size_t Cmax4 = (size_t)((c.Cmax + 3) & ~3);
@@ -459,8 +462,8 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaMemcpy(c.att_first, afirst.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
     KVO_CUDA(&c, cudaMemcpy(c.att_count, acount.data(), sizeof(int32_t) * c.G, cudaMemcpyHostToDevice));
     KVO_CUDA(&c, part_alloc(c, (int)att.size()));
-    KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * c.G, &sb));
-    KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
+    KVO_CUDA(&c, dalloc(&c.att_done, sizeof(uint32_t) * 2 * c.G, &sb));
+    KVO_CUDA(&c, cudaMemsetAsync(c.att_done, 0, sizeof(uint32_t) * 2 * c.G, c.s_compute));
     KVO_CUDA(&c, kvo::prepare_attention(c));
     if (c.resident) {   // partials of the fetched-block attention of chain steps
         const size_t parts = (size_t)c.G * kvo::merge_part_split(c) * c.r;
@@ -836,19 +839,29 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         const bool pending = c.res_pending[l] != 0;
         // the previous step's prefetch of this layer has read T and written the slot table
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rassign[l], 0));
-        // 1. retrieval index (true; speculative -> next step's prediction)
-        KVO_CUDA(&c, timed(kvo::PK_SELECT, sc, [&] {
-            return kvo::launch_select(c, l, ql, qsl, T, q_spec ? pred_next + l * gk : nullptr, sc);
-        }));
         // A chain step splits attention: the blocks resident already and the window
         // are attended beside the urgent copies, the fetched blocks after them,
         // and the two results merge by log-sum-exp.
         const bool split = alone_step && c.att_impl >= 1 && !o_spec;
-        // 2. urgent assign: T resident, sparing the prediction fetched for this step
-        KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
-            return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0,
-                                               sc, -1, split ? hit_slot : nullptr, split ? hit_cnt : nullptr);
-        }));
+        // 1. retrieval index (true; speculative -> next step's prediction), and
+        // 2. urgent assign: T resident, sparing the prediction fetched for this
+        // step -- without a speculative query, in the selection kernel itself
+        if (!q_spec) {
+            const kvo::ResAssignArgs aa =
+                kvo::resident_assign_args(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot, 0, -1,
+                                          split ? hit_slot : nullptr, split ? hit_cnt : nullptr);
+            KVO_CUDA(&c, timed(kvo::PK_SELECT, sc, [&] {
+                return kvo::launch_select(c, l, ql, nullptr, T, nullptr, sc, &aa);
+            }));
+        } else {
+            KVO_CUDA(&c, timed(kvo::PK_SELECT, sc, [&] {
+                return kvo::launch_select(c, l, ql, qsl, T, pred_next + l * gk, sc);
+            }));
+            KVO_CUDA(&c, timed(kvo::PK_DIFF, sc, [&] {
+                return kvo::launch_resident_assign(c, l, T, have ? pred_cur + l * gk : nullptr, miss, mcnt, dsl, slot,
+                                                   0, sc, -1, split ? hit_slot : nullptr, split ? hit_cnt : nullptr);
+            }));
+        }
         // 3. urgent gather of the blocks that were missing
         KVO_CUDA(&c, cudaEventRecord(E.sel[l], sc));
         KVO_CUDA(&c, cudaStreamWaitEvent(su, E.sel[l], 0));
@@ -870,7 +883,7 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             float* lA = c.res_lA + (size_t)(l & 1) * lse_layer;
             KVO_CUDA(&c, timed(kvo::PK_ATTENTION, su, [&] {
                 return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, su, true,
-                                             hit_cnt, true);
+                                             hit_cnt, true, l & 1);
             }));
             // the fetched blocks once they have landed, merged with the hits
             KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));

@@ -16,6 +16,7 @@
 // last CTA of a group (atomic ticket) finishes a 4-pass MSB radix select on
 // the L2-resident keys and compacts the winners in ascending id order.
 #include "kvo_internal.cuh"
+#include "resident_assign.cuh"
 
 namespace kvo {
 
@@ -123,13 +124,17 @@ __device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, in
 template <bool BF16LM, int SEL_RPT>
 constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 4 : (BF16LM ? 1 : 4); }
 
-template <int D, bool BF16LM, bool DUAL, int SEL_RPT>
+// ASSIGN: the last CTA of a group then assigns the group's resident slots for
+// its true index (the routine of resident_assign.cuh, `aa` with need = the
+// true index; res_assign_ints(k) ints of dynamic shared memory), so a step
+// without a speculative query needs no separate assignment launch.
+template <int D, bool BF16LM, bool DUAL, int SEL_RPT, bool ASSIGN>
 __global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
 select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
               const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
               uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
               int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
-              int Hkv, int k) {
+              int Hkv, int k, const ResAssignArgs aa) {
     constexpr int NQ = DUAL ? 2 : 1;
     __shared__ __align__(16) float u_s[NQ][D];
     __shared__ uint32_t h_s[NQ][256];
@@ -364,33 +369,69 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         __syncthreads();
     }
     if (tid == 0) done[bg] = 0u;
+    if constexpr (ASSIGN) {
+        // the true index this CTA wrote is visible to all its threads after the
+        // barrier that closed the loop above
+        extern __shared__ __align__(16) int32_t sel_rs[];
+        __shared__ uint32_t s_tot;
+        resident_assign_group(aa, bg, sel_rs, warp_sums, &s_tot);
+    }
 }
 
 cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
-                          int32_t* idx_pred, cudaStream_t s) {
+                          int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign) {
     const int Cmax4 = (c.Cmax + 3) & ~3;
     const bool dual = q_spec != nullptr;
     const bool bf = c.B == 1;
+    if (assign && dual) return cudaErrorInvalidValue;     // the fused assignment is for single-query steps
+    ResAssignArgs aa{};
+    size_t dyn = 0;
+    if (assign) {
+        aa = *assign;
+        aa.need = idx_true;
+        dyn = sizeof(int32_t) * res_assign_ints(c.k);
+    }
+#define KVO_SEL_L(D_, BF_, DU_, RPT_, AS_)                                                                     \
+    select_kernel<D_, BF_, DU_, RPT_, AS_><<<c.n_sel_items, SEL_THREADS, dyn, s>>>(                            \
+        c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C, c.sel_keys, \
+        c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k, aa)
 #define KVO_SEL(D_, BF_, DU_)                                                                                  \
     do {                                                                                                       \
-        if (c.sel_rpt == 1)                                                                                    \
-            select_kernel<D_, BF_, DU_, 1><<<c.n_sel_items, SEL_THREADS, 0, s>>>(                              \
-                c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C,   \
-                c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k);  \
-        else                                                                                                   \
-            select_kernel<D_, BF_, DU_, 4><<<c.n_sel_items, SEL_THREADS, 0, s>>>(                              \
-                c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C,   \
-                c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k);  \
+        if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, DU_, 1, false); else KVO_SEL_L(D_, BF_, DU_, 4, false);         \
     } while (0)
-    if (c.d == 128) {
+#define KVO_SEL_A(D_, BF_)                                                                                     \
+    do {                                                                                                       \
+        if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, false, 1, true); else KVO_SEL_L(D_, BF_, false, 4, true);       \
+    } while (0)
+    if (assign) {
+        if (c.d == 128) { if (bf) KVO_SEL_A(128, true); else KVO_SEL_A(128, false); }
+        else            { if (bf) KVO_SEL_A(64, true); else KVO_SEL_A(64, false); }
+    } else if (c.d == 128) {
         if (bf) { if (dual) KVO_SEL(128, true, true); else KVO_SEL(128, true, false); }
         else    { if (dual) KVO_SEL(128, false, true); else KVO_SEL(128, false, false); }
     } else {
         if (bf) { if (dual) KVO_SEL(64, true, true); else KVO_SEL(64, true, false); }
         else    { if (dual) KVO_SEL(64, false, true); else KVO_SEL(64, false, false); }
     }
+#undef KVO_SEL_A
 #undef KVO_SEL
+#undef KVO_SEL_L
     return cudaGetLastError();
+}
+
+// Dynamic shared memory of the fused selection + assignment kernels (the
+// assignment's lists; above the default 48 KB only for k > 2457).
+cudaError_t prepare_select_assign(const Ctx& c) {
+    const int bytes = (int)(sizeof(int32_t) * res_assign_ints(c.k));
+    cudaError_t e = cudaSuccess;
+#define KVO_SEL_ATTR(D_, BF_, RPT_)                                                                            \
+    if (e == cudaSuccess)                                                                                      \
+        e = cudaFuncSetAttribute(select_kernel<D_, BF_, false, RPT_, true>,                                    \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+    KVO_SEL_ATTR(128, true, 1); KVO_SEL_ATTR(128, true, 4); KVO_SEL_ATTR(128, false, 1); KVO_SEL_ATTR(128, false, 4);
+    KVO_SEL_ATTR(64, true, 1); KVO_SEL_ATTR(64, true, 4); KVO_SEL_ATTR(64, false, 1); KVO_SEL_ATTR(64, false, 4);
+#undef KVO_SEL_ATTR
+    return e;
 }
 
 }  // namespace kvo
