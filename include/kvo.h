@@ -560,7 +560,8 @@ kvo_status kvo_plan_attention(int n_groups, int sparse_tokens, int window_tokens
  * the step launches, on the stream it runs on; kvo_profile(ctx, 0) stops.
  * kvo_profile_read synchronizes, then writes per kernel kind the summed
  * launch durations (ms) and launch counts, and clears the record.  Kinds:
- * 0 select, 1 index diff (and residency assignment), 2 run coalescing,
+ * 0 select (with resident = 1 and no speculative query, the urgent residency
+ * assignment runs inside it), 1 index diff (and residency assignment), 2 run coalescing,
  * 3 prefetch gather, 4 urgent gather, 5 attention, 6 low-rank key
  * reconstruction (n_kinds >= 7).
  */

@@ -930,7 +930,8 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
     if (tid < ATT_WARPS * STG) mbar_init(smem_u32(&full[tid]), 1);
     if (tid == 0) *s_abort = 0;
     // dep_mode 2: launched as a programmatic dependent of the kernel before it
-    // on the stream, which may have written any input -- nothing is read before it is done
+    // on the stream, which may have written any input -- nothing is read before
+    // it is done (0: an ordinary launch)
     if (dep_mode == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     // the group's slot list into shared memory, asynchronously (read after the first copies are out)
     if (tab) {
@@ -1122,10 +1123,6 @@ attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
     }
     // no CTA leaves (and frees its shared memory) while another may still read it
     if (S > 1) cluster_barrier();
-    // dep_mode 1: launched as a programmatic dependent of a kernel whose output
-    // it does not read; it completes only after that kernel, so the launches
-    // behind it see that kernel's writes
-    if (dep_mode == 1 && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, int NR>
@@ -1192,7 +1189,7 @@ static cudaError_t launch_cluster(const Ctx& c, int S, int buf, const void* q, c
                                   const uint16_t* wk, const uint16_t* wv, const int32_t* slot, float* o, float* lse,
                                   float* o_spec, float* lse_spec, cudaStream_t s, const int32_t* sp_cnt,
                                   int dep_mode, float scale_log2) {
-    const bool pdl = dep_mode != 0;
+    const bool pdl = dep_mode == 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(c.G * S));
     cfg.blockDim = dim3(ATT_WARPS * 32);
