@@ -14,6 +14,7 @@ namespace kvo {
 
 // ---------------------------------------------------------------- tunables
 constexpr int SEL_THREADS = 256;          // select: threads per CTA
+constexpr int SEL_KEY_CACHE = 8192;       // select: keys per group the last CTA stages in shared memory (32 KB)
 constexpr int SEL_RPT_MAX = 4;            // select: landmark rows per thread (1 or 4, chosen at init)
 constexpr int ATT_WARPS = 4;              // attention: warps per CTA
 constexpr int ATT_TILE = 16;              // attention: tokens per mma tile

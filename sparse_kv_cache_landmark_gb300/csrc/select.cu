@@ -15,6 +15,8 @@
 // write order-preserving uint32 keys and a histogram of their top 8 bits; the
 // last CTA of a group (atomic ticket) finishes a 4-pass MSB radix select on
 // the L2-resident keys and compacts the winners in ascending id order.
+#include <algorithm>
+
 #include "kvo_internal.cuh"
 #include "resident_assign.cuh"
 
@@ -134,7 +136,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
               const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
               uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
               int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
-              int Hkv, int k, const ResAssignArgs aa) {
+              int Hkv, int k, int key_cache, const ResAssignArgs aa) {
     constexpr int NQ = DUAL ? 2 : 1;
     __shared__ __align__(16) float u_s[NQ][D];
     __shared__ uint32_t h_s[NQ][256];
@@ -263,11 +265,20 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     // ---- last CTA of the group: exact top-k for each query.  Thread t owns the
     // contiguous keys [c0, c1) of the group (a multiple of 4 of them, so 16-byte
     // loads stay inside the padded key row), read 16 at a time with independent
-    // loads; the compaction then needs two block scans in all.
+    // loads; the compaction then needs two block scans in all.  With key_cache
+    // the group's keys are first copied into shared memory (one round trip to
+    // L2), and the radix passes and the compaction read them there.
+    extern __shared__ __align__(16) uint32_t sel_dyn[];
     const int per = ((C + SEL_THREADS - 1) / SEL_THREADS + 3) & ~3;
     const int c0 = min(C, tid * per), c1 = min(C, c0 + per);
     for (int qi = 0; qi < NQ; ++qi) {
         const uint32_t* kq = keys + ((int64_t)qi * G + bg) * Cmax4;
+        if (key_cache) {
+            for (int i = 4 * tid; i < C; i += 4 * SEL_THREADS)
+                *reinterpret_cast<uint4*>(sel_dyn + i) = __ldcg(reinterpret_cast<const uint4*>(kq + i));
+            __syncthreads();
+            kq = sel_dyn;
+        }
         int32_t* out = (qi == 0 ? idx_true : idx_pred) + (int64_t)bg * k;
         uint32_t* hg = hist + ((int64_t)qi * G + bg) * 256;
         uint32_t k_rem = (uint32_t)min(k, C);
@@ -276,14 +287,16 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         pick_digit(cnt0, warp_sums, &s_digit, &s_krem, k_rem);
         uint32_t prefix = (uint32_t)s_digit << 24, mask = 0xFF000000u;
         k_rem = s_krem;
+        // four keys from the cache or from L2
+        auto ld4 = [&](int j) -> uint4 {
+            return key_cache ? *reinterpret_cast<const uint4*>(kq + j) : __ldcg(reinterpret_cast<const uint4*>(kq + j));
+        };
         // visit this thread's keys in ascending order: f(j, key)
         auto scan_chunk = [&](auto&& f) {
             for (int j = c0; j < c1; j += 16) {
                 uint4 kv[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    kv[u] = j + 4 * u < c1 ? __ldcg(reinterpret_cast<const uint4*>(kq + j + 4 * u))
-                                           : make_uint4(0u, 0u, 0u, 0u);
+                for (int u = 0; u < 4; ++u) kv[u] = j + 4 * u < c1 ? ld4(j + 4 * u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
@@ -300,7 +313,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             if (small) {
                 const int j0 = 4 * tid;
                 if (j0 < C) {
-                    const uint4 kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
+                    const uint4 kv4 = ld4(j0);
                     const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -327,7 +340,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             // one sweep: 4 keys per thread in id order, two block scans
             const int j0 = 4 * tid;
             uint4 kv4 = make_uint4(0u, 0u, 0u, 0u);
-            if (j0 < C) kv4 = __ldcg(reinterpret_cast<const uint4*>(kq + j0));
+            if (j0 < C) kv4 = ld4(j0);
             const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
             uint32_t n_eq = 0;
 #pragma unroll
@@ -391,10 +404,13 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
         aa.need = idx_true;
         dyn = sizeof(int32_t) * res_assign_ints(c.k);
     }
+    // the last CTA's key cache (the same shared memory the assignment uses after it)
+    const int key_cache = Cmax4 <= SEL_KEY_CACHE ? 1 : 0;
+    if (key_cache) dyn = std::max(dyn, sizeof(uint32_t) * (size_t)Cmax4);
 #define KVO_SEL_L(D_, BF_, DU_, RPT_, AS_)                                                                     \
     select_kernel<D_, BF_, DU_, RPT_, AS_><<<c.n_sel_items, SEL_THREADS, dyn, s>>>(                            \
         c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C, c.sel_keys, \
-        c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k, aa)
+        c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k, key_cache, aa)
 #define KVO_SEL(D_, BF_, DU_)                                                                                  \
     do {                                                                                                       \
         if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, DU_, 1, false); else KVO_SEL_L(D_, BF_, DU_, 4, false);         \
@@ -420,9 +436,12 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
 }
 
 // Dynamic shared memory of the fused selection + assignment kernels (the
-// assignment's lists; above the default 48 KB only for k > 2457).
+// assignment's lists or the key cache, whichever is larger; above the default
+// 48 KB only for k > 2457).
 cudaError_t prepare_select_assign(const Ctx& c) {
-    const int bytes = (int)(sizeof(int32_t) * res_assign_ints(c.k));
+    const int Cmax4 = (c.Cmax + 3) & ~3;
+    const int bytes = (int)std::max(sizeof(int32_t) * res_assign_ints(c.k),
+                                    Cmax4 <= SEL_KEY_CACHE ? sizeof(uint32_t) * (size_t)Cmax4 : (size_t)0);
     cudaError_t e = cudaSuccess;
 #define KVO_SEL_ATTR(D_, BF_, RPT_)                                                                            \
     if (e == cudaSuccess)                                                                                      \
