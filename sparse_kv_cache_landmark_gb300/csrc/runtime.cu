@@ -421,11 +421,24 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaMemsetAsync(c.sel_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
     std::vector<int2> sel_items;
     std::vector<int32_t> nch(c.G);
-    // 1024 rows per CTA, or 256 when that leaves fewer than ~8 CTAs per SM
+    // 1024 rows per CTA when that gives ~8 CTAs per SM or more; otherwise 512
+    // or 256, whichever needs fewer waves of the 4 CTAs an SM holds (256 on a
+    // tie: more CTAs share the HBM)
     {
-        int64_t n4 = 0;
-        for (int g = 0; g < c.G; ++g) n4 += (Ccap[g] + kvo::SEL_THREADS * 4 - 1) / (kvo::SEL_THREADS * 4);
-        c.sel_rpt = n4 < 8 * 152 ? 1 : 4;
+        int64_t n[3] = {0, 0, 0};
+        for (int g = 0; g < c.G; ++g)
+            for (int i = 0; i < 3; ++i) {
+                const int rows = kvo::SEL_THREADS << i;
+                n[i] += (Ccap[g] + rows - 1) / rows;
+            }
+        int dev = 0, sms = 0;
+        KVO_CUDA(&c, cudaGetDevice(&dev));
+        KVO_CUDA(&c, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        sms = std::max(1, sms);
+        const int64_t slots = 4 * (int64_t)sms;
+        auto waves = [&](int64_t x) { return (x + slots - 1) / slots; };
+        if (n[2] >= 8 * (int64_t)sms) c.sel_rpt = 4;
+        else c.sel_rpt = waves(n[1]) < waves(n[0]) ? 2 : 1;
     }
     const int sel_rows = kvo::SEL_THREADS * c.sel_rpt;
     for (int g = 0; g < c.G; ++g) {

@@ -124,7 +124,7 @@ __device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, in
 // large workloads, 4 for fp32 landmarks and none for bf16 ones, whose deeper
 // per-thread load batches beat occupancy
 template <bool BF16LM, int SEL_RPT>
-constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 4 : (BF16LM ? 1 : 4); }
+constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 4 : (BF16LM ? (SEL_RPT == 2 ? 2 : 1) : 4); }
 
 // ASSIGN: the last CTA of a group then assigns the group's resident slots for
 // its true index (the routine of resident_assign.cuh, `aa` with need = the
@@ -413,11 +413,15 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
         c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k, key_cache, aa)
 #define KVO_SEL(D_, BF_, DU_)                                                                                  \
     do {                                                                                                       \
-        if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, DU_, 1, false); else KVO_SEL_L(D_, BF_, DU_, 4, false);         \
+        if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, DU_, 1, false);                                                  \
+        else if (c.sel_rpt == 2) KVO_SEL_L(D_, BF_, DU_, 2, false);                                             \
+        else KVO_SEL_L(D_, BF_, DU_, 4, false);                                                                \
     } while (0)
 #define KVO_SEL_A(D_, BF_)                                                                                     \
     do {                                                                                                       \
-        if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, false, 1, true); else KVO_SEL_L(D_, BF_, false, 4, true);       \
+        if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, false, 1, true);                                                \
+        else if (c.sel_rpt == 2) KVO_SEL_L(D_, BF_, false, 2, true);                                           \
+        else KVO_SEL_L(D_, BF_, false, 4, true);                                                               \
     } while (0)
     if (assign) {
         if (c.d == 128) { if (bf) KVO_SEL_A(128, true); else KVO_SEL_A(128, false); }
@@ -447,8 +451,10 @@ cudaError_t prepare_select_assign(const Ctx& c) {
     if (e == cudaSuccess)                                                                                      \
         e = cudaFuncSetAttribute(select_kernel<D_, BF_, false, RPT_, true>,                                    \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-    KVO_SEL_ATTR(128, true, 1); KVO_SEL_ATTR(128, true, 4); KVO_SEL_ATTR(128, false, 1); KVO_SEL_ATTR(128, false, 4);
-    KVO_SEL_ATTR(64, true, 1); KVO_SEL_ATTR(64, true, 4); KVO_SEL_ATTR(64, false, 1); KVO_SEL_ATTR(64, false, 4);
+    KVO_SEL_ATTR(128, true, 1); KVO_SEL_ATTR(128, true, 2); KVO_SEL_ATTR(128, true, 4);
+    KVO_SEL_ATTR(128, false, 1); KVO_SEL_ATTR(128, false, 2); KVO_SEL_ATTR(128, false, 4);
+    KVO_SEL_ATTR(64, true, 1); KVO_SEL_ATTR(64, true, 2); KVO_SEL_ATTR(64, true, 4);
+    KVO_SEL_ATTR(64, false, 1); KVO_SEL_ATTR(64, false, 2); KVO_SEL_ATTR(64, false, 4);
 #undef KVO_SEL_ATTR
     return e;
 }
