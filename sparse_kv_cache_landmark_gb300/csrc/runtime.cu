@@ -854,8 +854,11 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rassign[l], 0));
         // A chain step splits attention: the blocks resident already and the window
         // are attended beside the urgent copies, the fetched blocks after them,
-        // and the two results merge by log-sum-exp.
-        const bool split = alone_step && c.att_impl >= 1 && !o_spec;
+        // and the two results merge by log-sum-exp.  (Only chain steps, which are
+        // replayed from graphs: launched stream by stream, the hit pass did not
+        // start beside the copy -- a chain step took 0.76 ms instead of 0.50 on
+        // long context -- and a speculative step got slower split than whole.)
+        const bool split = alone_step && c.att_impl >= 1 && !o_spec && c.lr_rank[l] == 0;
         // 1. retrieval index (true; speculative -> next step's prediction), and
         // 2. urgent assign: T resident, sparing the prediction fetched for this
         // step -- without a speculative query, in the selection kernel itself
@@ -881,8 +884,10 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // layer l's hit pass reuses layer l - 2's half of the hit-pass scratch:
         // that layer's merge has read it
         if (split && l >= 2) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.attn[l - 2], 0));
-        // without a prediction nothing is spared: in-flight prefetch copies must land first
-        if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
+        // In-flight prefetch copies of this layer land first when nothing is spared
+        // (no prediction), and when the hit pass follows the copy: it reads blocks
+        // the prefetch may still be writing.  (The link carries both either way.)
+        if (pending && (!have || split)) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, su, [&] {
             return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask);
@@ -906,23 +911,24 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
                                                    lse + l * lse_layer, sa);
             }));
             KVO_CUDA(&c, cudaEventRecord(E.attn[l], sa));
-            continue;
-        }
-        if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
-            KVO_CUDA(&c, timed(kvo::PK_RECON, sc, [&] {
-                return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, sc);
+            c.res_pending[l] = 0;
+        } else {
+            if (c.lr_rank[l] > 0)           // keys rebuilt on the compute stream, beside the V copies
+                KVO_CUDA(&c, timed(kvo::PK_RECON, sc, [&] {
+                    return kvo::launch_lowrank_k(c, l, buf, miss, mcnt, 0, dsl, sc);
+                }));
+            // 4. attention over the resident set once the urgent and prefetched blocks have landed
+            KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
+            KVO_CUDA(&c, cudaStreamWaitEvent(sa, E.urg[l], 0));
+            if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rpref[l], 0));
+            c.res_pending[l] = 0;
+            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
+                return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
+                                             lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
+                                             lse_spec ? lse_spec + l * lse_layer : nullptr, 1, sa, true);
             }));
-        // 4. attention over the resident set once the urgent and prefetched blocks have landed
-        KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
-        KVO_CUDA(&c, cudaStreamWaitEvent(sa, E.urg[l], 0));
-        if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rpref[l], 0));
-        c.res_pending[l] = 0;
-        KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sa, [&] {
-            return kvo::launch_attention(c, l, buf, ql, o_spec ? qsl : nullptr, slot, o + l * o_layer,
-                                         lse + l * lse_layer, o_spec ? o_spec + l * o_layer : nullptr,
-                                         lse_spec ? lse_spec + l * lse_layer : nullptr, 1, sa, true);
-        }));
-        if (!alone_step) KVO_CUDA(&c, cudaEventRecord(E.attn[l], sc));
+            KVO_CUDA(&c, cudaEventRecord(E.attn[l], sa));
+        }
         // 5. prefetch of the next step's prediction, sparing T (with the adaptive
         // policy the assign fetches nothing while the layer's prefetches do not pay)
         if (q_spec) {
