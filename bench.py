@@ -863,23 +863,51 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
     qs0 = qs_dev[0] if qs_dev is not None else (q0.float() * 0.5).to(torch.bfloat16)
     T, _ = ctx.select_topk(0, q0)
     miss, cnt, slot = ctx.index_diff(T, None)
-    ctx.gather_coalesced(0, 0, miss, cnt, slot_base=w.top_k, urgent=True)
+    # layer 0's selection in both ping-pong halves: attention calls alternate
+    # between them, so consecutive calls read different bytes
+    for half in (0, 1):
+        ctx.gather_coalesced(0, half, miss, cnt, slot_base=w.top_k, urgent=True)
+    n_sel_layers = min(w.n_layers, 8)
+    T_l = [T] + [ctx.select_topk(l, q_dev[l])[0] for l in range(1, n_sel_layers)]
     torch.cuda.synchronize()
+    by_iso = workload_bytes(w, lens)
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush_buf = None
 
-    def _t(fn, n=20):
-        for _ in range(3):
-            fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n):
-            fn()
-        b.record(stream)
-        b.synchronize()
-        return a.elapsed_time(b) / n * 1e3
-    one = _t(lambda: ctx.sparse_decode_attn(0, 0, q0, slot))
-    sel = _t(lambda: ctx.select_topk(0, q0, idx_true=T))
+    def _t(fns, ws_bytes, n=20):
+        """Mean time of n calls cycling through fns.  When the bytes the cycle
+        reads are under twice the L2, each call runs after a write of a buffer
+        larger than the L2 and is timed alone."""
+        nonlocal flush_buf
+        for i in range(3):
+            fns[i % len(fns)]()
+        if ws_bytes >= 2 * l2:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(n):
+                fns[i % len(fns)]()
+            b.record(stream)
+            b.synchronize()
+            return a.elapsed_time(b) / n * 1e3
+        if flush_buf is None:
+            flush_buf = torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush_buf.fill_(i)
+            ev[i][0].record(stream)
+            fns[i % len(fns)]()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n * 1e3
+    att_fns = [lambda h=h: ctx.sparse_decode_attn(0, h, q0, slot) for h in (0, 1)]
+    sel_fns = [lambda l=l: ctx.select_topk(l, q_dev[l], idx_true=T_l[l]) for l in range(n_sel_layers)]
+    one = _t(att_fns, 2 * by_iso["attended_per_layer"])
+    sel = _t(sel_fns, n_sel_layers * by_iso["landmark_per_layer"])
     m["isolated"] = {"attention_us": round(one, 2), "select_us": round(sel, 2),
-                     "note": "layer 0, 20 back-to-back calls, nothing else running"}
+                     "note": "20 calls, nothing else running, alternating between both ping-pong halves "
+                             f"(attention) and over {n_sel_layers} layers' landmarks (selection); when the "
+                             "alternated inputs are under twice the L2, a buffer larger than the L2 is "
+                             "written before each call and each call is timed alone"}
     m["gather_engines"] = None
     if headline and args.gather_engines and not args.resident:
         # one layer's prefetch-sized gather (k blocks per group, the true index) per engine
@@ -889,14 +917,16 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
         ge = {"runs": n_runs, "bytes": by, "note": "layer 0's true index into ping-pong half 0, mean of 5 calls"}
         for eng in [int(x) for x in args.gather_engines.split(",") if x]:
             ctx.set_gather_engine(eng, 0)
-            ms = _t(lambda: ctx.gather_coalesced(0, 0, T, None, slot_base=0, want_runs=False,
-                                                 stream=stream.cuda_stream), n=5) / 1e3
+            ms = _t([lambda: ctx.gather_coalesced(0, 0, T, None, slot_base=0, want_runs=False,
+                                                  stream=stream.cuda_stream)], by, n=5) / 1e3
             ge[f"engine{eng}"] = {"ms": round(ms, 3), "gbs": round(by / (ms * 1e-3) / 1e9, 1)}
         ctx.set_gather_engine(args.gather_engine if args.gather_engine >= 0 else 3, args.gather_drivers)
         m["gather_engines"] = ge
     if headline and 2 * w.group_size <= 16:
-        two = _t(lambda: (ctx.sparse_decode_attn(0, 0, q0, slot), ctx.sparse_decode_attn(0, 0, qs0, slot)))
-        co = _t(lambda: ctx.sparse_decode_attn_cobatch(0, 0, q0, qs0, slot))
+        two = _t([lambda h=h: (ctx.sparse_decode_attn(0, h, q0, slot), ctx.sparse_decode_attn(0, h, qs0, slot))
+                  for h in (0, 1)], 2 * by_iso["attended_per_layer"])
+        co = _t([lambda h=h: ctx.sparse_decode_attn_cobatch(0, h, q0, qs0, slot) for h in (0, 1)],
+                2 * by_iso["attended_per_layer"])
         m["cob"] = {"single_us": round(one, 2), "two_launches_us": round(two, 2), "cobatched_us": round(co, 2),
                     "cobatched_over_two": round(co / two, 3),
                     "note": "one layer's attention, isolated (no gather running), 20 back-to-back calls"}

@@ -232,8 +232,11 @@ cudaError_t launch_landmarks(const Ctx& c, int layer, cudaStream_t s);
 struct ResAssignArgs;   // resident_assign.cuh
 // With `assign` (single-query steps only), the last CTA of each group also
 // assigns the group's resident slots for the true index it selected.
+// pdl: launched as a programmatic dependent of the kernel before it on the
+// stream (waits for it before reading anything; standalone calls only).
 cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
-                          int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign = nullptr);
+                          int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign = nullptr,
+                          bool pdl = false);
 cudaError_t prepare_select_assign(const Ctx& c);
 cudaError_t launch_index_diff(const Ctx& c, const int32_t* idx_true, const int32_t* idx_pred, int32_t* miss,
                               int32_t* miss_cnt, int32_t* slot, cudaStream_t s);

@@ -565,7 +565,8 @@ kvo_status select_topk(kvo_ctx* ctx, int layer, const void* q, const void* q_spe
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "layer out of range");
     if (!q || !idx_true) return fail(&c, KVO_ERR_INVALID, "null q or idx_true");
     if (q_spec && !idx_pred) return fail(&c, KVO_ERR_INVALID, "q_spec given without idx_pred");
-    KVO_CUDA(&c, kvo::launch_select(c, layer, q, q_spec, idx_true, q_spec ? idx_pred : nullptr, pick(c, stream)));
+    KVO_CUDA(&c, kvo::launch_select(c, layer, q, q_spec, idx_true, q_spec ? idx_pred : nullptr, pick(c, stream),
+                                    nullptr, true));
     return KVO_OK;
 }
 

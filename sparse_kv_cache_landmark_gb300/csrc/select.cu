@@ -136,7 +136,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
               const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
               uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
               int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
-              int Hkv, int k, int key_cache, const ResAssignArgs aa) {
+              int Hkv, int k, int key_cache, int dep_wait, const ResAssignArgs aa) {
     constexpr int NQ = DUAL ? 2 : 1;
     __shared__ __align__(16) float u_s[NQ][D];
     __shared__ uint32_t h_s[NQ][256];
@@ -146,6 +146,10 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     __shared__ uint32_t s_krem;
 
     const int tid = threadIdx.x;
+    // dep_wait: launched as a programmatic dependent of the kernel before it on
+    // the stream, which may have written any input (and a selection before it
+    // resets the histograms and tickets last) -- nothing is read before it is done
+    if (dep_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int2 it = items[blockIdx.x];
     const int bg = it.x, chunk = it.y;
     const int b = bg / Hkv, g = bg % Hkv;
@@ -249,6 +253,8 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         const uint32_t v = (&h_s[0][0])[i];
         if (v) atomicAdd(&hist[((int64_t)(i / 256) * G + bg) * 256 + (i % 256)], v);
     }
+    // the kernel behind this one may be scheduled once every CTA has scored
+    if (dep_wait) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the CTA's key and histogram writes reach thread 0 through the barrier; its
     // release fence orders them before the ticket, the last CTA's acquire fence
     // orders the selection's loads after it
@@ -392,7 +398,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
 }
 
 cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
-                          int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign) {
+                          int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign, bool pdl) {
     const int Cmax4 = (c.Cmax + 3) & ~3;
     const bool dual = q_spec != nullptr;
     const bool bf = c.B == 1;
@@ -407,10 +413,23 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
     // the last CTA's key cache (the same shared memory the assignment uses after it)
     const int key_cache = Cmax4 <= SEL_KEY_CACHE ? 1 : 0;
     if (key_cache) dyn = std::max(dyn, sizeof(uint32_t) * (size_t)Cmax4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)c.n_sel_items);
+    cfg.blockDim = dim3(SEL_THREADS);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const int dep_wait = pdl ? 1 : 0;
+    cudaError_t err = cudaSuccess;
 #define KVO_SEL_L(D_, BF_, DU_, RPT_, AS_)                                                                     \
-    select_kernel<D_, BF_, DU_, RPT_, AS_><<<c.n_sel_items, SEL_THREADS, dyn, s>>>(                            \
-        c.lm[layer], (const uint16_t*)q, (const uint16_t*)q_spec, c.sel_items, c.sel_nchunks, c.g_C, c.sel_keys, \
-        c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, Cmax4, c.Cmax, c.r, c.Hkv, c.k, key_cache, aa)
+    err = cudaLaunchKernelEx(&cfg, select_kernel<D_, BF_, DU_, RPT_, AS_>, c.lm[layer], (const uint16_t*)q,     \
+                             (const uint16_t*)q_spec, (const int2*)c.sel_items, (const int32_t*)c.sel_nchunks,  \
+                             (const int32_t*)c.g_C, c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, \
+                             Cmax4, c.Cmax, c.r, c.Hkv, c.k, key_cache, dep_wait, aa)
 #define KVO_SEL(D_, BF_, DU_)                                                                                  \
     do {                                                                                                       \
         if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, DU_, 1, false);                                                  \
@@ -436,7 +455,7 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
 #undef KVO_SEL_A
 #undef KVO_SEL
 #undef KVO_SEL_L
-    return cudaGetLastError();
+    return err;
 }
 
 // Dynamic shared memory of the fused selection + assignment kernels (the
