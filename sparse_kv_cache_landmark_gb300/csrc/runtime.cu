@@ -166,12 +166,11 @@ kvo_status build_tma_plans(kvo::Ctx& c) {
         held = std::min(c.gather_ctas > 0 ? c.gather_ctas : 2 * c.n_sms, c.n_sms - 1);
     const int64_t step = (int64_t)c.tma_per_sm * (c.n_sms - held);
     // group-split clusters: as many CTAs per group as the resident CTAs allow,
-    // 1 .. 8 (the portable cluster size), one more when that fills less than
-    // 3/4 of the slots and one more stays within 5/4 of them (the Llama layer
-    // beside the decode step's gather: 256 CTAs on 228 slots beat 128); chosen
-    // automatically only when the groups' CTAs then fill at least 3/4 of the
-    // slots -- fewer groups leave SMs idle, and the persistent kernel's
-    // balanced tile ranges measured faster there
+    // 1 .. 8 (the portable cluster size); chosen automatically only when the
+    // groups' CTAs then fill at least 3/4 of the slots -- fewer groups leave
+    // SMs idle, and the persistent kernel's balanced tile ranges measured
+    // faster there (the Llama layer beside the decode step's gather: 128 CTAs
+    // on 228 slots; 64-73 us live against 78-85 us for 256 clusters' CTAs)
     auto plan_clu = [&](int i, int64_t slots) {
         if (c.att_cluster > 0) {
             c.clu_S[i] = c.att_cluster;
@@ -179,8 +178,7 @@ kvo_status build_tma_plans(kvo::Ctx& c) {
             return;
         }
         const int64_t G = std::max(1, c.G);
-        int64_t S = std::max<int64_t>(1, std::min<int64_t>(8, slots / G));
-        if (4 * G * S < 3 * slots && S < 8 && 4 * G * (S + 1) <= 5 * slots) ++S;
+        const int64_t S = std::max<int64_t>(1, std::min<int64_t>(8, slots / G));
         c.clu_S[i] = (int)S;
         c.clu_use[i] = 4 * G * S >= 3 * slots;
     };
