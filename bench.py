@@ -875,13 +875,14 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
     flush_buf = None
 
     def _t(fns, ws_bytes, n=20):
-        """Mean time of n calls cycling through fns.  When the bytes the cycle
-        reads are under twice the L2, each call runs after a write of a buffer
-        larger than the L2 and is timed alone."""
+        """Mean time of n calls cycling through fns, back to back when the bytes
+        the cycle reads exceed the L2; otherwise each call runs after a
+        read-modify-write of a buffer twice the L2 and is timed alone (which
+        then includes its launch)."""
         nonlocal flush_buf
         for i in range(3):
             fns[i % len(fns)]()
-        if ws_bytes >= 2 * l2:
+        if ws_bytes > l2:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for i in range(n):
@@ -890,10 +891,10 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
             b.synchronize()
             return a.elapsed_time(b) / n * 1e3
         if flush_buf is None:
-            flush_buf = torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
+            flush_buf = torch.zeros(2 * l2 // 4, dtype=torch.int32, device="cuda")
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         for i in range(n):
-            flush_buf.fill_(i)
+            flush_buf.add_(1)
             ev[i][0].record(stream)
             fns[i % len(fns)]()
             ev[i][1].record(stream)
@@ -905,9 +906,9 @@ def measure(args, ws, rank, smi_id, headline, steps, numa_node=None):
     sel = _t(sel_fns, n_sel_layers * by_iso["landmark_per_layer"])
     m["isolated"] = {"attention_us": round(one, 2), "select_us": round(sel, 2),
                      "note": "20 calls, nothing else running, alternating between both ping-pong halves "
-                             f"(attention) and over {n_sel_layers} layers' landmarks (selection); when the "
-                             "alternated inputs are under twice the L2, a buffer larger than the L2 is "
-                             "written before each call and each call is timed alone"}
+                             f"(attention) and over {n_sel_layers} layers' landmarks (selection), so the "
+                             "inputs of a cycle exceed the L2; where they do not, a buffer twice the L2 is "
+                             "read and written before each call and each call is timed alone"}
     m["gather_engines"] = None
     if headline and args.gather_engines and not args.resident:
         # one layer's prefetch-sized gather (k blocks per group, the true index) per engine
