@@ -152,6 +152,9 @@ kvo_status kv_offload_destroy(kvo_ctx* ctx);
  *   blocks in ascending id order, ties to the lower id.  When q_spec is given,
  *   idx_pred[G][k] receives the same for q_spec from the same landmark pass
  *   (the speculative look-ahead query of the dual-token scheme, §5.2).
+ *   Launched as a programmatic dependent of the kernel before it on `stream`:
+ *   it reads nothing before that kernel has completed (stream order holds);
+ *   only its launch overlaps that kernel's tail.
  *   Concurrency: [sel] -- one select_topk at a time per context.
  */
 kvo_status select_topk(kvo_ctx* ctx, int layer, const void* q, const void* q_spec,
@@ -201,6 +204,9 @@ kvo_status gather_coalesced(kvo_ctx* ctx, int layer, int buf, const int32_t* idx
  *   window and sparse parts fused by log-sum-exp.  fuse_window_merge = 0:
  *   o[2][b][Hq][d], lse[2][b][Hq]: part 0 sparse, part 1 window (an empty
  *   part has lse = -inf, o = 0).
+ *   With the group-split kernel (kvo_set_attn_impl 2) the launch is a
+ *   programmatic dependent of the kernel before it on `stream`, reading
+ *   nothing before that kernel has completed.
  *   Concurrency: [att], and it reads [buf] -- one attention call at a time
  *   per context, with no write to the slots it reads in flight.
  */
