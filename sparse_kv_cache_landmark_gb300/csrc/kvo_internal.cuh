@@ -148,6 +148,7 @@ struct Ctx {
     size_t scratch_bytes = 0;
     cudaStream_t s_compute = nullptr, s_prefetch = nullptr, s_urgent = nullptr;
     cudaStream_t s_urgent2 = nullptr;   // a chain step's odd layers' copies
+    cudaStream_t s_hit = nullptr;       // a speculative step's hit passes (compute priority)
     // decode-step state
     int32_t* st_true = nullptr;     // [L][G][k]
     int32_t* st_pred = nullptr;     // [2][L][G][k]  predictions by step parity
@@ -159,7 +160,7 @@ struct Ctx {
     // ordering events of the decode step; captured steps use their own set (an
     // event recorded inside a capture cannot be waited on outside it)
     struct EvSet {
-        std::vector<cudaEvent_t> sel, attn, pref, urg;
+        std::vector<cudaEvent_t> sel, attn, pref, urg, hit;   // hit: a split step's hit pass done
         std::vector<cudaEvent_t> rassign, rpref;   // resident mode, per layer: prefetch assigned / landed
         cudaEvent_t start = nullptr;
     } ev_eager, ev_graph;

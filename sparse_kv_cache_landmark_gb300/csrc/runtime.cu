@@ -209,7 +209,7 @@ void free_ctx(kvo::Ctx& c) {
     if (c.h_nruns) cudaFreeHost(c.h_nruns);
     F(c.st_true); F(c.st_pred); F(c.st_miss); F(c.st_miss_cnt); F(c.st_slot);
     for (auto* E : {&c.ev_eager, &c.ev_graph}) {
-        for (auto* v : {&E->sel, &E->attn, &E->pref, &E->urg, &E->rassign, &E->rpref})
+        for (auto* v : {&E->sel, &E->attn, &E->pref, &E->urg, &E->hit, &E->rassign, &E->rpref})
             for (cudaEvent_t e : *v) if (e) cudaEventDestroy(e);
         if (E->start) cudaEventDestroy(E->start);
     }
@@ -217,7 +217,7 @@ void free_ctx(kvo::Ctx& c) {
     if (c.ev_gout) cudaEventDestroy(c.ev_gout);
     for (cudaGraphExec_t g : c.gexec) if (g) cudaGraphExecDestroy(g);
     for (cudaEvent_t e : c.prof_pool) if (e) cudaEventDestroy(e);
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph}) if (s) cudaStreamDestroy(s);
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit, c.s_graph}) if (s) cudaStreamDestroy(s);
 }
 
 // Records a timing event on `s` when profiling is on; returns its pool index or -1.
@@ -320,6 +320,7 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_prefetch, cudaStreamNonBlocking, least));
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_urgent, cudaStreamNonBlocking, greatest));
     KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_urgent2, cudaStreamNonBlocking, greatest));
+    KVO_CUDA(&c, cudaStreamCreateWithPriority(&c.s_hit, cudaStreamNonBlocking, (least + greatest) / 2));
     size_t sb = 0;
     KVO_CUDA(&c, dalloc(&c.g_off, sizeof(int64_t) * c.G, &sb));
     KVO_CUDA(&c, dalloc(&c.g_C, sizeof(int32_t) * c.G, &sb));
@@ -498,7 +499,7 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, dalloc(&c.st_slot, sizeof(int32_t) * lgk, &sb));
     c.scratch_bytes = sb;
     for (auto* E : {&c.ev_eager, &c.ev_graph}) {
-        for (auto* v : {&E->sel, &E->attn, &E->urg}) {
+        for (auto* v : {&E->sel, &E->attn, &E->urg, &E->hit}) {
             v->assign(c.L, nullptr);
             for (auto& e : *v) KVO_CUDA(&c, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
         }
@@ -549,7 +550,7 @@ kvo_status kv_offload_init(const kvo_config* cfg, void* const* k_host, void* con
 
 kvo_status kv_offload_destroy(kvo_ctx* ctx) {
     if (!ctx) return KVO_OK;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph})
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph})
         if (s) cudaStreamSynchronize(s);
     free_ctx(ctx->c);
     delete ctx;
@@ -791,7 +792,8 @@ static bool resident_alone(const kvo::Ctx& c, const void* q_spec) {
 // prefetched, because the urgent assign spares them.
 // Without a speculative query (nothing in flight, no low-rank layer) the step
 // is one chain on the compute stream; its attention is split around the
-// urgent copy (see below).
+// urgent copy (see below), and so is a speculative step's when no layer is
+// low-rank.
 static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* q_spec, float* o, float* lse,
                                        float* o_spec, float* lse_spec, cudaStream_t s_user) {
     kvo::Ctx& c = ctx->c;
@@ -816,9 +818,17 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     const bool alone_step = resident_alone(c, q_spec);
     const cudaStream_t sc = c.s_compute;                          // select, assign (and attention when speculating)
     const cudaStream_t sa = alone_step ? c.s_prefetch : sc;       // attention
+    // A speculative step splits attention too when no layer rebuilds keys (a
+    // whole-layer attention would share the hit passes' scratch): its hit pass
+    // is launched plainly, at the compute stream's priority, on a stream of its
+    // own beside the copy.  (At the urgent streams' priority its CTAs took SMs
+    // ahead of the prefetch gathers that keep the link busy: always-prefetch
+    // steps on long context slowed from 1.08 to 1.34-1.48 ms.)
+    bool spec_split = q_spec && !alone_step && c.att_impl >= 1 && !o_spec;
+    for (int l = 0; l < c.L && spec_split; ++l) spec_split = c.lr_rank[l] == 0;
 
     KVO_CUDA(&c, cudaEventRecord(E.start, s_user));
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2})
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit})
         KVO_CUDA(&c, cudaStreamWaitEvent(s, E.start, 0));
     int cur_layer = -1;
     auto timed = [&](int kind, cudaStream_t s, auto&& launch) -> cudaError_t {
@@ -846,18 +856,20 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         int32_t* mcnt = c.st_miss_cnt + (size_t)l * c.G;
         int32_t* dsl = c.res_dslot + l * gk;
         int32_t* hit_slot = c.res_hit_slot + l * gk;       // per layer: layer l + 1's assign runs beside
-        int32_t* hit_cnt = c.res_hit_cnt + (size_t)l * c.G;  // layer l's attention in a chain step
+        int32_t* hit_cnt = c.res_hit_cnt + (size_t)l * c.G;  // layer l's attention in a split step
         const cudaStream_t su = alone_step && (l & 1) ? c.s_urgent2 : c.s_urgent;   // urgent copies
         const bool pending = c.res_pending[l] != 0;
         // the previous step's prefetch of this layer has read T and written the slot table
         if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sc, E.rassign[l], 0));
-        // A chain step splits attention: the blocks resident already and the window
-        // are attended beside the urgent copies, the fetched blocks after them,
-        // and the two results merge by log-sum-exp.  (Only chain steps, which are
-        // replayed from graphs: launched stream by stream, the hit pass did not
-        // start beside the copy -- a chain step took 0.76 ms instead of 0.50 on
-        // long context -- and a speculative step got slower split than whole.)
-        const bool split = alone_step && c.att_impl >= 1 && !o_spec && c.lr_rank[l] == 0;
+        // A split step attends to the blocks resident already and the window
+        // beside the urgent copies, to the fetched blocks after them, and merges
+        // the two results by log-sum-exp.  A chain step's hit pass is a dependent
+        // launch of the copy (under graph replay it starts beside the copy;
+        // launched stream by stream it did not -- a chain step took 0.76 ms
+        // instead of 0.50 on long context -- so steps that are not replayed
+        // split only with a speculative query, their hit pass on a stream of
+        // its own).
+        const bool split = (alone_step && c.att_impl >= 1 && !o_spec && c.lr_rank[l] == 0) || spec_split;
         // 1. retrieval index (true; speculative -> next step's prediction), and
         // 2. urgent assign: T resident, sparing the prediction fetched for this
         // step -- without a speculative query, in the selection kernel itself
@@ -884,24 +896,40 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // that layer's merge has read it
         if (split && l >= 2) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.attn[l - 2], 0));
         // In-flight prefetch copies of this layer land first when nothing is spared
-        // (no prediction), and when the hit pass follows the copy: it reads blocks
-        // the prefetch may still be writing.  (The link carries both either way.)
-        if (pending && (!have || split)) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
+        // (no prediction).  (A chain step has none in flight; a speculative hit
+        // pass waits for them itself.)
+        if (pending && !have) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.rpref[l], 0));
         const int urg_mask = c.lr_rank[l] > 0 ? 2 : 3;      // low-rank layer: V only, keys rebuilt
         KVO_CUDA(&c, timed(kvo::PK_GATHER_URGENT, su, [&] {
             return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask);
         }));
         if (split) {
-            // hits + window beside the copy: a programmatic dependent of the copy,
-            // dispatched once the copy's SM-exclusive CTAs are all resident (so it
-            // cannot take their SMs), completing after it; layer l - 1's merge may
-            // still run -- it reads the other half of the hit-pass scratch
             float* oA = c.res_oA + (size_t)(l & 1) * o_layer;
             float* lA = c.res_lA + (size_t)(l & 1) * lse_layer;
-            KVO_CUDA(&c, timed(kvo::PK_ATTENTION, su, [&] {
-                return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, su, true,
-                                             hit_cnt, true, l & 1);
-            }));
+            if (alone_step) {
+                // hits + window beside the copy: a programmatic dependent of the copy,
+                // dispatched once the copy's SM-exclusive CTAs are all resident (so it
+                // cannot take their SMs), completing after it; layer l - 1's merge may
+                // still run -- it reads the other half of the hit-pass scratch
+                KVO_CUDA(&c, timed(kvo::PK_ATTENTION, su, [&] {
+                    return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, su,
+                                                 true, hit_cnt, true, l & 1);
+                }));
+            } else {
+                // hits + window on their own stream once the assign has listed them,
+                // layer l - 2's merge has read this half of the scratch and the
+                // blocks prefetched for this step have landed
+                const cudaStream_t sh = c.s_hit;
+                KVO_CUDA(&c, cudaStreamWaitEvent(sh, E.sel[l], 0));
+                if (l >= 2) KVO_CUDA(&c, cudaStreamWaitEvent(sh, E.attn[l - 2], 0));
+                if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sh, E.rpref[l], 0));
+                KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sh, [&] {
+                    return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, sh,
+                                                 true, hit_cnt, false, l & 1);
+                }));
+                KVO_CUDA(&c, cudaEventRecord(E.hit[l], sh));
+                KVO_CUDA(&c, cudaStreamWaitEvent(sa, E.hit[l], 0));
+            }
             // the fetched blocks once they have landed, merged with the hits
             KVO_CUDA(&c, cudaEventRecord(E.urg[l], su));
             KVO_CUDA(&c, cudaStreamWaitEvent(sa, E.urg[l], 0));
@@ -948,8 +976,8 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
     }
     // the caller's stream waits for the outputs; prefetches stay in flight (a
     // chain step's attention stream is joined)
-    for (cudaStream_t s : {c.s_compute, c.s_urgent, c.s_prefetch, c.s_urgent2}) {
-        if (s == c.s_prefetch && !alone_step) break;
+    for (cudaStream_t s : {c.s_compute, c.s_urgent, c.s_prefetch, c.s_urgent2, c.s_hit}) {
+        if (s == c.s_prefetch && !alone_step) continue;
         KVO_CUDA(&c, cudaEventRecord(E.start, s));
         KVO_CUDA(&c, cudaStreamWaitEvent(s_user, E.start, 0));
     }
@@ -1029,7 +1057,7 @@ kvo_status kvo_set_graphs(kvo_ctx* ctx, int enable) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     if (enable && ctx->c.gather_engine == 4)
         return fail(&ctx->c, KVO_ERR_STATE, "graph replay needs a device-side gather engine (not engine 4)");
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph})
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph})
         cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     ctx->c.use_graphs = enable != 0;
@@ -1080,7 +1108,7 @@ kvo_status kvo_append(kvo_ctx* ctx, const void* k_new, const void* v_new, kvo_st
 
 kvo_status kvo_reset_prediction(kvo_ctx* ctx) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph}) cudaStreamSynchronize(s);
     ctx->c.have_pred = false;
     ctx->c.step_parity = 0;
     return KVO_OK;
@@ -1097,7 +1125,7 @@ kvo_status kvo_device_status(kvo_ctx* ctx, int32_t* code_out, kvo_stream_t strea
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
     kvo::Ctx& c = ctx->c;
     if (stream) KVO_CUDA(&c, cudaStreamSynchronize((cudaStream_t)stream));
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     int32_t v = 0;
     KVO_CUDA(&c, cudaMemcpy(&v, c.status, sizeof(v), cudaMemcpyDeviceToHost));
     KVO_CUDA(&c, cudaMemset(c.status, 0, sizeof(int32_t)));
@@ -1137,7 +1165,7 @@ kvo_status kvo_resident_slots(kvo_ctx* ctx, int layer, int32_t* slots_out) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (layer < 0 || layer >= c.L || !slots_out) return fail(&c, KVO_ERR_INVALID, "bad layer or null output");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     const size_t n = (size_t)c.G * 2 * c.k;
     KVO_CUDA(&c, cudaMemcpy(slots_out, c.res_slots + (size_t)layer * n, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
     return KVO_OK;
@@ -1149,7 +1177,7 @@ kvo_status kvo_set_lowrank_keys(kvo_ctx* ctx, int layer, int rank, const void* c
     if (layer < 0 || layer >= c.L) return fail(&c, KVO_ERR_INVALID, "bad layer");
     if (rank < 0 || rank > 64) return fail(&c, KVO_ERR_INVALID, "rank must be in 0..64");
     if (rank > 0 && (!coef || !basis)) return fail(&c, KVO_ERR_INVALID, "rank > 0 needs coef and basis");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     drop_graphs(c);
     c.lr_rank[layer] = rank;
     c.lr_coef[layer] = rank > 0 ? (const uint16_t*)coef : nullptr;
@@ -1162,7 +1190,7 @@ kvo_status kvo_set_prefetch_budget(kvo_ctx* ctx, int blocks) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (blocks < -1) return fail(&c, KVO_ERR_INVALID, "blocks must be >= -1");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     c.res_budget = blocks;
     return KVO_OK;
 }
@@ -1172,7 +1200,7 @@ kvo_status kvo_set_spec_policy(kvo_ctx* ctx, int mode) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (mode < 0 || mode > 1) return fail(&c, KVO_ERR_INVALID, "mode must be 0 or 1");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph})
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit, c.s_graph})
         KVO_CUDA(&c, cudaStreamSynchronize(s));
     drop_graphs(c);
     // every layer starts a fresh window with its prefetch on
@@ -1188,7 +1216,7 @@ kvo_status kvo_spec_stats(kvo_ctx* ctx, int64_t* out3) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (!out3) return fail(&c, KVO_ERR_INVALID, "null output");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     std::vector<unsigned long long> h(2 * (size_t)c.L), p(8 * (size_t)c.L);
     KVO_CUDA(&c, cudaMemcpy(h.data(), c.res_stat, sizeof(unsigned long long) * 2 * c.L, cudaMemcpyDeviceToHost));
     KVO_CUDA(&c, cudaMemcpy(p.data(), c.res_pol, sizeof(unsigned long long) * 8 * c.L, cudaMemcpyDeviceToHost));
@@ -1205,7 +1233,7 @@ kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset) {
     kvo::Ctx& c = ctx->c;
     if (!c.resident) return fail(&c, KVO_ERR_STATE, "context built with resident = 0");
     if (!out2) return fail(&c, KVO_ERR_INVALID, "null output");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     unsigned long long h[2];
     KVO_CUDA(&c, cudaMemcpy(h, c.res_fetched, sizeof(h), cudaMemcpyDeviceToHost));
     out2[0] = (int64_t)h[0];
@@ -1243,7 +1271,7 @@ kvo_status kvo_plan_attention(int n_groups, int sparse_tokens, int window_tokens
 
 kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     const int max_threads = ctx->c.gather_engine == 3 ? 1024 : kvo::GATHER_THREADS;
     if (ctas < 0 || ctas > 65535 || threads < 32 || threads > max_threads || threads % 32 ||
@@ -1258,7 +1286,7 @@ kvo_status kvo_set_gather_shape(kvo_ctx* ctx, int ctas, int threads, int unroll)
 
 kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     if (smem_bytes < 0 || smem_bytes > 227 * 1024 - 128)
         return fail(&ctx->c, KVO_ERR_INVALID, "0 <= smem_bytes <= 232320 (227 KiB less 128 bytes)");
@@ -1268,7 +1296,7 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes) {
 
 kvo_status kvo_set_gather_engine(kvo_ctx* ctx, int engine, int drivers) {
     if (check_ctx(ctx)) return KVO_ERR_INVALID;
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     // engine 1: 4 batches per driver; engine 2: 8 batches per driver (one driver per CTA)
     if (engine < 0 || engine > 4 || drivers < 0 || drivers > 4096)
@@ -1301,7 +1329,7 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas) {
     if (impl < 0 || impl > 2 || ctas < 0 || (impl == 2 && ctas > 8))
         return fail(&ctx->c, KVO_ERR_INVALID,
                     "attention implementation must be 0, 1 or 2, ctas >= 0, and ctas <= 8 for implementation 2");
-    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_graph}) cudaStreamSynchronize(s);
+    for (cudaStream_t s : {ctx->c.s_compute, ctx->c.s_prefetch, ctx->c.s_urgent, ctx->c.s_urgent2, ctx->c.s_hit, ctx->c.s_graph}) cudaStreamSynchronize(s);
     drop_graphs(ctx->c);
     ctx->c.att_impl = impl;
     ctx->c.tma_ctas = impl == 2 ? 0 : ctas;
@@ -1314,7 +1342,7 @@ kvo_status kvo_set_wait_test(kvo_ctx* ctx, int64_t limit_ns, int skip_tile) {
     kvo::Ctx& c = ctx->c;
     if (limit_ns < 1000000 || limit_ns > 10000000000LL || skip_tile < -1)
         return fail(&c, KVO_ERR_INVALID, "need 1 ms <= limit_ns <= 10 s and skip_tile >= -1");
-    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit, c.s_graph}) KVO_CUDA(&c, cudaStreamSynchronize(s));
     drop_graphs(c);
     c.att_wait_ns = limit_ns;
     c.att_skip_tile = skip_tile;
