@@ -84,6 +84,9 @@ def parse(argv=None):
     ap.add_argument("--attn-impl", type=int, default=-1,
                     help="attention kernel: 0 register-direct, 1 TMA-staged persistent (-1: default)")
     ap.add_argument("--attn-ctas", type=int, default=0, help="TMA-staged attention grid (0: fill the SMs)")
+    ap.add_argument("--select-impl", type=int, default=-1,
+                    help="selection kernel: 0 ticket, 2 one cluster per group where it fits, 1 automatic "
+                         "(-1: default)")
     ap.add_argument("--resident", type=int, default=0,
                     help="1: cross-step delta prefetch (per-layer resident block sets), queries drifting per step; "
                          "2: the resident sets without speculation (each step fetches only its misses)")
@@ -574,6 +577,8 @@ def build_workload(args, ws=1, numa_node=None):
         B.ctx.set_graphs(bool(args.graphs))
     if args.attn_impl >= 0:
         B.ctx.set_attn_impl(args.attn_impl, args.attn_ctas)
+    if args.select_impl >= 0:
+        B.ctx.set_select_impl(args.select_impl)
     if args.resident and args.prefetch_budget >= 0:
         B.ctx.set_prefetch_budget(args.prefetch_budget)
     if args.resident == 1:      # speculation only while it pays, unless asked otherwise
@@ -1096,6 +1101,7 @@ def run_ours(args):
                              "drivers": args.gather_drivers or "default"},
             "attention_kernel": {"impl": "default" if args.attn_impl < 0 else args.attn_impl,
                                  "ctas": args.attn_ctas or "default"},
+            "selection_kernel": {"impl": "default" if args.select_impl < 0 else args.select_impl},
             "lowrank_keys": None if not head["recon_rank"] else {
                 "rank": head["recon_rank"], "rebuilt_blocks_per_step": head["misses"],
                 "host_bytes_saved_per_step": head["misses"] * w.block_size * 2 * w.head_dim,

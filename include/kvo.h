@@ -538,6 +538,26 @@ kvo_status kvo_set_gather_reserve(kvo_ctx* ctx, int smem_bytes);
 kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
 
 /*
+ * kvo_set_select_impl -- which kernel computes select_topk and the decode
+ * step's selection.  Both compute the exact top-k (DualDecoder §4.1, Fig. 6)
+ * and give identical indices.  A group's landmark rows are split over CTAs of
+ * 256 threads x 1, 2 or 4 rows (the same split for every group).
+ * impl 0: the CTAs score their rows into global keys and histograms; the last
+ * CTA of each group (an atomic ticket) selects on its own.
+ * impl 2: where every group's CTAs number at most 8 they form one
+ * thread-block cluster per group; each keeps its keys in shared memory and
+ * the radix select runs on all of them, exchanging digit histograms and
+ * winner counts through distributed shared memory (nothing through global
+ * memory).  Otherwise impl 0 runs.
+ * impl 1 (default): impl 2 where the ticket kernel's tail would be long and
+ * exposed (groups of more than 1024 blocks and a grid that fits one wave of
+ * 4 CTAs per SM), else impl 0.
+ * Synchronises the context's streams and drops captured graphs.  Errors:
+ * KVO_ERR_INVALID for a null context or impl outside 0..2.
+ */
+kvo_status kvo_set_select_impl(kvo_ctx* ctx, int impl);
+
+/*
  * kvo_plan_attention -- the work split of the TMA-staged attention kernel
  * (kvo_set_attn_impl 1) for a shape, computed on the host: no context, no GPU.
  * The tiles (16 tokens) of every group -- its sparse part of sparse_tokens

@@ -128,6 +128,23 @@ int64_t plan_tma_items(int G, int sp_tokens, int w_tokens, int64_t grid, std::ve
     return grid;
 }
 
+// The selection kernel: a cluster per group where the group's CTAs fit one
+// (at most 8, the portable cluster size; shorter groups' extra CTAs score no
+// rows), else the ticket kernel.  Automatically only where the ticket
+// kernel's single-CTA tail is long and exposed: more than 4 keys per thread
+// (groups of more than 1024 blocks) in a grid of one wave, so no other
+// group's scoring runs beside the tails.  Measured, 20 isolated calls each:
+// wide_budget (64 groups x ~4000 blocks, 8 CTAs per cluster) 43.0 -> 39.6 us;
+// llama3_8b_decode (1008 blocks per group) 17.4 / 17.6 us, long_ctx_predict
+// (2.5 waves) 138.5 / 140.8 us, and the Llama chain step 2.10 / 2.15 ms with
+// the ticket / cluster kernel.
+static void set_sel_clu(kvo::Ctx& c) {
+    const int S = std::max(1, c.sel_chunks_max);
+    const bool exposed = c.Cmax > 4 * kvo::SEL_THREADS && c.n_sel_items <= c.sel_slots;
+    const bool want = c.sel_impl == 2 || (c.sel_impl == 1 && exposed);
+    c.sel_clu = want && S <= 8 ? S : 0;
+}
+
 kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
     const int w_max = c.max_append > 0 ? c.W + c.B - 1 : c.W;
     std::vector<int4> items;
@@ -435,6 +452,7 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         KVO_CUDA(&c, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         sms = std::max(1, sms);
         const int64_t slots = 4 * (int64_t)sms;
+        c.sel_slots = slots;
         auto waves = [&](int64_t x) { return (x + slots - 1) / slots; };
         if (n[2] >= 8 * (int64_t)sms) c.sel_rpt = 4;
         else c.sel_rpt = waves(n[1]) < waves(n[0]) ? 2 : 1;
@@ -443,7 +461,9 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     for (int g = 0; g < c.G; ++g) {
         nch[g] = (Ccap[g] + sel_rows - 1) / sel_rows;     // rows past the current C_b are skipped
         for (int j = 0; j < nch[g]; ++j) sel_items.push_back(make_int2(g, j));
+        c.sel_chunks_max = std::max(c.sel_chunks_max, nch[g]);
     }
+    set_sel_clu(c);
     c.n_sel_items = (int)sel_items.size();
     KVO_CUDA(&c, dalloc(&c.sel_items, sizeof(int2) * sel_items.size(), &sb));
     KVO_CUDA(&c, dalloc(&c.sel_nchunks, sizeof(int32_t) * c.G, &sb));
@@ -1335,6 +1355,18 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas) {
     ctx->c.tma_ctas = impl == 2 ? 0 : ctas;
     ctx->c.att_cluster = impl == 2 ? ctas : 0;
     return build_tma_plans(ctx->c);
+}
+
+kvo_status kvo_set_select_impl(kvo_ctx* ctx, int impl) {
+    if (check_ctx(ctx)) return KVO_ERR_INVALID;
+    kvo::Ctx& c = ctx->c;
+    if (impl < 0 || impl > 2) return fail(&c, KVO_ERR_INVALID, "selection implementation must be 0, 1 or 2");
+    for (cudaStream_t s : {c.s_compute, c.s_prefetch, c.s_urgent, c.s_urgent2, c.s_hit, c.s_graph})
+        KVO_CUDA(&c, cudaStreamSynchronize(s));
+    drop_graphs(c);
+    c.sel_impl = impl;
+    set_sel_clu(c);
+    return KVO_OK;
 }
 
 kvo_status kvo_set_wait_test(kvo_ctx* ctx, int64_t limit_ns, int skip_tile) {

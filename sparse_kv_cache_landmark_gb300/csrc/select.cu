@@ -19,6 +19,7 @@
 
 #include "kvo_internal.cuh"
 #include "resident_assign.cuh"
+#include "tma_ptx.cuh"
 
 namespace kvo {
 
@@ -126,38 +127,11 @@ __device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, in
 template <bool BF16LM, int SEL_RPT>
 constexpr int sel_min_blocks() { return SEL_RPT == 1 ? 4 : (BF16LM ? (SEL_RPT == 2 ? 2 : 1) : 4); }
 
-// ASSIGN: the last CTA of a group then assigns the group's resident slots for
-// its true index (the routine of resident_assign.cuh, `aa` with need = the
-// true index; res_assign_ints(k) ints of dynamic shared memory), so a step
-// without a speculative query needs no separate assignment launch.
-template <int D, bool BF16LM, bool DUAL, int SEL_RPT, bool ASSIGN>
-__global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
-select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
-              const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
-              uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
-              int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
-              int Hkv, int k, int key_cache, int dep_wait, const ResAssignArgs aa) {
-    constexpr int NQ = DUAL ? 2 : 1;
-    __shared__ __align__(16) float u_s[NQ][D];
-    __shared__ uint32_t h_s[NQ][256];
-    __shared__ uint32_t warp_sums[32];
-    __shared__ int s_last;
-    __shared__ int s_digit;
-    __shared__ uint32_t s_krem;
-
-    const int tid = threadIdx.x;
-    // dep_wait: launched as a programmatic dependent of the kernel before it on
-    // the stream, which may have written any input (and a selection before it
-    // resets the histograms and tickets last) -- nothing is read before it is done
-    if (dep_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int2 it = items[blockIdx.x];
-    const int bg = it.x, chunk = it.y;
-    const int b = bg / Hkv, g = bg % Hkv;
-    const int C = g_C[bg];
-    const int Hq = Hkv * r;
-
-    // summed query of the group, fp32
-    for (int c = tid; c < D; c += SEL_THREADS) {
+// The group's summed query (and speculative query with DUAL), fp32, into u_s.
+template <int D, bool DUAL>
+__device__ __forceinline__ void sum_queries(const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs, int b,
+                                            int g, int Hq, int r, float (*u_s)[D]) {
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
         const uint16_t* qp = q + ((int64_t)b * Hq + g * r) * D + c;
         float a = 0.f;
         for (int h = 0; h < r; ++h) a += __uint_as_float((uint32_t)qp[h * D] << 16);
@@ -166,16 +140,16 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             const uint16_t* sp = qs + ((int64_t)b * Hq + g * r) * D + c;
             float e = 0.f;
             for (int h = 0; h < r; ++h) e += __uint_as_float((uint32_t)sp[h * D] << 16);
-            u_s[NQ - 1][c] = e;
+            u_s[1][c] = e;
         }
     }
-    for (int i = tid; i < NQ * 256; i += SEL_THREADS) (&h_s[0][0])[i] = 0u;
-    __syncthreads();
+}
 
-    // ---- score SEL_RPT rows per thread (rows strided by the CTA width)
-    constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;
-    const int row0 = chunk * SEL_ROWS + tid;
-    float acc[NQ][SEL_RPT];
+// Scores of SEL_RPT landmark rows per thread (rows row0 + i * SEL_THREADS,
+// those at or past C scoring 0) against the NQ summed queries in u_s.
+template <int D, bool BF16LM, int NQ, int SEL_RPT>
+__device__ __forceinline__ void score_rows(const void* __restrict__ lm_v, int bg, int Cmax, int C, int row0,
+                                           const float (*u_s)[D], float (&acc)[NQ][SEL_RPT]) {
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi)
 #pragma unroll
@@ -235,6 +209,47 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             }
         }
     }
+}
+
+// ASSIGN: the last CTA of a group then assigns the group's resident slots for
+// its true index (the routine of resident_assign.cuh, `aa` with need = the
+// true index; res_assign_ints(k) ints of dynamic shared memory), so a step
+// without a speculative query needs no separate assignment launch.
+template <int D, bool BF16LM, bool DUAL, int SEL_RPT, bool ASSIGN>
+__global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
+select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
+              const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
+              uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
+              int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
+              int Hkv, int k, int key_cache, int dep_wait, const ResAssignArgs aa) {
+    constexpr int NQ = DUAL ? 2 : 1;
+    __shared__ __align__(16) float u_s[NQ][D];
+    __shared__ uint32_t h_s[NQ][256];
+    __shared__ uint32_t warp_sums[32];
+    __shared__ int s_last;
+    __shared__ int s_digit;
+    __shared__ uint32_t s_krem;
+
+    const int tid = threadIdx.x;
+    // dep_wait: launched as a programmatic dependent of the kernel before it on
+    // the stream, which may have written any input (and a selection before it
+    // resets the histograms and tickets last) -- nothing is read before it is done
+    if (dep_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int2 it = items[blockIdx.x];
+    const int bg = it.x, chunk = it.y;
+    const int b = bg / Hkv, g = bg % Hkv;
+    const int C = g_C[bg];
+    const int Hq = Hkv * r;
+
+    sum_queries<D, DUAL>(q, qs, b, g, Hq, r, u_s);
+    for (int i = tid; i < NQ * 256; i += SEL_THREADS) (&h_s[0][0])[i] = 0u;
+    __syncthreads();
+
+    // ---- score SEL_RPT rows per thread (rows strided by the CTA width)
+    constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;
+    const int row0 = chunk * SEL_ROWS + tid;
+    float acc[NQ][SEL_RPT];
+    score_rows<D, BF16LM, NQ, SEL_RPT>(lm_v, bg, Cmax, C, row0, u_s, acc);
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
         uint32_t* kq = keys + ((int64_t)qi * G + bg) * Cmax4;
@@ -397,6 +412,167 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     }
 }
 
+// Cluster selection: a group's landmark rows are split over the S CTAs of one
+// thread-block cluster (S <= 8; rank r scores rows [r * SEL_ROWS, (r + 1) *
+// SEL_ROWS)), each CTA keeping its keys in its own shared memory.  The radix
+// select runs on all S CTAs at once: every pass each CTA histograms the digit
+// of its own keys that still match the prefix, a cluster barrier publishes the
+// histograms, and every CTA sums the S histograms of a bin through distributed
+// shared memory and picks the same digit.  A pass whose bin holds exactly the
+// keys still wanted ends the search early (they are all taken).  The winners
+// are written in ascending id order: each CTA publishes its counts of keys
+// above and equal to the threshold, and offsets its writes by those of the
+// lower ranks.  No keys, histograms or tickets go through global memory.
+// With ASSIGN, rank 0 assigns the group's resident slots once every rank's
+// writes of the true index are visible to it (the release / acquire cluster
+// barrier).
+__device__ __forceinline__ void pick_digit_cnt(uint32_t cnt, uint32_t* warp_sums, int* s_digit, uint32_t* s_krem,
+                                               uint32_t* s_bincnt, uint32_t k_rem) {
+    uint32_t total;
+    const uint32_t excl = block_exclusive_scan(cnt, warp_sums, &total);
+    if (excl < k_rem && excl + cnt >= k_rem) {
+        *s_digit = 255 - (int)threadIdx.x;
+        *s_krem = k_rem - excl;
+        *s_bincnt = cnt;
+    }
+    __syncthreads();
+}
+
+template <int D, bool BF16LM, bool DUAL, int SEL_RPT, bool ASSIGN>
+__global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
+select_cluster_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
+                      const int32_t* __restrict__ g_C, int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred,
+                      int Cmax, int r, int Hkv, int k, int dep_wait, const ResAssignArgs aa) {
+    constexpr int NQ = DUAL ? 2 : 1;
+    constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;
+    __shared__ __align__(16) float u_s[NQ][D];
+    __shared__ __align__(16) uint32_t k_s[NQ][SEL_ROWS];   // this CTA's keys, local row order
+    __shared__ uint32_t h_s[NQ][256];                        // top-byte histogram of this CTA's keys
+    __shared__ uint32_t hc[2][256];                          // later passes' histograms, alternating
+    __shared__ uint32_t cnt_s[NQ][2];                        // keys above / equal to the threshold
+    __shared__ uint32_t warp_sums[32];
+    __shared__ int s_digit;
+    __shared__ uint32_t s_krem, s_bincnt;
+
+    const int tid = threadIdx.x;
+    if (dep_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t S = cluster_size(), rank = cluster_rank();
+    const int bg = (int)(blockIdx.x / S);
+    const int b = bg / Hkv, g = bg % Hkv;
+    const int C = g_C[bg];
+    const int base = (int)rank * SEL_ROWS;                   // first row of this CTA
+    const int nloc = max(0, min(C - base, SEL_ROWS));        // rows of this CTA
+
+    sum_queries<D, DUAL>(q, qs, b, g, Hkv * r, r, u_s);
+    for (int i = tid; i < NQ * 256; i += SEL_THREADS) (&h_s[0][0])[i] = 0u;
+    __syncthreads();
+
+    float acc[NQ][SEL_RPT];
+    score_rows<D, BF16LM, NQ, SEL_RPT>(lm_v, bg, Cmax, C, base + tid, u_s, acc);
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi)
+#pragma unroll
+        for (int i = 0; i < SEL_RPT; ++i) {
+            const int j = tid + i * SEL_THREADS;
+            if (j < nloc) {
+                const uint32_t key = float_to_ordered(acc[qi][i]);
+                k_s[qi][j] = key;
+                atomicAdd(&h_s[qi][key >> 24], 1u);
+            }
+        }
+    // the kernel behind this one may be scheduled once every CTA has scored
+    if (dep_wait) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    cluster_barrier();                                       // keys and top-byte histograms complete
+
+    // thread t's keys for the passes and the compaction: local rows
+    // [t * SEL_RPT, (t + 1) * SEL_RPT), in id order
+    const int j0 = tid * SEL_RPT;
+    for (int qi = 0; qi < NQ; ++qi) {
+        uint32_t kr[SEL_RPT];
+        if constexpr (SEL_RPT == 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(&k_s[qi][j0]);
+            kr[0] = v.x; kr[1] = v.y; kr[2] = v.z; kr[3] = v.w;
+        } else if constexpr (SEL_RPT == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(&k_s[qi][j0]);
+            kr[0] = v.x; kr[1] = v.y;
+        } else {
+            kr[0] = k_s[qi][j0];
+        }
+        const int n_mine = min(SEL_RPT, max(0, nloc - j0));
+        int32_t* out = (qi == 0 ? idx_true : idx_pred) + (int64_t)bg * k;
+        uint32_t k_rem = (uint32_t)min(k, C);
+        if (k_rem == 0) continue;                            // the same for every rank of the cluster
+        uint32_t prefix = 0u, mask = 0u;
+        const uint32_t* hsrc = h_s[qi];
+        int shift = 24, hb = 0;
+        while (true) {
+            uint32_t cnt = 0;
+            for (uint32_t rr = 0; rr < S; ++rr) cnt += ld_cluster_u32(hsrc + 255 - tid, rr);
+            // the buffer the next pass fills: its last remote readers passed the barrier before this pass
+            hc[hb][tid] = 0u;
+            pick_digit_cnt(cnt, warp_sums, &s_digit, &s_krem, &s_bincnt, k_rem);
+            prefix |= (uint32_t)s_digit << shift;
+            mask |= 0xFFu << shift;
+            const bool whole_bin = s_krem == s_bincnt;
+            k_rem = s_krem;
+            if (shift == 0 || whole_bin) break;              // the same decision on every rank
+            shift -= 8;
+#pragma unroll
+            for (int e = 0; e < SEL_RPT; ++e)
+                if (e < n_mine && (kr[e] & mask) == prefix) atomicAdd(&hc[hb][(kr[e] >> shift) & 0xFFu], 1u);
+            cluster_barrier();
+            hsrc = hc[hb];
+            hb ^= 1;
+        }
+        // take every key whose masked value is above the prefix and the first
+        // k_rem equal to it (all of them when the search ended on a whole bin)
+        const uint32_t k_eq = k_rem;
+        uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+        for (int e = 0; e < SEL_RPT; ++e)
+            if (e < n_mine) {
+                n_gt += (kr[e] & mask) > prefix;
+                n_eq += (kr[e] & mask) == prefix;
+            }
+        uint32_t tot_eq, tot_gt;
+        const uint32_t eq_excl = block_exclusive_scan(n_eq, warp_sums, &tot_eq);
+        const uint32_t gt_excl = block_exclusive_scan(n_gt, warp_sums, &tot_gt);
+        if (tid == 0) {
+            cnt_s[qi][0] = tot_gt;
+            cnt_s[qi][1] = tot_eq;
+        }
+        cluster_barrier();                                   // every rank's counts published
+        uint32_t pos_base = 0, eq_base = 0;
+        for (uint32_t rr = 0; rr < rank; ++rr) {
+            const uint32_t gt_r = ld_cluster_u32(&cnt_s[qi][0], rr), eq_r = ld_cluster_u32(&cnt_s[qi][1], rr);
+            pos_base += gt_r + (eq_base >= k_eq ? 0u : min(eq_r, k_eq - eq_base));
+            eq_base += eq_r;
+        }
+        // thread t writes after the lower ranks' winners, this CTA's keys above
+        // the threshold before it and its equal keys taken before it
+        uint32_t eq_run = eq_base + eq_excl;
+        uint32_t pos = pos_base + gt_excl + (eq_base >= k_eq ? 0u : min(eq_excl, k_eq - eq_base));
+#pragma unroll
+        for (int e = 0; e < SEL_RPT; ++e)
+            if (e < n_mine) {
+                const uint32_t m = kr[e] & mask;
+                bool take = m > prefix;
+                if (m == prefix) take = eq_run++ < k_eq;
+                if (take) out[pos++] = base + j0 + e;
+            }
+    }
+    // no CTA leaves while another may still read its shared memory; with
+    // ASSIGN the barrier also makes every rank's index writes visible to rank 0
+    cluster_barrier();
+    if constexpr (ASSIGN) {
+        if (rank == 0) {
+            extern __shared__ __align__(16) int32_t sel_rs[];
+            __shared__ uint32_t s_tot;
+            resident_assign_group(aa, bg, sel_rs, warp_sums, &s_tot);
+        }
+    }
+}
+
 cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_spec, int32_t* idx_true,
                           int32_t* idx_pred, cudaStream_t s, const ResAssignArgs* assign, bool pdl) {
     const int Cmax4 = (c.Cmax + 3) & ~3;
@@ -425,6 +601,42 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
     cfg.numAttrs = pdl ? 1 : 0;
     const int dep_wait = pdl ? 1 : 0;
     cudaError_t err = cudaSuccess;
+    if (c.sel_clu > 0) {
+        // one cluster of sel_clu CTAs per group; only the assignment's lists are dynamic
+        cudaLaunchAttribute ca[2];
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = (unsigned)c.sel_clu;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = 1;
+        ca[1] = attr[0];
+        cfg.gridDim = dim3((unsigned)(c.G * c.sel_clu));
+        cfg.dynamicSmemBytes = assign ? sizeof(int32_t) * res_assign_ints(c.k) : 0;
+        cfg.attrs = ca;
+        cfg.numAttrs = pdl ? 2 : 1;
+#define KVO_SELC_L(D_, BF_, DU_, RPT_, AS_)                                                                    \
+    err = cudaLaunchKernelEx(&cfg, select_cluster_kernel<D_, BF_, DU_, RPT_, AS_>, c.lm[layer],                \
+                             (const uint16_t*)q, (const uint16_t*)q_spec, (const int32_t*)c.g_C, idx_true,     \
+                             idx_pred, c.Cmax, c.r, c.Hkv, c.k, dep_wait, aa)
+#define KVO_SELC(D_, BF_, DU_, AS_)                                                                            \
+    do {                                                                                                       \
+        if (c.sel_rpt == 1) KVO_SELC_L(D_, BF_, DU_, 1, AS_);                                                  \
+        else if (c.sel_rpt == 2) KVO_SELC_L(D_, BF_, DU_, 2, AS_);                                             \
+        else KVO_SELC_L(D_, BF_, DU_, 4, AS_);                                                                 \
+    } while (0)
+        if (assign) {
+            if (c.d == 128) { if (bf) KVO_SELC(128, true, false, true); else KVO_SELC(128, false, false, true); }
+            else            { if (bf) KVO_SELC(64, true, false, true); else KVO_SELC(64, false, false, true); }
+        } else if (c.d == 128) {
+            if (bf) { if (dual) KVO_SELC(128, true, true, false); else KVO_SELC(128, true, false, false); }
+            else    { if (dual) KVO_SELC(128, false, true, false); else KVO_SELC(128, false, false, false); }
+        } else {
+            if (bf) { if (dual) KVO_SELC(64, true, true, false); else KVO_SELC(64, true, false, false); }
+            else    { if (dual) KVO_SELC(64, false, true, false); else KVO_SELC(64, false, false, false); }
+        }
+#undef KVO_SELC
+#undef KVO_SELC_L
+        return err;
+    }
 #define KVO_SEL_L(D_, BF_, DU_, RPT_, AS_)                                                                     \
     err = cudaLaunchKernelEx(&cfg, select_kernel<D_, BF_, DU_, RPT_, AS_>, c.lm[layer], (const uint16_t*)q,     \
                              (const uint16_t*)q_spec, (const int2*)c.sel_items, (const int32_t*)c.sel_nchunks,  \
@@ -475,6 +687,16 @@ cudaError_t prepare_select_assign(const Ctx& c) {
     KVO_SEL_ATTR(64, true, 1); KVO_SEL_ATTR(64, true, 2); KVO_SEL_ATTR(64, true, 4);
     KVO_SEL_ATTR(64, false, 1); KVO_SEL_ATTR(64, false, 2); KVO_SEL_ATTR(64, false, 4);
 #undef KVO_SEL_ATTR
+    const int abytes = (int)(sizeof(int32_t) * res_assign_ints(c.k));
+#define KVO_SELC_ATTR(D_, BF_, RPT_)                                                                           \
+    if (e == cudaSuccess)                                                                                      \
+        e = cudaFuncSetAttribute(select_cluster_kernel<D_, BF_, false, RPT_, true>,                            \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, abytes)
+    KVO_SELC_ATTR(128, true, 1); KVO_SELC_ATTR(128, true, 2); KVO_SELC_ATTR(128, true, 4);
+    KVO_SELC_ATTR(128, false, 1); KVO_SELC_ATTR(128, false, 2); KVO_SELC_ATTR(128, false, 4);
+    KVO_SELC_ATTR(64, true, 1); KVO_SELC_ATTR(64, true, 2); KVO_SELC_ATTR(64, true, 4);
+    KVO_SELC_ATTR(64, false, 1); KVO_SELC_ATTR(64, false, 2); KVO_SELC_ATTR(64, false, 4);
+#undef KVO_SELC_ATTR
     return e;
 }
 

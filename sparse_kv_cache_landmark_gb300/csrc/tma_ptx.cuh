@@ -69,6 +69,13 @@ __device__ __forceinline__ float ld_cluster_f32(const void* local, uint32_t rank
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u32(const void* local, uint32_t rank) {
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // named barrier over the first n threads of the CTA (n a multiple of 32)
 __device__ __forceinline__ void bar_named(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");

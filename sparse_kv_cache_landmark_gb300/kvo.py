@@ -24,7 +24,7 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_device_status", "kvo_landmarks", "kvo_buffer", "kvo_info", "kvo_profile", "kvo_profile_read",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
-           "kvo_set_attn_impl", "kvo_resident_slots", "kvo_resident_fetched",
+           "kvo_set_attn_impl", "kvo_set_select_impl", "kvo_resident_slots", "kvo_resident_fetched",
            "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention", "kvo_set_wait_test",
            "kvo_set_spec_policy", "kvo_spec_stats"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention", "recon"]
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.kvo_set_gather_reserve.argtypes = [P, I]
         L.kvo_set_graphs.argtypes = [P, I]
         L.kvo_set_attn_impl.argtypes = [P, I, I]
+        L.kvo_set_select_impl.argtypes = [P, I]
         L.kvo_resident_slots.argtypes = [P, I, ctypes.POINTER(ctypes.c_int32)]
         L.kvo_resident_fetched.argtypes = [P, ctypes.POINTER(ctypes.c_int64), I]
         L.kvo_set_prefetch_budget.argtypes = [P, I]
@@ -396,6 +397,12 @@ class Context:
         ``ctas`` CTAs (0: as many as fit), 2 (default) group-split clusters of
         ``ctas`` CTAs per group (0: automatic) (C: kvo_set_attn_impl)."""
         self._c(lib().kvo_set_attn_impl(self.ctx, impl, ctas))
+
+    def set_select_impl(self, impl: int):
+        """Selection kernel: 0 ticket, 2 one cluster per group where a group's
+        CTAs fit one, 1 (default) the cluster kernel where the ticket kernel's
+        tail would be long and exposed (C: kvo_set_select_impl)."""
+        self._c(lib().kvo_set_select_impl(self.ctx, impl))
 
     def set_wait_test(self, limit_ns: int = 2_000_000_000, skip_tile: int = -1):
         """Bounded-wait test switch of the TMA-staged attention (C: kvo_set_wait_test)."""

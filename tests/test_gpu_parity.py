@@ -26,6 +26,9 @@ CASES = {
     "clustered": Workload("clustered", 1, 16, 2, 128, 64, 8, 64, 1, (6464, 6464), key_dist="clustered",
                           n_centroids=32, centroid_sigma=0.3),
     "multi_chunk": Workload("multi_chunk", 2, 8, 2, 128, 2, 64, 16, 1, (6016, 6016), spec_sigma=0.2),
+    # 750-1500 blocks per group: six selection CTAs per group's cluster, the
+    # shorter groups' last three scoring no rows
+    "sel_cluster6": Workload("sel_cluster6", 3, 8, 2, 128, 4, 32, 16, 1, (3016, 6016), spec_sigma=0.3),
     # 800 register-direct tiles per group = 50 work items: more than the merge's
     # shared-memory table holds at d = 64, so the online merge runs
     "many_items": Workload("many_items", 1, 8, 2, 64, 32, 400, 32, 1, (32 + 32 * 420, 32 + 32 * 420)),
@@ -81,6 +84,33 @@ def test_select_topk_bit_exact(case):
     T2, _ = c.ctx.select_topk(0, c.q_dev(0))
     assert torch.equal(T2.cpu(), T)
     assert c.ctx.device_status() == 0
+
+
+@pytest.mark.parametrize("impl", [0, 2])
+def test_select_kernels_match_the_oracle(case, impl):
+    """The ticket kernel (impl 0) and the cluster kernel (impl 2, where a
+    group's CTAs fit a cluster) give the oracle's indices, true and speculative."""
+    c, refs = case
+    w = c.w
+    try:
+        c.ctx.set_select_impl(impl)
+        for _ in range(2):                 # the second call finds the scratch as the first left it
+            T, P = c.ctx.select_topk(0, c.q_dev(0), c.q_dev(0, spec=True))
+            T, P = T.cpu(), (None if P is None else P.cpu())
+            for (b, g), ref in refs.items():
+                assert T[b * w.n_kv_heads + g].tolist() == ref.T.tolist(), (impl, b, g)
+                if P is not None:
+                    assert P[b * w.n_kv_heads + g].tolist() == ref.P.tolist(), (impl, b, g)
+        assert c.ctx.device_status() == 0
+    finally:
+        c.ctx.set_select_impl(1)
+
+
+def test_select_impl_setter_checks_its_argument(case):
+    c, _ = case
+    for bad in (-1, 3):
+        with pytest.raises(KvoError):
+            c.ctx.set_select_impl(bad)
 
 
 def test_diff_gather_attention_chain(case):

@@ -58,6 +58,8 @@ def _attempts(c, steps, drift):
     (False, 1, 16, 8, False, None, 32, "many", False),  # 320 groups: one CTA per group for the fetched blocks
     (False, 2, 32, 12, False, None, 64, True, "impl0"),  # chain steps with the register-direct attention
     (False, 2, 32, 12, False, None, 64, True, "impl2g"),  # chain steps, group-split cluster attention, graphs
+    (False, 2, 1, 24, False, None, 32, True, "sel2"),  # B = 1: 600-640 blocks, three selection CTAs per cluster
+    (False, 2, 1, 24, False, None, 32, True, "sel0"),  # ... with the ticket selection kernel
     (True, 2, 16, 16, True, None, 32, False, "impl2")])  # speculative resident steps, cluster attention
 def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged, graphs):
     drift, steps, seed = 0.15, 6, 321
@@ -74,7 +76,11 @@ def test_resident_steps_match_the_oracle(spec, L, B, k, dual, budget, W, ragged,
         att = _attempts(c, steps, drift)
         if budget is not None:
             c.ctx.set_prefetch_budget(budget)     # admission cap on speculative fetches
-        if graphs == "impl0":
+        if graphs in ("sel0", "sel2"):
+            # the fused assignment in the ticket kernel's last CTA / the cluster's first CTA
+            c.ctx.set_select_impl(0 if graphs == "sel0" else 2)
+            graphs = False
+        elif graphs == "impl0":
             c.ctx.set_attn_impl(0)                # one attention pass after the copy, whole set
             graphs = False
         elif graphs in ("impl2", "impl2g"):
