@@ -413,9 +413,9 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
         const size_t rows = (size_t)c.batch * c.Hq;
         KVO_CUDA(&c, dalloc(&c.res_hit_slot, sizeof(int32_t) * lg * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_hit_cnt, sizeof(int32_t) * lg, &sb));
-        // two layers' worth: a chain step attends to layer l's hits while layer l - 1's merge runs
-        KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * 2 * rows * c.d, &sb));
-        KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * 2 * rows, &sb));
+        // one per layer: a layer's hit pass never waits for an earlier layer's merge
+        KVO_CUDA(&c, dalloc(&c.res_oA, sizeof(float) * c.L * rows * c.d, &sb));
+        KVO_CUDA(&c, dalloc(&c.res_lA, sizeof(float) * c.L * rows, &sb));
         KVO_CUDA(&c, cudaMemsetAsync(c.res_fetched, 0, sizeof(unsigned long long) * 2, c.s_compute));
         KVO_CUDA(&c, dalloc(&c.res_pfbit, (size_t)c.L * c.G * 2 * c.k, &sb));
         KVO_CUDA(&c, dalloc(&c.res_stat, sizeof(unsigned long long) * 2 * c.L, &sb));
@@ -912,9 +912,6 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
         // 3. urgent gather of the blocks that were missing
         KVO_CUDA(&c, cudaEventRecord(E.sel[l], sc));
         KVO_CUDA(&c, cudaStreamWaitEvent(su, E.sel[l], 0));
-        // layer l's hit pass reuses layer l - 2's half of the hit-pass scratch:
-        // that layer's merge has read it
-        if (split && l >= 2) KVO_CUDA(&c, cudaStreamWaitEvent(su, E.attn[l - 2], 0));
         // In-flight prefetch copies of this layer land first when nothing is spared
         // (no prediction).  (A chain step has none in flight; a speculative hit
         // pass waits for them itself.)
@@ -924,24 +921,25 @@ static kvo_status decode_step_resident(kvo_ctx* ctx, const void* q, const void* 
             return kvo::launch_gather_flat(c, l, buf, miss, mcnt, 0, su, dsl, urg_mask);
         }));
         if (split) {
-            float* oA = c.res_oA + (size_t)(l & 1) * o_layer;
-            float* lA = c.res_lA + (size_t)(l & 1) * lse_layer;
+            // the hits' result has a buffer per layer; the partials and tickets of the
+            // persistent kernel alternate by layer parity, so each set serves the
+            // layers of one stream (a chain step's urgent streams take the layers
+            // in turn; a speculative step's hit passes share one stream)
+            float* oA = c.res_oA + (size_t)l * o_layer;
+            float* lA = c.res_lA + (size_t)l * lse_layer;
             if (alone_step) {
                 // hits + window beside the copy: a programmatic dependent of the copy,
                 // dispatched once the copy's SM-exclusive CTAs are all resident (so it
-                // cannot take their SMs), completing after it; layer l - 1's merge may
-                // still run -- it reads the other half of the hit-pass scratch
+                // cannot take their SMs), completing after it
                 KVO_CUDA(&c, timed(kvo::PK_ATTENTION, su, [&] {
                     return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, su,
                                                  true, hit_cnt, true, l & 1);
                 }));
             } else {
-                // hits + window on their own stream once the assign has listed them,
-                // layer l - 2's merge has read this half of the scratch and the
-                // blocks prefetched for this step have landed
+                // hits + window on their own stream once the assign has listed them
+                // and the blocks prefetched for this step have landed
                 const cudaStream_t sh = c.s_hit;
                 KVO_CUDA(&c, cudaStreamWaitEvent(sh, E.sel[l], 0));
-                if (l >= 2) KVO_CUDA(&c, cudaStreamWaitEvent(sh, E.attn[l - 2], 0));
                 if (pending) KVO_CUDA(&c, cudaStreamWaitEvent(sh, E.rpref[l], 0));
                 KVO_CUDA(&c, timed(kvo::PK_ATTENTION, sh, [&] {
                     return kvo::launch_attention(c, l, buf, ql, nullptr, hit_slot, oA, lA, nullptr, nullptr, 1, sh,
