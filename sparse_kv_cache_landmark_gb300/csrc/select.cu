@@ -13,8 +13,11 @@
 //   B == 1: uint4  [G][d/8][Cmax]   (8 bf16 per chunk)
 // Selection is one kernel: CTAs score chunks of landmark rows of one group,
 // write order-preserving uint32 keys and a histogram of their top 8 bits; the
-// last CTA of a group (atomic ticket) finishes a 4-pass MSB radix select on
-// the L2-resident keys and compacts the winners in ascending id order.
+// last CTA of a group (atomic ticket) finishes an MSB radix select (up to 4
+// passes of 8 bits, ending early on a bin whose keys are all wanted) on
+// the L2-resident keys and compacts the winners in ascending id order.  Where
+// a group's CTAs fit one thread-block cluster, select_cluster_kernel (below)
+// can run the radix select on all of them instead.
 #include <algorithm>
 
 #include "kvo_internal.cuh"
@@ -109,14 +112,17 @@ cudaError_t copy_landmarks_logical(const Ctx& c, int layer, void* dst, cudaStrea
 
 // ------------------------------------------------------------- selection
 // Thread t of a 256-thread CTA owns radix bin 255 - t (descending).  Given
-// per-bin counts, find the bin holding the k_rem-th largest key.
-__device__ __forceinline__ void pick_digit(uint32_t cnt, uint32_t* warp_sums, int* s_digit, uint32_t* s_krem,
-                                           uint32_t k_rem) {
+// per-bin counts, find the bin holding the k_rem-th largest key: its digit,
+// the keys still wanted from it and its count (when the two are equal the
+// whole bin is taken and the search can end).
+__device__ __forceinline__ void pick_digit_cnt(uint32_t cnt, uint32_t* warp_sums, int* s_digit, uint32_t* s_krem,
+                                               uint32_t* s_bincnt, uint32_t k_rem) {
     uint32_t total;
     const uint32_t excl = block_exclusive_scan(cnt, warp_sums, &total);
     if (excl < k_rem && excl + cnt >= k_rem) {
         *s_digit = 255 - (int)threadIdx.x;
         *s_krem = k_rem - excl;
+        *s_bincnt = cnt;
     }
     __syncthreads();
 }
@@ -228,7 +234,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     __shared__ uint32_t warp_sums[32];
     __shared__ int s_last;
     __shared__ int s_digit;
-    __shared__ uint32_t s_krem;
+    __shared__ uint32_t s_krem, s_bincnt;
 
     const int tid = threadIdx.x;
     // dep_wait: launched as a programmatic dependent of the kernel before it on
@@ -305,8 +311,9 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
         uint32_t k_rem = (uint32_t)min(k, C);
         const uint32_t cnt0 = __ldcg(hg + 255 - tid);
         hg[255 - tid] = 0u;                                  // leave the histogram zeroed
-        pick_digit(cnt0, warp_sums, &s_digit, &s_krem, k_rem);
+        pick_digit_cnt(cnt0, warp_sums, &s_digit, &s_krem, &s_bincnt, k_rem);
         uint32_t prefix = (uint32_t)s_digit << 24, mask = 0xFF000000u;
+        bool whole_bin = s_krem == s_bincnt;                  // the bin's keys are all wanted: done
         k_rem = s_krem;
         // four keys from the cache or from L2
         auto ld4 = [&](int j) -> uint4 {
@@ -328,7 +335,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             }
         };
         const bool small = C <= 4 * SEL_THREADS;             // at most 4 keys per thread
-        for (int shift = 16; shift >= 0; shift -= 8) {
+        for (int shift = 16; shift >= 0 && !whole_bin; shift -= 8) {
             h_s[0][tid] = 0u;
             __syncthreads();
             if (small) {
@@ -348,13 +355,15 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             __syncthreads();
             const uint32_t cnt = h_s[0][255 - tid];
             __syncthreads();
-            pick_digit(cnt, warp_sums, &s_digit, &s_krem, k_rem);
+            pick_digit_cnt(cnt, warp_sums, &s_digit, &s_krem, &s_bincnt, k_rem);
             prefix |= (uint32_t)s_digit << shift;
             mask |= 0xFFu << shift;
+            whole_bin = s_krem == s_bincnt;
             k_rem = s_krem;
         }
-        // prefix == key of the k-th largest; take every larger key and the first
-        // k_rem keys equal to it, in ascending id order.
+        // under the mask, prefix is the k-th largest key: take every key above it
+        // and the first k_rem equal to it (all of them when the search ended on a
+        // whole bin), in ascending id order
         const uint32_t thr = prefix;
         const uint32_t k_eq = k_rem;
         if (small) {
@@ -365,7 +374,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             const uint32_t kv[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
             uint32_t n_eq = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) n_eq += (j0 + e < C && kv[e] == thr);
+            for (int e = 0; e < 4; ++e) n_eq += (j0 + e < C && (kv[e] & mask) == thr);
             uint32_t tot;
             uint32_t eq_run = block_exclusive_scan(n_eq, warp_sums, &tot);
             uint32_t sel = 0;
@@ -373,8 +382,8 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const bool valid = j0 + e < C;
-                bool t = valid && kv[e] > thr;
-                if (valid && kv[e] == thr) t = eq_run++ < k_eq;
+                bool t = valid && (kv[e] & mask) > thr;
+                if (valid && (kv[e] & mask) == thr) t = eq_run++ < k_eq;
                 take[e] = t;
                 sel += t;
             }
@@ -386,8 +395,8 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             // counts per chunk, two block scans for the offsets, then the writes
             uint32_t n_gt = 0, n_eq = 0;
             scan_chunk([&](int, uint32_t key) {
-                n_gt += key > thr;
-                n_eq += key == thr;
+                n_gt += (key & mask) > thr;
+                n_eq += (key & mask) == thr;
             });
             uint32_t tot;
             const uint32_t eq_before = block_exclusive_scan(n_eq, warp_sums, &tot);
@@ -395,8 +404,8 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
             uint32_t pos = block_exclusive_scan(n_gt + eq_take, warp_sums, &tot);
             uint32_t eq_run = eq_before;
             scan_chunk([&](int j, uint32_t key) {
-                bool take = key > thr;
-                if (key == thr) take = eq_run++ < k_eq;
+                bool take = (key & mask) > thr;
+                if ((key & mask) == thr) take = eq_run++ < k_eq;
                 if (take) out[pos++] = j;
             });
         }
@@ -426,18 +435,6 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
 // With ASSIGN, rank 0 assigns the group's resident slots once every rank's
 // writes of the true index are visible to it (the release / acquire cluster
 // barrier).
-__device__ __forceinline__ void pick_digit_cnt(uint32_t cnt, uint32_t* warp_sums, int* s_digit, uint32_t* s_krem,
-                                               uint32_t* s_bincnt, uint32_t k_rem) {
-    uint32_t total;
-    const uint32_t excl = block_exclusive_scan(cnt, warp_sums, &total);
-    if (excl < k_rem && excl + cnt >= k_rem) {
-        *s_digit = 255 - (int)threadIdx.x;
-        *s_krem = k_rem - excl;
-        *s_bincnt = cnt;
-    }
-    __syncthreads();
-}
-
 template <int D, bool BF16LM, bool DUAL, int SEL_RPT, bool ASSIGN>
 __global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
 select_cluster_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
