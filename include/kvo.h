@@ -355,7 +355,10 @@ kvo_status kvo_buffer(kvo_ctx* ctx, int buf, void** k_out, void** v_out);
  * dependent of the copy so that it takes the SMs the copy leaves free), then
  * the fetched blocks, merged into the first result by log-sum-exp (with the
  * register-direct attention kernel, kvo_set_attn_impl 0, the step attends to
- * the whole set after the copy instead).  The copies of this mode always use
+ * the whole set after the copy instead).  A step with a speculative query and
+ * no low-rank layer splits its attention the same way, the first part
+ * launched plainly on a stream of its own (compute priority) once the
+ * blocks prefetched for the step have landed.  The copies of this mode always use
  * the flat gather engine (engine 3, with per-entry destination slots)
  * whatever kvo_set_gather_engine chose.
  *   kvo_resident_slots: synchronize, copy layer `layer`'s slot table
