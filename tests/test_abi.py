@@ -76,6 +76,8 @@ def test_null_arguments_are_rejected(lib):
     assert lib.select_topk(None, 0, None, None, None, None, None) == kvo.KVO_ERR_INVALID
     assert lib.merge_lse(None, None, None, None, None, None, -1, 4, None) == kvo.KVO_ERR_INVALID
     assert lib.merge_lse(None, None, None, None, None, None, 3, 4, None) == kvo.KVO_ERR_INVALID
+    assert lib.kvo_set_select_impl(None, 1) == kvo.KVO_ERR_INVALID
+    assert lib.kvo_set_attn_impl(None, 2, 0) == kvo.KVO_ERR_INVALID
     assert lib.kv_offload_destroy(None) == kvo.KVO_OK
     assert lib.merge_lse(None, None, None, None, None, None, 0, 4, None) == kvo.KVO_OK
 
