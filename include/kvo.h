@@ -58,8 +58,8 @@
  *             may overlap them on the same context.
  *    Calls of different classes may overlap freely (e.g. select_topk of layer
  *    l + 1 on one stream beside sparse_decode_attn of layer l on another).
- *    index_diff uses no context scratch (only its own outputs); merge_lse and
- *    kvo_plan_attention need no context.  The device status word is updated
+ *    index_diff uses no context scratch (only its own outputs); merge_lse,
+ *    kvo_plan_select and kvo_plan_attention need no context.  The device status word is updated
  *    atomically and may be written by overlapping calls.  Host-side calls that
  *    change settings (kvo_set_*, kvo_reset_prediction, kvo_profile*) first
  *    synchronize the context's own streams but not the caller's: make sure no
@@ -559,6 +559,21 @@ kvo_status kvo_set_attn_impl(kvo_ctx* ctx, int impl, int ctas);
  * KVO_ERR_INVALID for a null context or impl outside 0..2.
  */
 kvo_status kvo_set_select_impl(kvo_ctx* ctx, int impl);
+
+/*
+ * kvo_plan_select -- the selection kernels' launch plan for a shape, computed
+ * on the host: no context, no GPU.  blocks_per_group[n_groups] (host int32,
+ * >= 0): each group's candidate blocks at capacity (C_b, or the count it may
+ * grow to).  n_sms: the device's SMs (each holds 4 selection CTAs of 256
+ * threads).  impl: as kvo_set_select_impl.  Writes host out4 = {rows per
+ * thread (1, 2 or 4: 1024 rows per CTA when that gives about 8 CTAs per SM
+ * or more, else 512 or 256, whichever needs fewer waves, 256 on a tie), the
+ * most CTAs a group needs, the CTAs of the ticket kernel's grid, the CTAs per
+ * cluster of the cluster kernel or 0 when the ticket kernel runs}.
+ * Errors: KVO_ERR_INVALID for n_groups or n_sms <= 0, impl outside 0..2, a
+ * negative count or a null pointer.
+ */
+kvo_status kvo_plan_select(int n_groups, const int32_t* blocks_per_group, int n_sms, int impl, int32_t* out4);
 
 /*
  * kvo_plan_attention -- the work split of the TMA-staged attention kernel

@@ -101,7 +101,7 @@ struct Ctx {
     int sel_impl = 1;               // 0 ticket, 1 automatic, 2 cluster wherever a group's CTAs fit one
     int sel_clu = 0;                // CTAs per group of the cluster selection (0: the ticket kernel runs)
     int sel_chunks_max = 0;         // the most selection CTAs a group needs
-    int64_t sel_slots = 0;          // resident selection CTAs of the device (4 per SM)
+    int sel_sms = 1;                // SMs of the device (the selection plan's wave size: 4 CTAs each)
     // coalesce scratch: [2 (prefetch|urgent)][G][k][4], [2][G]
     int32_t* runs = nullptr;
     int32_t* nruns = nullptr;

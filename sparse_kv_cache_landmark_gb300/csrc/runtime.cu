@@ -138,11 +138,34 @@ int64_t plan_tma_items(int G, int sp_tokens, int w_tokens, int64_t grid, std::ve
 // llama3_8b_decode (1008 blocks per group) 17.4 / 17.6 us, long_ctx_predict
 // (2.5 waves) 138.5 / 140.8 us, and the Llama chain step 2.10 / 2.15 ms with
 // the ticket / cluster kernel.
+// Pure host logic (kvo_plan_select): returns the cluster's CTA count, or 0.
+static int select_cluster_ctas(int impl, int chunks_max, int64_t n_ctas, int Cmax, int sms) {
+    const int S = std::max(1, chunks_max);
+    const bool exposed = Cmax > 4 * kvo::SEL_THREADS && n_ctas <= 4 * (int64_t)sms;
+    const bool want = impl == 2 || (impl == 1 && exposed);
+    return want && S <= 8 ? S : 0;
+}
+
 static void set_sel_clu(kvo::Ctx& c) {
-    const int S = std::max(1, c.sel_chunks_max);
-    const bool exposed = c.Cmax > 4 * kvo::SEL_THREADS && c.n_sel_items <= c.sel_slots;
-    const bool want = c.sel_impl == 2 || (c.sel_impl == 1 && exposed);
-    c.sel_clu = want && S <= 8 ? S : 0;
+    c.sel_clu = select_cluster_ctas(c.sel_impl, c.sel_chunks_max, c.n_sel_items, c.Cmax, c.sel_sms);
+}
+
+// Rows per thread of the selection kernels (1, 2 or 4; 256 threads per CTA)
+// for groups of Ccap[g] candidate blocks on `sms` SMs holding 4 selection CTAs
+// each: 1024 rows per CTA when that gives ~8 CTAs per SM or more; otherwise
+// 512 or 256, whichever needs fewer waves (256 on a tie: more CTAs share the
+// HBM).  Pure host logic (kvo_plan_select).
+static int select_rows_per_thread(int G, const int32_t* Ccap, int sms) {
+    int64_t n[3] = {0, 0, 0};
+    for (int g = 0; g < G; ++g)
+        for (int i = 0; i < 3; ++i) {
+            const int rows = kvo::SEL_THREADS << i;
+            n[i] += (Ccap[g] + rows - 1) / rows;
+        }
+    const int64_t slots = 4 * (int64_t)std::max(1, sms);
+    auto waves = [&](int64_t x) { return (x + slots - 1) / slots; };
+    if (n[2] >= 8 * (int64_t)std::max(1, sms)) return 4;
+    return waves(n[1]) < waves(n[0]) ? 2 : 1;
 }
 
 kvo_status build_tma_plan(kvo::Ctx& c, kvo::Ctx::TmaPlan& pl, int64_t grid) {
@@ -437,34 +460,21 @@ kvo_status init_impl(kvo::Ctx& c, const kvo_config* cfg, void* const* k_host, vo
     KVO_CUDA(&c, cudaMemsetAsync(c.sel_done, 0, sizeof(uint32_t) * c.G, c.s_compute));
     std::vector<int2> sel_items;
     std::vector<int32_t> nch(c.G);
-    // 1024 rows per CTA when that gives ~8 CTAs per SM or more; otherwise 512
-    // or 256, whichever needs fewer waves of the 4 CTAs an SM holds (256 on a
-    // tie: more CTAs share the HBM)
     {
-        int64_t n[3] = {0, 0, 0};
-        for (int g = 0; g < c.G; ++g)
-            for (int i = 0; i < 3; ++i) {
-                const int rows = kvo::SEL_THREADS << i;
-                n[i] += (Ccap[g] + rows - 1) / rows;
-            }
         int dev = 0, sms = 0;
         KVO_CUDA(&c, cudaGetDevice(&dev));
         KVO_CUDA(&c, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        sms = std::max(1, sms);
-        const int64_t slots = 4 * (int64_t)sms;
-        c.sel_slots = slots;
-        auto waves = [&](int64_t x) { return (x + slots - 1) / slots; };
-        if (n[2] >= 8 * (int64_t)sms) c.sel_rpt = 4;
-        else c.sel_rpt = waves(n[1]) < waves(n[0]) ? 2 : 1;
+        c.sel_sms = std::max(1, sms);
     }
+    c.sel_rpt = select_rows_per_thread(c.G, Ccap.data(), c.sel_sms);
     const int sel_rows = kvo::SEL_THREADS * c.sel_rpt;
     for (int g = 0; g < c.G; ++g) {
         nch[g] = (Ccap[g] + sel_rows - 1) / sel_rows;     // rows past the current C_b are skipped
         for (int j = 0; j < nch[g]; ++j) sel_items.push_back(make_int2(g, j));
         c.sel_chunks_max = std::max(c.sel_chunks_max, nch[g]);
     }
-    set_sel_clu(c);
     c.n_sel_items = (int)sel_items.size();
+    set_sel_clu(c);
     KVO_CUDA(&c, dalloc(&c.sel_items, sizeof(int2) * sel_items.size(), &sb));
     KVO_CUDA(&c, dalloc(&c.sel_nchunks, sizeof(int32_t) * c.G, &sb));
     KVO_CUDA(&c, cudaMemcpy(c.sel_items, sel_items.data(), sizeof(int2) * sel_items.size(), cudaMemcpyHostToDevice));
@@ -1257,6 +1267,35 @@ kvo_status kvo_resident_fetched(kvo_ctx* ctx, int64_t* out2, int reset) {
     out2[0] = (int64_t)h[0];
     out2[1] = (int64_t)h[1];
     if (reset) KVO_CUDA(&c, cudaMemset(c.res_fetched, 0, sizeof(h)));
+    return KVO_OK;
+}
+
+kvo_status kvo_plan_select(int n_groups, const int32_t* blocks_per_group, int n_sms, int impl, int32_t* out4) {
+    if (n_groups <= 0 || !blocks_per_group || n_sms <= 0 || impl < 0 || impl > 2 || !out4) {
+        kvo::set_last_error("kvo_plan_select: need n_groups, n_sms > 0, impl in 0..2, non-null arrays");
+        return KVO_ERR_INVALID;
+    }
+    int Cmax = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        if (blocks_per_group[g] < 0) {
+            kvo::set_last_error("kvo_plan_select: negative block count");
+            return KVO_ERR_INVALID;
+        }
+        Cmax = std::max(Cmax, (int)blocks_per_group[g]);
+    }
+    const int rpt = select_rows_per_thread(n_groups, blocks_per_group, n_sms);
+    const int rows = kvo::SEL_THREADS * rpt;
+    int64_t n_ctas = 0;
+    int chunks_max = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        const int n = (blocks_per_group[g] + rows - 1) / rows;
+        n_ctas += n;
+        chunks_max = std::max(chunks_max, n);
+    }
+    out4[0] = rpt;
+    out4[1] = chunks_max;
+    out4[2] = (int32_t)std::min<int64_t>(n_ctas, INT32_MAX);
+    out4[3] = select_cluster_ctas(impl, chunks_max, n_ctas, Cmax, n_sms);
     return KVO_OK;
 }
 

@@ -25,7 +25,7 @@ EXPORTS = ["kv_offload_init", "kv_offload_destroy", "select_topk", "index_diff",
            "kvo_last_error", "sparse_decode_attn_static", "kvo_set_gather_shape", "kvo_set_gather_engine", "kvo_profile_trace", "sparse_decode_attn_cobatch",
            "kvo_decode_step_dual", "kvo_set_gather_reserve", "kvo_set_graphs", "kvo_append",
            "kvo_set_attn_impl", "kvo_set_select_impl", "kvo_resident_slots", "kvo_resident_fetched",
-           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention", "kvo_set_wait_test",
+           "kvo_set_prefetch_budget", "kvo_set_lowrank_keys", "kvo_plan_attention", "kvo_plan_select", "kvo_set_wait_test",
            "kvo_set_spec_policy", "kvo_spec_stats"]
 PROFILE_KINDS = ["select", "diff", "coalesce", "gather_prefetch", "gather_urgent", "attention", "recon"]
 
@@ -131,6 +131,16 @@ def merge_lse(o1, lse1, o2, lse2, o=None, lse=None, stream=None):
     lse = torch.empty_like(lse1) if lse is None else lse
     _check(lib().merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(o), _ptr(lse), rows, d, _stream(stream)))
     return o, lse
+
+
+def plan_select(blocks_per_group, n_sms: int, impl: int = 1) -> dict:
+    """Launch plan of the selection kernels (C: kvo_plan_select; host only):
+    rows per thread, the most CTAs a group needs, the ticket kernel's CTAs, and
+    the cluster kernel's CTAs per cluster (0: the ticket kernel runs)."""
+    blocks = (ctypes.c_int32 * len(blocks_per_group))(*[int(x) for x in blocks_per_group])
+    out = (ctypes.c_int32 * 4)()
+    _check(lib().kvo_plan_select(len(blocks_per_group), blocks, n_sms, impl, out))
+    return {"rows_per_thread": out[0], "ctas_per_group": out[1], "ctas": out[2], "cluster_ctas": out[3]}
 
 
 def plan_attention(n_groups: int, sparse_tokens: int, window_tokens: int, grid: int):
