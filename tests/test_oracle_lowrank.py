@@ -3,7 +3,6 @@ unit coefficient, integer factors), the fp64 product within the bf16 and fp32
 rounding bounds, the float32 -> bf16 rounding on hand values, and agreement
 with the generator's independently written low-rank keys.  CPU only."""
 import numpy as np
-import torch
 
 import oracle as orc
 from sparse_kv_cache_landmark_gb300 import synth

@@ -1,7 +1,6 @@
 """Oracle on the synthetic workloads: the planted structure is recovered and
 the selection margins hold (CPU)."""
 import numpy as np
-import torch
 
 import oracle as orc
 from sparse_kv_cache_landmark_gb300 import synth
