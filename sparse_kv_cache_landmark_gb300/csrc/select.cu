@@ -151,6 +151,22 @@ __device__ __forceinline__ void sum_queries(const uint16_t* __restrict__ q, cons
     }
 }
 
+// Bulk L2 prefetch of the first pf_chunks 16-byte chunks of landmark rows
+// [row0, row0 + nrows) of group bg (one contiguous run of 16 * nrows bytes per
+// chunk), issued by the first warp before the CTA sums its query, so the
+// landmark bytes stream from HBM while that prologue runs.
+template <int D, bool BF16LM>
+__device__ __forceinline__ void prefetch_rows_l2(const void* lm_v, int bg, int Cmax, int row0, int nrows,
+                                                 int pf_chunks) {
+    constexpr int NCH = BF16LM ? D / 8 : D / 4;
+    if (threadIdx.x >= 32 || nrows <= 0) return;
+    const char* g0 = reinterpret_cast<const char*>(lm_v) + ((int64_t)bg * NCH * Cmax + row0) * 16;
+    for (int c = threadIdx.x; c < min(pf_chunks, NCH); c += 32)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g0 + (int64_t)c * Cmax * 16),
+                     "r"((uint32_t)nrows * 16u)
+                     : "memory");
+}
+
 // Scores of SEL_RPT landmark rows per thread (rows row0 + i * SEL_THREADS,
 // those at or past C scoring 0) against the NQ summed queries in u_s.
 template <int D, bool BF16LM, int NQ, int SEL_RPT>
@@ -227,7 +243,7 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
               const int2* __restrict__ items, const int32_t* __restrict__ nchunks, const int32_t* __restrict__ g_C,
               uint32_t* __restrict__ keys, uint32_t* __restrict__ hist, uint32_t* __restrict__ done,
               int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred, int G, int Cmax4, int Cmax, int r,
-              int Hkv, int k, int key_cache, int dep_wait, const ResAssignArgs aa) {
+              int Hkv, int k, int key_cache, int dep_wait, int pf_chunks, const ResAssignArgs aa) {
     constexpr int NQ = DUAL ? 2 : 1;
     __shared__ __align__(16) float u_s[NQ][D];
     __shared__ uint32_t h_s[NQ][256];
@@ -246,6 +262,8 @@ select_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, con
     const int b = bg / Hkv, g = bg % Hkv;
     const int C = g_C[bg];
     const int Hq = Hkv * r;
+    prefetch_rows_l2<D, BF16LM>(lm_v, bg, Cmax, chunk * SEL_THREADS * SEL_RPT,
+                                min(SEL_THREADS * SEL_RPT, C - chunk * SEL_THREADS * SEL_RPT), pf_chunks);
 
     sum_queries<D, DUAL>(q, qs, b, g, Hq, r, u_s);
     for (int i = tid; i < NQ * 256; i += SEL_THREADS) (&h_s[0][0])[i] = 0u;
@@ -439,7 +457,7 @@ template <int D, bool BF16LM, bool DUAL, int SEL_RPT, bool ASSIGN>
 __global__ void __launch_bounds__(SEL_THREADS, sel_min_blocks<BF16LM, SEL_RPT>())
 select_cluster_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict__ q, const uint16_t* __restrict__ qs,
                       const int32_t* __restrict__ g_C, int32_t* __restrict__ idx_true, int32_t* __restrict__ idx_pred,
-                      int Cmax, int r, int Hkv, int k, int dep_wait, const ResAssignArgs aa) {
+                      int Cmax, int r, int Hkv, int k, int dep_wait, int pf_chunks, const ResAssignArgs aa) {
     constexpr int NQ = DUAL ? 2 : 1;
     constexpr int SEL_ROWS = SEL_THREADS * SEL_RPT;
     __shared__ __align__(16) float u_s[NQ][D];
@@ -459,6 +477,7 @@ select_cluster_kernel(const void* __restrict__ lm_v, const uint16_t* __restrict_
     const int C = g_C[bg];
     const int base = (int)rank * SEL_ROWS;                   // first row of this CTA
     const int nloc = max(0, min(C - base, SEL_ROWS));        // rows of this CTA
+    prefetch_rows_l2<D, BF16LM>(lm_v, bg, Cmax, base, nloc, pf_chunks);
 
     sum_queries<D, DUAL>(q, qs, b, g, Hkv * r, r, u_s);
     for (int i = tid; i < NQ * 256; i += SEL_THREADS) (&h_s[0][0])[i] = 0u;
@@ -597,6 +616,17 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const int dep_wait = pdl ? 1 : 0;
+    // Grids of more than one wave prefetch the first chunks of each CTA's rows
+    // into the L2 up front (as many as keep the resident CTAs' prefetched
+    // bytes within 48 MB of the 129 MB L2): a CTA of a later wave then streams
+    // while it sums its query.  Long-context layer (2.5 waves): 135.3 ->
+    // 129.7 us.  One-wave grids start every CTA at once and gained nothing
+    // (Llama layer 16.4-16.5 -> 16.7 us, wide budget 39.7-39.9 -> 40.2 us).
+    const int64_t rows_cta = (int64_t)SEL_THREADS * c.sel_rpt;
+    const int64_t grid_ctas = c.sel_clu > 0 ? (int64_t)c.G * c.sel_clu : c.n_sel_items;
+    const int64_t resident = std::min<int64_t>(grid_ctas, 4 * (int64_t)c.sel_sms);
+    const int pf_chunks = grid_ctas <= resident ? 0 :
+        (int)std::min<int64_t>(bf ? c.d / 8 : c.d / 4, (48ll << 20) / std::max<int64_t>(1, resident * rows_cta * 16));
     cudaError_t err = cudaSuccess;
     if (c.sel_clu > 0) {
         // one cluster of sel_clu CTAs per group; only the assignment's lists are dynamic
@@ -613,7 +643,7 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
 #define KVO_SELC_L(D_, BF_, DU_, RPT_, AS_)                                                                    \
     err = cudaLaunchKernelEx(&cfg, select_cluster_kernel<D_, BF_, DU_, RPT_, AS_>, c.lm[layer],                \
                              (const uint16_t*)q, (const uint16_t*)q_spec, (const int32_t*)c.g_C, idx_true,     \
-                             idx_pred, c.Cmax, c.r, c.Hkv, c.k, dep_wait, aa)
+                             idx_pred, c.Cmax, c.r, c.Hkv, c.k, dep_wait, pf_chunks, aa)
 #define KVO_SELC(D_, BF_, DU_, AS_)                                                                            \
     do {                                                                                                       \
         if (c.sel_rpt == 1) KVO_SELC_L(D_, BF_, DU_, 1, AS_);                                                  \
@@ -638,7 +668,7 @@ cudaError_t launch_select(const Ctx& c, int layer, const void* q, const void* q_
     err = cudaLaunchKernelEx(&cfg, select_kernel<D_, BF_, DU_, RPT_, AS_>, c.lm[layer], (const uint16_t*)q,     \
                              (const uint16_t*)q_spec, (const int2*)c.sel_items, (const int32_t*)c.sel_nchunks,  \
                              (const int32_t*)c.g_C, c.sel_keys, c.sel_hist, c.sel_done, idx_true, idx_pred, c.G, \
-                             Cmax4, c.Cmax, c.r, c.Hkv, c.k, key_cache, dep_wait, aa)
+                             Cmax4, c.Cmax, c.r, c.Hkv, c.k, key_cache, dep_wait, pf_chunks, aa)
 #define KVO_SEL(D_, BF_, DU_)                                                                                  \
     do {                                                                                                       \
         if (c.sel_rpt == 1) KVO_SEL_L(D_, BF_, DU_, 1, false);                                                  \
